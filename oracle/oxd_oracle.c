@@ -1,0 +1,237 @@
+/*
+ * Oracle for batched paged-KV decode attention -- TEST INFRASTRUCTURE ONLY.
+ * See oxd_oracle.h for the definition it restates and where it comes from.
+ *
+ * Deliberately plain: one query head at a time, tokens visited in logical
+ * order (page by page through the block table, then token by token inside a
+ * page), every bf16 widened exactly to double, every sum in double, no
+ * blocking, no online rescaling, no fusion. Threads only split the list of
+ * independent query heads, so the result does not depend on the thread count.
+ */
+#include "oxd_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_f64(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Element offset of (page, token t, kv head h, dim d) in a K or V pool. */
+static size_t pool_offset(int layout, int64_t page, int t, int h, int d, int page_size, int Hkv,
+                          int D) {
+    if (layout == ORACLE_LAYOUT_NHD)
+        return (((size_t)page * (size_t)page_size + (size_t)t) * (size_t)Hkv + (size_t)h) *
+                   (size_t)D +
+               (size_t)d;
+    return (((size_t)page * (size_t)Hkv + (size_t)h) * (size_t)page_size + (size_t)t) *
+               (size_t)D +
+           (size_t)d;
+}
+
+int64_t oracle_kv_len(const int32_t* indptr, const int32_t* last_page_len, int page_size, int b) {
+    int64_t pages = (int64_t)indptr[b + 1] - (int64_t)indptr[b];
+    return (pages - 1) * (int64_t)page_size + (int64_t)last_page_len[b];
+}
+
+/* Checks the block tables the way the definition needs them. */
+static int check_tables(int B, int page_size, int64_t num_pages, const int32_t* indptr,
+                        const int32_t* indices, const int32_t* last_page_len) {
+    for (int b = 0; b < B; ++b) {
+        if (indptr[b + 1] - indptr[b] < 1) return ORACLE_EINVAL;
+        if (last_page_len[b] < 1 || last_page_len[b] > page_size) return ORACLE_EINVAL;
+        for (int32_t p = indptr[b]; p < indptr[b + 1]; ++p)
+            if (indices[p] < 0 || (int64_t)indices[p] >= num_pages) return ORACLE_EINVAL;
+    }
+    return ORACLE_OK;
+}
+
+typedef struct {
+    int B, Hq, Hkv, D, page_size, layout;
+    const uint16_t *q, *k, *v;
+    const int32_t *indptr, *indices, *last_page_len;
+    double sm_scale;
+} problem;
+
+/*
+ * Logits of head (b, hq) for logical tokens [t0, t1) of request b, written to
+ * s[0 .. t1-t0). Logical token j lives in page indices[indptr[b] + j / ps] at
+ * slot j % ps.
+ */
+static void logits(const problem* P, int b, int hq, int64_t t0, int64_t t1, double* s) {
+    int G = P->Hq / P->Hkv;
+    int h = hq / G; /* consecutive query heads share one KV head */
+    const uint16_t* qrow = P->q + ((size_t)b * (size_t)P->Hq + (size_t)hq) * (size_t)P->D;
+    for (int64_t j = t0; j < t1; ++j) {
+        int64_t page = P->indices[P->indptr[b] + j / P->page_size];
+        int t = (int)(j % P->page_size);
+        double dot = 0.0;
+        for (int d = 0; d < P->D; ++d)
+            dot += bf16_to_f64(qrow[d]) *
+                   bf16_to_f64(P->k[pool_offset(P->layout, page, t, h, d, P->page_size,
+                                                P->Hkv, P->D)]);
+        s[j - t0] = P->sm_scale * dot;
+    }
+}
+
+/* Softmax-weighted mean of V over tokens [t0, t1) and its log-sum-exp. */
+static int head_state(const problem* P, int b, int hq, int64_t t0, int64_t t1, double* o,
+                      double* lse) {
+    for (int d = 0; d < P->D; ++d) o[d] = 0.0;
+    if (t1 <= t0) {
+        *lse = -INFINITY;
+        return ORACLE_OK;
+    }
+    int64_t n = t1 - t0;
+    double* s = (double*)malloc((size_t)n * sizeof(double));
+    if (!s) return ORACLE_ENOMEM;
+    logits(P, b, hq, t0, t1, s);
+
+    double M = -INFINITY;
+    for (int64_t j = 0; j < n; ++j)
+        if (s[j] > M) M = s[j];
+    double Z = 0.0;
+    for (int64_t j = 0; j < n; ++j) Z += exp(s[j] - M);
+
+    int G = P->Hq / P->Hkv;
+    int h = hq / G;
+    for (int64_t j = 0; j < n; ++j) {
+        double w = exp(s[j] - M) / Z;
+        int64_t lj = t0 + j;
+        int64_t page = P->indices[P->indptr[b] + lj / P->page_size];
+        int t = (int)(lj % P->page_size);
+        for (int d = 0; d < P->D; ++d)
+            o[d] += w * bf16_to_f64(P->v[pool_offset(P->layout, page, t, h, d, P->page_size,
+                                                     P->Hkv, P->D)]);
+    }
+    *lse = M + log(Z);
+    free(s);
+    return ORACLE_OK;
+}
+
+typedef struct {
+    const problem* P;
+    const int32_t* heads; /* NULL: all heads in (b, hq) order */
+    int n_heads;
+    int worker, nworkers;
+    double *out, *lse;
+    int status;
+} job;
+
+static void* run_job(void* arg) {
+    job* J = (job*)arg;
+    const problem* P = J->P;
+    J->status = ORACLE_OK;
+    for (int i = J->worker; i < J->n_heads; i += J->nworkers) {
+        int b, hq;
+        if (J->heads) {
+            b = J->heads[2 * i];
+            hq = J->heads[2 * i + 1];
+        } else {
+            b = i / P->Hq;
+            hq = i % P->Hq;
+        }
+        int64_t L = oracle_kv_len(P->indptr, P->last_page_len, P->page_size, b);
+        int rc = head_state(P, b, hq, 0, L, J->out + (size_t)i * (size_t)P->D, J->lse + i);
+        if (rc != ORACLE_OK) {
+            J->status = rc;
+            return NULL;
+        }
+    }
+    return NULL;
+}
+
+static int check_shape(int B, int Hq, int Hkv, int D, int page_size, int layout) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || page_size < 1) return ORACLE_EINVAL;
+    if (Hq % Hkv != 0) return ORACLE_EINVAL;
+    if (layout != ORACLE_LAYOUT_NHD && layout != ORACLE_LAYOUT_HND) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+int oracle_paged_decode_f64(int B, int Hq, int Hkv, int D, int page_size, int layout,
+                            int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* v, const int32_t* indptr, const int32_t* indices,
+                            const int32_t* last_page_len, double sm_scale,
+                            const int32_t* heads, int n_heads, double* out, double* lse,
+                            int nthreads) {
+    if (check_shape(B, Hq, Hkv, D, page_size, layout) != ORACLE_OK) return ORACLE_EINVAL;
+    if (check_tables(B, page_size, num_pages, indptr, indices, last_page_len) != ORACLE_OK)
+        return ORACLE_EINVAL;
+    if (heads) {
+        for (int i = 0; i < n_heads; ++i)
+            if (heads[2 * i] < 0 || heads[2 * i] >= B || heads[2 * i + 1] < 0 ||
+                heads[2 * i + 1] >= Hq)
+                return ORACLE_EINVAL;
+    } else {
+        n_heads = B * Hq;
+    }
+    problem P = {B, Hq, Hkv, D, page_size, layout, q, k, v, indptr, indices, last_page_len,
+                 sm_scale};
+
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n_heads) nthreads = n_heads > 0 ? n_heads : 1;
+
+    job* jobs = (job*)calloc((size_t)nthreads, sizeof(job));
+    pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return ORACLE_ENOMEM;
+    }
+    for (int w = 0; w < nthreads; ++w) {
+        jobs[w] = (job){&P, heads, n_heads, w, nthreads, out, lse, ORACLE_OK};
+        if (w > 0) pthread_create(&tids[w], NULL, run_job, &jobs[w]);
+    }
+    run_job(&jobs[0]);
+    int status = jobs[0].status;
+    for (int w = 1; w < nthreads; ++w) {
+        pthread_join(tids[w], NULL);
+        if (jobs[w].status != ORACLE_OK) status = jobs[w].status;
+    }
+    free(jobs);
+    free(tids);
+    return status;
+}
+
+int oracle_partial_state_f64(int B, int Hq, int Hkv, int D, int page_size, int layout,
+                             int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                             const uint16_t* v, const int32_t* indptr, const int32_t* indices,
+                             const int32_t* last_page_len, double sm_scale, int b, int hq,
+                             int64_t tok_begin, int64_t tok_end, double* o, double* lse) {
+    if (check_shape(B, Hq, Hkv, D, page_size, layout) != ORACLE_OK) return ORACLE_EINVAL;
+    if (check_tables(B, page_size, num_pages, indptr, indices, last_page_len) != ORACLE_OK)
+        return ORACLE_EINVAL;
+    if (b < 0 || b >= B || hq < 0 || hq >= Hq) return ORACLE_EINVAL;
+    int64_t L = oracle_kv_len(indptr, last_page_len, page_size, b);
+    if (tok_begin < 0 || tok_end > L || tok_begin > tok_end) return ORACLE_EINVAL;
+    problem P = {B, Hq, Hkv, D, page_size, layout, q, k, v, indptr, indices, last_page_len,
+                 sm_scale};
+    return head_state(&P, b, hq, tok_begin, tok_end, o, lse);
+}
+
+void oracle_merge_states_f64(int S, int D, const double* v, const double* s, double* out,
+                             double* lse) {
+    double M = -INFINITY;
+    for (int i = 0; i < S; ++i)
+        if (s[i] > M) M = s[i];
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (M == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double W = 0.0;
+    for (int i = 0; i < S; ++i) W += exp(s[i] - M);
+    for (int i = 0; i < S; ++i) {
+        double w = exp(s[i] - M) / W;
+        for (int d = 0; d < D; ++d) out[d] += w * v[(size_t)i * (size_t)D + (size_t)d];
+    }
+    *lse = M + log(W);
+}
