@@ -1,0 +1,240 @@
+/*
+ * oxd -- batched paged-KV decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * One BF16 query token per request attends, with full softmax attention, over
+ * that request's KV cache, which lives in fixed-size pages of a shared K pool
+ * and V pool and is addressed through CSR block tables
+ * (indptr / indices / last_page_len). MHA, GQA and MQA head groupings; NHD or
+ * HND page layout; head dimension 128.
+ *
+ * What the operation is: the "FlashInfer parity matrix" page, section
+ * "Admitted attention matrix", row "Paged batch decode" (MHA, MQA, GQA, mixed
+ * lengths, page order, read-only page reuse), with the softmax state kept in
+ * F32 as every attention row there fixes; "Domain coverage" names the NHD and
+ * HND paged layouts; the "Single decode split-K" row gives split partitions with
+ * an F32 partial workspace followed by a merge; "Attention state and cascade"
+ * names the state merge.
+ *
+ * How it is driven: the "Oxide Infer" README, section "One execution model"
+ * (spec -> plan -> operands -> command scope -> completion; planning fixes the
+ * algorithm, workspace and launch configuration and enqueue never tunes or
+ * falls back) and section "Providers" (caller-selected stream, checked span,
+ * alignment, alias and capacity rules, explicit workspace requirements,
+ * completion-owned resource leases, typed device-status failures).
+ *
+ * Conventions for every entry point:
+ *  - Returns an oxd_status. On any error nothing has been enqueued and no
+ *    caller memory has been written.
+ *  - "device" pointers are CUDA device (or managed) addresses on the plan's
+ *    device; "host" pointers are ordinary host memory read during the call.
+ *  - The caller owns every buffer and the stream. The library allocates no
+ *    device memory and never synchronises a stream, except
+ *    oxd_read_device_status, which says so.
+ *  - Streams are passed as void* and are cudaStream_t values (NULL = the
+ *    legacy default stream).
+ *
+ * Numerics: logits, the running maximum, the softmax denominator and the
+ * output accumulator are F32; QK^T and PV products run on tensor cores for
+ * grouped heads (Hq/Hkv >= 3) with BF16 operands (the softmax weights P are
+ * rounded to BF16 before the PV product) and on CUDA cores for Hq/Hkv <= 2.
+ * out is rounded once to BF16 (nearest even). lse is the natural logarithm of
+ * sum_j exp(sm_scale * q.k_j). Results are deterministic: the same plan and
+ * inputs give bitwise identical out and lse (no floating-point atomics).
+ */
+#ifndef OXD_H
+#define OXD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OXD_OK = 0,
+    OXD_ERR_INVALID_ARGUMENT = 1,   /* bad shape, NULL pointer, bad block table */
+    OXD_ERR_UNSUPPORTED = 2,        /* valid request outside the implemented contract */
+    OXD_ERR_ALIGNMENT = 3,          /* a pointer misses its required alignment */
+    OXD_ERR_ALIAS = 4,              /* an output overlaps an input or another output */
+    OXD_ERR_WORKSPACE_TOO_SMALL = 5,
+    OXD_ERR_PLAN_MISMATCH = 6,      /* plan used with another device, or a destroyed plan */
+    OXD_ERR_CUDA = 7,               /* a CUDA runtime call failed (launch, copy, query) */
+    OXD_ERR_DEVICE_STATUS = 8,      /* the kernels reported an error; see the code */
+    OXD_ERR_NO_MEMORY = 9           /* host allocation failed while planning */
+} oxd_status;
+
+typedef enum {
+    /* page = [page_size][num_kv_heads][head_dim]; element (p, t, h, d) at
+     * ((p*page_size + t)*num_kv_heads + h)*head_dim + d */
+    OXD_LAYOUT_NHD = 0,
+    /* page = [num_kv_heads][page_size][head_dim]; element (p, h, t, d) at
+     * ((p*num_kv_heads + h)*page_size + t)*head_dim + d */
+    OXD_LAYOUT_HND = 1
+} oxd_kv_layout;
+
+/* Codes the kernels write into the workspace status word (first error wins). */
+#define OXD_DEVICE_OK 0
+#define OXD_DEVICE_BAD_PAGE 1       /* a listed page index is outside [0, num_pages) */
+#define OXD_DEVICE_PLAN_MISMATCH 2  /* device indptr/last_page_len differ from the plan's */
+#define OXD_DEVICE_WAIT_TIMEOUT 3   /* an internal pipeline wait gave up (about 1 s) */
+
+typedef struct oxd_plan_s* oxd_plan; /* opaque, host-owned, immutable after planning */
+
+typedef struct {
+    int32_t batch;          /* B >= 1 requests, one query token each */
+    int32_t num_qo_heads;   /* Hq >= 1 */
+    int32_t num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0, G = Hq/Hkv <= 32 */
+    int32_t head_dim;       /* D; must be 128 */
+    int32_t page_size;      /* ps in {8, 16, 32, 64} tokens */
+    int32_t layout;         /* oxd_kv_layout */
+    int64_t num_pages;      /* pages in each of the K and V pools; 1 <= num_pages < 2^31 */
+    int32_t max_splits;     /* 0 = planner's choice; 1 = never split; n = at most n per request */
+    int32_t force_splits;   /* 0 = off; n > 0: split every request into min(n, P_b) chunks */
+    int32_t num_sms;        /* 0 = query the device; > 0 = plan for that many SMs */
+    int32_t reserved[3];    /* must be zero */
+} oxd_paged_decode_desc;
+
+typedef struct {
+    int32_t num_work_items;     /* (request, page-range) chunks; the grid is this x Hkv */
+    int32_t num_split_requests; /* requests whose chunks need a merge */
+    int32_t max_chunks;         /* most chunks any request got */
+    int32_t chunk_pages;        /* planner's chunk length in pages */
+    int32_t num_slots;          /* partial-state slots in the workspace */
+    int32_t kernel_variant;     /* 0/1: CUDA-core G=1/G=2; 2,3,4: tensor-core G<=8, <=16, <=32 */
+    int32_t grid_ctas;          /* decode CTAs launched per run */
+    int32_t ctas_per_sm;        /* resident decode CTAs per SM assumed by the planner */
+    int32_t num_sms;
+    int32_t launches_per_run;   /* kernels one run enqueues (1 or 2) */
+    int64_t workspace_bytes;
+    int64_t upload_bytes;       /* host->device bytes one run copies (the work list) */
+    int64_t total_kv_tokens;    /* sum_b L_b */
+} oxd_plan_info;
+
+/*
+ * Plan one batch of decode ("One execution model": the plan fixes the
+ * algorithm, the split of each request's pages into chunks, the launch shape
+ * and the workspace size; a run never re-plans).
+ *
+ *   desc               shapes and options (host)
+ *   indptr_host        [B+1] int32, host: request b owns index entries
+ *                      [indptr[b], indptr[b+1]); at least one page each;
+ *                      non-decreasing, indptr[0] >= 0
+ *   last_page_len_host [B] int32, host: tokens used in request b's last page,
+ *                      in [1, page_size]; L_b = (P_b - 1)*page_size + last
+ *   device             CUDA device ordinal the plan will run on (ignored when
+ *                      desc->num_sms > 0; then planning makes no device query)
+ *   plan_out           receives the plan; destroy with oxd_plan_destroy
+ *   workspace_bytes_out receives the device workspace size run needs
+ *
+ * The plan keeps a page-locked host copy of the work list; each run copies it
+ * to the workspace asynchronously, so the plan must outlive every run that
+ * used it until that run's stream work has completed.
+ * Errors: OXD_ERR_INVALID_ARGUMENT (NULL pointer, non-positive sizes,
+ * Hq % Hkv != 0, empty request, last_page_len outside [1, page_size], nonzero
+ * reserved fields), OXD_ERR_UNSUPPORTED (head_dim != 128, page_size not in
+ * {8,16,32,64}, G > 32), OXD_ERR_CUDA (device query failed),
+ * OXD_ERR_NO_MEMORY.
+ */
+oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_t* indptr_host,
+                                 const int32_t* last_page_len_host, int device,
+                                 oxd_plan* plan_out, size_t* workspace_bytes_out);
+
+/*
+ * Enqueue one decode step on `stream` ("Paged batch decode" row of
+ * "Admitted attention matrix"):
+ *   out[b, hq, :] = sum_j softmax_j(sm_scale * q[b, hq, :] . k_j) v_j
+ *   lse[b, hq]    = ln sum_j exp(sm_scale * q[b, hq, :] . k_j)
+ * over the L_b tokens of request b, taken from pages
+ * indices[indptr[b] .. indptr[b+1]) in order, KV head h = hq / (Hq/Hkv).
+ *
+ *   q             device bf16 [B][Hq][128], 16-byte aligned
+ *   k_pages       device bf16 pool of num_pages pages in the plan's layout,
+ *   v_pages       16-byte aligned; read only (pages may be listed by many
+ *                 requests -- read-only page reuse)
+ *   indptr        device int32 [B+1], same values as the plan's host copy
+ *   indices       device int32 [indptr[B]], physical page of each logical page
+ *   last_page_len device int32 [B], same values as the plan's host copy
+ *   sm_scale      finite logit scale (no implicit 1/sqrt(D))
+ *   out           device bf16 [B][Hq][128], 16-byte aligned
+ *   lse           device f32 [B][Hq], 4-byte aligned, or NULL
+ *   workspace     device scratch of at least the planned size, 256-byte
+ *                 aligned; holds the work list, the split partial states and
+ *                 the device status word; must not be shared by runs that can
+ *                 overlap on the GPU
+ *   stream        cudaStream_t
+ *
+ * Host-side errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT,
+ * OXD_ERR_ALIGNMENT, OXD_ERR_ALIAS (out, lse and workspace must not overlap
+ * each other or any input), OXD_ERR_WORKSPACE_TOO_SMALL,
+ * OXD_ERR_PLAN_MISMATCH (destroyed plan, or the calling thread's current
+ * device differs from the plan's), OXD_ERR_CUDA (copy or launch failed).
+ * Device-side errors (an out-of-range page index, device block tables that
+ * differ from the plan's) do not fault: the kernels record a code in the
+ * workspace status word, read with oxd_read_device_status; out/lse of the
+ * affected heads are then unspecified (finite for a bad page: the kernel
+ * reads page 0 in its place, so no access leaves the pools).
+ */
+oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_pages,
+                                const void* v_pages, const int32_t* indptr,
+                                const int32_t* indices, const int32_t* last_page_len,
+                                float sm_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Merge attention states ("Attention state and cascade": state merge).
+ * For each n < N and h < H, combine the S states (v[n, i, h, :], s[n, i, h]):
+ *   M = max_i s_i, w_i = exp(s_i - M),
+ *   v_out[n, h, :] = sum_i w_i v_i / sum_i w_i,  s_out[n, h] = M + ln sum_i w_i.
+ * States with s_i = -inf carry no weight; if all are -inf, v_out = 0 and
+ * s_out = -inf. s uses the natural logarithm, as lse from a run does.
+ *
+ *   v      device f32 [N][S][H][D], 16-byte aligned, D % 4 == 0
+ *   s      device f32 [N][S][H], 4-byte aligned
+ *   v_out  device bf16 [N][H][D], 8-byte aligned
+ *   s_out  device f32 [N][H] or NULL
+ * Errors: OXD_ERR_INVALID_ARGUMENT (non-positive sizes, D % 4 != 0, NULL),
+ * OXD_ERR_ALIGNMENT, OXD_ERR_ALIAS (outputs overlap inputs or each other),
+ * OXD_ERR_CUDA.
+ */
+oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S, int32_t H,
+                            int32_t D, void* v_out, float* s_out, void* stream);
+
+/* Planner decisions of a plan (host only). */
+oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info);
+
+/*
+ * Record caller-created CUDA events immediately before and after the decode
+ * kernel of every later run of this plan (cudaEvent_t values; NULL, NULL
+ * turns it off). For measuring the kernel alone; the plan is otherwise
+ * unchanged.
+ */
+oxd_status oxd_plan_set_timing_events(oxd_plan plan, void* event_before, void* event_after);
+
+/*
+ * Release a plan. Only after every run that used it has completed on the GPU
+ * (its page-locked work list may still be being copied until then; the
+ * "Providers" section's completion-owned lease).
+ */
+oxd_status oxd_plan_destroy(oxd_plan plan);
+
+/*
+ * Synchronise `stream`, then read the device status word of `workspace` (the
+ * one the last run on that workspace wrote) into *code. Returns OXD_OK when
+ * the code is OXD_DEVICE_OK, OXD_ERR_DEVICE_STATUS otherwise, OXD_ERR_CUDA if
+ * the copy failed. This is the one call that blocks the host.
+ */
+oxd_status oxd_read_device_status(const void* workspace, void* stream, int32_t* code);
+
+/* Static strings for a status and a device status code. */
+const char* oxd_status_string(oxd_status status);
+const char* oxd_device_status_string(int32_t code);
+
+/* Library version string, e.g. "oxd 0.1.0 sm_103a". */
+const char* oxd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OXD_H */

@@ -1,0 +1,767 @@
+// Paged-KV decode attention kernels for sm_103a.
+//
+// Operation: "FlashInfer parity matrix" page, "Admitted attention matrix",
+// row "Paged batch decode" (direct kernel for MHA, eight-warp token-parallel
+// kernel for MQA/GQA), with the F32 online softmax every attention row there
+// fixes and the split partitions + F32 partial workspace of the
+// "Single decode split-K" row.
+//
+// One CTA handles one work item: a run of consecutive pages of one request
+// for one KV head. Inside the CTA:
+//   * a producer warp reads the item's page indices (32 at a time, coalesced,
+//     one window ahead), checks them against the pool size and issues one TMA
+//     tensor copy per (page, 64-wide half of D) into a ring of shared-memory
+//     stages, each guarded by a "full" and an "empty" mbarrier;
+//   * consumer warps split every stage token-parallel, 16 tokens per warp, and
+//     keep their own running max, denominator and output accumulator (F32);
+//     for grouped heads (G >= 3) the group's query rows form the A operand of
+//     mma.sync m16n8k16 (QK^T) and the softmax weights, rounded to bf16, the A
+//     operand of the PV product, so one K/V read serves all G heads; for
+//     G <= 2 the dot products run on CUDA cores;
+//   * at the end the warps' states are merged in shared memory and the CTA
+//     writes either the final bf16 output and LSE or, for a split request, an
+//     F32 partial state that the merge kernel combines.
+// Every wait on an mbarrier is bounded (about one second); a wait that gives
+// up records OXD_DEVICE_WAIT_TIMEOUT, drains the copies already issued and
+// returns without writing outputs.
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <type_traits>
+
+#include "oxd_internal.h"
+
+namespace oxd {
+namespace {
+
+constexpr int kDeviceBadPage = 1;
+constexpr int kDevicePlanMismatch = 2;
+constexpr int kDeviceWaitTimeout = 3;
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr int kAccStride = kHeadDim + 8;  // padded row of the epilogue accumulator dump
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with `parity` to complete. Gives up (returns false)
+// after kWaitTimeoutNs, or early once *abort is set by another warp.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort != nullptr && *abort) return false;
+        if (global_ns() - t0 > static_cast<uint64_t>(kWaitTimeoutNs)) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A * B + D, m16n8k16, bf16 inputs, f32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ void record_status(int32_t* status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------------ tile addressing
+//
+// A stage holds K then V for kStageTokens tokens. Each is a sequence of TMA
+// boxes of R = page_size rows (one page of one KV head); a box is two
+// [R][64] bf16 halves (d < 64, then d >= 64), 128-byte rows, written by TMA
+// with the 128-byte swizzle: 16-byte chunk cc of row r sits at chunk
+// cc ^ (r % 8). Every half starts on a 1024-byte boundary (R is a multiple
+// of 8), so the swizzle phase is r % 8 = t % 8.
+//
+// Byte offset of 16-byte chunk c (0..15, i.e. d = 8c..8c+7) of token t:
+//   (t / R) * R * 256 + (c / 8) * R * 128 + (t % R) * 128 + ((c % 8) ^ (t % 8)) * 16
+// and (t / R) * R * 256 + (t % R) * 128 = t * 256 - (t % R) * 128.
+struct RowAddr {
+    uint32_t base;  // tile base + t * 256 - (t % R) * 128
+    uint32_t xr;    // t % 8
+};
+
+__device__ __forceinline__ RowAddr row_addr(uint32_t tile, int t, int rmask) {
+    const int r = t & rmask;
+    return {tile + static_cast<uint32_t>(t * 256 - r * 128), static_cast<uint32_t>(t & 7)};
+}
+
+__device__ __forceinline__ uint32_t chunk_addr(const RowAddr& ra, int c, int half_bytes) {
+    return ra.base + static_cast<uint32_t>((c >> 3) * half_bytes) +
+           ((static_cast<uint32_t>(c & 7) ^ ra.xr) << 4);
+}
+
+// ------------------------------------------------------------------ configuration
+
+template <int kMtiles_, bool kHiRows_, int kSlices_, int kStages_, bool kMma_, int kFmaGroup_>
+struct Cfg {
+    static constexpr int kMtiles = kMtiles_;       // 16-row query tiles (mma)
+    static constexpr bool kHiRows = kHiRows_;      // rows 8..15 of a tile in use
+    static constexpr int kSlices = kSlices_;       // token slices per stage
+    static constexpr int kStages = kStages_;
+    static constexpr bool kMma = kMma_;
+    static constexpr int kFmaGroup = kFmaGroup_;   // G of the CUDA-core variant
+    static constexpr int kConsumerWarps = kMma ? kSlices * kMtiles : kSlices;
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    static constexpr int kStageTokens = kSlices * kSliceTokens;
+    static constexpr int kStageBytes = kStageTokens * kHeadDim * 2 * 2;  // K and V
+    static constexpr int kDumpBytes = kConsumerWarps * 16 * kAccStride * 4;
+    static constexpr int kTileBytes =
+        kStages * kStageBytes > kDumpBytes ? kStages * kStageBytes : kDumpBytes;
+    // tiles | full[kStages] | empty[kStages] | issued[kStages] | flags[4] | red_m | red_l
+    static constexpr int kBarOffset = kTileBytes;
+    static constexpr int kIssuedOffset = kBarOffset + 2 * kStages * 8;
+    static constexpr int kFlagOffset = kIssuedOffset + kStages * 4;
+    static constexpr int kRedOffset = kFlagOffset + 16;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRedOffset +
+                                      2 * kConsumerWarps * 16 * 4;
+};
+
+using CfgFmaG1 = Cfg<1, false, 4, 3, false, 1>;
+using CfgFmaG2 = Cfg<1, false, 4, 3, false, 2>;
+using CfgMma8 = Cfg<1, false, 4, 3, true, 0>;
+using CfgMma16 = Cfg<1, true, 4, 3, true, 0>;
+using CfgMma32 = Cfg<2, true, 4, 3, true, 0>;
+
+// ------------------------------------------------------------------ consumers
+
+// Tensor-core consumer: one warp owns query rows [16*mt, 16*mt + 16) of the
+// group and one 16-token slice of every stage.
+template <class C>
+struct MmaConsumer {
+    uint32_t qa[8][4];   // A fragments of the query rows, one per 16-wide k step
+    float m[2];          // running max (log2 domain) of rows g, g + 8
+    float l[2];          // running denominator (this thread's columns)
+    float acc[16][4];    // output accumulator, 16 n-tiles of 8 columns
+
+    __device__ __forceinline__ void init(const DecodeParams& p, int b, int hkv, int mt, int lane) {
+        const int g = lane >> 2, tq = lane & 3;
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * p.group + r0) * kHeadDim);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * p.group + r1) * kHeadDim);
+        const bool v0 = r0 < p.group, v1 = C::kHiRows && r1 < p.group;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int w = ks * 8 + tq;  // 32-bit word = columns 16ks + 2tq, +1
+            qa[ks][0] = v0 ? __ldg(q0 + w) : 0u;
+            qa[ks][1] = v1 ? __ldg(q1 + w) : 0u;
+            qa[ks][2] = v0 ? __ldg(q0 + w + 4) : 0u;
+            qa[ks][3] = v1 ? __ldg(q1 + w + 4) : 0u;
+        }
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    }
+
+    // Tokens [u0, u0 + 16) of the work item sit at rows t0.. of the stage tiles.
+    __device__ __forceinline__ void consume(uint32_t tk, uint32_t tv, int t0, int u0, int valid,
+                                            int rmask, int half_bytes, float scale_log2,
+                                            int lane) {
+        const int mi = lane >> 3, ri = lane & 7;
+        // ---- S = Q K^T for 16 tokens: two n-tiles of 8 tokens
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const RowAddr rk = row_addr(tk, t0 + ((mi >> 1) << 3) + ri, rmask);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(chunk_addr(rk, 2 * ks + (mi & 1), half_bytes), b0, b1, b2, b3);
+            mma_bf16(s[0], qa[ks], b0, b1);
+            mma_bf16(s[1], qa[ks], b2, b3);
+        }
+        // ---- online softmax in the log2 domain
+        const int tq = lane & 3;
+        const bool partial = u0 + kSliceTokens > valid;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = u0 + nt * 8 + 2 * tq + (e & 1);
+                const float x = s[nt][e] * scale_log2;
+                s[nt][e] = (partial && tok >= valid) ? -INFINITY : x;
+            }
+        }
+        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        const float mn0 = fmaxf(m[0], mx0);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float al0 = fast_exp2(m[0] - mu0);
+        m[0] = mn0;
+        s[0][0] = fast_exp2(s[0][0] - mu0);
+        s[0][1] = fast_exp2(s[0][1] - mu0);
+        s[1][0] = fast_exp2(s[1][0] - mu0);
+        s[1][1] = fast_exp2(s[1][1] - mu0);
+        l[0] = l[0] * al0 + ((s[0][0] + s[0][1]) + (s[1][0] + s[1][1]));
+        float al1 = 1.f;
+        if constexpr (C::kHiRows) {
+            float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn1 = fmaxf(m[1], mx1);
+            const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+            al1 = fast_exp2(m[1] - mu1);
+            m[1] = mn1;
+            s[0][2] = fast_exp2(s[0][2] - mu1);
+            s[0][3] = fast_exp2(s[0][3] - mu1);
+            s[1][2] = fast_exp2(s[1][2] - mu1);
+            s[1][3] = fast_exp2(s[1][3] - mu1);
+            l[1] = l[1] * al1 + ((s[0][2] + s[0][3]) + (s[1][2] + s[1][3]));
+        } else {
+            s[0][2] = s[0][3] = s[1][2] = s[1][3] = 0.f;
+        }
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            acc[n][0] *= al0;
+            acc[n][1] *= al0;
+            if constexpr (C::kHiRows) {
+                acc[n][2] *= al1;
+                acc[n][3] *= al1;
+            }
+        }
+        // ---- O += P V: P (bf16) is the A operand, built from the S fragments
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(s[0][0], s[0][1]);
+        pa[1] = pack_bf16x2(s[0][2], s[0][3]);
+        pa[2] = pack_bf16x2(s[1][0], s[1][1]);
+        pa[3] = pack_bf16x2(s[1][2], s[1][3]);
+        // V rows of tokens past `valid` may hold anything (even NaN): zero the
+        // corresponding halves of the B fragments, not just their weights.
+        uint32_t keep0 = 0xffffffffu, keep1 = 0xffffffffu;
+        if (partial) {
+            const int k0 = u0 + 2 * tq;
+            keep0 = (k0 < valid ? 0x0000ffffu : 0u) | (k0 + 1 < valid ? 0xffff0000u : 0u);
+            keep1 = (k0 + 8 < valid ? 0x0000ffffu : 0u) | (k0 + 9 < valid ? 0xffff0000u : 0u);
+        }
+        const RowAddr rv = row_addr(tv, t0 + ((mi & 1) << 3) + ri, rmask);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(chunk_addr(rv, 2 * np + (mi >> 1), half_bytes), b0, b1, b2, b3);
+            mma_bf16(acc[2 * np], pa, b0 & keep0, b1 & keep1);
+            mma_bf16(acc[2 * np + 1], pa, b2 & keep0, b3 & keep1);
+        }
+    }
+
+    // Dump raw state: red_m/red_l [cw][16], A [cw][16][kAccStride].
+    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* A, int cw, int lane) {
+        const int g = lane >> 2, tq = lane & 3;
+        float l0 = l[0], l1 = l[1];
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (tq == 0) {
+            red_m[cw * 16 + g] = m[0];
+            red_l[cw * 16 + g] = l0;
+            red_m[cw * 16 + g + 8] = C::kHiRows ? m[1] : -INFINITY;
+            red_l[cw * 16 + g + 8] = C::kHiRows ? l1 : 0.f;
+        }
+        float* a0 = A + (cw * 16 + g) * kAccStride + 2 * tq;
+        float* a1 = a0 + 8 * kAccStride;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            *reinterpret_cast<float2*>(a0 + n * 8) = make_float2(acc[n][0], acc[n][1]);
+            if constexpr (C::kHiRows)
+                *reinterpret_cast<float2*>(a1 + n * 8) = make_float2(acc[n][2], acc[n][3]);
+        }
+    }
+};
+
+// CUDA-core consumer for G <= 2: lane = (token parity, 16-byte chunk of D).
+template <class C>
+struct FmaConsumer {
+    static constexpr int G = C::kFmaGroup;
+    float qf[G][8];
+    float m[G];
+    float l[G];
+    float acc[G][8];
+
+    __device__ __forceinline__ void init(const DecodeParams& p, int b, int hkv, int /*mt*/,
+                                         int lane) {
+        const int c = lane & 15;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * G + g) * kHeadDim +
+                c * 8));
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                qf[g][2 * j] = bf16_lo(w[j]);
+                qf[g][2 * j + 1] = bf16_hi(w[j]);
+            }
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[g][j] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void consume(uint32_t tk, uint32_t tv, int t0, int u0, int valid,
+                                            int rmask, int half_bytes, float scale_log2,
+                                            int lane) {
+        const int par = lane >> 4, c = lane & 15;
+        float s[G][8];
+        // ---- logits: each half-warp reduces one token's dot product
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const RowAddr ra = row_addr(tk, t0 + 2 * i + par, rmask);
+            uint4 kv;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(kv.x), "=r"(kv.y), "=r"(kv.z), "=r"(kv.w)
+                         : "r"(chunk_addr(ra, c, half_bytes)));
+            const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+            float kf[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                kf[2 * j] = bf16_lo(w[j]);
+                kf[2 * j + 1] = bf16_hi(w[j]);
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float d = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) d = fmaf(qf[g][j], kf[j], d);
+                d += __shfl_xor_sync(0xffffffffu, d, 1);
+                d += __shfl_xor_sync(0xffffffffu, d, 2);
+                d += __shfl_xor_sync(0xffffffffu, d, 4);
+                d += __shfl_xor_sync(0xffffffffu, d, 8);
+                const int tok = u0 + 2 * i + par;
+                s[g][i] = tok < valid ? d * scale_log2 : -INFINITY;
+            }
+        }
+        // ---- online softmax (both half-warps share one running max)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mx = s[g][0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i) mx = fmaxf(mx, s[g][i]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m[g], mx);
+            const float mu = mn == -INFINITY ? 0.f : mn;
+            const float al = fast_exp2(m[g] - mu);
+            m[g] = mn;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                s[g][i] = fast_exp2(s[g][i] - mu);
+                sum += s[g][i];
+            }
+            l[g] = l[g] * al + sum;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[g][j] *= al;
+        }
+        // ---- accumulate P V over this half-warp's tokens
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int tok = u0 + 2 * i + par;
+            if (tok < valid) {
+                const RowAddr ra = row_addr(tv, t0 + 2 * i + par, rmask);
+                uint4 vv;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(vv.x), "=r"(vv.y), "=r"(vv.z), "=r"(vv.w)
+                             : "r"(chunk_addr(ra, c, half_bytes)));
+                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[g][2 * j] = fmaf(s[g][i], bf16_lo(w[j]), acc[g][2 * j]);
+                        acc[g][2 * j + 1] = fmaf(s[g][i], bf16_hi(w[j]), acc[g][2 * j + 1]);
+                    }
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* A, int cw, int lane) {
+        const int par = lane >> 4, c = lane & 15;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            // both half-warps used the same running max, so their sums add
+            const float lt = l[g] + __shfl_xor_sync(0xffffffffu, l[g], 16);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[g][j] += __shfl_xor_sync(0xffffffffu, acc[g][j], 16);
+            if (lane == 0) {
+                red_m[cw * 16 + g] = m[g];
+                red_l[cw * 16 + g] = lt;
+            }
+            if (par == 0) {
+                float* a = A + (cw * 16 + g) * kAccStride + c * 8;
+                *reinterpret_cast<float4*>(a) = make_float4(acc[g][0], acc[g][1], acc[g][2],
+                                                            acc[g][3]);
+                *reinterpret_cast<float4*>(a + 4) = make_float4(acc[g][4], acc[g][5], acc[g][6],
+                                                                acc[g][7]);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ the kernel
+
+template <class C>
+__global__ void __launch_bounds__(C::kThreads)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* empty = full + C::kStages;
+    int* issued = reinterpret_cast<int*>(smem + C::kIssuedOffset);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);
+    float* red_m = reinterpret_cast<float*>(smem + C::kRedOffset);
+    float* red_l = red_m + C::kConsumerWarps * 16;
+    float* dumpA = reinterpret_cast<float*>(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item_id = blockIdx.x / p.num_kv_heads;
+    const int hkv = blockIdx.x - item_id * p.num_kv_heads;
+    const int4 item = p.items[item_id];
+    const int b = item.w, n_pages = item.y, valid = item.z;
+    const int ps = p.page_size;
+    const int rmask = ps - 1;
+    const int half_bytes = ps * 128;
+    const int pages_per_stage = C::kStageTokens / ps;
+    const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kConsumerWarps);
+            issued[s] = 0;
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::kConsumerWarps && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    __syncthreads();
+
+    using Consumer = typename std::conditional<C::kMma, MmaConsumer<C>, FmaConsumer<C>>::type;
+    Consumer cs;  // used by the consumer warps only
+    if (warp == C::kConsumerWarps) {
+        // ------------------------------------------------ producer warp
+        int4 rq = make_int4(0, 0, 0, 0);
+        int ip0 = 0, ip1 = 0, lst = 0;
+        if (lane == 0) {
+            rq = p.req[b];
+            ip0 = p.indptr[b];
+            ip1 = p.indptr[b + 1];
+            lst = p.last_page_len[b];
+        }
+        const int32_t* idx = p.indices + item.x;
+        // A page index outside [0, num_pages) is recorded in the status word
+        // and replaced by page 0, so every copy stays inside the pool.
+        int win = lane < n_pages ? __ldg(idx + lane) : 0;
+        int nxt = 32 + lane < n_pages ? __ldg(idx + 32 + lane) : 0;
+        int win_base = 0;
+        bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(p.status, kDeviceBadPage);
+        win = bad ? 0 : win;
+        const uint32_t tiles = smem_addr(smem);
+        for (int s = 0; s < n_stages; ++s) {
+            const int stage = s % C::kStages;
+            const int pg0 = s * pages_per_stage;
+            const int npg = min(pages_per_stage, n_pages - pg0);
+            if (pg0 >= win_base + 32) {
+                win = nxt;
+                win_base += 32;
+                nxt = win_base + 32 + lane < n_pages ? __ldg(idx + win_base + 32 + lane) : 0;
+                bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+                if (__any_sync(0xffffffffu, bad) && lane == 0)
+                    record_status(p.status, kDeviceBadPage);
+                win = bad ? 0 : win;
+            }
+            int ok = 1;
+            if (lane == 0) {
+                if (s >= C::kStages)
+                    ok = mbar_wait(&empty[stage], ((s / C::kStages) + 1) & 1, flags) ? 1 : 0;
+                if (ok) mbar_arrive_expect_tx(&full[stage], npg * ps * kHeadDim * 2 * 2);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    flags[0] = 1;
+                    record_status(p.status, kDeviceWaitTimeout);
+                }
+                break;
+            }
+            const uint32_t tk = tiles + stage * C::kStageBytes;
+            const uint32_t tv = tk + C::kStageBytes / 2;
+            for (int j = 0; j < npg; ++j) {
+                const int page = __shfl_sync(0xffffffffu, win, pg0 - win_base + j);
+                if (lane == 0) {
+                    const uint32_t off = j * ps * 256;
+                    // coordinates (d, A, B, page): NHD (d, head, token, page),
+                    // HND (d, token, head, page); the box covers all ps tokens
+                    const int ca = p.layout == 0 ? hkv : 0;
+                    const int cb = p.layout == 0 ? 0 : hkv;
+                    tma_load_4d(tk + off, &tmap_k, &full[stage], 0, ca, cb, page);
+                    tma_load_4d(tk + off + half_bytes, &tmap_k, &full[stage], 64, ca, cb, page);
+                    tma_load_4d(tv + off, &tmap_v, &full[stage], 0, ca, cb, page);
+                    tma_load_4d(tv + off + half_bytes, &tmap_v, &full[stage], 64, ca, cb, page);
+                }
+            }
+            if (lane == 0) issued[stage] += 1;
+        }
+        if (lane == 0 && (ip0 != rq.x || ip1 != rq.y || lst != rq.z))
+            record_status(p.status, kDevicePlanMismatch);
+    } else {
+        // ------------------------------------------------ consumer warps
+        const int slice = warp % C::kSlices;
+        const int mt = warp / C::kSlices;
+        cs.init(p, b, hkv, mt, lane);
+        const uint32_t tiles = smem_addr(smem);
+        for (int s = 0; s < n_stages; ++s) {
+            const int stage = s % C::kStages;
+            const bool ok = mbar_wait(&full[stage], (s / C::kStages) & 1, flags);
+            if (!__all_sync(0xffffffffu, ok)) {  // leave the loop as a whole warp
+                if (lane == 0) {
+                    flags[0] = 1;
+                    record_status(p.status, kDeviceWaitTimeout);
+                }
+                break;
+            }
+            const int t0 = slice * kSliceTokens;
+            const int u0 = s * C::kStageTokens + t0;
+            if (u0 < valid) {
+                const uint32_t tk = tiles + stage * C::kStageBytes;
+                cs.consume(tk, tk + C::kStageBytes / 2, t0, u0, valid, rmask, half_bytes,
+                           p.scale_log2, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+        }
+    }
+    __syncthreads();  // every warp is out of the stage ring
+
+    if (flags[0]) {
+        // Aborted: wait (bounded) for the copies already issued, then leave.
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < C::kStages; ++s)
+                if (issued[s] > 0) mbar_wait(&full[s], (issued[s] - 1) & 1, nullptr);
+        }
+        return;
+    }
+    // All issued copies have landed and been consumed: the tiles become the
+    // scratch for the warps' states.
+    if (warp < C::kConsumerWarps) cs.dump(red_m, red_l, dumpA, warp, lane);
+    __syncthreads();
+
+    // ------------------------------------------------ merge warp states, write
+    const int slot = p.item_slot[item_id];
+    const int G = p.group;
+    for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += C::kThreads) {
+        const int r = i / (kHeadDim / 4);
+        const int d4 = i - r * (kHeadDim / 4);
+        const int mtile = r >> 4, rr = r & 15;
+        const int w0 = mtile * C::kSlices;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::kSlices; ++w) M = fmaxf(M, red_m[(w0 + w) * 16 + rr]);
+        float L = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::kSlices; ++w) {
+                const float sc = fast_exp2(red_m[(w0 + w) * 16 + rr] - M);
+                L += red_l[(w0 + w) * 16 + rr] * sc;
+                const float4 a =
+                    *reinterpret_cast<const float4*>(dumpA + ((w0 + w) * 16 + rr) * kAccStride +
+                                                     d4 * 4);
+                o.x += a.x * sc;
+                o.y += a.y * sc;
+                o.z += a.z * sc;
+                o.w += a.w * sc;
+            }
+        }
+        float lse_nat = -INFINITY;
+        if (L > 0.f) {
+            const float inv = 1.f / L;
+            o.x *= inv;
+            o.y *= inv;
+            o.z *= inv;
+            o.w *= inv;
+            lse_nat = (M + __log2f(L)) * kLn2;
+        }
+        const int hq = hkv * G + r;
+        if (slot < 0) {
+            const size_t row = static_cast<size_t>(b) * p.num_qo_heads + hq;
+            uint2 packed;
+            packed.x = pack_bf16x2(o.x, o.y);
+            packed.y = pack_bf16x2(o.z, o.w);
+            *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
+            if (d4 == 0 && p.lse != nullptr) p.lse[row] = lse_nat;
+        } else {
+            const size_t row = static_cast<size_t>(slot) * p.num_qo_heads + hq;
+            *reinterpret_cast<float4*>(p.part_o + row * kHeadDim + d4 * 4) = o;
+            if (d4 == 0) p.part_lse[row] = lse_nat;
+        }
+    }
+}
+
+// cudaFuncSetAttribute is per device; remember which devices are set up.
+template <class C>
+cudaError_t ensure_smem_attribute() {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(paged_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
+
+template <class C>
+cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                   cudaStream_t stream) {
+    cudaError_t e = ensure_smem_attribute<C>();
+    if (e != cudaSuccess) return e;
+    paged_decode_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <class C>
+VariantShape shape_of() {
+    return {C::kThreads, C::kStageTokens, C::kStages, C::kSmemBytes};
+}
+
+template <class C>
+cudaError_t occupancy_of(int* n) {
+    cudaError_t e = ensure_smem_attribute<C>();
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, paged_decode_kernel<C>, C::kThreads,
+                                                         C::kSmemBytes);
+}
+
+}  // namespace
+
+VariantShape variant_shape(int variant) {
+    switch (variant) {
+        case kVariantFmaG1: return shape_of<CfgFmaG1>();
+        case kVariantFmaG2: return shape_of<CfgFmaG2>();
+        case kVariantMma8: return shape_of<CfgMma8>();
+        case kVariantMma16: return shape_of<CfgMma16>();
+        default: return shape_of<CfgMma32>();
+    }
+}
+
+cudaError_t variant_occupancy(int variant, int* n) {
+    switch (variant) {
+        case kVariantFmaG1: return occupancy_of<CfgFmaG1>(n);
+        case kVariantFmaG2: return occupancy_of<CfgFmaG2>(n);
+        case kVariantMma8: return occupancy_of<CfgMma8>(n);
+        case kVariantMma16: return occupancy_of<CfgMma16>(n);
+        default: return occupancy_of<CfgMma32>(n);
+    }
+}
+
+cudaError_t launch_decode(int variant, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t stream) {
+    switch (variant) {
+        case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, grid, stream);
+        case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, grid, stream);
+        case kVariantMma8: return launch<CfgMma8>(tk, tv, p, grid, stream);
+        case kVariantMma16: return launch<CfgMma16>(tk, tv, p, grid, stream);
+        default: return launch<CfgMma32>(tk, tv, p, grid, stream);
+    }
+}
+
+}  // namespace oxd

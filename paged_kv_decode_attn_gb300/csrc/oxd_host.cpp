@@ -1,0 +1,541 @@
+// Host side of the C ABI: planning, operand checks and enqueue.
+//
+// Lifecycle from the "Oxide Infer" README, "One execution model": the plan
+// fixes the kernel variant, the chunking of every request's pages, the launch
+// shape and the workspace contract; a run only checks operands and enqueues
+// (one host-to-device copy of the work list, the decode kernel, and the merge
+// kernel when some request was split). "Providers": checked span, alignment,
+// alias and capacity rules; explicit workspace; caller stream; typed device
+// status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/oxd.h"
+#include "oxd_internal.h"
+
+using namespace oxd;
+
+struct oxd_plan_s {
+    oxd_paged_decode_desc desc;
+    int device;  // -1 for a host-only plan (desc.num_sms given)
+    int group;
+    int variant;
+    int n_items;
+    int n_slots;
+    int n_split;
+    int max_chunks;
+    int chunk_pages;
+    int ctas_per_sm;
+    int num_sms;
+    int64_t nnz;
+    int64_t total_tokens;
+    size_t off_items, off_slot, off_req, off_split, off_part_o, off_part_lse;
+    size_t meta_bytes, ws_bytes;
+    void* meta;
+    bool pinned;
+    cudaEvent_t ev_before;
+    cudaEvent_t ev_after;
+};
+
+namespace {
+
+constexpr int kWaves = 4;  // target grid ~ kWaves x resident CTAs when splitting
+
+std::mutex g_plans_mu;
+std::unordered_set<oxd_plan> g_plans;
+
+bool plan_alive(oxd_plan p) {
+    std::lock_guard<std::mutex> lk(g_plans_mu);
+    return g_plans.count(p) != 0;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Span span(const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+
+bool overlap(const Span& a, const Span& b) {
+    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
+}
+
+int choose_variant(int G) {
+    if (G == 1) return kVariantFmaG1;
+    if (G == 2) return kVariantFmaG2;
+    if (G <= 8) return kVariantMma8;
+    if (G <= 16) return kVariantMma16;
+    return kVariantMma32;
+}
+
+// Resident CTAs per SM without a device: limited by shared memory (228 KB
+// per SM on sm_100-class parts, 1 KB reserved per CTA) and threads.
+int estimate_ctas_per_sm(const VariantShape& v) {
+    const int by_smem = (228 * 1024) / (v.smem_bytes + 1024);
+    const int by_threads = 2048 / v.threads;
+    return std::max(1, std::min(by_smem, by_threads));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 4-D map over a K or V pool: (d, A, B, page) with (A, B) = (head, token)
+// for NHD and (token, head) for HND; the box is 64 columns x all page_size
+// tokens of one head, stored with the 128-byte swizzle.
+bool encode_pool(CUtensorMap* map, const void* pool, const oxd_paged_decode_desc& d) {
+    EncodeTiledFn enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t D = static_cast<cuuint64_t>(d.head_dim);
+    const cuuint64_t ps = static_cast<cuuint64_t>(d.page_size);
+    const cuuint64_t H = static_cast<cuuint64_t>(d.num_kv_heads);
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    dims[0] = D;
+    dims[3] = static_cast<cuuint64_t>(d.num_pages);
+    if (d.layout == OXD_LAYOUT_NHD) {
+        dims[1] = H;
+        dims[2] = ps;
+        strides[0] = D * 2;
+        strides[1] = H * D * 2;
+        box[1] = 1;
+        box[2] = static_cast<cuuint32_t>(ps);
+    } else {
+        dims[1] = ps;
+        dims[2] = H;
+        strides[0] = D * 2;
+        strides[1] = ps * D * 2;
+        box[1] = static_cast<cuuint32_t>(ps);
+        box[2] = 1;
+    }
+    strides[2] = ps * H * D * 2;
+    box[0] = 64;
+    box[3] = 1;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
+                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+oxd_status check_desc(const oxd_paged_decode_desc* d) {
+    if (d->batch < 1 || d->num_qo_heads < 1 || d->num_kv_heads < 1 || d->head_dim < 1 ||
+        d->page_size < 1 || d->num_pages < 1)
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (d->num_qo_heads % d->num_kv_heads != 0) return OXD_ERR_INVALID_ARGUMENT;
+    if (d->layout != OXD_LAYOUT_NHD && d->layout != OXD_LAYOUT_HND)
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (d->max_splits < 0 || d->force_splits < 0 || d->num_sms < 0)
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (d->reserved[0] != 0 || d->reserved[1] != 0 || d->reserved[2] != 0)
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (d->head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
+    if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
+        return OXD_ERR_UNSUPPORTED;
+    if (d->num_qo_heads / d->num_kv_heads > kMaxGroup) return OXD_ERR_UNSUPPORTED;
+    if (d->num_pages >= (int64_t{1} << 31)) return OXD_ERR_UNSUPPORTED;
+    return OXD_OK;
+}
+
+struct Item {
+    int idx_begin, n_pages, valid, b, slot;
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* oxd_version(void) { return "oxd 0.1.0 sm_103a"; }
+
+const char* oxd_status_string(oxd_status s) {
+    switch (s) {
+        case OXD_OK: return "ok";
+        case OXD_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case OXD_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case OXD_ERR_ALIGNMENT: return "pointer misaligned";
+        case OXD_ERR_ALIAS: return "output overlaps an input or another output";
+        case OXD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case OXD_ERR_PLAN_MISMATCH: return "plan does not match this call";
+        case OXD_ERR_CUDA: return "CUDA runtime call failed";
+        case OXD_ERR_DEVICE_STATUS: return "kernel reported an error";
+        case OXD_ERR_NO_MEMORY: return "host allocation failed";
+    }
+    return "unknown status";
+}
+
+const char* oxd_device_status_string(int32_t code) {
+    switch (code) {
+        case OXD_DEVICE_OK: return "ok";
+        case OXD_DEVICE_BAD_PAGE: return "page index outside the pool";
+        case OXD_DEVICE_PLAN_MISMATCH: return "device block tables differ from the plan";
+        case OXD_DEVICE_WAIT_TIMEOUT: return "pipeline wait timed out";
+    }
+    return "unknown device status";
+}
+
+oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_t* indptr,
+                                 const int32_t* last, int device, oxd_plan* plan_out,
+                                 size_t* ws_out) {
+    if (desc == nullptr || indptr == nullptr || last == nullptr || plan_out == nullptr ||
+        ws_out == nullptr)
+        return OXD_ERR_INVALID_ARGUMENT;
+    oxd_status st = check_desc(desc);
+    if (st != OXD_OK) return st;
+    const oxd_paged_decode_desc& d = *desc;
+    const int B = d.batch, ps = d.page_size;
+    if (indptr[0] < 0) return OXD_ERR_INVALID_ARGUMENT;
+    int64_t total_pages = 0, total_tokens = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t P = static_cast<int64_t>(indptr[b + 1]) - indptr[b];
+        if (P < 1) return OXD_ERR_INVALID_ARGUMENT;
+        if (last[b] < 1 || last[b] > ps) return OXD_ERR_INVALID_ARGUMENT;
+        total_pages += P;
+        total_tokens += (P - 1) * ps + last[b];
+    }
+
+    const int G = d.num_qo_heads / d.num_kv_heads;
+    const int variant = choose_variant(G);
+    const VariantShape vs = variant_shape(variant);
+    int num_sms = d.num_sms, ctas_per_sm = 0, plan_device = -1;
+    if (num_sms == 0) {
+        int prev = 0;
+        if (cudaGetDevice(&prev) != cudaSuccess) return OXD_ERR_CUDA;
+        if (cudaSetDevice(device) != cudaSuccess) return OXD_ERR_CUDA;
+        cudaError_t e1 = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+        cudaError_t e2 = variant_occupancy(variant, &ctas_per_sm);
+        cudaSetDevice(prev);
+        if (e1 != cudaSuccess || e2 != cudaSuccess || num_sms < 1) return OXD_ERR_CUDA;
+        plan_device = device;
+    }
+    if (ctas_per_sm < 1) ctas_per_sm = estimate_ctas_per_sm(vs);
+
+    // ---- chunking
+    const int pps = std::max(1, vs.stage_tokens / ps);  // pages per pipeline stage
+    std::vector<Item> items;
+    items.reserve(static_cast<size_t>(B) * 2);
+    int n_slots = 0, n_split = 0, max_chunks = 1;
+    int chunk_pages = 0;
+    if (d.force_splits == 0 && d.max_splits != 1) {
+        const int64_t conc = static_cast<int64_t>(num_sms) * ctas_per_sm * kWaves;
+        const int64_t head_pages = total_pages * d.num_kv_heads;
+        int64_t c = (head_pages + conc - 1) / conc;
+        c = std::max<int64_t>(c, pps);
+        c = (c + pps - 1) / pps * pps;
+        chunk_pages = static_cast<int>(std::min<int64_t>(c, 1 << 30));
+    }
+    std::vector<int4> split_tab;
+    for (int b = 0; b < B; ++b) {
+        const int P = indptr[b + 1] - indptr[b];
+        const int L = (P - 1) * ps + last[b];
+        std::vector<std::pair<int, int>> ranges;  // [p0, p1)
+        if (d.force_splits > 0) {
+            const int n = std::min(d.force_splits, P);
+            for (int c = 0; c < n; ++c)
+                ranges.push_back({static_cast<int>(static_cast<int64_t>(P) * c / n),
+                                  static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
+        } else if (chunk_pages == 0) {
+            ranges.push_back({0, P});
+        } else {
+            int n = (P + chunk_pages - 1) / chunk_pages;
+            if (d.max_splits > 0) n = std::min(n, d.max_splits);
+            int cb = (P + n - 1) / n;
+            cb = (cb + pps - 1) / pps * pps;
+            for (int p0 = 0; p0 < P; p0 += cb) ranges.push_back({p0, std::min(P, p0 + cb)});
+        }
+        const int n = static_cast<int>(ranges.size());
+        max_chunks = std::max(max_chunks, n);
+        const int slot_base = n > 1 ? n_slots : -1;
+        if (n > 1) {
+            split_tab.push_back(make_int4(b, n_slots, n, 0));
+            n_slots += n;
+            ++n_split;
+        }
+        for (int c = 0; c < n; ++c) {
+            const int p0 = ranges[c].first, p1 = ranges[c].second;
+            Item it;
+            it.idx_begin = indptr[b] + p0;
+            it.n_pages = p1 - p0;
+            it.valid = std::min((p1 - p0) * ps, L - p0 * ps);
+            it.b = b;
+            it.slot = n > 1 ? slot_base + c : -1;
+            items.push_back(it);
+        }
+    }
+    // Longest items first, so the short tails fill in behind them.
+    std::stable_sort(items.begin(), items.end(),
+                     [](const Item& a, const Item& b) { return a.n_pages > b.n_pages; });
+    const int64_t grid = static_cast<int64_t>(items.size()) * d.num_kv_heads;
+    if (grid > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
+
+    // ---- workspace layout
+    oxd_plan P = new (std::nothrow) oxd_plan_s();
+    if (P == nullptr) return OXD_ERR_NO_MEMORY;
+    P->desc = d;
+    P->device = plan_device;
+    P->group = G;
+    P->variant = variant;
+    P->n_items = static_cast<int>(items.size());
+    P->n_slots = n_slots;
+    P->n_split = n_split;
+    P->max_chunks = max_chunks;
+    P->chunk_pages = chunk_pages;
+    P->ctas_per_sm = ctas_per_sm;
+    P->num_sms = num_sms;
+    P->nnz = indptr[B];
+    P->total_tokens = total_tokens;
+    P->off_items = sizeof(WsHeader);
+    P->off_slot = align_up(P->off_items + 16 * items.size(), 256);
+    P->off_req = align_up(P->off_slot + 4 * items.size(), 256);
+    P->off_split = align_up(P->off_req + 16 * static_cast<size_t>(B), 256);
+    P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
+    P->off_part_o = P->meta_bytes;
+    P->off_part_lse = align_up(
+        P->off_part_o + static_cast<size_t>(n_slots) * d.num_qo_heads * kHeadDim * 4, 256);
+    P->ws_bytes =
+        align_up(P->off_part_lse + static_cast<size_t>(n_slots) * d.num_qo_heads * 4, 256);
+
+    P->pinned = cudaHostAlloc(&P->meta, P->meta_bytes, cudaHostAllocDefault) == cudaSuccess;
+    if (!P->pinned) {
+        cudaGetLastError();  // a host-only plan on a machine without a GPU lands here
+        P->meta = std::malloc(P->meta_bytes);
+        if (P->meta == nullptr) {
+            delete P;
+            return OXD_ERR_NO_MEMORY;
+        }
+    }
+    uint8_t* m = static_cast<uint8_t*>(P->meta);
+    std::memset(m, 0, P->meta_bytes);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(m);
+    hdr->status = 0;
+    hdr->n_items = P->n_items;
+    hdr->batch = B;
+    hdr->num_kv_heads = d.num_kv_heads;
+    int4* it4 = reinterpret_cast<int4*>(m + P->off_items);
+    int32_t* slot = reinterpret_cast<int32_t*>(m + P->off_slot);
+    for (size_t i = 0; i < items.size(); ++i) {
+        it4[i] = make_int4(items[i].idx_begin, items[i].n_pages, items[i].valid, items[i].b);
+        slot[i] = items[i].slot;
+    }
+    int4* rq = reinterpret_cast<int4*>(m + P->off_req);
+    for (int b = 0; b < B; ++b) rq[b] = make_int4(indptr[b], indptr[b + 1], last[b], 0);
+    int4* sp = reinterpret_cast<int4*>(m + P->off_split);
+    for (size_t i = 0; i < split_tab.size(); ++i) sp[i] = split_tab[i];
+    P->ev_before = nullptr;
+    P->ev_after = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_plans_mu);
+        g_plans.insert(P);
+    }
+    *plan_out = P;
+    *ws_out = P->ws_bytes;
+    return OXD_OK;
+}
+
+oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
+    if (info == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    if (plan == nullptr || !plan_alive(plan)) return OXD_ERR_PLAN_MISMATCH;
+    oxd_plan_info r{};
+    r.num_work_items = plan->n_items;
+    r.num_split_requests = plan->n_split;
+    r.max_chunks = plan->max_chunks;
+    r.chunk_pages = plan->chunk_pages;
+    r.num_slots = plan->n_slots;
+    r.kernel_variant = plan->variant;
+    r.grid_ctas = plan->n_items * plan->desc.num_kv_heads;
+    r.ctas_per_sm = plan->ctas_per_sm;
+    r.num_sms = plan->num_sms;
+    r.launches_per_run = plan->n_split > 0 ? 2 : 1;
+    r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
+    r.upload_bytes = static_cast<int64_t>(plan->meta_bytes);
+    r.total_kv_tokens = plan->total_tokens;
+    *info = r;
+    return OXD_OK;
+}
+
+oxd_status oxd_plan_set_timing_events(oxd_plan plan, void* before, void* after) {
+    if (plan == nullptr || !plan_alive(plan)) return OXD_ERR_PLAN_MISMATCH;
+    if ((before == nullptr) != (after == nullptr)) return OXD_ERR_INVALID_ARGUMENT;
+    plan->ev_before = static_cast<cudaEvent_t>(before);
+    plan->ev_after = static_cast<cudaEvent_t>(after);
+    return OXD_OK;
+}
+
+oxd_status oxd_plan_destroy(oxd_plan plan) {
+    if (plan == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    {
+        std::lock_guard<std::mutex> lk(g_plans_mu);
+        if (g_plans.erase(plan) == 0) return OXD_ERR_PLAN_MISMATCH;
+    }
+    if (plan->pinned)
+        cudaFreeHost(plan->meta);
+    else
+        std::free(plan->meta);
+    delete plan;
+    return OXD_OK;
+}
+
+oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_pages,
+                                const void* v_pages, const int32_t* indptr,
+                                const int32_t* indices, const int32_t* last_page_len,
+                                float sm_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (plan == nullptr || !plan_alive(plan)) return OXD_ERR_PLAN_MISMATCH;
+    if (q == nullptr || k_pages == nullptr || v_pages == nullptr || indptr == nullptr ||
+        indices == nullptr || last_page_len == nullptr || out == nullptr || workspace == nullptr)
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(sm_scale)) return OXD_ERR_INVALID_ARGUMENT;
+    const oxd_paged_decode_desc& d = plan->desc;
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
+        !aligned(indptr, 4) || !aligned(indices, 4) || !aligned(last_page_len, 4) ||
+        !aligned(lse, 4) || !aligned(workspace, 256))
+        return OXD_ERR_ALIGNMENT;
+    if (workspace_bytes < plan->ws_bytes) return OXD_ERR_WORKSPACE_TOO_SMALL;
+
+    const size_t rows = static_cast<size_t>(d.batch) * d.num_qo_heads;
+    const size_t pool = static_cast<size_t>(d.num_pages) * d.page_size * d.num_kv_heads *
+                        d.head_dim * 2;
+    const Span in[] = {span(q, rows * kHeadDim * 2),
+                       span(k_pages, pool),
+                       span(v_pages, pool),
+                       span(indptr, (static_cast<size_t>(d.batch) + 1) * 4),
+                       span(indices, static_cast<size_t>(plan->nnz) * 4),
+                       span(last_page_len, static_cast<size_t>(d.batch) * 4)};
+    const Span outs[] = {span(out, rows * kHeadDim * 2),
+                         lse ? span(lse, rows * 4) : Span{0, 0},
+                         span(workspace, plan->ws_bytes)};
+    for (const Span& o : outs) {
+        for (const Span& i : in)
+            if (overlap(o, i)) return OXD_ERR_ALIAS;
+    }
+    if (overlap(outs[0], outs[1]) || overlap(outs[0], outs[2]) || overlap(outs[1], outs[2]))
+        return OXD_ERR_ALIAS;
+
+    if (plan->device >= 0) {
+        int cur = -1;
+        if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
+        if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
+    }
+    CUtensorMap tk, tv;
+    if (!encode_pool(&tk, k_pages, d) || !encode_pool(&tv, v_pages, d)) return OXD_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (cudaMemcpyAsync(ws, plan->meta, plan->meta_bytes, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return OXD_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.indptr = indptr;
+    p.indices = indices;
+    p.last_page_len = last_page_len;
+    p.items = reinterpret_cast<const int4*>(ws + plan->off_items);
+    p.item_slot = reinterpret_cast<const int32_t*>(ws + plan->off_slot);
+    p.req = reinterpret_cast<const int4*>(ws + plan->off_req);
+    p.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
+    p.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
+    p.status = reinterpret_cast<int32_t*>(ws);
+    p.num_qo_heads = d.num_qo_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.group = plan->group;
+    p.page_size = d.page_size;
+    p.layout = d.layout;
+    p.n_items = plan->n_items;
+    p.num_pages = d.num_pages;
+    p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
+
+    if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
+        return OXD_ERR_CUDA;
+    if (launch_decode(plan->variant, tk, tv, p, plan->n_items * d.num_kv_heads, s) !=
+        cudaSuccess)
+        return OXD_ERR_CUDA;
+    if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
+        return OXD_ERR_CUDA;
+    if (plan->n_split > 0) {
+        MergeParams mp{};
+        mp.v = p.part_o;
+        mp.s = p.part_lse;
+        mp.out = p.out;
+        mp.lse = lse;
+        mp.split = reinterpret_cast<const int4*>(ws + plan->off_split);
+        mp.n = plan->n_split;
+        mp.S = 0;
+        mp.H = d.num_qo_heads;
+        mp.D = kHeadDim;
+        if (launch_merge(mp, s) != cudaSuccess) return OXD_ERR_CUDA;
+    }
+    return OXD_OK;
+}
+
+oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S, int32_t H,
+                            int32_t D, void* v_out, float* s_out, void* stream) {
+    if (v == nullptr || s == nullptr || v_out == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    if (N < 1 || S < 1 || H < 1 || D < 4 || D % 4 != 0) return OXD_ERR_INVALID_ARGUMENT;
+    if (!aligned(v, 16) || !aligned(s, 4) || !aligned(v_out, 8) || !aligned(s_out, 4))
+        return OXD_ERR_ALIGNMENT;
+    const size_t NH = static_cast<size_t>(N) * H;
+    const Span in[] = {span(v, NH * S * D * 4), span(s, NH * S * 4)};
+    const Span outs[] = {span(v_out, NH * D * 2), s_out ? span(s_out, NH * 4) : Span{0, 0}};
+    for (const Span& o : outs)
+        for (const Span& i : in)
+            if (overlap(o, i)) return OXD_ERR_ALIAS;
+    if (overlap(outs[0], outs[1])) return OXD_ERR_ALIAS;
+    MergeParams mp{};
+    mp.v = v;
+    mp.s = s;
+    mp.out = static_cast<uint16_t*>(v_out);
+    mp.lse = s_out;
+    mp.split = nullptr;
+    mp.n = N;
+    mp.S = S;
+    mp.H = H;
+    mp.D = D;
+    if (launch_merge(mp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return OXD_ERR_CUDA;
+    return OXD_OK;
+}
+
+oxd_status oxd_read_device_status(const void* workspace, void* stream, int32_t* code) {
+    if (workspace == nullptr || code == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    int32_t c = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&c, workspace, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return OXD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return OXD_ERR_CUDA;
+    *code = c;
+    return c == OXD_DEVICE_OK ? OXD_OK : OXD_ERR_DEVICE_STATUS;
+}
+
+}  // extern "C"

@@ -1,0 +1,308 @@
+"""C-ABI checks that need no GPU: exported symbols, planning, operand rejection.
+
+Planning with ``num_sms > 0`` makes no CUDA call, and ``oxd_paged_decode_run``
+/ ``oxd_merge_states`` check every operand before touching the device, so the
+negative cases run here with fake (never dereferenced) addresses. These are
+the pages' "lifetime and negative gates" ("Oxide Infer" README, "Evidence
+before claims") and the "checked span, alignment, alias, and capacity rules"
+of "Providers".
+"""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_decode_attn_gb300 as oxd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE = 1 << 40  # fake device addresses, far apart and 256-byte aligned
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    oxd.build()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "oxd.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(oxd_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert set(names) == set(oxd.EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(oxd.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert oxd.oxd_version().startswith("oxd ")
+
+
+def test_status_strings_cover_every_code():
+    seen = {oxd.oxd_status_string(s) for s in range(10)}
+    assert len(seen) == 10 and "unknown status" not in seen
+    assert oxd.oxd_status_string(99) == "unknown status"
+    assert {oxd.oxd_device_status_string(c) for c in range(4)} >= {"ok"}
+
+
+def host_plan(lengths, Hq=32, Hkv=8, ps=16, layout="NHD", num_pages=None, **kw):
+    lengths = np.asarray(lengths, np.int64)
+    pages = (lengths + ps - 1) // ps
+    indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    last = (lengths - (pages - 1) * ps).astype(np.int32)
+    desc = oxd.make_desc(len(lengths), Hq, Hkv, ps, layout,
+                         int(pages.sum()) if num_pages is None else num_pages,
+                         num_sms=kw.pop("num_sms", 152), **kw)
+    return oxd.oxd_paged_decode_plan(desc, indptr, last), indptr, last
+
+
+# ------------------------------------------------------------------ planning
+
+def test_planner_chunks_long_requests_and_sizes_workspace():
+    plan, indptr, _ = host_plan([4096] * 32)
+    info = plan.info
+    assert info.kernel_variant == 2                       # G = 4: tensor-core variant
+    assert info.num_split_requests == 32 and info.max_chunks > 1
+    assert info.chunk_pages % 4 == 0                      # whole 64-token stages at ps 16
+    assert info.num_work_items == 32 * info.max_chunks
+    assert info.grid_ctas == info.num_work_items * 8
+    assert info.num_slots == info.num_work_items
+    part = info.num_slots * 32 * 128 * 4 + info.num_slots * 32 * 4
+    assert info.workspace_bytes >= part + info.upload_bytes
+    assert info.workspace_bytes == plan.workspace_bytes
+    assert info.launches_per_run == 2
+    assert info.total_kv_tokens == 32 * 4096
+
+
+def test_short_batch_is_not_split_when_splitting_is_off():
+    plan, _, _ = host_plan([100, 5000, 17], max_splits=1)
+    info = plan.info
+    assert info.num_split_requests == 0 and info.num_work_items == 3
+    assert info.launches_per_run == 1 and info.num_slots == 0
+
+
+@pytest.mark.parametrize("force", [1, 2, 3, 7])
+def test_forced_splits(force):
+    lengths = [1, 16, 17, 100, 1000]
+    plan, indptr, _ = host_plan(lengths, force_splits=force)
+    pages = np.diff(indptr)
+    chunks = np.minimum(force, pages)
+    info = plan.info
+    assert info.num_work_items == chunks.sum()
+    assert info.num_split_requests == int((chunks > 1).sum())
+    assert info.num_slots == int(chunks[chunks > 1].sum())
+
+
+def test_max_splits_caps_chunks():
+    plan, _, _ = host_plan([32768] * 4, Hq=32, Hkv=1, ps=64, max_splits=3)
+    assert plan.info.max_chunks <= 3
+
+
+@pytest.mark.parametrize("G,variant", [(1, 0), (2, 1), (3, 2), (8, 2), (9, 3), (16, 3),
+                                       (17, 4), (32, 4)])
+def test_variant_follows_group_size(G, variant):
+    plan, _, _ = host_plan([64], Hq=G * 2, Hkv=2)
+    assert plan.info.kernel_variant == variant
+
+
+BAD_DESC = {
+    "batch0": dict(batch=0),
+    "hq_not_multiple": dict(num_qo_heads=30),
+    "head_dim": dict(head_dim=64),
+    "page_size": dict(page_size=12),
+    "group_64": dict(num_qo_heads=64, num_kv_heads=1),
+    "layout": dict(layout=2),
+    "num_pages0": dict(num_pages=0),
+    "reserved": "reserved",
+    "negative_splits": dict(max_splits=-1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BAD_DESC))
+def test_bad_descriptors_are_rejected(name):
+    desc = oxd.make_desc(2, 32, 8, 16, "NHD", 10, num_sms=152)
+    mod = BAD_DESC[name]
+    if mod == "reserved":
+        desc.reserved[1] = 1
+    else:
+        for k, v in mod.items():
+            setattr(desc, k, v)
+    expect = oxd.OXD_ERR_UNSUPPORTED if name in ("head_dim", "page_size", "group_64") \
+        else oxd.OXD_ERR_INVALID_ARGUMENT
+    indptr = np.array([0, 5, 10], np.int32)
+    last = np.array([16, 3], np.int32)
+    if name == "batch0":
+        indptr, last = np.array([0], np.int32), np.zeros(0, np.int32)
+    with pytest.raises(oxd.OxdError) as e:
+        oxd.oxd_paged_decode_plan(desc, indptr, last)
+    assert e.value.status == expect
+
+
+@pytest.mark.parametrize("indptr,last", [
+    ([0, 0, 5], [3, 3]),        # empty request
+    ([0, 5, 4], [3, 3]),        # decreasing indptr
+    ([0, 2, 5], [0, 3]),        # last_page_len 0
+    ([0, 2, 5], [3, 17]),       # last_page_len > page_size
+    ([-1, 2, 5], [3, 3]),       # negative start
+])
+def test_bad_block_tables_are_rejected(indptr, last):
+    desc = oxd.make_desc(2, 32, 8, 16, "NHD", 10, num_sms=152)
+    with pytest.raises(oxd.OxdError) as e:
+        oxd.oxd_paged_decode_plan(desc, np.array(indptr, np.int32), np.array(last, np.int32))
+    assert e.value.status == oxd.OXD_ERR_INVALID_ARGUMENT
+
+
+def test_null_arguments_to_plan():
+    L = oxd.lib()
+    desc = oxd.make_desc(1, 8, 8, 16, "NHD", 4, num_sms=152)
+    h, ws = ctypes.c_void_p(), ctypes.c_size_t()
+    ind = np.array([0, 4], np.int32)
+    last = np.array([16], np.int32)
+    assert L.oxd_paged_decode_plan(None, ind.ctypes.data, last.ctypes.data, 0,
+                                   ctypes.byref(h), ctypes.byref(ws)) == 1
+    assert L.oxd_paged_decode_plan(ctypes.byref(desc), None, last.ctypes.data, 0,
+                                   ctypes.byref(h), ctypes.byref(ws)) == 1
+    assert h.value is None  # nothing written on error
+
+
+# ------------------------------------------------------------------ run operand checks
+
+def fake_operands(plan, B, Hq, num_pages, ps=16, Hkv=8):
+    rows = B * Hq
+    pool = num_pages * ps * Hkv * 128 * 2
+    step = 1 << 36
+    return dict(q=BASE, k_pages=BASE + step, v_pages=BASE + 2 * step, indptr=BASE + 3 * step,
+                indices=BASE + 4 * step, last_page_len=BASE + 5 * step, sm_scale=0.088,
+                out=BASE + 6 * step, lse=BASE + 7 * step, workspace=BASE + 8 * step,
+                workspace_bytes=plan.workspace_bytes, stream=0), rows, pool
+
+
+def run_status(plan, **ops):
+    L = oxd.lib()
+    return L.oxd_paged_decode_run(
+        oxd._handle(plan), ops["q"], ops["k_pages"], ops["v_pages"], ops["indptr"],
+        ops["indices"], ops["last_page_len"], ctypes.c_float(ops["sm_scale"]), ops["out"],
+        ops["lse"], ops["workspace"], ops["workspace_bytes"], ops["stream"])
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("q_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("k_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("out_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("lse_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("ws_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("indices_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("ws_small", oxd.OXD_ERR_WORKSPACE_TOO_SMALL),
+    ("out_is_q", oxd.OXD_ERR_ALIAS),
+    ("out_in_kpool", oxd.OXD_ERR_ALIAS),
+    ("lse_in_out", oxd.OXD_ERR_ALIAS),
+    ("ws_over_indices", oxd.OXD_ERR_ALIAS),
+    ("ws_over_out", oxd.OXD_ERR_ALIAS),
+    ("null_q", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("null_ws", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("nan_scale", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("inf_scale", oxd.OXD_ERR_INVALID_ARGUMENT),
+])
+def test_run_rejects_bad_operands_before_enqueue(case, expect):
+    plan, indptr, _ = host_plan([300, 50], Hq=32, Hkv=8)
+    ops, rows, pool = fake_operands(plan, 2, 32, int(indptr[-1]))
+    if case == "q_misaligned":
+        ops["q"] += 8
+    elif case == "k_misaligned":
+        ops["k_pages"] += 2
+    elif case == "out_misaligned":
+        ops["out"] += 4
+    elif case == "lse_misaligned":
+        ops["lse"] += 2
+    elif case == "ws_misaligned":
+        ops["workspace"] += 128
+    elif case == "indices_misaligned":
+        ops["indices"] += 1
+    elif case == "ws_small":
+        ops["workspace_bytes"] -= 256
+    elif case == "out_is_q":
+        ops["out"] = ops["q"]
+    elif case == "out_in_kpool":
+        ops["out"] = ops["k_pages"] + pool - 256
+    elif case == "lse_in_out":
+        ops["lse"] = ops["out"] + rows * 256 - 64
+    elif case == "ws_over_indices":
+        ops["workspace"] = ops["indices"] - 256
+    elif case == "ws_over_out":
+        ops["workspace"] = ops["out"]
+    elif case == "null_q":
+        ops["q"] = None
+    elif case == "null_ws":
+        ops["workspace"] = None
+    elif case == "nan_scale":
+        ops["sm_scale"] = math.nan
+    elif case == "inf_scale":
+        ops["sm_scale"] = math.inf
+    assert run_status(plan, **ops) == expect
+
+
+def test_adjacent_buffers_are_not_aliases():
+    # out ends exactly where lse starts: touching is not overlapping. The
+    # call then passes every host check and only fails at the device step.
+    plan, indptr, _ = host_plan([40], Hq=8, Hkv=8)
+    ops, rows, pool = fake_operands(plan, 1, 8, int(indptr[-1]))
+    ops["lse"] = ops["out"] + rows * 256
+    assert run_status(plan, **ops) not in (oxd.OXD_ERR_ALIAS, oxd.OXD_ERR_ALIGNMENT,
+                                           oxd.OXD_ERR_INVALID_ARGUMENT)
+
+
+def test_destroyed_plan_is_refused():
+    plan, indptr, _ = host_plan([40], Hq=8, Hkv=8)
+    ops, _, _ = fake_operands(plan, 1, 8, int(indptr[-1]))
+    h = plan.handle
+    plan.destroy()
+    assert oxd.lib().oxd_plan_destroy(h) == oxd.OXD_ERR_PLAN_MISMATCH
+    ops["workspace_bytes"] = 1 << 20
+    L = oxd.lib()
+    st = L.oxd_paged_decode_run(h, ops["q"], ops["k_pages"], ops["v_pages"], ops["indptr"],
+                                ops["indices"], ops["last_page_len"], ctypes.c_float(1.0),
+                                ops["out"], ops["lse"], ops["workspace"], 1 << 20, 0)
+    assert st == oxd.OXD_ERR_PLAN_MISMATCH
+    info = oxd.PlanInfo()
+    assert L.oxd_plan_get_info(h, ctypes.byref(info)) == oxd.OXD_ERR_PLAN_MISMATCH
+
+
+def test_timing_events_must_come_in_pairs():
+    plan, _, _ = host_plan([40], Hq=8, Hkv=8)
+    L = oxd.lib()
+    assert L.oxd_plan_set_timing_events(plan.handle, 0x1000, None) == 1
+    assert L.oxd_plan_set_timing_events(plan.handle, None, None) == 0
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("ok_shape_bad_D", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("zero_N", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("v_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("out_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("out_over_v", oxd.OXD_ERR_ALIAS),
+    ("s_out_over_s", oxd.OXD_ERR_ALIAS),
+    ("s_out_over_out", oxd.OXD_ERR_ALIAS),
+])
+def test_merge_rejects_bad_operands(case, expect):
+    N, S, H, D = 3, 4, 8, 128
+    v, s, o, so = BASE, BASE + (1 << 36), BASE + (2 << 36), BASE + (3 << 36)
+    if case == "ok_shape_bad_D":
+        D = 126
+    elif case == "zero_N":
+        N = 0
+    elif case == "v_misaligned":
+        v += 4
+    elif case == "out_misaligned":
+        o += 2
+    elif case == "out_over_v":
+        o = v + 64
+    elif case == "s_out_over_s":
+        so = s
+    elif case == "s_out_over_out":
+        so = o + 16
+    st = oxd.lib().oxd_merge_states(v, s, N, S, H, D, o, so, None)
+    assert st == expect
