@@ -1,0 +1,479 @@
+"""Benchmark of batched paged-KV decode attention on GB300.
+
+One step = one ``oxd_paged_decode_run`` (work-list upload, decode kernel and,
+when a request is split, the merge kernel) over one batch of the workload,
+with the plan already built. Metric: KV-read GB/s (logical KV bytes
+sum_b L_b * Hkv * D * 2 (K, V) * 2 B per step over the step time) and us per
+step.
+
+Default workload: GQA4, Hq=32, Hkv=8, D=128, B=32, KV lengths uniform in
+[512, 4096], page size 16, NHD, bf16 ~N(0,1), random page order
+(``--config`` picks another of the five workloads in ``workloads``).
+
+Timing: W untimed warm-up steps, then K steps, each between its own pair of
+CUDA events on the launching stream; before every step (outside its events)
+a 512 MiB buffer is written to flush the 129 MB L2. The kernel-only time
+comes from events the library records around the decode launch. ``e2e``
+repeats the step through the public API from pinned host buffers: H2D copies
+of q, the K/V pools and the block tables, the run, and the D2H read of out
+and lse, all inside the events. Clocks are sampled with nvidia-smi during
+the timed loop.
+
+``--impl reference`` times the f64 CPU oracle (the reference arm) on a
+bounded sample of the same workload on the host cores.
+
+Multi-GPU (torchrun, one rank per GPU): requests are independent, so each rank
+decodes its own batch of the workload (weak scaling) with no collective on
+the data path; the only collectives are the timing barrier and the max of
+the ranks' times.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: KV-read HBM GB/s (% of GB300 peak), µs per batch step"
+DEFAULT_CONFIG = "gqa4_b32_u512to4096_ps16_nhd"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["oxd", "reference"], default="oxd")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=W.CONFIG_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target wall time of the oracle baseline sample")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="wall-time budget of a whole --impl reference run")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_seed(cfg, rank):
+    """Each rank decodes its own batch: same workload shape, seed offset by rank."""
+    return cfg.seed + 1000 * rank
+
+
+def shard_config(cfg, rank):
+    import dataclasses
+
+    return dataclasses.replace(cfg, seed=rank_seed(cfg, rank))
+
+
+def max_over_ranks(ms: float, device=None) -> float:
+    """Slowest rank's time (every rank must call this)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
+    """Aggregate throughput: every rank's bytes over the slowest rank's time."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
+# ------------------------------------------------------------------ measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a window."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        used = inside or rows[-3:]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in used for n, v in zip(names, r[3][1:]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": used[0][2],
+                "reasons": reasons, "samples": len(used),
+                "samples_in_window": len(inside)}
+
+
+def gpu_id_for_smi(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_attn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it still applies."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ the oracle baseline
+
+def oracle_time(case, heads=None, reps=1):
+    import oracle
+
+    args = (W.bf16_bits(case.q), W.bf16_bits(case.k), W.bf16_bits(case.v), case.tables.indptr,
+            case.tables.indices, case.tables.last_page_len)
+    kw = dict(num_kv_heads=case.num_kv_heads, page_size=case.page_size,
+              layout=0 if case.layout == "NHD" else 1, sm_scale=case.sm_scale, heads=heads)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.paged_decode(*args, **kw)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case_host, target_s):
+    """Oracle (as it stands) on the whole batch, repeated to about target_s seconds."""
+    cores = os.cpu_count() or 1
+    t1 = oracle_time(case_host)
+    reps = max(1, min(1000, int(math.ceil(target_s / max(t1, 1e-6)))) - 1)
+    t = oracle_time(case_host, reps=reps) if reps > 0 else t1
+    reps = max(reps, 1)
+    per = t / reps
+    gbs = case_host.kv_bytes() / per / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"whole workload batch ({case_host.batch} requests, "
+                      f"{case_host.batch * case_host.num_qo_heads} heads), f64 oracle over "
+                      f"{cores} threads, {reps} repetition(s), {per * 1e3:.1f} ms each",
+            "seconds": t}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = W.CONFIGS[args.config]
+    case = W.make_case(cfg, device="cpu")
+    import oracle
+
+    oracle.build()
+    L = case.tables.lengths
+    # One step = the oracle over a bounded subset of heads, sized so that the
+    # whole run (K + W steps) takes about two minutes.
+    t_one = oracle_time(case, heads=[(0, 0)])
+    per_head = max(t_one, 1e-5)
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
+    n_heads_total = case.batch * case.num_qo_heads
+    n = int(max(1, min(n_heads_total, budget / per_head)))
+    rng = np.random.default_rng(cfg.seed)
+    flat = rng.permutation(n_heads_total)[:n]
+    heads = [(int(i // case.num_qo_heads), int(i % case.num_qo_heads)) for i in flat]
+    sample_bytes = sum(int(L[b]) for b, _ in heads) * case.head_dim * 4
+    for _ in range(args.warmup):
+        oracle_time(case, heads=heads)
+    times = [oracle_time(case, heads=heads) for _ in range(args.steps)]
+    per = statistics.mean(times)
+    gbs = sample_bytes / per / 1e9
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(cfg, case),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {n_heads_total} query heads per step (each head's "
+                                   "whole KV sequence), f64 oracle"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(cfg, case):
+    return {"workload": cfg.name, "batch": case.batch, "num_qo_heads": case.num_qo_heads,
+            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+            "page_size": case.page_size, "layout": case.layout,
+            "kv_lengths": list(cfg.lengths), "value_sigma": cfg.sigma,
+            "kv_tokens": int(case.tables.lengths.sum()), "kv_bytes_per_step": case.kv_bytes(),
+            "unique_kv_bytes_per_step": case.unique_kv_bytes(),
+            "shared_prefix_tokens": cfg.shared_prefix_tokens,
+            "l2": "flushed (512 MiB write) before every timed step, outside its events"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_oxd(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import paged_kv_decode_attn_gb300 as oxd
+
+    oxd.build()
+    cfg = shard_config(W.CONFIGS[args.config], rank)
+    case = W.make_case(cfg, device=dev)
+    t = case.tables
+    desc = oxd.make_desc(case.batch, case.num_qo_heads, case.num_kv_heads, case.page_size,
+                         case.layout, t.num_pages)
+    tp0 = time.perf_counter()
+    plan = oxd.oxd_paged_decode_plan(desc, t.indptr, t.last_page_len, dev.index)
+    plan_us = (time.perf_counter() - tp0) * 1e6
+    info = plan.info
+    indptr = torch.as_tensor(t.indptr, device=dev)
+    indices = torch.as_tensor(t.indices, device=dev)
+    last = torch.as_tensor(t.last_page_len, device=dev)
+    out = torch.empty_like(case.q)
+    lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        oxd.oxd_paged_decode_run(plan, case.q, case.k, case.v, indptr, indices, last,
+                                 case.sm_scale, out, lse, ws, plan.workspace_bytes, stream)
+
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        flush.zero_()
+        step()
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in kev:  # materialise the events so their handles exist
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_start()
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        oxd.oxd_plan_set_timing_events(plan, kev[k][0], kev[k][1])
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if sampler:
+        sampler.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
+    oxd.oxd_plan_set_timing_events(plan, None, None)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    clocks = sampler.stop() if sampler else None
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error during the timed steps")
+
+    ms = max_over_ranks(statistics.mean(step_ms), dev)
+    kv_bytes = case.kv_bytes()
+    value = whole_job_gbs(kv_bytes, world, ms)
+    kern = statistics.mean(kern_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = kv_bytes / (kern * 1e-3) / 1e9
+
+    # ---- end to end through the public API from pinned host buffers
+    host = {name: x.cpu().pin_memory() for name, x in
+            (("q", case.q), ("k", case.k), ("v", case.v), ("indptr", indptr),
+             ("indices", indices), ("last", last))}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
+    dind, dptr, dlast = torch.empty_like(indices), torch.empty_like(indptr), torch.empty_like(last)
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    def e2e_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dk.copy_(host["k"], non_blocking=True)
+        dv.copy_(host["v"], non_blocking=True)
+        dptr.copy_(host["indptr"], non_blocking=True)
+        dind.copy_(host["indices"], non_blocking=True)
+        dlast.copy_(host["last"], non_blocking=True)
+        oxd.oxd_paged_decode_run(plan, dq, dk, dv, dptr, dind, dlast, case.sm_scale, out, lse,
+                                 ws, plan.workspace_bytes, stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n_e2e = max(3, min(args.e2e_steps, K))
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_e2e)]
+    for a, b in e_ev:
+        flush.zero_()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_ev), dev)
+    if not torch.equal(out_h, out.cpu()):
+        raise RuntimeError("e2e output mismatch")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        host_case = W.Case(case.batch, case.num_qo_heads, case.num_kv_heads, case.head_dim,
+                           case.page_size, case.layout, case.sm_scale, case.tables,
+                           host["q"], host["k"], host["v"])
+        cpu = cpu_baseline(host_case, args.cpu_seconds)
+
+    if rank == 0:
+        srt = sorted(step_ms)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(cfg, case),
+            "us_per_step": ms * 1e3,
+            "us_per_step_p10_p50_p90": [srt[len(srt) // 10] * 1e3, srt[len(srt) // 2] * 1e3,
+                                        srt[(9 * len(srt)) // 10] * 1e3],
+            "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": recorded_traffic(cfg.name),
+                         "kernel": f"paged_decode_kernel variant {info.kernel_variant}",
+                         "kernel_us": kern * 1e3,
+                         "algorithmic_bytes_per_launch": kv_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": whole_job_gbs(kv_bytes, world, e2e_ms), "unit": "GB/s",
+                    "ms_per_step": e2e_ms, "steps": n_e2e,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * info.launches_per_run,
+            "clocks": clocks,
+            "plan": {"host_us": plan_us, **info.as_dict()},
+            "wall_s_timed_loop": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_oxd(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
