@@ -12,8 +12,10 @@ Default workload: GQA4, Hq=32, Hkv=8, D=128, B=32, KV lengths uniform in
 
 Timing: W untimed warm-up steps, then K steps, each between its own pair of
 CUDA events on the launching stream; before every step (outside its events)
-a 512 MiB buffer is written to flush the 129 MB L2. The kernel-only time
-comes from events the library records around the decode launch. ``e2e``
+L2 (129 MB) is flushed by writing a 512 MiB buffer and then reading another
+512 MiB buffer (so no dirty flush lines are written back during the step).
+The kernel-only time comes from events the library records around the
+decode launch. ``e2e``
 repeats the step through the public API from pinned host buffers: H2D copies
 of q, the K/V pools and the block tables, the run, and the D2H read of out
 and lse, all inside the events. Clocks are sampled with nvidia-smi during
@@ -293,7 +295,8 @@ def config_block(cfg, case):
             "kv_tokens": int(case.tables.lengths.sum()), "kv_bytes_per_step": case.kv_bytes(),
             "unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "shared_prefix_tokens": cfg.shared_prefix_tokens,
-            "l2": "flushed (512 MiB write) before every timed step, outside its events"}
+            "l2": "flushed before every timed step, outside its events: 512 MiB write, "
+                  "then a 512 MiB read of another buffer"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -327,8 +330,16 @@ def run_oxd(args):
     out = torch.empty_like(case.q)
     lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush():
+        # Write 512 MiB, then read another 512 MiB: L2 (129 MB) ends up with
+        # clean lines of neither the workload nor the written buffer, so no
+        # write-back of flush data lands inside the next timed step.
+        flush_w.zero_()
+        flush_r.sum()
 
     def step():
         oxd.oxd_paged_decode_run(plan, case.q, case.k, case.v, indptr, indices, last,
@@ -336,7 +347,7 @@ def run_oxd(args):
 
     K, Wm = args.steps, args.warmup
     for _ in range(Wm):
-        flush.zero_()
+        flush()
         step()
     if oxd.oxd_read_device_status(ws, stream) != 0:
         raise RuntimeError("device status error during warm-up")
@@ -360,7 +371,7 @@ def run_oxd(args):
         sampler.mark_start()
     wall0 = time.perf_counter()
     for k in range(K):
-        flush.zero_()
+        flush()
         oxd.oxd_plan_set_timing_events(plan, kev[k][0], kev[k][1])
         ev[k][0].record(stream)
         step()
@@ -415,7 +426,7 @@ def run_oxd(args):
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(n_e2e)]
     for a, b in e_ev:
-        flush.zero_()
+        flush()
         a.record(stream)
         e2e_step()
         b.record(stream)

@@ -96,16 +96,16 @@ typedef struct {
 } oxd_paged_decode_desc;
 
 typedef struct {
-    int32_t num_work_items;     /* (request, page-range) chunks; the grid is this x Hkv */
+    int32_t num_work_items;     /* (request, page-range) chunks; work units = this x Hkv */
     int32_t num_split_requests; /* requests whose chunks need a merge */
     int32_t max_chunks;         /* most chunks any request got */
     int32_t chunk_pages;        /* planner's chunk length in pages */
     int32_t num_slots;          /* partial-state slots in the workspace */
     int32_t kernel_variant;     /* 0/1: CUDA-core G=1/G=2; 2,3,4: tensor-core G<=8, <=16, <=32 */
-    int32_t grid_ctas;          /* decode CTAs launched per run */
+    int32_t grid_ctas;          /* persistent decode CTAs launched per run */
     int32_t ctas_per_sm;        /* resident decode CTAs per SM assumed by the planner */
     int32_t num_sms;
-    int32_t launches_per_run;   /* kernels one run enqueues (1 or 2) */
+    int32_t launches_per_run;   /* kernels one run enqueues (1: split requests merge in place) */
     int64_t workspace_bytes;
     int64_t upload_bytes;       /* host->device bytes one run copies (the work list) */
     int64_t total_kv_tokens;    /* sum_b L_b */

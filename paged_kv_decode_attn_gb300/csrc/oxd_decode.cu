@@ -3,27 +3,33 @@
 // Operation: "FlashInfer parity matrix" page, "Admitted attention matrix",
 // row "Paged batch decode" (direct kernel for MHA, eight-warp token-parallel
 // kernel for MQA/GQA), with the F32 online softmax every attention row there
-// fixes and the split partitions + F32 partial workspace of the
+// fixes, and the split partitions + F32 partial workspace + merge of the
 // "Single decode split-K" row.
 //
-// One CTA handles one work item: a run of consecutive pages of one request
-// for one KV head. Inside the CTA:
-//   * a producer warp reads the item's page indices (32 at a time, coalesced,
-//     one window ahead), checks them against the pool size and issues one TMA
-//     tensor copy per (page, 64-wide half of D) into a ring of shared-memory
-//     stages, each guarded by a "full" and an "empty" mbarrier;
-//   * consumer warps split every stage token-parallel, 16 tokens per warp, and
-//     keep their own running max, denominator and output accumulator (F32);
-//     for grouped heads (G >= 3) the group's query rows form the A operand of
-//     mma.sync m16n8k16 (QK^T) and the softmax weights, rounded to bf16, the A
-//     operand of the PV product, so one K/V read serves all G heads; for
-//     G <= 2 the dot products run on CUDA cores;
-//   * at the end the warps' states are merged in shared memory and the CTA
-//     writes either the final bf16 output and LSE or, for a split request, an
-//     F32 partial state that the merge kernel combines.
-// Every wait on an mbarrier is bounded (about one second); a wait that gives
-// up records OXD_DEVICE_WAIT_TIMEOUT, drains the copies already issued and
-// returns without writing outputs.
+// Persistent, warp-specialised CTAs (a few per SM) pull work units -- one
+// run of consecutive pages of one request for one KV head -- from an atomic
+// queue (units are ordered longest first by the planner):
+//   * the producer warp claims the next unit while the current one is still
+//     streaming, reads its page indices 32 at a time (coalesced), checks them
+//     against the pool, and fills a ring of shared-memory stages: one TMA
+//     tensor copy per (page, 64-column half) for K and for V, plus, on a
+//     unit's first stage, a bulk copy of the group's G query rows; every
+//     stage carries a small record (request, head, stage index, output slot)
+//     and is guarded by a "full" and an "empty" mbarrier;
+//   * consumer warps split each stage token-parallel, 16 tokens per warp, and
+//     keep their own running max, denominator and F32 accumulator; for
+//     grouped heads (G >= 3) the group's query rows are the A operand of
+//     mma.sync m16n8k16 for Q K^T and the bf16-rounded softmax weights the A
+//     operand of P V, so one K/V read serves all G heads; for G <= 2 the dot
+//     products run on CUDA cores;
+//   * after a unit's last stage the consumers merge their states through the
+//     stage's own buffer and write the bf16 output and LSE, or, for a split
+//     request, an F32 partial state; the last unit of a split request to
+//     finish (atomic counter) merges the partials in order and writes the
+//     output, so a run is one kernel launch.
+// Every wait (mbarriers, including the consumer-only barrier) gives up after
+// about one second: it records OXD_DEVICE_WAIT_TIMEOUT, all warps leave, the
+// copies already issued are drained, and the CTA returns.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -38,7 +44,6 @@ constexpr int kDeviceBadPage = 1;
 constexpr int kDevicePlanMismatch = 2;
 constexpr int kDeviceWaitTimeout = 3;
 constexpr float kLn2 = 0.693147180559945309f;
-constexpr int kAccStride = kHeadDim + 8;  // padded row of the epilogue accumulator dump
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -106,6 +111,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -122,6 +136,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
 }
 
 // D = A * B + D, m16n8k16, bf16 inputs, f32 accumulate.
@@ -152,6 +180,7 @@ __device__ __forceinline__ void record_status(int32_t* status, int code) {
     atomicCAS(status, 0, code);
 }
 
+
 // ------------------------------------------------------------------ tile addressing
 //
 // A stage holds K then V for kStageTokens tokens. Each is a sequence of TMA
@@ -179,6 +208,11 @@ __device__ __forceinline__ uint32_t chunk_addr(const RowAddr& ra, int c, int hal
            ((static_cast<uint32_t>(c & 7) ^ ra.xr) << 4);
 }
 
+// Epilogue scratch: per consumer warp slice, a [16][128] f32 block of its
+// accumulator rows, stored in the stage buffer the unit finished with. Column
+// groups of 8 are XOR-swizzled by row % 8 to spread the banks.
+__device__ __forceinline__ int dump_col(int row, int col) { return col ^ ((row & 7) << 3); }
+
 // ------------------------------------------------------------------ configuration
 
 template <int kMtiles_, bool kHiRows_, int kSlices_, int kStages_, bool kMma_, int kFmaGroup_>
@@ -190,15 +224,18 @@ struct Cfg {
     static constexpr bool kMma = kMma_;
     static constexpr int kFmaGroup = kFmaGroup_;   // G of the CUDA-core variant
     static constexpr int kConsumerWarps = kMma ? kSlices * kMtiles : kSlices;
-    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+    static constexpr int kConsumerThreads = kConsumerWarps * 32;
+    static constexpr int kThreads = kConsumerThreads + 32;
     static constexpr int kStageTokens = kSlices * kSliceTokens;
     static constexpr int kStageBytes = kStageTokens * kHeadDim * 2 * 2;  // K and V
-    static constexpr int kDumpBytes = kConsumerWarps * 16 * kAccStride * 4;
-    static constexpr int kTileBytes =
-        kStages * kStageBytes > kDumpBytes ? kStages * kStageBytes : kDumpBytes;
-    // tiles | full[kStages] | empty[kStages] | issued[kStages] | flags[4] | red_m | red_l
-    static constexpr int kBarOffset = kTileBytes;
-    static constexpr int kIssuedOffset = kBarOffset + 2 * kStages * 8;
+    static constexpr int kQRows = kMma ? (kHiRows ? 16 * kMtiles : 8) : kFmaGroup;
+    static constexpr int kQBytes = kQRows * kHeadDim * 2;
+    static_assert(kSlices * 16 * kHeadDim * 4 <= kStageBytes, "epilogue scratch fits a stage");
+    // ring | q[kStages] | rec[kStages] | full, empty, cbar | issued | flags | red_m | red_l
+    static constexpr int kQOffset = kStages * kStageBytes;
+    static constexpr int kRecOffset = kQOffset + kStages * kQBytes;
+    static constexpr int kBarOffset = kRecOffset + kStages * 32;
+    static constexpr int kIssuedOffset = kBarOffset + (2 * kStages + 1) * 8;
     static constexpr int kFlagOffset = kIssuedOffset + kStages * 4;
     static constexpr int kRedOffset = kFlagOffset + 16;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRedOffset +
@@ -209,7 +246,12 @@ using CfgFmaG1 = Cfg<1, false, 4, 3, false, 1>;
 using CfgFmaG2 = Cfg<1, false, 4, 3, false, 2>;
 using CfgMma8 = Cfg<1, false, 4, 3, true, 0>;
 using CfgMma16 = Cfg<1, true, 4, 3, true, 0>;
-using CfgMma32 = Cfg<2, true, 4, 3, true, 0>;
+using CfgMma32 = Cfg<2, true, 4, 4, true, 0>;
+
+// What the producer tells the consumers about each stage it fills.
+struct StageRec {
+    int b, hkv, valid, n_stages, s, slot, slot_base, n_chunks;
+};
 
 // ------------------------------------------------------------------ consumers
 
@@ -222,21 +264,19 @@ struct MmaConsumer {
     float l[2];          // running denominator (this thread's columns)
     float acc[16][4];    // output accumulator, 16 n-tiles of 8 columns
 
-    __device__ __forceinline__ void init(const DecodeParams& p, int b, int hkv, int mt, int lane) {
+    // q rows come from the stage's query buffer (row r at qbuf + 256 r).
+    __device__ __forceinline__ void init(uint32_t qbuf, int G, int mt, int lane) {
         const int g = lane >> 2, tq = lane & 3;
         const int r0 = mt * 16 + g, r1 = r0 + 8;
-        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-            p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * p.group + r0) * kHeadDim);
-        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-            p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * p.group + r1) * kHeadDim);
-        const bool v0 = r0 < p.group, v1 = C::kHiRows && r1 < p.group;
+        const bool v0 = r0 < G, v1 = C::kHiRows && r1 < G;
+        const uint32_t a0 = qbuf + r0 * 256 + tq * 4;
+        const uint32_t a1 = qbuf + r1 * 256 + tq * 4;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const int w = ks * 8 + tq;  // 32-bit word = columns 16ks + 2tq, +1
-            qa[ks][0] = v0 ? __ldg(q0 + w) : 0u;
-            qa[ks][1] = v1 ? __ldg(q1 + w) : 0u;
-            qa[ks][2] = v0 ? __ldg(q0 + w + 4) : 0u;
-            qa[ks][3] = v1 ? __ldg(q1 + w + 4) : 0u;
+            qa[ks][0] = v0 ? lds32(a0 + ks * 32) : 0u;
+            qa[ks][1] = v1 ? lds32(a1 + ks * 32) : 0u;
+            qa[ks][2] = v0 ? lds32(a0 + ks * 32 + 16) : 0u;
+            qa[ks][3] = v1 ? lds32(a1 + ks * 32 + 16) : 0u;
         }
         m[0] = m[1] = -INFINITY;
         l[0] = l[1] = 0.f;
@@ -244,7 +284,7 @@ struct MmaConsumer {
         for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
     }
 
-    // Tokens [u0, u0 + 16) of the work item sit at rows t0.. of the stage tiles.
+    // Tokens [u0, u0 + 16) of the unit sit at rows t0.. of the stage tiles.
     __device__ __forceinline__ void consume(uint32_t tk, uint32_t tv, int t0, int u0, int valid,
                                             int rmask, int half_bytes, float scale_log2,
                                             int lane) {
@@ -333,8 +373,10 @@ struct MmaConsumer {
         }
     }
 
-    // Dump raw state: red_m/red_l [cw][16], A [cw][16][kAccStride].
-    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* A, int cw, int lane) {
+    // Raw state of this warp's 16 rows: red_m/red_l [slice][16] and the
+    // accumulator into dump + slice * 16 * 128 (rows swizzled by dump_col).
+    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* dump, int slice,
+                                         int lane) {
         const int g = lane >> 2, tq = lane & 3;
         float l0 = l[0], l1 = l[1];
         l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -342,18 +384,20 @@ struct MmaConsumer {
         l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
         l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
         if (tq == 0) {
-            red_m[cw * 16 + g] = m[0];
-            red_l[cw * 16 + g] = l0;
-            red_m[cw * 16 + g + 8] = C::kHiRows ? m[1] : -INFINITY;
-            red_l[cw * 16 + g + 8] = C::kHiRows ? l1 : 0.f;
+            red_m[slice * 16 + g] = m[0];
+            red_l[slice * 16 + g] = l0;
+            red_m[slice * 16 + g + 8] = C::kHiRows ? m[1] : -INFINITY;
+            red_l[slice * 16 + g + 8] = C::kHiRows ? l1 : 0.f;
         }
-        float* a0 = A + (cw * 16 + g) * kAccStride + 2 * tq;
-        float* a1 = a0 + 8 * kAccStride;
+        float* base = dump + slice * 16 * kHeadDim;
 #pragma unroll
         for (int n = 0; n < 16; ++n) {
-            *reinterpret_cast<float2*>(a0 + n * 8) = make_float2(acc[n][0], acc[n][1]);
+            const int col = n * 8 + 2 * tq;
+            *reinterpret_cast<float2*>(base + g * kHeadDim + dump_col(g, col)) =
+                make_float2(acc[n][0], acc[n][1]);
             if constexpr (C::kHiRows)
-                *reinterpret_cast<float2*>(a1 + n * 8) = make_float2(acc[n][2], acc[n][3]);
+                *reinterpret_cast<float2*>(base + (g + 8) * kHeadDim + dump_col(g + 8, col)) =
+                    make_float2(acc[n][2], acc[n][3]);
         }
     }
 };
@@ -367,14 +411,11 @@ struct FmaConsumer {
     float l[G];
     float acc[G][8];
 
-    __device__ __forceinline__ void init(const DecodeParams& p, int b, int hkv, int /*mt*/,
-                                         int lane) {
+    __device__ __forceinline__ void init(uint32_t qbuf, int /*G*/, int /*mt*/, int lane) {
         const int c = lane & 15;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * G + g) * kHeadDim +
-                c * 8));
+            const uint4 raw = lds128(qbuf + g * 256 + c * 16);
             const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -397,10 +438,7 @@ struct FmaConsumer {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const RowAddr ra = row_addr(tk, t0 + 2 * i + par, rmask);
-            uint4 kv;
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(kv.x), "=r"(kv.y), "=r"(kv.z), "=r"(kv.w)
-                         : "r"(chunk_addr(ra, c, half_bytes)));
+            const uint4 kv = lds128(chunk_addr(ra, c, half_bytes));
             const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
             float kf[8];
 #pragma unroll
@@ -448,10 +486,7 @@ struct FmaConsumer {
             const int tok = u0 + 2 * i + par;
             if (tok < valid) {
                 const RowAddr ra = row_addr(tv, t0 + 2 * i + par, rmask);
-                uint4 vv;
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(vv.x), "=r"(vv.y), "=r"(vv.z), "=r"(vv.w)
-                             : "r"(chunk_addr(ra, c, half_bytes)));
+                const uint4 vv = lds128(chunk_addr(ra, c, half_bytes));
                 const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -465,8 +500,10 @@ struct FmaConsumer {
         }
     }
 
-    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* A, int cw, int lane) {
+    __device__ __forceinline__ void dump(float* red_m, float* red_l, float* dump, int slice,
+                                         int lane) {
         const int par = lane >> 4, c = lane & 15;
+        float* base = dump + slice * 16 * kHeadDim;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             // both half-warps used the same running max, so their sums add
@@ -474,17 +511,71 @@ struct FmaConsumer {
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[g][j] += __shfl_xor_sync(0xffffffffu, acc[g][j], 16);
             if (lane == 0) {
-                red_m[cw * 16 + g] = m[g];
-                red_l[cw * 16 + g] = lt;
+                red_m[slice * 16 + g] = m[g];
+                red_l[slice * 16 + g] = lt;
             }
             if (par == 0) {
-                float* a = A + (cw * 16 + g) * kAccStride + c * 8;
-                *reinterpret_cast<float4*>(a) = make_float4(acc[g][0], acc[g][1], acc[g][2],
-                                                            acc[g][3]);
-                *reinterpret_cast<float4*>(a + 4) = make_float4(acc[g][4], acc[g][5], acc[g][6],
-                                                                acc[g][7]);
+                float* row = base + g * kHeadDim;
+                *reinterpret_cast<float4*>(row + dump_col(g, c * 8)) =
+                    make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+                *reinterpret_cast<float4*>(row + dump_col(g, c * 8 + 4)) =
+                    make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
             }
         }
+    }
+};
+
+// ------------------------------------------------------------------ shared state
+
+template <class C>
+struct Smem {
+    uint8_t* base;
+    __device__ __forceinline__ uint32_t ring(int slot) const {
+        return smem_addr(base) + slot * C::kStageBytes;
+    }
+    __device__ __forceinline__ float* dump(int slot) const {
+        return reinterpret_cast<float*>(base + slot * C::kStageBytes);
+    }
+    __device__ __forceinline__ uint32_t qbuf(int slot) const {
+        return smem_addr(base) + C::kQOffset + slot * C::kQBytes;
+    }
+    __device__ __forceinline__ StageRec* rec(int slot) const {
+        return reinterpret_cast<StageRec*>(base + C::kRecOffset) + slot;
+    }
+    __device__ __forceinline__ uint64_t* full(int slot) const {
+        return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + slot;
+    }
+    __device__ __forceinline__ uint64_t* empty(int slot) const {
+        return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + C::kStages + slot;
+    }
+    __device__ __forceinline__ uint64_t* cbar() const {
+        return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + 2 * C::kStages;
+    }
+    __device__ __forceinline__ int* issued() const {
+        return reinterpret_cast<int*>(base + C::kIssuedOffset);
+    }
+    __device__ __forceinline__ volatile int* flags() const {
+        return reinterpret_cast<volatile int*>(base + C::kFlagOffset);
+    }
+    __device__ __forceinline__ float* red_m() const {
+        return reinterpret_cast<float*>(base + C::kRedOffset);
+    }
+    __device__ __forceinline__ float* red_l() const {
+        return red_m() + C::kConsumerWarps * 16;
+    }
+};
+
+// Barrier among the consumer warps only (the producer keeps streaming), built
+// on an mbarrier so that it can give up like every other wait.
+struct ConsumerBarrier {
+    uint64_t* bar;
+    uint32_t parity;
+    __device__ __forceinline__ bool sync(int lane, const volatile int* abort) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
+        const bool ok = mbar_wait(bar, parity, abort);
+        parity ^= 1u;
+        return __all_sync(0xffffffffu, ok);
     }
 };
 
@@ -495,34 +586,26 @@ __global__ void __launch_bounds__(C::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-    uint64_t* empty = full + C::kStages;
-    int* issued = reinterpret_cast<int*>(smem + C::kIssuedOffset);
-    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);
-    float* red_m = reinterpret_cast<float*>(smem + C::kRedOffset);
-    float* red_l = red_m + C::kConsumerWarps * 16;
-    float* dumpA = reinterpret_cast<float*>(smem);
+    const Smem<C> sm{reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))};
+    volatile int* flags = sm.flags();  // [0] abort, [1] "last unit of its request"
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item_id = blockIdx.x / p.num_kv_heads;
-    const int hkv = blockIdx.x - item_id * p.num_kv_heads;
-    const int4 item = p.items[item_id];
-    const int b = item.w, n_pages = item.y, valid = item.z;
     const int ps = p.page_size;
     const int rmask = ps - 1;
     const int half_bytes = ps * 128;
     const int pages_per_stage = C::kStageTokens / ps;
-    const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+    const int G = p.group;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], C::kConsumerWarps);
-            issued[s] = 0;
+            mbar_init(sm.full(s), 1);
+            mbar_init(sm.empty(s), C::kConsumerWarps);
+            sm.issued()[s] = 0;
         }
+        mbar_init(sm.cbar(), C::kConsumerWarps);
         flags[0] = 0;
+        flags[1] = 0;
         fence_mbar_init();
     }
     if (warp == C::kConsumerWarps && lane == 0) {
@@ -532,165 +615,315 @@ __global__ void __launch_bounds__(C::kThreads)
     __syncthreads();
 
     using Consumer = typename std::conditional<C::kMma, MmaConsumer<C>, FmaConsumer<C>>::type;
-    Consumer cs;  // used by the consumer warps only
+
     if (warp == C::kConsumerWarps) {
-        // ------------------------------------------------ producer warp
-        int4 rq = make_int4(0, 0, 0, 0);
-        int ip0 = 0, ip1 = 0, lst = 0;
-        if (lane == 0) {
-            rq = p.req[b];
-            ip0 = p.indptr[b];
-            ip1 = p.indptr[b + 1];
-            lst = p.last_page_len[b];
-        }
-        const int32_t* idx = p.indices + item.x;
-        // A page index outside [0, num_pages) is recorded in the status word
-        // and replaced by page 0, so every copy stays inside the pool.
-        int win = lane < n_pages ? __ldg(idx + lane) : 0;
-        int nxt = 32 + lane < n_pages ? __ldg(idx + 32 + lane) : 0;
-        int win_base = 0;
-        bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
-        if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(p.status, kDeviceBadPage);
-        win = bad ? 0 : win;
-        const uint32_t tiles = smem_addr(smem);
-        for (int s = 0; s < n_stages; ++s) {
-            const int stage = s % C::kStages;
-            const int pg0 = s * pages_per_stage;
-            const int npg = min(pages_per_stage, n_pages - pg0);
-            if (pg0 >= win_base + 32) {
-                win = nxt;
-                win_base += 32;
-                nxt = win_base + 32 + lane < n_pages ? __ldg(idx + win_base + 32 + lane) : 0;
-                bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
-                if (__any_sync(0xffffffffu, bad) && lane == 0)
-                    record_status(p.status, kDeviceBadPage);
-                win = bad ? 0 : win;
+        // ================================================ producer warp
+        // The next unit is claimed as soon as the current one starts; its
+        // work-list entry is read after the current unit's first stage is
+        // issued and its first page indices after the second, so these
+        // dependent loads overlap the current unit's streaming.
+        struct Unit {
+            int unit;
+            int4 A, Bm;
+            int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
+        };
+        auto load_item = [&](Unit& u) {
+            if (u.unit < p.n_units) {
+                const int item = u.unit / p.num_kv_heads;
+                u.A = p.items[2 * item];
+                u.Bm = p.items[2 * item + 1];
             }
-            int ok = 1;
+        };
+        auto load_idx = [&](Unit& u) {
+            u.win = u.nxt = 0;
+            if (u.unit < p.n_units) {
+                const int32_t* idx = p.indices + u.A.x;
+                if (lane < u.A.y) u.win = __ldg(idx + lane);
+                if (32 + lane < u.A.y) u.nxt = __ldg(idx + 32 + lane);
+            }
+        };
+        int g = 0;  // ring position
+        bool ok = true;
+        Unit cur;
+        cur.unit = 0;
+        if (lane == 0) cur.unit = atomicAdd(p.work_counter, 1);
+        cur.unit = __shfl_sync(0xffffffffu, cur.unit, 0);
+        load_item(cur);
+        load_idx(cur);
+        while (cur.unit < p.n_units) {
+            Unit nx;
+            nx.unit = 0;
+            if (lane == 0) nx.unit = atomicAdd(p.work_counter, 1);
+            bool nx_item = false, nx_idx = false;
+            const int hkv = cur.unit - (cur.unit / p.num_kv_heads) * p.num_kv_heads;
+            const int4 A = cur.A;
+            const int4 Bm = cur.Bm;
+            const int b = A.w, n_pages = A.y;
+            const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+            int4 rq = make_int4(0, 0, 0, 0);
+            int ip0 = 0, ip1 = 0, lst = 0;
             if (lane == 0) {
-                if (s >= C::kStages)
-                    ok = mbar_wait(&empty[stage], ((s / C::kStages) + 1) & 1, flags) ? 1 : 0;
-                if (ok) mbar_arrive_expect_tx(&full[stage], npg * ps * kHeadDim * 2 * 2);
+                rq = p.req[b];
+                ip0 = p.indptr[b];
+                ip1 = p.indptr[b + 1];
+                lst = p.last_page_len[b];
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    flags[0] = 1;
-                    record_status(p.status, kDeviceWaitTimeout);
+            // An index outside [0, num_pages) is recorded and replaced by page
+            // 0, so every copy stays inside the pool.
+            const int32_t* idx = p.indices + A.x;
+            int win = cur.win, nxt = cur.nxt;
+            int win_base = 0;
+            bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+            if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(p.status, kDeviceBadPage);
+            win = bad ? 0 : win;
+            for (int s = 0; s < n_stages; ++s, ++g) {
+                const int slot = g % C::kStages;
+                const int pg0 = s * pages_per_stage;
+                const int npg = min(pages_per_stage, n_pages - pg0);
+                if (pg0 >= win_base + 32) {
+                    win = nxt;
+                    win_base += 32;
+                    nxt = win_base + 32 + lane < n_pages ? __ldg(idx + win_base + 32 + lane) : 0;
+                    bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+                    if (__any_sync(0xffffffffu, bad) && lane == 0)
+                        record_status(p.status, kDeviceBadPage);
+                    win = bad ? 0 : win;
                 }
-                break;
-            }
-            const uint32_t tk = tiles + stage * C::kStageBytes;
-            const uint32_t tv = tk + C::kStageBytes / 2;
-            for (int j = 0; j < npg; ++j) {
-                const int page = __shfl_sync(0xffffffffu, win, pg0 - win_base + j);
+                int okw = 1;
+                if (lane == 0 && g >= C::kStages)
+                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) {
-                    const uint32_t off = j * ps * 256;
-                    // coordinates (d, A, B, page): NHD (d, head, token, page),
-                    // HND (d, token, head, page); the box covers all ps tokens
-                    const int ca = p.layout == 0 ? hkv : 0;
-                    const int cb = p.layout == 0 ? 0 : hkv;
-                    tma_load_4d(tk + off, &tmap_k, &full[stage], 0, ca, cb, page);
-                    tma_load_4d(tk + off + half_bytes, &tmap_k, &full[stage], 64, ca, cb, page);
-                    tma_load_4d(tv + off, &tmap_v, &full[stage], 0, ca, cb, page);
-                    tma_load_4d(tv + off + half_bytes, &tmap_v, &full[stage], 64, ca, cb, page);
+                    StageRec* r = sm.rec(slot);
+                    r->b = b;
+                    r->hkv = hkv;
+                    r->valid = A.z;
+                    r->n_stages = n_stages;
+                    r->s = s;
+                    r->slot = Bm.x;
+                    r->slot_base = Bm.y;
+                    r->n_chunks = Bm.z;
+                    const uint32_t qbytes = s == 0 ? static_cast<uint32_t>(G * kHeadDim * 2) : 0u;
+                    mbar_arrive_expect_tx(sm.full(slot), npg * ps * kHeadDim * 2 * 2 + qbytes);
+                    if (s == 0)
+                        bulk_load(sm.qbuf(slot),
+                                  p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * G) *
+                                            kHeadDim,
+                                  qbytes, sm.full(slot));
+                }
+                const uint32_t tk = sm.ring(slot);
+                const uint32_t tv = tk + C::kStageBytes / 2;
+                const int ca = p.layout == 0 ? hkv : 0;  // coordinates (d, A, B, page):
+                const int cb = p.layout == 0 ? 0 : hkv;  // NHD (d, head, token, page)
+                for (int j = 0; j < npg; ++j) {          // HND (d, token, head, page)
+                    const int page = __shfl_sync(0xffffffffu, win, pg0 - win_base + j);
+                    if (lane == 0) {
+                        const uint32_t off = j * ps * 256;
+                        tma_load_4d(tk + off, &tmap_k, sm.full(slot), 0, ca, cb, page);
+                        tma_load_4d(tk + off + half_bytes, &tmap_k, sm.full(slot), 64, ca, cb,
+                                    page);
+                        tma_load_4d(tv + off, &tmap_v, sm.full(slot), 0, ca, cb, page);
+                        tma_load_4d(tv + off + half_bytes, &tmap_v, sm.full(slot), 64, ca, cb,
+                                    page);
+                    }
+                }
+                if (lane == 0) sm.issued()[slot] += 1;
+                if (s == 0) {
+                    nx.unit = __shfl_sync(0xffffffffu, nx.unit, 0);
+                    load_item(nx);
+                    nx_item = true;
+                } else if (s == 1) {
+                    load_idx(nx);
+                    nx_idx = true;
                 }
             }
-            if (lane == 0) issued[stage] += 1;
+            if (!ok) break;
+            if (!nx_item) {
+                nx.unit = __shfl_sync(0xffffffffu, nx.unit, 0);
+                load_item(nx);
+            }
+            if (!nx_idx) load_idx(nx);
+            if (lane == 0 && (ip0 != rq.x || ip1 != rq.y || lst != rq.z))
+                record_status(p.status, kDevicePlanMismatch);
+            cur = nx;
         }
-        if (lane == 0 && (ip0 != rq.x || ip1 != rq.y || lst != rq.z))
-            record_status(p.status, kDevicePlanMismatch);
+        if (ok) {
+            // End marker: a stage whose record says s = -1, completed by a
+            // plain arrive (no bytes).
+            const int slot = g % C::kStages;
+            int okw = 1;
+            if (lane == 0) {
+                if (g >= C::kStages)
+                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags) ? 1 : 0;
+                if (okw) {
+                    sm.rec(slot)->s = -1;
+                    mbar_arrive(sm.full(slot));
+                    sm.issued()[slot] += 1;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        }
+        if (!ok && lane == 0) {
+            flags[0] = 1;
+            record_status(p.status, kDeviceWaitTimeout);
+        }
     } else {
-        // ------------------------------------------------ consumer warps
+        // ================================================ consumer warps
+        Consumer cs;
         const int slice = warp % C::kSlices;
         const int mt = warp / C::kSlices;
-        cs.init(p, b, hkv, mt, lane);
-        const uint32_t tiles = smem_addr(smem);
-        for (int s = 0; s < n_stages; ++s) {
-            const int stage = s % C::kStages;
-            const bool ok = mbar_wait(&full[stage], (s / C::kStages) & 1, flags);
-            if (!__all_sync(0xffffffffu, ok)) {  // leave the loop as a whole warp
-                if (lane == 0) {
-                    flags[0] = 1;
-                    record_status(p.status, kDeviceWaitTimeout);
-                }
+        const int ctid = threadIdx.x;  // 0 .. kConsumerThreads-1
+        ConsumerBarrier cbar{sm.cbar(), 0u};
+        bool ok = true;
+        for (int g = 0;; ++g) {
+            const int slot = g % C::kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(sm.full(slot), (g / C::kStages) & 1, flags))) {
+                ok = false;
                 break;
             }
+            const StageRec r = *sm.rec(slot);
+            if (r.s < 0) break;
+            if (r.s == 0) cs.init(sm.qbuf(slot), G, mt, lane);
             const int t0 = slice * kSliceTokens;
-            const int u0 = s * C::kStageTokens + t0;
-            if (u0 < valid) {
-                const uint32_t tk = tiles + stage * C::kStageBytes;
-                cs.consume(tk, tk + C::kStageBytes / 2, t0, u0, valid, rmask, half_bytes,
+            const int u0 = r.s * C::kStageTokens + t0;
+            if (u0 < r.valid) {
+                const uint32_t tk = sm.ring(slot);
+                cs.consume(tk, tk + C::kStageBytes / 2, t0, u0, r.valid, rmask, half_bytes,
                            p.scale_log2, lane);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-        }
-    }
-    __syncthreads();  // every warp is out of the stage ring
-
-    if (flags[0]) {
-        // Aborted: wait (bounded) for the copies already issued, then leave.
-        if (threadIdx.x == 0) {
-            for (int s = 0; s < C::kStages; ++s)
-                if (issued[s] > 0) mbar_wait(&full[s], (issued[s] - 1) & 1, nullptr);
-        }
-        return;
-    }
-    // All issued copies have landed and been consumed: the tiles become the
-    // scratch for the warps' states.
-    if (warp < C::kConsumerWarps) cs.dump(red_m, red_l, dumpA, warp, lane);
-    __syncthreads();
-
-    // ------------------------------------------------ merge warp states, write
-    const int slot = p.item_slot[item_id];
-    const int G = p.group;
-    for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += C::kThreads) {
-        const int r = i / (kHeadDim / 4);
-        const int d4 = i - r * (kHeadDim / 4);
-        const int mtile = r >> 4, rr = r & 15;
-        const int w0 = mtile * C::kSlices;
-        float M = -INFINITY;
+            if (r.s == r.n_stages - 1) {
+                // ---- unit epilogue: merge the warps' states through this
+                // stage's buffer (held until the end), then write.
+                float* dump = sm.dump(slot);
+                float* red_m = sm.red_m();
+                float* red_l = sm.red_l();
+                ok = cbar.sync(lane, flags);  // every warp is done reading K/V here
+                const int hq0 = r.hkv * G;
+                for (int round = 0; ok && round < C::kMtiles; ++round) {
+                    if (mt == round) cs.dump(red_m, red_l, dump, slice, lane);
+                    if (!(ok = cbar.sync(lane, flags))) break;
+                    const int rows = min(16, G - round * 16);
+                    for (int i = ctid; i < rows * (kHeadDim / 4); i += C::kConsumerThreads) {
+                        const int rr = i / (kHeadDim / 4);
+                        const int d4 = i - rr * (kHeadDim / 4);
+                        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::kSlices; ++w) M = fmaxf(M, red_m[(w0 + w) * 16 + rr]);
-        float L = 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
+                        for (int w = 0; w < C::kSlices; ++w) M = fmaxf(M, red_m[w * 16 + rr]);
+                        float L = 0.f;
+                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < C::kSlices; ++w) {
-                const float sc = fast_exp2(red_m[(w0 + w) * 16 + rr] - M);
-                L += red_l[(w0 + w) * 16 + rr] * sc;
-                const float4 a =
-                    *reinterpret_cast<const float4*>(dumpA + ((w0 + w) * 16 + rr) * kAccStride +
-                                                     d4 * 4);
-                o.x += a.x * sc;
-                o.y += a.y * sc;
-                o.z += a.z * sc;
-                o.w += a.w * sc;
+                            for (int w = 0; w < C::kSlices; ++w) {
+                                const float sc = fast_exp2(red_m[w * 16 + rr] - M);
+                                L += red_l[w * 16 + rr] * sc;
+                                const float4 a = *reinterpret_cast<const float4*>(
+                                    dump + (w * 16 + rr) * kHeadDim + dump_col(rr, d4 * 4));
+                                o.x += a.x * sc;
+                                o.y += a.y * sc;
+                                o.z += a.z * sc;
+                                o.w += a.w * sc;
+                            }
+                        }
+                        float lse2 = -INFINITY;
+                        if (L > 0.f) {
+                            const float inv = 1.f / L;
+                            o.x *= inv;
+                            o.y *= inv;
+                            o.z *= inv;
+                            o.w *= inv;
+                            lse2 = M + __log2f(L);
+                        }
+                        const int hq = hq0 + round * 16 + rr;
+                        if (r.slot < 0) {
+                            const size_t row = static_cast<size_t>(r.b) * p.num_qo_heads + hq;
+                            uint2 packed;
+                            packed.x = pack_bf16x2(o.x, o.y);
+                            packed.y = pack_bf16x2(o.z, o.w);
+                            *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
+                            if (d4 == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
+                        } else {
+                            const size_t row = static_cast<size_t>(r.slot) * p.num_qo_heads + hq;
+                            *reinterpret_cast<float4*>(p.part_o + row * kHeadDim + d4 * 4) = o;
+                            if (d4 == 0) p.part_lse[row] = lse2;
+                        }
+                    }
+                    ok = cbar.sync(lane, flags);  // dump reads done before reuse
+                }
+                if (ok && r.slot >= 0) {
+                    // ---- split request: the last of its items to finish merges
+                    __threadfence();
+                    if (!(ok = cbar.sync(lane, flags))) break;
+                    if (ctid == 0) {
+                        const int done =
+                            atomicAdd(p.counters + r.b * p.num_kv_heads + r.hkv, 1) + 1;
+                        flags[1] = done == r.n_chunks ? 1 : 0;
+                    }
+                    if (!(ok = cbar.sync(lane, flags))) break;
+                    if (flags[1]) {
+                        __threadfence();
+                        // Partials of other CTAs: read through L2 (ld.global.cg),
+                        // in slot order; the loads are independent, so many are in
+                        // flight at once.
+                        for (int i = ctid; i < G * (kHeadDim / 4); i += C::kConsumerThreads) {
+                            const int rr = i / (kHeadDim / 4);
+                            const int d4 = i - rr * (kHeadDim / 4);
+                            const int hq = hq0 + rr;
+                            const float* lse_c =
+                                p.part_lse + static_cast<size_t>(r.slot_base) * p.num_qo_heads + hq;
+                            const float4* o_c = reinterpret_cast<const float4*>(
+                                p.part_o +
+                                (static_cast<size_t>(r.slot_base) * p.num_qo_heads + hq) *
+                                    kHeadDim) + d4;
+                            const size_t lse_stride = p.num_qo_heads;
+                            const size_t o_stride = static_cast<size_t>(p.num_qo_heads) * 32;
+                            float M = -INFINITY;
+#pragma unroll 8
+                            for (int c = 0; c < r.n_chunks; ++c)
+                                M = fmaxf(M, __ldcg(lse_c + c * lse_stride));
+                            float W = 0.f;
+                            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (M != -INFINITY) {
+#pragma unroll 4
+                                for (int c = 0; c < r.n_chunks; ++c) {
+                                    const float w = fast_exp2(__ldcg(lse_c + c * lse_stride) - M);
+                                    const float4 v = __ldcg(o_c + c * o_stride);
+                                    W += w;
+                                    o.x = fmaf(w, v.x, o.x);
+                                    o.y = fmaf(w, v.y, o.y);
+                                    o.z = fmaf(w, v.z, o.z);
+                                    o.w = fmaf(w, v.w, o.w);
+                                }
+                            }
+                            const float inv = W > 0.f ? 1.f / W : 0.f;
+                            const size_t row = static_cast<size_t>(r.b) * p.num_qo_heads + hq;
+                            uint2 packed;
+                            packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+                            packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+                            *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
+                            if (d4 == 0 && p.lse != nullptr)
+                                p.lse[row] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
+                        }
+                    }
+                }
+                if (!ok) break;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sm.empty(slot));
         }
-        float lse_nat = -INFINITY;
-        if (L > 0.f) {
-            const float inv = 1.f / L;
-            o.x *= inv;
-            o.y *= inv;
-            o.z *= inv;
-            o.w *= inv;
-            lse_nat = (M + __log2f(L)) * kLn2;
+        if (!ok && lane == 0) {
+            flags[0] = 1;
+            record_status(p.status, kDeviceWaitTimeout);
         }
-        const int hq = hkv * G + r;
-        if (slot < 0) {
-            const size_t row = static_cast<size_t>(b) * p.num_qo_heads + hq;
-            uint2 packed;
-            packed.x = pack_bf16x2(o.x, o.y);
-            packed.y = pack_bf16x2(o.z, o.w);
-            *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
-            if (d4 == 0 && p.lse != nullptr) p.lse[row] = lse_nat;
-        } else {
-            const size_t row = static_cast<size_t>(slot) * p.num_qo_heads + hq;
-            *reinterpret_cast<float4*>(p.part_o + row * kHeadDim + d4 * 4) = o;
-            if (d4 == 0) p.part_lse[row] = lse_nat;
-        }
+    }
+    __syncthreads();  // every warp has left its loop
+
+    if (flags[0] && threadIdx.x == 0) {
+        // Aborted: wait (bounded) for the copies already issued, then leave.
+        for (int s = 0; s < C::kStages; ++s)
+            if (sm.issued()[s] > 0) mbar_wait(sm.full(s), (sm.issued()[s] - 1) & 1, nullptr);
     }
 }
 

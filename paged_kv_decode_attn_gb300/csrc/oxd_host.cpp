@@ -3,16 +3,17 @@
 // Lifecycle from the "Oxide Infer" README, "One execution model": the plan
 // fixes the kernel variant, the chunking of every request's pages, the launch
 // shape and the workspace contract; a run only checks operands and enqueues
-// (one host-to-device copy of the work list, the decode kernel, and the merge
-// kernel when some request was split). "Providers": checked span, alignment,
-// alias and capacity rules; explicit workspace; caller stream; typed device
-// status.
+// one host-to-device copy of the work list (which also zeroes the status word
+// and the counters) and one decode launch, which merges split requests
+// itself. "Providers": checked span, alignment, alias and capacity rules;
+// explicit workspace; caller stream; typed device status.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -38,7 +39,8 @@ struct oxd_plan_s {
     int num_sms;
     int64_t nnz;
     int64_t total_tokens;
-    size_t off_items, off_slot, off_req, off_split, off_part_o, off_part_lse;
+    int grid;
+    size_t off_items, off_req, off_counters, off_part_o, off_part_lse;
     size_t meta_bytes, ws_bytes;
     void* meta;
     bool pinned;
@@ -48,7 +50,7 @@ struct oxd_plan_s {
 
 namespace {
 
-constexpr int kWaves = 4;  // target grid ~ kWaves x resident CTAs when splitting
+constexpr int kWaves = 4;  // target ~ kWaves work units per resident CTA when splitting
 
 std::mutex g_plans_mu;
 std::unordered_set<oxd_plan> g_plans;
@@ -169,7 +171,7 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
 }
 
 struct Item {
-    int idx_begin, n_pages, valid, b, slot;
+    int idx_begin, n_pages, valid, b, slot, slot_base, n_chunks;
 };
 
 }  // namespace
@@ -254,7 +256,6 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         c = (c + pps - 1) / pps * pps;
         chunk_pages = static_cast<int>(std::min<int64_t>(c, 1 << 30));
     }
-    std::vector<int4> split_tab;
     for (int b = 0; b < B; ++b) {
         const int P = indptr[b + 1] - indptr[b];
         const int L = (P - 1) * ps + last[b];
@@ -277,7 +278,6 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         max_chunks = std::max(max_chunks, n);
         const int slot_base = n > 1 ? n_slots : -1;
         if (n > 1) {
-            split_tab.push_back(make_int4(b, n_slots, n, 0));
             n_slots += n;
             ++n_split;
         }
@@ -289,14 +289,18 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             it.valid = std::min((p1 - p0) * ps, L - p0 * ps);
             it.b = b;
             it.slot = n > 1 ? slot_base + c : -1;
+            it.slot_base = slot_base;
+            it.n_chunks = n;
             items.push_back(it);
         }
     }
     // Longest items first, so the short tails fill in behind them.
     std::stable_sort(items.begin(), items.end(),
                      [](const Item& a, const Item& b) { return a.n_pages > b.n_pages; });
-    const int64_t grid = static_cast<int64_t>(items.size()) * d.num_kv_heads;
-    if (grid > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
+    const int64_t n_units = static_cast<int64_t>(items.size()) * d.num_kv_heads;
+    if (n_units > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
+    // Persistent grid: at most the resident CTAs of the device.
+    const int64_t grid = std::min<int64_t>(n_units, static_cast<int64_t>(num_sms) * ctas_per_sm);
 
     // ---- workspace layout
     oxd_plan P = new (std::nothrow) oxd_plan_s();
@@ -312,13 +316,14 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->chunk_pages = chunk_pages;
     P->ctas_per_sm = ctas_per_sm;
     P->num_sms = num_sms;
+    P->grid = static_cast<int>(grid);
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
     P->off_items = sizeof(WsHeader);
-    P->off_slot = align_up(P->off_items + 16 * items.size(), 256);
-    P->off_req = align_up(P->off_slot + 4 * items.size(), 256);
-    P->off_split = align_up(P->off_req + 16 * static_cast<size_t>(B), 256);
-    P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
+    P->off_req = align_up(P->off_items + 32 * items.size(), 256);
+    P->off_counters = align_up(P->off_req + 16 * static_cast<size_t>(B), 256);
+    P->meta_bytes =
+        align_up(P->off_counters + 4 * static_cast<size_t>(B) * d.num_kv_heads, 256);
     P->off_part_o = P->meta_bytes;
     P->off_part_lse = align_up(
         P->off_part_o + static_cast<size_t>(n_slots) * d.num_qo_heads * kHeadDim * 4, 256);
@@ -342,15 +347,13 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     hdr->batch = B;
     hdr->num_kv_heads = d.num_kv_heads;
     int4* it4 = reinterpret_cast<int4*>(m + P->off_items);
-    int32_t* slot = reinterpret_cast<int32_t*>(m + P->off_slot);
     for (size_t i = 0; i < items.size(); ++i) {
-        it4[i] = make_int4(items[i].idx_begin, items[i].n_pages, items[i].valid, items[i].b);
-        slot[i] = items[i].slot;
+        it4[2 * i] = make_int4(items[i].idx_begin, items[i].n_pages, items[i].valid, items[i].b);
+        it4[2 * i + 1] = make_int4(items[i].slot, items[i].slot_base, items[i].n_chunks, 0);
     }
     int4* rq = reinterpret_cast<int4*>(m + P->off_req);
     for (int b = 0; b < B; ++b) rq[b] = make_int4(indptr[b], indptr[b + 1], last[b], 0);
-    int4* sp = reinterpret_cast<int4*>(m + P->off_split);
-    for (size_t i = 0; i < split_tab.size(); ++i) sp[i] = split_tab[i];
+    // counters stay zero: the upload resets them every run
     P->ev_before = nullptr;
     P->ev_after = nullptr;
     {
@@ -372,10 +375,10 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.chunk_pages = plan->chunk_pages;
     r.num_slots = plan->n_slots;
     r.kernel_variant = plan->variant;
-    r.grid_ctas = plan->n_items * plan->desc.num_kv_heads;
+    r.grid_ctas = plan->grid;
     r.ctas_per_sm = plan->ctas_per_sm;
     r.num_sms = plan->num_sms;
-    r.launches_per_run = plan->n_split > 0 ? 2 : 1;
+    r.launches_per_run = 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.upload_bytes = static_cast<int64_t>(plan->meta_bytes);
     r.total_kv_tokens = plan->total_tokens;
@@ -463,8 +466,9 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.indices = indices;
     p.last_page_len = last_page_len;
     p.items = reinterpret_cast<const int4*>(ws + plan->off_items);
-    p.item_slot = reinterpret_cast<const int32_t*>(ws + plan->off_slot);
     p.req = reinterpret_cast<const int4*>(ws + plan->off_req);
+    p.counters = reinterpret_cast<int32_t*>(ws + plan->off_counters);
+    p.work_counter = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, work_counter));
     p.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
     p.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
     p.status = reinterpret_cast<int32_t*>(ws);
@@ -473,30 +477,16 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.group = plan->group;
     p.page_size = d.page_size;
     p.layout = d.layout;
-    p.n_items = plan->n_items;
+    p.n_units = plan->n_items * d.num_kv_heads;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_decode(plan->variant, tk, tv, p, plan->n_items * d.num_kv_heads, s) !=
-        cudaSuccess)
+    if (launch_decode(plan->variant, tk, tv, p, plan->grid, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (plan->n_split > 0) {
-        MergeParams mp{};
-        mp.v = p.part_o;
-        mp.s = p.part_lse;
-        mp.out = p.out;
-        mp.lse = lse;
-        mp.split = reinterpret_cast<const int4*>(ws + plan->off_split);
-        mp.n = plan->n_split;
-        mp.S = 0;
-        mp.H = d.num_qo_heads;
-        mp.D = kHeadDim;
-        if (launch_merge(mp, s) != cudaSuccess) return OXD_ERR_CUDA;
-    }
     return OXD_OK;
 }
 
@@ -518,7 +508,6 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
     mp.s = s;
     mp.out = static_cast<uint16_t*>(v_out);
     mp.lse = s_out;
-    mp.split = nullptr;
     mp.n = N;
     mp.S = S;
     mp.H = H;

@@ -11,7 +11,7 @@ namespace oxd {
 constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 32;           // G = Hq / Hkv handled by the decode kernels
 constexpr int kSliceTokens = 16;        // tokens one consumer warp handles per stage
-constexpr long long kWaitTimeoutNs = 1000000000LL;  // bounded pipeline waits (1 s)
+constexpr long long kWaitTimeoutNs = 1000000000LL;  // bounded waits (1 s)
 
 // Decode kernel variants (oxd_plan_info.kernel_variant).
 enum Variant : int {
@@ -30,33 +30,32 @@ struct VariantShape {
     int smem_bytes;     // dynamic shared memory per CTA
 };
 
-// Work list entry, one per (request, chunk of consecutive pages).
-//   x: absolute offset of the chunk's first page in `indices`
-//   y: pages in the chunk
-//   z: valid tokens in the chunk (the last page of a request may be partial)
-//   w: request index b
-// A parallel int32 array gives the partial-state slot of each item, or -1
-// when the item covers its whole request and writes out/lse directly.
-//
+// Work list, two int4 per item (one item = consecutive pages of one request,
+// processed once per KV head):
+//   A: x = absolute offset of the item's first page in `indices`,
+//      y = pages in the item, z = valid tokens in the item, w = request b
+//   B: x = partial-state slot of this item or -1 when the item covers its
+//      whole request (then it writes out/lse directly), y = first slot of the
+//      request's items, z = number of items of the request, w = 0
 // Per-request table (int4): x = indptr[b], y = indptr[b+1], z = last_page_len[b]
-// as planned (the kernels compare them with the device block tables), w = 0.
-// Split-request table (int4): x = b, y = first slot, z = number of slots, w = 0.
+// as planned (the kernel compares them with the device block tables), w = 0.
 //
-// Workspace layout (byte offsets, each 256-aligned), all written by the
-// run's single host-to-device copy except the partial states:
-//   [0, 256)         header: int32 status word, then plan facts
-//   items            int4[n_items]
-//   item_slot        int32[n_items]
-//   req              int4[B]
-//   split            int4[n_split]
-//   part_o           f32[n_slots][Hq][128]   (not uploaded)
-//   part_lse         f32[n_slots][Hq]        (not uploaded)
+// Workspace layout (byte offsets, each 256-aligned); everything before
+// part_o is written by the run's single host-to-device copy, which also
+// zeroes the status word and all counters:
+//   [0, 256)     header: int32 status word, int32 work counter
+//   items        int4[2 * n_items]
+//   req          int4[B]
+//   counters     int32[B * Hkv]   finished items per (request, KV head)
+//   part_o       f32[n_slots][Hq][128]
+//   part_lse     f32[n_slots][Hq]  (log2 domain)
 struct WsHeader {
     int32_t status;
+    int32_t work_counter;
     int32_t n_items;
     int32_t batch;
     int32_t num_kv_heads;
-    int32_t pad[60];
+    int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -68,29 +67,29 @@ struct DecodeParams {
     const int32_t* indices;
     const int32_t* last_page_len;
     const int4* items;
-    const int32_t* item_slot;
     const int4* req;
+    int32_t* counters;
     float* part_o;
     float* part_lse;
     int32_t* status;
+    int32_t* work_counter;
     int32_t num_qo_heads;
     int32_t num_kv_heads;
     int32_t group;                // G
     int32_t page_size;
     int32_t layout;               // 0 NHD, 1 HND
-    int32_t n_items;
+    int32_t n_units;              // n_items * num_kv_heads
     int64_t num_pages;
     float scale_log2;             // sm_scale * log2(e)
 };
 
 struct MergeParams {
-    const float* v;               // states [.][S][H][D] (slot-major)
-    const float* s;               // [.][S][H]
+    const float* v;               // states [N][S][H][D]
+    const float* s;               // [N][S][H], natural log
     uint16_t* out;                // bf16 [N][H][D]
     float* lse;                   // [N][H] or nullptr
-    const int4* split;            // ragged mode: {b, first state, count, 0}; nullptr: uniform
-    int32_t n;                    // number of (request) rows
-    int32_t S;                    // uniform state count
+    int32_t n;
+    int32_t S;
     int32_t H;
     int32_t D;
 };

@@ -1,6 +1,7 @@
 // Attention-state merge for sm_103a ("FlashInfer parity matrix" page,
-// "Domain coverage": attention state and cascade, state merge; and the merge
-// step of the "Single decode split-K" row of "Admitted attention matrix").
+// "Domain coverage": attention state and cascade, state merge). The decode
+// kernel merges its own split partitions in place; this kernel serves the
+// public oxd_merge_states entry point.
 //
 // For one row (request) and head h it combines S states (v_i, s_i):
 //   M = max_i s_i, w_i = exp(s_i - M), v = sum w_i v_i / sum w_i,
@@ -29,13 +30,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
     if (gw >= static_cast<long long>(p.n) * p.H) return;
     const int n = static_cast<int>(gw / p.H);
     const int h = static_cast<int>(gw - static_cast<long long>(n) * p.H);
-    int row = n, first = n * p.S, count = p.S;
-    if (p.split != nullptr) {
-        const int4 sr = p.split[n];
-        row = sr.x;
-        first = sr.y;
-        count = sr.z;
-    }
+    const int row = n, first = n * p.S, count = p.S;
     // pass 1: maximum LSE over the states (lanes stride over them)
     float M = -INFINITY;
     for (int i = lane; i < count; i += 32)

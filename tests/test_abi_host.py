@@ -69,12 +69,13 @@ def test_planner_chunks_long_requests_and_sizes_workspace():
     assert info.num_split_requests == 32 and info.max_chunks > 1
     assert info.chunk_pages % 4 == 0                      # whole 64-token stages at ps 16
     assert info.num_work_items == 32 * info.max_chunks
-    assert info.grid_ctas == info.num_work_items * 8
+    # persistent grid: never more CTAs than units, nor than resident slots
+    assert info.grid_ctas == min(info.num_work_items * 8, 152 * info.ctas_per_sm)
     assert info.num_slots == info.num_work_items
     part = info.num_slots * 32 * 128 * 4 + info.num_slots * 32 * 4
     assert info.workspace_bytes >= part + info.upload_bytes
     assert info.workspace_bytes == plan.workspace_bytes
-    assert info.launches_per_run == 2
+    assert info.launches_per_run == 1
     assert info.total_kv_tokens == 32 * 4096
 
 
@@ -83,6 +84,7 @@ def test_short_batch_is_not_split_when_splitting_is_off():
     info = plan.info
     assert info.num_split_requests == 0 and info.num_work_items == 3
     assert info.launches_per_run == 1 and info.num_slots == 0
+    assert info.grid_ctas == 3 * 8
 
 
 @pytest.mark.parametrize("force", [1, 2, 3, 7])
