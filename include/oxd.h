@@ -182,6 +182,36 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * oxd_paged_decode_run without a caller-provided workspace. The source pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * call cudaMalloc: a serving process that reserves all of its device memory
+ * at start-up and allows no later allocation (so memory never fragments and
+ * no allocation stalls a decode step), or a host that reaches this library
+ * through a plugin interface that passes only input and output tensors.
+ *
+ * The scratch is a 32 MiB array inside the library, reserved on every GPU
+ * that loads the library and held until the process exits. The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call).
+ * Arguments and results are those of oxd_paged_decode_run minus the
+ * workspace. A plan whose workspace_bytes exceeds 32 MiB is rejected with
+ * OXD_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call on a device shares the one array,
+ * which keeps the last call's contents (each run rewrites the part it reads
+ * first, including a zeroed status word): calls that can overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * The device status word lives in that array, so oxd_read_device_status
+ * cannot be used with this entry point.
+ */
+oxd_status oxd_paged_decode_run_static_workspace(oxd_plan plan, const void* q,
+                                                 const void* k_pages, const void* v_pages,
+                                                 const int32_t* indptr, const int32_t* indices,
+                                                 const int32_t* last_page_len, float sm_scale,
+                                                 void* out, float* lse, void* stream);
+
+/*
  * Merge attention states ("Attention state and cascade": state merge).
  * For each n < N and h < H, combine the S states (v[n, i, h, :], s[n, i, h]):
  *   M = max_i s_i, w_i = exp(s_i - M),

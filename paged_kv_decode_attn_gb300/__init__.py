@@ -34,6 +34,7 @@ from .build import build
 __all__ = [
     "OXD_OK", "OXD_LAYOUT_NHD", "OXD_LAYOUT_HND", "OxdError", "LibraryNotBuilt", "Desc",
     "PlanInfo", "Plan", "build", "lib", "oxd_paged_decode_plan", "oxd_paged_decode_run",
+    "oxd_paged_decode_run_static_workspace",
     "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
     "oxd_read_device_status", "oxd_status_string", "oxd_device_status_string", "oxd_version",
     "EXPORTED_SYMBOLS",
@@ -62,6 +63,7 @@ EXPORTED_SYMBOLS = (
     "oxd_paged_decode_plan", "oxd_paged_decode_run", "oxd_merge_states", "oxd_plan_get_info",
     "oxd_plan_set_timing_events", "oxd_plan_destroy", "oxd_read_device_status",
     "oxd_status_string", "oxd_device_status_string", "oxd_version",
+    "oxd_paged_decode_run_static_workspace",
 )
 
 
@@ -125,12 +127,15 @@ def lib():
                                                 ctypes.POINTER(vp), ctypes.POINTER(sz)]
             L.oxd_paged_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                                vp, vp, sz, vp]
+            L.oxd_paged_decode_run_static_workspace.argtypes = [
+                vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
             L.oxd_merge_states.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
             L.oxd_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
             L.oxd_plan_set_timing_events.argtypes = [vp, vp, vp]
             L.oxd_plan_destroy.argtypes = [vp]
             L.oxd_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
-            for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run", "oxd_merge_states",
+            for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run",
+                      "oxd_paged_decode_run_static_workspace", "oxd_merge_states",
                       "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
                       "oxd_read_device_status"):
                 getattr(L, f).restype = ctypes.c_int
@@ -257,6 +262,19 @@ def oxd_paged_decode_run(plan, q, k_pages, v_pages, indptr, indices, last_page_l
         _addr(last_page_len), float(sm_scale), _addr(out), _addr(lse), _addr(workspace),
         int(workspace_bytes), _stream(stream, q))
     _check("oxd_paged_decode_run", st)
+
+
+def oxd_paged_decode_run_static_workspace(plan, q, k_pages, v_pages, indptr, indices,
+                                          last_page_len, sm_scale, out, lse,
+                                          stream=None) -> None:
+    """Enqueue one decode step using the library's own scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory; see
+    ``oxd_paged_decode_run_static_workspace`` in include/oxd.h for its 32 MiB
+    limit and the rule that overlapping calls race)."""
+    st = lib().oxd_paged_decode_run_static_workspace(
+        _handle(plan), _addr(q), _addr(k_pages), _addr(v_pages), _addr(indptr), _addr(indices),
+        _addr(last_page_len), float(sm_scale), _addr(out), _addr(lse), _stream(stream, q))
+    _check("oxd_paged_decode_run_static_workspace", st)
 
 
 def oxd_merge_states(v, s, N, S, H, D, v_out, s_out=None, stream=None) -> None:
