@@ -612,6 +612,9 @@ __global__ void __launch_bounds__(C::kThreads)
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
+    // A separate merge kernel, when the plan uses one, may be scheduled now;
+    // it waits for this grid to complete before it reads anything.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     using Consumer = typename std::conditional<C::kMma, MmaConsumer<C>, FmaConsumer<C>>::type;
@@ -852,18 +855,19 @@ __global__ void __launch_bounds__(C::kThreads)
                     }
                     ok = cbar.sync(lane, flags);  // dump reads done before reuse
                 }
-                if (ok && r.slot >= 0) {
-                    // ---- split request: the last of its items to finish merges
-                    __threadfence();
-                    if (!(ok = cbar.sync(lane, flags))) break;
+                if (ok && r.slot >= 0 && p.fused_merge) {
+                    // ---- split request: the last of its items to finish merges.
+                    // The consumer barrier orders every thread's partial writes
+                    // before one thread's device-scope fence and count.
                     if (ctid == 0) {
+                        __threadfence();
                         const int done =
                             atomicAdd(p.counters + r.b * p.num_kv_heads + r.hkv, 1) + 1;
+                        __threadfence();
                         flags[1] = done == r.n_chunks ? 1 : 0;
                     }
                     if (!(ok = cbar.sync(lane, flags))) break;
                     if (flags[1]) {
-                        __threadfence();
                         // Partials of other CTAs: read through L2 (ld.global.cg),
                         // in slot order; the loads are independent, so many are in
                         // flight at once.

@@ -4,13 +4,14 @@
 // fixes the kernel variant, the chunking of every request's pages, the launch
 // shape and the workspace contract; a run only checks operands and enqueues
 // one host-to-device copy of the work list (which also zeroes the status word
-// and the counters) and one decode launch, which merges split requests
-// itself. "Providers": checked span, alignment, alias and capacity rules;
+// and the counters) and one decode launch, which merges small splits itself;
+// large splits get a merge launch right behind it. "Providers": checked span, alignment, alias and capacity rules;
 // explicit workspace; caller stream; typed device status.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <functional>
 #include <cmath>
 #include <cstdlib>
 #include <cstddef>
@@ -40,7 +41,8 @@ struct oxd_plan_s {
     int64_t nnz;
     int64_t total_tokens;
     int grid;
-    size_t off_items, off_req, off_counters, off_part_o, off_part_lse;
+    bool fused_merge;
+    size_t off_items, off_req, off_counters, off_split, off_part_o, off_part_lse;
     size_t meta_bytes, ws_bytes;
     void* meta;
     bool pinned;
@@ -50,7 +52,13 @@ struct oxd_plan_s {
 
 namespace {
 
-constexpr int kWaves = 4;  // target ~ kWaves work units per resident CTA when splitting
+// Planner cost model (microseconds; GB300 HBM measured at about 6.8 TB/s).
+constexpr double kHbmBytesPerUs = 6.8e6;
+constexpr double kUnitOverheadUs = 1.0;       // prologue/epilogue not hidden by prefetch
+constexpr double kSplitOverheadUs = 0.5;      // partial write + counter
+constexpr double kFusedMergeMaxBytes = 64.0 * 1024;  // largest merge done inside the kernel
+constexpr double kFusedMergeBytesPerUs = 2.0e4;      // one CTA reading partials from L2
+constexpr double kMergeKernelUs = 3.0;        // a separate merge launch behind the decode
 
 std::mutex g_plans_mu;
 std::unordered_set<oxd_plan> g_plans;
@@ -244,63 +252,140 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
 
     // ---- chunking
     const int pps = std::max(1, vs.stage_tokens / ps);  // pages per pipeline stage
-    std::vector<Item> items;
-    items.reserve(static_cast<size_t>(B) * 2);
-    int n_slots = 0, n_split = 0, max_chunks = 1;
-    int chunk_pages = 0;
-    if (d.force_splits == 0 && d.max_splits != 1) {
-        const int64_t conc = static_cast<int64_t>(num_sms) * ctas_per_sm * kWaves;
-        const int64_t head_pages = total_pages * d.num_kv_heads;
-        int64_t c = (head_pages + conc - 1) / conc;
-        c = std::max<int64_t>(c, pps);
-        c = (c + pps - 1) / pps * pps;
-        chunk_pages = static_cast<int>(std::min<int64_t>(c, 1 << 30));
-    }
-    for (int b = 0; b < B; ++b) {
-        const int P = indptr[b + 1] - indptr[b];
-        const int L = (P - 1) * ps + last[b];
+    const int64_t resident = static_cast<int64_t>(num_sms) * ctas_per_sm;
+    // Items of one request for chunk length `cb` pages (0 = whole request).
+    auto chunks_of = [&](int P, int cb) {
         std::vector<std::pair<int, int>> ranges;  // [p0, p1)
         if (d.force_splits > 0) {
             const int n = std::min(d.force_splits, P);
             for (int c = 0; c < n; ++c)
                 ranges.push_back({static_cast<int>(static_cast<int64_t>(P) * c / n),
                                   static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
-        } else if (chunk_pages == 0) {
+            return ranges;
+        }
+        if (cb == 0 || P <= cb) {
             ranges.push_back({0, P});
-        } else {
-            int n = (P + chunk_pages - 1) / chunk_pages;
-            if (d.max_splits > 0) n = std::min(n, d.max_splits);
-            int cb = (P + n - 1) / n;
-            cb = (cb + pps - 1) / pps * pps;
-            for (int p0 = 0; p0 < P; p0 += cb) ranges.push_back({p0, std::min(P, p0 + cb)});
+            return ranges;
         }
-        const int n = static_cast<int>(ranges.size());
-        max_chunks = std::max(max_chunks, n);
-        const int slot_base = n > 1 ? n_slots : -1;
-        if (n > 1) {
-            n_slots += n;
-            ++n_split;
+        int n = (P + cb - 1) / cb;
+        if (d.max_splits > 0) n = std::min(n, d.max_splits);
+        int len = (P + n - 1) / n;
+        len = (len + pps - 1) / pps * pps;
+        for (int p0 = 0; p0 < P; p0 += len) ranges.push_back({p0, std::min(P, p0 + len)});
+        return ranges;
+    };
+    auto build_items = [&](int cb, std::vector<Item>& items, int& n_slots, int& n_split,
+                           int& max_chunks) {
+        items.clear();
+        n_slots = n_split = 0;
+        max_chunks = 1;
+        for (int b = 0; b < B; ++b) {
+            const int P = indptr[b + 1] - indptr[b];
+            const int L = (P - 1) * ps + last[b];
+            const auto ranges = chunks_of(P, cb);
+            const int n = static_cast<int>(ranges.size());
+            max_chunks = std::max(max_chunks, n);
+            const int slot_base = n > 1 ? n_slots : -1;
+            if (n > 1) {
+                n_slots += n;
+                ++n_split;
+            }
+            for (int c = 0; c < n; ++c) {
+                const int p0 = ranges[c].first, p1 = ranges[c].second;
+                Item it;
+                it.idx_begin = indptr[b] + p0;
+                it.n_pages = p1 - p0;
+                it.valid = std::min((p1 - p0) * ps, L - p0 * ps);
+                it.b = b;
+                it.slot = n > 1 ? slot_base + c : -1;
+                it.slot_base = slot_base;
+                it.n_chunks = n;
+                items.push_back(it);
+            }
         }
-        for (int c = 0; c < n; ++c) {
-            const int p0 = ranges[c].first, p1 = ranges[c].second;
-            Item it;
-            it.idx_begin = indptr[b] + p0;
-            it.n_pages = p1 - p0;
-            it.valid = std::min((p1 - p0) * ps, L - p0 * ps);
-            it.b = b;
-            it.slot = n > 1 ? slot_base + c : -1;
-            it.slot_base = slot_base;
-            it.n_chunks = n;
-            items.push_back(it);
+        // Longest items first, so the short tails fill in behind them.
+        std::stable_sort(items.begin(), items.end(),
+                         [](const Item& a, const Item& x) { return a.n_pages > x.n_pages; });
+    };
+    // Simulated completion time (us) of the persistent grid pulling the sorted
+    // units from its queue: each unit streams its KV bytes at the CTA's share
+    // of HBM bandwidth plus a fixed per-unit cost; split units add their
+    // partial write, and the plan pays its merge.
+    auto makespan = [&](const std::vector<Item>& items, int max_chunks) {
+        const double cta_bytes_per_us = kHbmBytesPerUs / static_cast<double>(resident);
+        const int64_t units = static_cast<int64_t>(items.size()) * d.num_kv_heads;
+        const int64_t lanes = std::min<int64_t>(units, resident);
+        std::vector<double> finish(static_cast<size_t>(lanes), 0.0);
+        std::make_heap(finish.begin(), finish.end(), std::greater<double>());
+        for (const Item& it : items) {
+            const double t = it.valid * 512.0 / cta_bytes_per_us + kUnitOverheadUs +
+                             (it.n_chunks > 1 ? kSplitOverheadUs : 0.0);
+            for (int h = 0; h < d.num_kv_heads; ++h) {
+                std::pop_heap(finish.begin(), finish.end(), std::greater<double>());
+                finish.back() += t;
+                std::push_heap(finish.begin(), finish.end(), std::greater<double>());
+            }
         }
+        double end = *std::max_element(finish.begin(), finish.end());
+        const double merge_bytes = static_cast<double>(max_chunks) * G * kHeadDim * 4;
+        if (max_chunks > 1)
+            end += merge_bytes <= kFusedMergeMaxBytes ? merge_bytes / kFusedMergeBytesPerUs
+                                                      : kMergeKernelUs;
+        return end;
+    };
+    std::vector<Item> items;
+    int n_slots = 0, n_split = 0, max_chunks = 1;
+    int chunk_pages = 0;
+    int max_pages = 0;
+    for (int b = 0; b < B; ++b) max_pages = std::max(max_pages, indptr[b + 1] - indptr[b]);
+    if (d.force_splits == 0 && d.max_splits != 1) {
+        // Candidate chunk lengths: whole stages, roughly geometric, up to the
+        // longest request; keep the one with the smallest simulated time
+        // (ties go to the longer chunk, i.e. fewer partial states).
+        std::vector<int> cand;
+        for (double c = pps; c < max_pages + pps; c *= 1.18) {
+            int cb = (static_cast<int>(c) + pps - 1) / pps * pps;
+            if (cand.empty() || cb != cand.back()) cand.push_back(cb);
+        }
+        std::vector<std::pair<int, double>> tried;
+        std::vector<Item> trial;
+        int ns, nsp, mc;
+        for (int cb : cand) {
+            build_items(cb, trial, ns, nsp, mc);
+            // beyond ~64 units per resident CTA the per-unit cost dominates
+            if (static_cast<int64_t>(trial.size()) * d.num_kv_heads > 64 * resident) continue;
+            tried.push_back({cb, makespan(trial, mc)});
+        }
+        int best_cb = max_pages;
+        if (!tried.empty()) {
+            double best = tried[0].second;
+            for (const auto& t : tried) best = std::min(best, t.second);
+            for (const auto& t : tried)
+                if (t.second <= best * 1.01) best_cb = t.first;  // longest near-best chunk
+        }
+        chunk_pages = best_cb >= max_pages ? 0 : best_cb;
     }
-    // Longest items first, so the short tails fill in behind them.
-    std::stable_sort(items.begin(), items.end(),
-                     [](const Item& a, const Item& b) { return a.n_pages > b.n_pages; });
+    build_items(chunk_pages, items, n_slots, n_split, max_chunks);
     const int64_t n_units = static_cast<int64_t>(items.size()) * d.num_kv_heads;
     if (n_units > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
     // Persistent grid: at most the resident CTAs of the device.
-    const int64_t grid = std::min<int64_t>(n_units, static_cast<int64_t>(num_sms) * ctas_per_sm);
+    const int64_t grid = std::min<int64_t>(n_units, resident);
+    // Split requests merge inside the decode kernel when the merge is small;
+    // a large one (many chunks x many heads) goes to a separate merge kernel
+    // that spreads it over every SM instead of one CTA.
+    const bool fused_merge =
+        static_cast<double>(max_chunks) * G * kHeadDim * 4 <= kFusedMergeMaxBytes;
+    std::vector<int4> split_tab;
+    {
+        std::vector<char> seen(static_cast<size_t>(B), 0);
+        for (const Item& it : items)
+            if (it.n_chunks > 1 && !seen[it.b]) {
+                seen[it.b] = 1;
+                split_tab.push_back(make_int4(it.b, it.slot_base, it.n_chunks, 0));
+            }
+        std::sort(split_tab.begin(), split_tab.end(),
+                  [](const int4& a, const int4& x) { return a.x < x.x; });
+    }
 
     // ---- workspace layout
     oxd_plan P = new (std::nothrow) oxd_plan_s();
@@ -317,13 +402,15 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->ctas_per_sm = ctas_per_sm;
     P->num_sms = num_sms;
     P->grid = static_cast<int>(grid);
+    P->fused_merge = fused_merge;
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
     P->off_items = sizeof(WsHeader);
     P->off_req = align_up(P->off_items + 32 * items.size(), 256);
     P->off_counters = align_up(P->off_req + 16 * static_cast<size_t>(B), 256);
-    P->meta_bytes =
+    P->off_split =
         align_up(P->off_counters + 4 * static_cast<size_t>(B) * d.num_kv_heads, 256);
+    P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
     P->off_part_o = P->meta_bytes;
     P->off_part_lse = align_up(
         P->off_part_o + static_cast<size_t>(n_slots) * d.num_qo_heads * kHeadDim * 4, 256);
@@ -354,6 +441,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     int4* rq = reinterpret_cast<int4*>(m + P->off_req);
     for (int b = 0; b < B; ++b) rq[b] = make_int4(indptr[b], indptr[b + 1], last[b], 0);
     // counters stay zero: the upload resets them every run
+    int4* sp = reinterpret_cast<int4*>(m + P->off_split);
+    for (size_t i = 0; i < split_tab.size(); ++i) sp[i] = split_tab[i];
     P->ev_before = nullptr;
     P->ev_after = nullptr;
     {
@@ -378,7 +467,7 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.grid_ctas = plan->grid;
     r.ctas_per_sm = plan->ctas_per_sm;
     r.num_sms = plan->num_sms;
-    r.launches_per_run = 1;
+    r.launches_per_run = (plan->n_split > 0 && !plan->fused_merge) ? 2 : 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.upload_bytes = static_cast<int64_t>(plan->meta_bytes);
     r.total_kv_tokens = plan->total_tokens;
@@ -478,6 +567,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.page_size = d.page_size;
     p.layout = d.layout;
     p.n_units = plan->n_items * d.num_kv_heads;
+    p.fused_merge = plan->fused_merge ? 1 : 0;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
 
@@ -487,6 +577,22 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
+    if (plan->n_split > 0 && !plan->fused_merge) {
+        MergeParams mp{};
+        mp.v = p.part_o;
+        mp.s = p.part_lse;
+        mp.out = p.out;
+        mp.lse = lse;
+        mp.split = reinterpret_cast<const int4*>(ws + plan->off_split);
+        mp.n = plan->n_split;
+        mp.S = 0;
+        mp.H = d.num_qo_heads;
+        mp.D = kHeadDim;
+        mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
+        // With timing events the decode kernel must end before ev_after, so
+        // the merge is then launched without the early-start attribute.
+        if (launch_merge(mp, s, plan->ev_after == nullptr) != cudaSuccess) return OXD_ERR_CUDA;
+    }
     return OXD_OK;
 }
 
@@ -508,11 +614,14 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
     mp.s = s;
     mp.out = static_cast<uint16_t*>(v_out);
     mp.lse = s_out;
+    mp.split = nullptr;
+    mp.s_to_ln = 1.0f;
     mp.n = N;
     mp.S = S;
     mp.H = H;
     mp.D = D;
-    if (launch_merge(mp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return OXD_ERR_CUDA;
+    if (launch_merge(mp, static_cast<cudaStream_t>(stream), false) != cudaSuccess)
+        return OXD_ERR_CUDA;
     return OXD_OK;
 }
 

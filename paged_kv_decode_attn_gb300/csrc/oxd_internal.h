@@ -47,6 +47,8 @@ struct VariantShape {
 //   items        int4[2 * n_items]
 //   req          int4[B]
 //   counters     int32[B * Hkv]   finished items per (request, KV head)
+//   split        int4[n_split]    {b, first slot, slots, 0} per split request
+//                                 (read by the separate merge kernel)
 //   part_o       f32[n_slots][Hq][128]
 //   part_lse     f32[n_slots][Hq]  (log2 domain)
 struct WsHeader {
@@ -79,19 +81,23 @@ struct DecodeParams {
     int32_t page_size;
     int32_t layout;               // 0 NHD, 1 HND
     int32_t n_units;              // n_items * num_kv_heads
+    int32_t fused_merge;          // 1: last unit of a split request merges; 0: merge kernel
     int64_t num_pages;
     float scale_log2;             // sm_scale * log2(e)
 };
 
 struct MergeParams {
-    const float* v;               // states [N][S][H][D]
-    const float* s;               // [N][S][H], natural log
-    uint16_t* out;                // bf16 [N][H][D]
-    float* lse;                   // [N][H] or nullptr
-    int32_t n;
-    int32_t S;
+    const float* v;               // states [.][H][D], state-major
+    const float* s;               // [.][H]
+    uint16_t* out;                // bf16 [rows][H][D]
+    float* lse;                   // [rows][H] natural log, or nullptr
+    const int4* split;            // per merged row {row, first state, count, 0}; nullptr:
+                                  // row n uses states [n*S, n*S + S)
+    int32_t n;                    // rows to merge
+    int32_t S;                    // states per row when split == nullptr
     int32_t H;
     int32_t D;
+    float s_to_ln;                // factor taking s to natural log (1, or ln 2 for log2)
 };
 
 // Implemented in oxd_decode.cu / oxd_merge.cu.
@@ -99,6 +105,8 @@ VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           const DecodeParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+// `after_decode`: launched behind the decode kernel with programmatic
+// dependent launch (the kernel waits for the decode grid before reading).
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool after_decode);
 
 }  // namespace oxd

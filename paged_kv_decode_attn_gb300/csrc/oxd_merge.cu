@@ -30,17 +30,26 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
     if (gw >= static_cast<long long>(p.n) * p.H) return;
     const int n = static_cast<int>(gw / p.H);
     const int h = static_cast<int>(gw - static_cast<long long>(n) * p.H);
-    const int row = n, first = n * p.S, count = p.S;
+    // Behind the decode kernel this waits for its grid to complete and its
+    // writes to be visible; launched on its own it returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int row = n, first = n * p.S, count = p.S;
+    if (p.split != nullptr) {
+        const int4 sr = p.split[n];
+        row = sr.x;
+        first = sr.y;
+        count = sr.z;
+    }
     // pass 1: maximum LSE over the states (lanes stride over them)
     float M = -INFINITY;
     for (int i = lane; i < count; i += 32)
-        M = fmaxf(M, p.s[static_cast<size_t>(first + i) * p.H + h]);
+        M = fmaxf(M, p.s[static_cast<size_t>(first + i) * p.H + h] * p.s_to_ln);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float W = 0.f;
     if (M != -INFINITY) {
         for (int i = lane; i < count; i += 32)
-            W += expf(p.s[static_cast<size_t>(first + i) * p.H + h] - M);
+            W += expf(p.s[static_cast<size_t>(first + i) * p.H + h] * p.s_to_ln - M);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     }
@@ -51,7 +60,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
         if (M != -INFINITY) {
             for (int i = 0; i < count; ++i) {
                 const size_t st = static_cast<size_t>(first + i) * p.H + h;
-                const float w = expf(p.s[st] - M);
+                const float w = expf(p.s[st] * p.s_to_ln - M);
                 const float4 v = *reinterpret_cast<const float4*>(p.v + st * p.D + c);
                 acc.x = fmaf(w, v.x, acc.x);
                 acc.y = fmaf(w, v.y, acc.y);
@@ -70,12 +79,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool after_decode) {
     const long long warps = static_cast<long long>(p.n) * p.H;
     const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    merge_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_decode ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 }  // namespace oxd
