@@ -105,9 +105,10 @@ typedef struct {
     int32_t grid_ctas;          /* persistent decode CTAs launched per run */
     int32_t ctas_per_sm;        /* resident decode CTAs per SM assumed by the planner */
     int32_t num_sms;
-    int32_t launches_per_run;   /* kernels one run enqueues (1: split requests merge in place) */
+    int32_t launches_per_run;   /* kernels one run enqueues: decode, plus merge if split */
     int64_t workspace_bytes;
-    int64_t upload_bytes;       /* host->device bytes one run copies (the work list) */
+    int64_t upload_bytes;       /* host->device bytes one run copies (0: work list fits the
+                                   kernel parameter buffer) */
     int64_t total_kv_tokens;    /* sum_b L_b */
 } oxd_plan_info;
 
@@ -127,9 +128,10 @@ typedef struct {
  *   plan_out           receives the plan; destroy with oxd_plan_destroy
  *   workspace_bytes_out receives the device workspace size run needs
  *
- * The plan keeps a page-locked host copy of the work list; each run copies it
- * to the workspace asynchronously, so the plan must outlive every run that
- * used it until that run's stream work has completed.
+ * A run passes the work list to the kernels in their parameter buffers; a
+ * list too long for them is kept page-locked by the plan and copied to the
+ * workspace asynchronously by each run, so the plan must outlive every run
+ * that used it until that run's stream work has completed.
  * Errors: OXD_ERR_INVALID_ARGUMENT (NULL pointer, non-positive sizes,
  * Hq % Hkv != 0, empty request, last_page_len outside [1, page_size], nonzero
  * reserved fields), OXD_ERR_UNSUPPORTED (head_dim != 128, page_size not in
@@ -159,9 +161,11 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
  *   out           device bf16 [B][Hq][128], 16-byte aligned
  *   lse           device f32 [B][Hq], 4-byte aligned, or NULL
  *   workspace     device scratch of at least the planned size, 256-byte
- *                 aligned; holds the work list, the split partial states and
- *                 the device status word; must not be shared by runs that can
- *                 overlap on the GPU
+ *                 aligned, any contents (the run zeroes its 16-byte header);
+ *                 holds the device status word, the work counter, the split
+ *                 partial states and, for work lists too long for the
+ *                 kernel's parameter buffer, the work list; must not be
+ *                 shared by runs that can overlap on the GPU
  *   stream        cudaStream_t
  *
  * Host-side errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT,
@@ -199,9 +203,10 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. Every call on a device shares the one array,
- * which keeps the last call's contents (each run rewrites the part it reads
- * first, including a zeroed status word): calls that can overlap on the GPU
- * (other streams, other threads) race and must be serialised by the caller.
+ * which keeps the last call's contents; each call first zeroes what must
+ * start at zero (the status word and the work counter) and writes everything
+ * else it reads. Calls that can overlap on the GPU (other streams, other
+ * threads) race on the array and must be serialised by the caller.
  * The device status word lives in that array, so oxd_read_device_status
  * cannot be used with this entry point.
  */
@@ -249,8 +254,9 @@ oxd_status oxd_plan_set_timing_events(oxd_plan plan, void* event_before, void* e
 oxd_status oxd_plan_destroy(oxd_plan plan);
 
 /*
- * Synchronise `stream`, then read the device status word of `workspace` (the
- * one the last run on that workspace wrote) into *code. Returns OXD_OK when
+ * Synchronise `stream`, then read into *code the device status word of
+ * `workspace`, i.e. the first error of the last run on it (OXD_DEVICE_OK if
+ * it recorded none). Returns OXD_OK when
  * the code is OXD_DEVICE_OK, OXD_ERR_DEVICE_STATUS otherwise, OXD_ERR_CUDA if
  * the copy failed. This is the one call that blocks the host.
  */

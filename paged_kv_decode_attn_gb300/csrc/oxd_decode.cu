@@ -7,7 +7,7 @@
 // "Single decode split-K" row.
 //
 // Persistent, warp-specialised CTAs (a few per SM) pull work units -- one
-// run of consecutive pages of one request for one KV head -- from an atomic
+// run of consecutive pages of one request for one KV head -- from a shared
 // queue (units are ordered longest first by the planner):
 //   * the producer warp claims the next unit while the current one is still
 //     streaming, reads its page indices 32 at a time (coalesced), checks them
@@ -24,12 +24,14 @@
 //     products run on CUDA cores;
 //   * after a unit's last stage the consumers merge their states through the
 //     stage's own buffer and write the bf16 output and LSE, or, for a split
-//     request, an F32 partial state; the last unit of a split request to
-//     finish (atomic counter) merges the partials in order and writes the
-//     output, so a run is one kernel launch.
-// Every wait (mbarriers, including the consumer-only barrier) gives up after
-// about one second: it records OXD_DEVICE_WAIT_TIMEOUT, all warps leave, the
-// copies already issued are drained, and the CTA returns.
+//     request, an F32 partial state that the merge kernel (launched right
+//     behind this one) combines.
+// The work list travels in the kernel's parameter buffer when it fits; each
+// run zeroes only the status word and the work counter before the kernel.
+// Every mbarrier wait gives up after about one second:
+// it records OXD_DEVICE_WAIT_TIMEOUT, all warps leave (the consumer warps
+// decide together through a barrier reduction, so no named barrier can be
+// left waiting), the copies already issued are drained, and the CTA returns.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -176,8 +178,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// First error of a run wins (the run zeroes the word before the kernel).
 __device__ __forceinline__ void record_status(int32_t* status, int code) {
     atomicCAS(status, 0, code);
+}
+
+// Named barrier 1 among the consumer warps (the producer warp never uses it).
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("barrier.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Same barrier, returning the AND of every participant's `v`.
+__device__ __forceinline__ bool consumer_all(int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 
@@ -231,11 +253,11 @@ struct Cfg {
     static constexpr int kQRows = kMma ? (kHiRows ? 16 * kMtiles : 8) : kFmaGroup;
     static constexpr int kQBytes = kQRows * kHeadDim * 2;
     static_assert(kSlices * 16 * kHeadDim * 4 <= kStageBytes, "epilogue scratch fits a stage");
-    // ring | q[kStages] | rec[kStages] | full, empty, cbar | issued | flags | red_m | red_l
+    // ring | q[kStages] | rec[kStages] | full, empty | issued | flags | red_m | red_l
     static constexpr int kQOffset = kStages * kStageBytes;
     static constexpr int kRecOffset = kQOffset + kStages * kQBytes;
     static constexpr int kBarOffset = kRecOffset + kStages * 32;
-    static constexpr int kIssuedOffset = kBarOffset + (2 * kStages + 1) * 8;
+    static constexpr int kIssuedOffset = kBarOffset + 2 * kStages * 8;
     static constexpr int kFlagOffset = kIssuedOffset + kStages * 4;
     static constexpr int kRedOffset = kFlagOffset + 16;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRedOffset +
@@ -250,7 +272,7 @@ using CfgMma32 = Cfg<2, true, 4, 4, true, 0>;
 
 // What the producer tells the consumers about each stage it fills.
 struct StageRec {
-    int b, hkv, valid, n_stages, s, slot, slot_base, n_chunks;
+    int b, hkv, valid, n_stages, s, slot, pad0, pad1;
 };
 
 // ------------------------------------------------------------------ consumers
@@ -548,9 +570,6 @@ struct Smem {
     __device__ __forceinline__ uint64_t* empty(int slot) const {
         return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + C::kStages + slot;
     }
-    __device__ __forceinline__ uint64_t* cbar() const {
-        return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + 2 * C::kStages;
-    }
     __device__ __forceinline__ int* issued() const {
         return reinterpret_cast<int*>(base + C::kIssuedOffset);
     }
@@ -565,30 +584,18 @@ struct Smem {
     }
 };
 
-// Barrier among the consumer warps only (the producer keeps streaming), built
-// on an mbarrier so that it can give up like every other wait.
-struct ConsumerBarrier {
-    uint64_t* bar;
-    uint32_t parity;
-    __device__ __forceinline__ bool sync(int lane, const volatile int* abort) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar);
-        const bool ok = mbar_wait(bar, parity, abort);
-        parity ^= 1u;
-        return __all_sync(0xffffffffu, ok);
-    }
-};
-
 // ------------------------------------------------------------------ the kernel
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ DecodeParams p,
+                        const __grid_constant__ InlineWork inline_work) {
     extern __shared__ uint8_t smem_raw[];
     const Smem<C> sm{reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))};
-    volatile int* flags = sm.flags();  // [0] abort, [1] "last unit of its request"
+    volatile int* flags = sm.flags();  // [0] abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = p.page_size;
@@ -596,6 +603,8 @@ __global__ void __launch_bounds__(C::kThreads)
     const int half_bytes = ps * 128;
     const int pages_per_stage = C::kStageTokens / ps;
     const int G = p.group;
+    // The work list sits in the parameter buffer unless it was too long.
+    const WorkItem* items = p.items != nullptr ? p.items : inline_work.item;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -603,17 +612,15 @@ __global__ void __launch_bounds__(C::kThreads)
             mbar_init(sm.empty(s), C::kConsumerWarps);
             sm.issued()[s] = 0;
         }
-        mbar_init(sm.cbar(), C::kConsumerWarps);
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
     }
     if (warp == C::kConsumerWarps && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
-    // A separate merge kernel, when the plan uses one, may be scheduled now;
-    // it waits for this grid to complete before it reads anything.
+    // The merge kernel, when the plan has one, may be scheduled now; it waits
+    // for this grid to complete before it reads anything.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
@@ -621,63 +628,57 @@ __global__ void __launch_bounds__(C::kThreads)
 
     if (warp == C::kConsumerWarps) {
         // ================================================ producer warp
-        // The next unit is claimed as soon as the current one starts; its
-        // work-list entry is read after the current unit's first stage is
-        // issued and its first page indices after the second, so these
-        // dependent loads overlap the current unit's streaming.
+        // Each CTA starts on unit blockIdx.x; later units are claimed from the
+        // shared counter as soon as the current unit starts, the next unit's
+        // work item is read after the current unit's first stage is issued and
+        // its first page indices after the second, so these dependent loads
+        // overlap the current unit's streaming.
         struct Unit {
             int unit;
-            int4 A, Bm;
+            WorkItem it;
             int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
         };
         auto load_item = [&](Unit& u) {
-            if (u.unit < p.n_units) {
-                const int item = u.unit / p.num_kv_heads;
-                u.A = p.items[2 * item];
-                u.Bm = p.items[2 * item + 1];
-            }
+            if (u.unit >= 0 && u.unit < p.n_units) u.it = items[u.unit / p.num_kv_heads];
         };
         auto load_idx = [&](Unit& u) {
             u.win = u.nxt = 0;
-            if (u.unit < p.n_units) {
-                const int32_t* idx = p.indices + u.A.x;
-                if (lane < u.A.y) u.win = __ldg(idx + lane);
-                if (32 + lane < u.A.y) u.nxt = __ldg(idx + 32 + lane);
+            if (u.unit >= 0 && u.unit < p.n_units) {
+                const int32_t* idx = p.indices + u.it.idx_begin;
+                if (lane < u.it.n_pages) u.win = __ldg(idx + lane);
+                if (32 + lane < u.it.n_pages) u.nxt = __ldg(idx + 32 + lane);
             }
         };
+        auto valid_unit = [&](int u) { return u >= 0 && u < p.n_units; };
         int g = 0;  // ring position
         bool ok = true;
         Unit cur;
-        cur.unit = 0;
-        if (lane == 0) cur.unit = atomicAdd(p.work_counter, 1);
-        cur.unit = __shfl_sync(0xffffffffu, cur.unit, 0);
+        cur.unit = blockIdx.x;
         load_item(cur);
         load_idx(cur);
-        while (cur.unit < p.n_units) {
+        while (valid_unit(cur.unit)) {
             Unit nx;
             nx.unit = 0;
-            if (lane == 0) nx.unit = atomicAdd(p.work_counter, 1);
+            if (lane == 0) nx.unit = static_cast<int>(gridDim.x) + atomicAdd(p.work_counter, 1);
             bool nx_item = false, nx_idx = false;
             const int hkv = cur.unit - (cur.unit / p.num_kv_heads) * p.num_kv_heads;
-            const int4 A = cur.A;
-            const int4 Bm = cur.Bm;
-            const int b = A.w, n_pages = A.y;
+            const WorkItem it = cur.it;
+            const int b = it.b, n_pages = it.n_pages;
             const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
-            int4 rq = make_int4(0, 0, 0, 0);
             int ip0 = 0, ip1 = 0, lst = 0;
             if (lane == 0) {
-                rq = p.req[b];
                 ip0 = p.indptr[b];
                 ip1 = p.indptr[b + 1];
                 lst = p.last_page_len[b];
             }
             // An index outside [0, num_pages) is recorded and replaced by page
             // 0, so every copy stays inside the pool.
-            const int32_t* idx = p.indices + A.x;
+            const int32_t* idx = p.indices + it.idx_begin;
             int win = cur.win, nxt = cur.nxt;
             int win_base = 0;
             bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
-            if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(p.status, kDeviceBadPage);
+            if (__any_sync(0xffffffffu, bad) && lane == 0)
+                record_status(p.status, kDeviceBadPage);
             win = bad ? 0 : win;
             for (int s = 0; s < n_stages; ++s, ++g) {
                 const int slot = g % C::kStages;
@@ -703,12 +704,10 @@ __global__ void __launch_bounds__(C::kThreads)
                     StageRec* r = sm.rec(slot);
                     r->b = b;
                     r->hkv = hkv;
-                    r->valid = A.z;
+                    r->valid = it.valid;
                     r->n_stages = n_stages;
                     r->s = s;
-                    r->slot = Bm.x;
-                    r->slot_base = Bm.y;
-                    r->n_chunks = Bm.z;
+                    r->slot = it.slot;
                     const uint32_t qbytes = s == 0 ? static_cast<uint32_t>(G * kHeadDim * 2) : 0u;
                     mbar_arrive_expect_tx(sm.full(slot), npg * ps * kHeadDim * 2 * 2 + qbytes);
                     if (s == 0)
@@ -749,7 +748,7 @@ __global__ void __launch_bounds__(C::kThreads)
                 load_item(nx);
             }
             if (!nx_idx) load_idx(nx);
-            if (lane == 0 && (ip0 != rq.x || ip1 != rq.y || lst != rq.z))
+            if (lane == 0 && (ip0 != it.indptr_b || ip1 != it.indptr_b1 || lst != it.last))
                 record_status(p.status, kDevicePlanMismatch);
             cur = nx;
         }
@@ -775,15 +774,18 @@ __global__ void __launch_bounds__(C::kThreads)
         }
     } else {
         // ================================================ consumer warps
+        // Every consumer-only barrier is named barrier 1. The consumer warps
+        // always take the same path through it: each stage's wait result is
+        // AND-reduced over all of them before anyone acts on it.
         Consumer cs;
         const int slice = warp % C::kSlices;
         const int mt = warp / C::kSlices;
         const int ctid = threadIdx.x;  // 0 .. kConsumerThreads-1
-        ConsumerBarrier cbar{sm.cbar(), 0u};
         bool ok = true;
         for (int g = 0;; ++g) {
             const int slot = g % C::kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(sm.full(slot), (g / C::kStages) & 1, flags))) {
+            const bool got = mbar_wait(sm.full(slot), (g / C::kStages) & 1, flags);
+            if (!consumer_all(C::kConsumerThreads, got)) {
                 ok = false;
                 break;
             }
@@ -803,11 +805,11 @@ __global__ void __launch_bounds__(C::kThreads)
                 float* dump = sm.dump(slot);
                 float* red_m = sm.red_m();
                 float* red_l = sm.red_l();
-                ok = cbar.sync(lane, flags);  // every warp is done reading K/V here
+                consumer_sync(C::kConsumerThreads);  // every warp is done reading K/V here
                 const int hq0 = r.hkv * G;
-                for (int round = 0; ok && round < C::kMtiles; ++round) {
+                for (int round = 0; round < C::kMtiles; ++round) {
                     if (mt == round) cs.dump(red_m, red_l, dump, slice, lane);
-                    if (!(ok = cbar.sync(lane, flags))) break;
+                    consumer_sync(C::kConsumerThreads);
                     const int rows = min(16, G - round * 16);
                     for (int i = ctid; i < rows * (kHeadDim / 4); i += C::kConsumerThreads) {
                         const int rr = i / (kHeadDim / 4);
@@ -853,66 +855,8 @@ __global__ void __launch_bounds__(C::kThreads)
                             if (d4 == 0) p.part_lse[row] = lse2;
                         }
                     }
-                    ok = cbar.sync(lane, flags);  // dump reads done before reuse
+                    consumer_sync(C::kConsumerThreads);  // dump reads done before reuse
                 }
-                if (ok && r.slot >= 0 && p.fused_merge) {
-                    // ---- split request: the last of its items to finish merges.
-                    // The consumer barrier orders every thread's partial writes
-                    // before one thread's device-scope fence and count.
-                    if (ctid == 0) {
-                        __threadfence();
-                        const int done =
-                            atomicAdd(p.counters + r.b * p.num_kv_heads + r.hkv, 1) + 1;
-                        __threadfence();
-                        flags[1] = done == r.n_chunks ? 1 : 0;
-                    }
-                    if (!(ok = cbar.sync(lane, flags))) break;
-                    if (flags[1]) {
-                        // Partials of other CTAs: read through L2 (ld.global.cg),
-                        // in slot order; the loads are independent, so many are in
-                        // flight at once.
-                        for (int i = ctid; i < G * (kHeadDim / 4); i += C::kConsumerThreads) {
-                            const int rr = i / (kHeadDim / 4);
-                            const int d4 = i - rr * (kHeadDim / 4);
-                            const int hq = hq0 + rr;
-                            const float* lse_c =
-                                p.part_lse + static_cast<size_t>(r.slot_base) * p.num_qo_heads + hq;
-                            const float4* o_c = reinterpret_cast<const float4*>(
-                                p.part_o +
-                                (static_cast<size_t>(r.slot_base) * p.num_qo_heads + hq) *
-                                    kHeadDim) + d4;
-                            const size_t lse_stride = p.num_qo_heads;
-                            const size_t o_stride = static_cast<size_t>(p.num_qo_heads) * 32;
-                            float M = -INFINITY;
-#pragma unroll 8
-                            for (int c = 0; c < r.n_chunks; ++c)
-                                M = fmaxf(M, __ldcg(lse_c + c * lse_stride));
-                            float W = 0.f;
-                            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (M != -INFINITY) {
-#pragma unroll 4
-                                for (int c = 0; c < r.n_chunks; ++c) {
-                                    const float w = fast_exp2(__ldcg(lse_c + c * lse_stride) - M);
-                                    const float4 v = __ldcg(o_c + c * o_stride);
-                                    W += w;
-                                    o.x = fmaf(w, v.x, o.x);
-                                    o.y = fmaf(w, v.y, o.y);
-                                    o.z = fmaf(w, v.z, o.z);
-                                    o.w = fmaf(w, v.w, o.w);
-                                }
-                            }
-                            const float inv = W > 0.f ? 1.f / W : 0.f;
-                            const size_t row = static_cast<size_t>(r.b) * p.num_qo_heads + hq;
-                            uint2 packed;
-                            packed.x = pack_bf16x2(o.x * inv, o.y * inv);
-                            packed.y = pack_bf16x2(o.z * inv, o.w * inv);
-                            *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
-                            if (d4 == 0 && p.lse != nullptr)
-                                p.lse[row] = W > 0.f ? (M + __log2f(W)) * kLn2 : -INFINITY;
-                        }
-                    }
-                }
-                if (!ok) break;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(sm.empty(slot));
@@ -947,11 +891,11 @@ cudaError_t ensure_smem_attribute() {
 }
 
 template <class C>
-cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                   const InlineWork& w, int grid, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attribute<C>();
     if (e != cudaSuccess) return e;
-    paged_decode_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
+    paged_decode_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p, w);
     return cudaGetLastError();
 }
 
@@ -991,13 +935,14 @@ cudaError_t variant_occupancy(int variant, int* n) {
 }
 
 cudaError_t launch_decode(int variant, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, int grid, cudaStream_t stream) {
+                          const DecodeParams& p, const InlineWork& w, int grid,
+                          cudaStream_t stream) {
     switch (variant) {
-        case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, grid, stream);
-        case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, grid, stream);
-        case kVariantMma8: return launch<CfgMma8>(tk, tv, p, grid, stream);
-        case kVariantMma16: return launch<CfgMma16>(tk, tv, p, grid, stream);
-        default: return launch<CfgMma32>(tk, tv, p, grid, stream);
+        case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, w, grid, stream);
+        case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, w, grid, stream);
+        case kVariantMma8: return launch<CfgMma8>(tk, tv, p, w, grid, stream);
+        case kVariantMma16: return launch<CfgMma16>(tk, tv, p, w, grid, stream);
+        default: return launch<CfgMma32>(tk, tv, p, w, grid, stream);
     }
 }
 

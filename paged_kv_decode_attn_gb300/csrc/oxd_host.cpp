@@ -3,14 +3,16 @@
 // Lifecycle from the "Oxide Infer" README, "One execution model": the plan
 // fixes the kernel variant, the chunking of every request's pages, the launch
 // shape and the workspace contract; a run only checks operands and enqueues
-// one host-to-device copy of the work list (which also zeroes the status word
-// and the counters) and one decode launch, which merges small splits itself;
-// large splits get a merge launch right behind it. "Providers": checked span, alignment, alias and capacity rules;
+// a 16-byte memset of the workspace header (status word, work counter), the
+// decode kernel, whose work list rides in its parameter buffer (long lists
+// are copied into the workspace first), and, when some request was split, a
+// merge kernel launched right behind it. "Providers": checked span, alignment, alias and capacity rules;
 // explicit workspace; caller stream; typed device status.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <functional>
 #include <cmath>
 #include <cstdlib>
@@ -41,9 +43,11 @@ struct oxd_plan_s {
     int64_t nnz;
     int64_t total_tokens;
     int grid;
-    bool fused_merge;
-    size_t off_items, off_req, off_counters, off_split, off_part_o, off_part_lse;
+    bool upload;  // work list or split table too long for the parameter buffers
+    size_t off_items, off_split, off_part_o, off_part_lse;
     size_t meta_bytes, ws_bytes;
+    InlineWork* inline_work;
+    InlineSplits* inline_splits;
     void* meta;
     bool pinned;
     cudaEvent_t ev_before;
@@ -56,9 +60,7 @@ namespace {
 constexpr double kHbmBytesPerUs = 6.8e6;
 constexpr double kUnitOverheadUs = 1.0;       // prologue/epilogue not hidden by prefetch
 constexpr double kSplitOverheadUs = 0.5;      // partial write + counter
-constexpr double kFusedMergeMaxBytes = 64.0 * 1024;  // largest merge done inside the kernel
-constexpr double kFusedMergeBytesPerUs = 2.0e4;      // one CTA reading partials from L2
-constexpr double kMergeKernelUs = 3.0;        // a separate merge launch behind the decode
+constexpr double kMergeKernelUs = 2.0;        // the merge launch behind the decode
 
 std::mutex g_plans_mu;
 std::unordered_set<oxd_plan> g_plans;
@@ -179,7 +181,7 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
 }
 
 struct Item {
-    int idx_begin, n_pages, valid, b, slot, slot_base, n_chunks;
+    int idx_begin, n_pages, valid, b, slot, slot_base, n_chunks;  // host-side view
 };
 
 }  // namespace
@@ -327,10 +329,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             }
         }
         double end = *std::max_element(finish.begin(), finish.end());
-        const double merge_bytes = static_cast<double>(max_chunks) * G * kHeadDim * 4;
-        if (max_chunks > 1)
-            end += merge_bytes <= kFusedMergeMaxBytes ? merge_bytes / kFusedMergeBytesPerUs
-                                                      : kMergeKernelUs;
+        if (max_chunks > 1) end += kMergeKernelUs;
         return end;
     };
     std::vector<Item> items;
@@ -370,11 +369,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     if (n_units > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
     // Persistent grid: at most the resident CTAs of the device.
     const int64_t grid = std::min<int64_t>(n_units, resident);
-    // Split requests merge inside the decode kernel when the merge is small;
-    // a large one (many chunks x many heads) goes to a separate merge kernel
-    // that spreads it over every SM instead of one CTA.
-    const bool fused_merge =
-        static_cast<double>(max_chunks) * G * kHeadDim * 4 <= kFusedMergeMaxBytes;
+    // Split requests are merged by a kernel behind the decode that spreads the
+    // merge over every SM.
     std::vector<int4> split_tab;
     {
         std::vector<char> seen(static_cast<size_t>(B), 0);
@@ -402,14 +398,12 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->ctas_per_sm = ctas_per_sm;
     P->num_sms = num_sms;
     P->grid = static_cast<int>(grid);
-    P->fused_merge = fused_merge;
+    P->upload = static_cast<int>(items.size()) > kInlineItems ||
+                static_cast<int>(split_tab.size()) > kInlineSplits;
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
     P->off_items = sizeof(WsHeader);
-    P->off_req = align_up(P->off_items + 32 * items.size(), 256);
-    P->off_counters = align_up(P->off_req + 16 * static_cast<size_t>(B), 256);
-    P->off_split =
-        align_up(P->off_counters + 4 * static_cast<size_t>(B) * d.num_kv_heads, 256);
+    P->off_split = align_up(P->off_items + sizeof(WorkItem) * items.size(), 256);
     P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
     P->off_part_o = P->meta_bytes;
     P->off_part_lse = align_up(
@@ -417,32 +411,44 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->ws_bytes =
         align_up(P->off_part_lse + static_cast<size_t>(n_slots) * d.num_qo_heads * 4, 256);
 
-    P->pinned = cudaHostAlloc(&P->meta, P->meta_bytes, cudaHostAllocDefault) == cudaSuccess;
-    if (!P->pinned) {
-        cudaGetLastError();  // a host-only plan on a machine without a GPU lands here
-        P->meta = std::malloc(P->meta_bytes);
+    P->inline_work = new (std::nothrow) InlineWork();
+    P->inline_splits = new (std::nothrow) InlineSplits();
+    P->meta = nullptr;
+    P->pinned = false;
+    if (P->inline_work == nullptr || P->inline_splits == nullptr) {
+        delete P->inline_work;
+        delete P->inline_splits;
+        delete P;
+        return OXD_ERR_NO_MEMORY;
+    }
+    std::vector<WorkItem> wl(items.size());
+    for (size_t i = 0; i < items.size(); ++i) {
+        const Item& it = items[i];
+        wl[i] = WorkItem{it.idx_begin, it.n_pages, it.valid, it.b, it.slot, indptr[it.b],
+                         indptr[it.b + 1], last[it.b]};
+    }
+    if (!P->upload) {
+        std::copy(wl.begin(), wl.end(), P->inline_work->item);
+        std::copy(split_tab.begin(), split_tab.end(), P->inline_splits->split);
+    } else {
+        // Too long for the parameter buffers: a page-locked copy is uploaded
+        // into the workspace by every run.
+        P->pinned = cudaHostAlloc(&P->meta, P->meta_bytes, cudaHostAllocDefault) == cudaSuccess;
+        if (!P->pinned) {
+            cudaGetLastError();  // a host-only plan on a machine without a GPU lands here
+            P->meta = std::malloc(P->meta_bytes);
+        }
         if (P->meta == nullptr) {
+            delete P->inline_work;
+            delete P->inline_splits;
             delete P;
             return OXD_ERR_NO_MEMORY;
         }
+        uint8_t* m = static_cast<uint8_t*>(P->meta);
+        std::memset(m, 0, P->meta_bytes);
+        std::memcpy(m + P->off_items, wl.data(), sizeof(WorkItem) * wl.size());
+        std::memcpy(m + P->off_split, split_tab.data(), 16 * split_tab.size());
     }
-    uint8_t* m = static_cast<uint8_t*>(P->meta);
-    std::memset(m, 0, P->meta_bytes);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(m);
-    hdr->status = 0;
-    hdr->n_items = P->n_items;
-    hdr->batch = B;
-    hdr->num_kv_heads = d.num_kv_heads;
-    int4* it4 = reinterpret_cast<int4*>(m + P->off_items);
-    for (size_t i = 0; i < items.size(); ++i) {
-        it4[2 * i] = make_int4(items[i].idx_begin, items[i].n_pages, items[i].valid, items[i].b);
-        it4[2 * i + 1] = make_int4(items[i].slot, items[i].slot_base, items[i].n_chunks, 0);
-    }
-    int4* rq = reinterpret_cast<int4*>(m + P->off_req);
-    for (int b = 0; b < B; ++b) rq[b] = make_int4(indptr[b], indptr[b + 1], last[b], 0);
-    // counters stay zero: the upload resets them every run
-    int4* sp = reinterpret_cast<int4*>(m + P->off_split);
-    for (size_t i = 0; i < split_tab.size(); ++i) sp[i] = split_tab[i];
     P->ev_before = nullptr;
     P->ev_after = nullptr;
     {
@@ -467,9 +473,10 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.grid_ctas = plan->grid;
     r.ctas_per_sm = plan->ctas_per_sm;
     r.num_sms = plan->num_sms;
-    r.launches_per_run = (plan->n_split > 0 && !plan->fused_merge) ? 2 : 1;
+    r.launches_per_run = plan->n_split > 0 ? 2 : 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
-    r.upload_bytes = static_cast<int64_t>(plan->meta_bytes);
+    r.upload_bytes =
+        plan->upload ? static_cast<int64_t>(plan->meta_bytes - plan->off_items) : 0;
     r.total_kv_tokens = plan->total_tokens;
     *info = r;
     return OXD_OK;
@@ -493,6 +500,8 @@ oxd_status oxd_plan_destroy(oxd_plan plan) {
         cudaFreeHost(plan->meta);
     else
         std::free(plan->meta);
+    delete plan->inline_work;
+    delete plan->inline_splits;
     delete plan;
     return OXD_OK;
 }
@@ -543,8 +552,12 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if (cudaMemcpyAsync(ws, plan->meta, plan->meta_bytes, cudaMemcpyHostToDevice, s) !=
-        cudaSuccess)
+    // The status word and the work counter start every run at zero.
+    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return OXD_ERR_CUDA;
+    if (plan->upload &&
+        cudaMemcpyAsync(ws + plan->off_items, static_cast<uint8_t*>(plan->meta) + plan->off_items,
+                        plan->meta_bytes - plan->off_items, cudaMemcpyHostToDevice,
+                        s) != cudaSuccess)
         return OXD_ERR_CUDA;
 
     DecodeParams p{};
@@ -554,36 +567,35 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.indptr = indptr;
     p.indices = indices;
     p.last_page_len = last_page_len;
-    p.items = reinterpret_cast<const int4*>(ws + plan->off_items);
-    p.req = reinterpret_cast<const int4*>(ws + plan->off_req);
-    p.counters = reinterpret_cast<int32_t*>(ws + plan->off_counters);
-    p.work_counter = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, work_counter));
+    p.items = plan->upload ? reinterpret_cast<const WorkItem*>(ws + plan->off_items) : nullptr;
     p.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
     p.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
-    p.status = reinterpret_cast<int32_t*>(ws);
+    p.status = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, status));
+    p.work_counter = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, work_counter));
     p.num_qo_heads = d.num_qo_heads;
     p.num_kv_heads = d.num_kv_heads;
     p.group = plan->group;
     p.page_size = d.page_size;
     p.layout = d.layout;
     p.n_units = plan->n_items * d.num_kv_heads;
-    p.fused_merge = plan->fused_merge ? 1 : 0;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_decode(plan->variant, tk, tv, p, plan->grid, s) != cudaSuccess)
+    if (launch_decode(plan->variant, tk, tv, p, *plan->inline_work, plan->grid, s) !=
+        cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (plan->n_split > 0 && !plan->fused_merge) {
+    if (plan->n_split > 0) {
         MergeParams mp{};
         mp.v = p.part_o;
         mp.s = p.part_lse;
         mp.out = p.out;
         mp.lse = lse;
-        mp.split = reinterpret_cast<const int4*>(ws + plan->off_split);
+        mp.split = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_split) : nullptr;
+        mp.split_mode = 1;
         mp.n = plan->n_split;
         mp.S = 0;
         mp.H = d.num_qo_heads;
@@ -591,7 +603,9 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
         // With timing events the decode kernel must end before ev_after, so
         // the merge is then launched without the early-start attribute.
-        if (launch_merge(mp, s, plan->ev_after == nullptr) != cudaSuccess) return OXD_ERR_CUDA;
+        if (launch_split_merge(mp, *plan->inline_splits, s, plan->ev_after == nullptr) !=
+            cudaSuccess)
+            return OXD_ERR_CUDA;
     }
     return OXD_OK;
 }
@@ -615,18 +629,20 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
     mp.out = static_cast<uint16_t*>(v_out);
     mp.lse = s_out;
     mp.split = nullptr;
+    mp.split_mode = 0;
     mp.s_to_ln = 1.0f;
     mp.n = N;
     mp.S = S;
     mp.H = H;
     mp.D = D;
-    if (launch_merge(mp, static_cast<cudaStream_t>(stream), false) != cudaSuccess)
+    if (launch_merge(mp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OXD_ERR_CUDA;
     return OXD_OK;
 }
 
 oxd_status oxd_read_device_status(const void* workspace, void* stream, int32_t* code) {
     if (workspace == nullptr || code == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256)) return OXD_ERR_ALIGNMENT;
     int32_t c = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(&c, workspace, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)

@@ -30,34 +30,46 @@ struct VariantShape {
     int smem_bytes;     // dynamic shared memory per CTA
 };
 
-// Work list, two int4 per item (one item = consecutive pages of one request,
-// processed once per KV head):
-//   A: x = absolute offset of the item's first page in `indices`,
-//      y = pages in the item, z = valid tokens in the item, w = request b
-//   B: x = partial-state slot of this item or -1 when the item covers its
-//      whole request (then it writes out/lse directly), y = first slot of the
-//      request's items, z = number of items of the request, w = 0
-// Per-request table (int4): x = indptr[b], y = indptr[b+1], z = last_page_len[b]
-// as planned (the kernel compares them with the device block tables), w = 0.
-//
-// Workspace layout (byte offsets, each 256-aligned); everything before
-// part_o is written by the run's single host-to-device copy, which also
-// zeroes the status word and all counters:
-//   [0, 256)     header: int32 status word, int32 work counter
-//   items        int4[2 * n_items]
-//   req          int4[B]
-//   counters     int32[B * Hkv]   finished items per (request, KV head)
-//   split        int4[n_split]    {b, first slot, slots, 0} per split request
-//                                 (read by the separate merge kernel)
+// One work item: consecutive pages of one request, processed once per KV
+// head (a work unit is an (item, KV head) pair; unit u = item u / Hkv, head
+// u % Hkv). The planned indptr/last_page_len of the request ride along so the
+// kernel can check the device block tables against the plan.
+struct WorkItem {
+    int32_t idx_begin;   // absolute offset of the item's first page in `indices`
+    int32_t n_pages;
+    int32_t valid;       // valid tokens in the item (the last page may be partial)
+    int32_t b;           // request
+    int32_t slot;        // partial-state slot, or -1: the item is its whole request
+    int32_t indptr_b;    // planned indptr[b], indptr[b+1], last_page_len[b]
+    int32_t indptr_b1;
+    int32_t last;
+};
+static_assert(sizeof(WorkItem) == 32, "work item is 32 bytes");
+
+// Work lists up to this length travel in the decode kernel's parameter
+// buffer; longer ones are copied into the workspace.
+constexpr int kInlineItems = 448;
+struct InlineWork {
+    WorkItem item[kInlineItems];
+};
+
+// Split requests, {b, first slot, slots, 0}; same rule for the merge kernel.
+constexpr int kInlineSplits = 1024;
+struct InlineSplits {
+    int4 split[kInlineSplits];
+};
+
+// Workspace layout (byte offsets, each 256-aligned):
+//   [0, 256)     header: int32 status word, int32 work counter (the run
+//                zeroes both with a 16-byte memset before the decode kernel)
+//   items        WorkItem[n_items]   (written by the run only when too long
+//   split        int4[n_split]        for the parameter buffers)
 //   part_o       f32[n_slots][Hq][128]
 //   part_lse     f32[n_slots][Hq]  (log2 domain)
 struct WsHeader {
     int32_t status;
     int32_t work_counter;
-    int32_t n_items;
-    int32_t batch;
-    int32_t num_kv_heads;
-    int32_t pad[59];
+    int32_t pad[62];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -68,9 +80,7 @@ struct DecodeParams {
     const int32_t* indptr;
     const int32_t* indices;
     const int32_t* last_page_len;
-    const int4* items;
-    const int4* req;
-    int32_t* counters;
+    const WorkItem* items;        // nullptr: the work list is the InlineWork parameter
     float* part_o;
     float* part_lse;
     int32_t* status;
@@ -81,7 +91,6 @@ struct DecodeParams {
     int32_t page_size;
     int32_t layout;               // 0 NHD, 1 HND
     int32_t n_units;              // n_items * num_kv_heads
-    int32_t fused_merge;          // 1: last unit of a split request merges; 0: merge kernel
     int64_t num_pages;
     float scale_log2;             // sm_scale * log2(e)
 };
@@ -91,10 +100,11 @@ struct MergeParams {
     const float* s;               // [.][H]
     uint16_t* out;                // bf16 [rows][H][D]
     float* lse;                   // [rows][H] natural log, or nullptr
-    const int4* split;            // per merged row {row, first state, count, 0}; nullptr:
-                                  // row n uses states [n*S, n*S + S)
+    const int4* split;            // split table in memory; nullptr: inline (split mode)
+    int32_t split_mode;           // 1: row n is split[n] = {row, first state, count, 0};
+                                  // 0: row n uses states [n*S, n*S + S)
     int32_t n;                    // rows to merge
-    int32_t S;                    // states per row when split == nullptr
+    int32_t S;                    // states per row when split_mode == 0
     int32_t H;
     int32_t D;
     float s_to_ln;                // factor taking s to natural log (1, or ln 2 for log2)
@@ -104,9 +114,14 @@ struct MergeParams {
 VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                          const DecodeParams& p, int grid, cudaStream_t stream);
-// `after_decode`: launched behind the decode kernel with programmatic
-// dependent launch (the kernel waits for the decode grid before reading).
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool after_decode);
+                          const DecodeParams& p, const InlineWork& work, int grid,
+                          cudaStream_t stream);
+// Uniform-state merge (the public entry point).
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+// Merge of the split requests of a decode run, launched behind the decode
+// kernel with programmatic dependent launch when `early` (it waits for the
+// decode grid before reading anything).
+cudaError_t launch_split_merge(const MergeParams& p, const InlineSplits& splits,
+                               cudaStream_t stream, bool early);
 
 }  // namespace oxd

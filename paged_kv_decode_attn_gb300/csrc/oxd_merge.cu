@@ -24,18 +24,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void merge_rows(const MergeParams& p, const int4* split);
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {
+    merge_rows(p, nullptr);
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    split_merge_kernel(const MergeParams p, const __grid_constant__ InlineSplits inl) {
+    // Behind the decode kernel this waits for its grid to complete and its
+    // writes to be visible; launched on its own it returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    merge_rows(p, p.split != nullptr ? p.split : inl.split);
+}
+
+__device__ __forceinline__ void merge_rows(const MergeParams& p, const int4* split) {
     const int lane = threadIdx.x & 31;
     const long long gw = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (gw >= static_cast<long long>(p.n) * p.H) return;
     const int n = static_cast<int>(gw / p.H);
     const int h = static_cast<int>(gw - static_cast<long long>(n) * p.H);
-    // Behind the decode kernel this waits for its grid to complete and its
-    // writes to be visible; launched on its own it returns at once.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     int row = n, first = n * p.S, count = p.S;
-    if (p.split != nullptr) {
-        const int4 sr = p.split[n];
+    if (split != nullptr) {
+        const int4 sr = split[n];
         row = sr.x;
         first = sr.y;
         count = sr.z;
@@ -79,7 +90,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool after_decode) {
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+    const long long warps = static_cast<long long>(p.n) * p.H;
+    const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    merge_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_merge(const MergeParams& p, const InlineSplits& splits,
+                               cudaStream_t stream, bool early) {
     const long long warps = static_cast<long long>(p.n) * p.H;
     const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
@@ -92,8 +112,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream, bool after_d
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = after_decode ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, split_merge_kernel, p, splits);
 }
 
 }  // namespace oxd

@@ -75,7 +75,8 @@ def test_planner_chunks_long_requests_and_sizes_workspace():
     part = info.num_slots * 32 * 128 * 4 + info.num_slots * 32 * 4
     assert info.workspace_bytes >= part + info.upload_bytes
     assert info.workspace_bytes == plan.workspace_bytes
-    assert info.launches_per_run == 1
+    assert info.launches_per_run == 2          # decode + merge of the split requests
+    assert info.upload_bytes == 0              # the work list fits the parameter buffer
     assert info.total_kv_tokens == 32 * 4096
 
 
@@ -97,6 +98,13 @@ def test_forced_splits(force):
     assert info.num_work_items == chunks.sum()
     assert info.num_split_requests == int((chunks > 1).sum())
     assert info.num_slots == int(chunks[chunks > 1].sum())
+
+
+def test_long_work_lists_are_uploaded():
+    plan, _, _ = host_plan([64] * 600, Hq=8, Hkv=8, max_splits=1)
+    info = plan.info
+    assert info.num_work_items == 600 and info.upload_bytes >= 600 * 32
+    assert info.launches_per_run == 1
 
 
 def test_max_splits_caps_chunks():
