@@ -161,11 +161,10 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
  *   out           device bf16 [B][Hq][128], 16-byte aligned
  *   lse           device f32 [B][Hq], 4-byte aligned, or NULL
  *   workspace     device scratch of at least the planned size, 256-byte
- *                 aligned, any contents (the run zeroes its 16-byte header);
- *                 holds the device status word, the work counter, the split
- *                 partial states and, for work lists too long for the
- *                 kernel's parameter buffer, the work list; must not be
- *                 shared by runs that can overlap on the GPU
+ *                 aligned, any contents (nothing needs zeroing); holds the
+ *                 device status word, the split partial states and, for work
+ *                 lists too long for the kernel's parameter buffer, the work
+ *                 list; must not be shared by runs that can overlap on the GPU
  *   stream        cudaStream_t
  *
  * Host-side errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT,
@@ -203,10 +202,11 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. Every call on a device shares the one array,
- * which keeps the last call's contents; each call first zeroes what must
- * start at zero (the status word and the work counter) and writes everything
- * else it reads. Calls that can overlap on the GPU (other streams, other
- * threads) race on the array and must be serialised by the caller.
+ * which keeps the last call's contents; nothing in it has to start at zero
+ * (a run writes everything it reads, and its status word is tagged with the
+ * run's epoch, so what an earlier call left is never read as this call's).
+ * Calls that can overlap on the GPU (other streams, other threads) race on
+ * the array and must be serialised by the caller.
  * The device status word lives in that array, so oxd_read_device_status
  * cannot be used with this entry point.
  */
@@ -254,9 +254,8 @@ oxd_status oxd_plan_set_timing_events(oxd_plan plan, void* event_before, void* e
 oxd_status oxd_plan_destroy(oxd_plan plan);
 
 /*
- * Synchronise `stream`, then read into *code the device status word of
- * `workspace`, i.e. the first error of the last run on it (OXD_DEVICE_OK if
- * it recorded none). Returns OXD_OK when
+ * Synchronise `stream`, then read into *code the first error the last run
+ * that started on `workspace` recorded (OXD_DEVICE_OK if it recorded none). Returns OXD_OK when
  * the code is OXD_DEVICE_OK, OXD_ERR_DEVICE_STATUS otherwise, OXD_ERR_CUDA if
  * the copy failed. This is the one call that blocks the host.
  */

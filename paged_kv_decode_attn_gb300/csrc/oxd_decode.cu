@@ -6,11 +6,12 @@
 // fixes, and the split partitions + F32 partial workspace + merge of the
 // "Single decode split-K" row.
 //
-// Persistent, warp-specialised CTAs (a few per SM) pull work units -- one
-// run of consecutive pages of one request for one KV head -- from a shared
-// queue (units are ordered longest first by the planner):
-//   * the producer warp claims the next unit while the current one is still
-//     streaming, reads its page indices 32 at a time (coalesced), checks them
+// Persistent, warp-specialised CTAs (a few per SM). The planner lays the
+// page streams of all (request, KV head) pairs end to end and cuts them into
+// one equal share per CTA; a share is a few work units, each a run of
+// consecutive pages of one request for one KV head:
+//   * the producer warp reads the next unit's entry while the current one is
+//     still streaming, reads its page indices 32 at a time (coalesced), checks them
 //     against the pool, and fills a ring of shared-memory stages: one TMA
 //     tensor copy per (page, 64-column half) for K and for V, plus, on a
 //     unit's first stage, a bulk copy of the group's G query rows; every
@@ -26,8 +27,9 @@
 //     stage's own buffer and write the bf16 output and LSE, or, for a split
 //     request, an F32 partial state that the merge kernel (launched right
 //     behind this one) combines.
-// The work list travels in the kernel's parameter buffer when it fits; each
-// run zeroes only the status word and the work counter before the kernel.
+// The work list travels in the kernel's parameter buffer when it fits, and
+// the device status word carries the run's epoch, so a run enqueues nothing
+// but its kernels.
 // Every mbarrier wait gives up after about one second:
 // it records OXD_DEVICE_WAIT_TIMEOUT, all warps leave (the consumer warps
 // decide together through a barrier reduction, so no named barrier can be
@@ -178,9 +180,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// First error of a run wins (the run zeroes the word before the kernel).
-__device__ __forceinline__ void record_status(int32_t* status, int code) {
-    atomicCAS(status, 0, code);
+// The status word is {run epoch : 32, code : 32}. The first error of a run
+// replaces whatever an older run left there; later errors of the same run
+// keep it. Only error paths touch the word, so nothing has to reset it.
+__device__ __forceinline__ void record_status(unsigned long long* st, uint32_t epoch, int code) {
+    const unsigned long long want =
+        (static_cast<unsigned long long>(epoch) << 32) | static_cast<uint32_t>(code);
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(st);
+    for (int tries = 0; tries < 4096; ++tries) {
+        if ((old >> 32) == epoch && static_cast<uint32_t>(old) != 0u) return;
+        const unsigned long long prev = atomicCAS(st, old, want);
+        if (prev == old) return;
+        old = prev;
+    }
 }
 
 // Named barrier 1 among the consumer warps (the producer warp never uses it).
@@ -268,11 +280,10 @@ using CfgFmaG1 = Cfg<1, false, 4, 3, false, 1>;
 using CfgFmaG2 = Cfg<1, false, 4, 3, false, 2>;
 using CfgMma8 = Cfg<1, false, 4, 3, true, 0>;
 using CfgMma16 = Cfg<1, true, 4, 3, true, 0>;
-using CfgMma32 = Cfg<2, true, 4, 4, true, 0>;
 
 // What the producer tells the consumers about each stage it fills.
 struct StageRec {
-    int b, hkv, valid, n_stages, s, slot, pad0, pad1;
+    int b, hkv, valid, n_stages, s, slot, row0, nrows;  // query rows [row0, row0+nrows) of the group
 };
 
 // ------------------------------------------------------------------ consumers
@@ -312,14 +323,25 @@ struct MmaConsumer {
                                             int lane) {
         const int mi = lane >> 3, ri = lane & 7;
         // ---- S = Q K^T for 16 tokens: two n-tiles of 8 tokens
+        // Even and odd k steps accumulate separately: two independent mma
+        // chains per n-tile halve the dependent latency; summed afterwards.
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const RowAddr rk = row_addr(tk, t0 + ((mi >> 1) << 3) + ri, rmask);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b0, b1, b2, b3;
+        for (int ks = 0; ks < 8; ks += 2) {
+            uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
             ldsm_x4(chunk_addr(rk, 2 * ks + (mi & 1), half_bytes), b0, b1, b2, b3);
+            ldsm_x4(chunk_addr(rk, 2 * ks + 2 + (mi & 1), half_bytes), c0, c1, c2, c3);
             mma_bf16(s[0], qa[ks], b0, b1);
             mma_bf16(s[1], qa[ks], b2, b3);
+            mma_bf16(s2[0], qa[ks + 1], c0, c1);
+            mma_bf16(s2[1], qa[ks + 1], c2, c3);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s[0][e] += s2[0][e];
+            s[1][e] += s2[1][e];
         }
         // ---- online softmax in the log2 domain
         const int tq = lane & 3;
@@ -591,7 +613,7 @@ __global__ void __launch_bounds__(C::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ DecodeParams p,
-                        const __grid_constant__ InlineWork inline_work) {
+                        const __grid_constant__ WorkList work) {
     extern __shared__ uint8_t smem_raw[];
     const Smem<C> sm{reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))};
@@ -604,7 +626,8 @@ __global__ void __launch_bounds__(C::kThreads)
     const int pages_per_stage = C::kStageTokens / ps;
     const int G = p.group;
     // The work list sits in the parameter buffer unless it was too long.
-    const WorkItem* items = p.items != nullptr ? p.items : inline_work.item;
+    const int4* units = p.units != nullptr ? p.units : work.unit;
+    const int32_t* cta_begin = p.cta_begin != nullptr ? p.cta_begin : work.cta_begin;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -614,6 +637,7 @@ __global__ void __launch_bounds__(C::kThreads)
         }
         flags[0] = 0;
         fence_mbar_init();
+        if (blockIdx.x == 0) *p.last_epoch = p.epoch;  // whose status the word may hold
     }
     if (warp == C::kConsumerWarps && lane == 0) {
         prefetch_tmap(&tmap_k);
@@ -628,57 +652,64 @@ __global__ void __launch_bounds__(C::kThreads)
 
     if (warp == C::kConsumerWarps) {
         // ================================================ producer warp
-        // Each CTA starts on unit blockIdx.x; later units are claimed from the
-        // shared counter as soon as the current unit starts, the next unit's
-        // work item is read after the current unit's first stage is issued and
-        // its first page indices after the second, so these dependent loads
-        // overlap the current unit's streaming.
+        // This CTA's share of the work is units [cta_begin[c], cta_begin[c+1]).
+        // The next unit's entry is read after the current unit's first stage
+        // is issued and its first page indices after the second, so these
+        // dependent loads overlap the current unit's streaming.
         struct Unit {
             int unit;
-            WorkItem it;
+            int4 it;
             int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
         };
+        const int u_end = cta_begin[blockIdx.x + 1];
+        auto pages_of = [](const int4& it) { return it.y & ((1 << kUnitPagesBits) - 1); };
         auto load_item = [&](Unit& u) {
-            if (u.unit >= 0 && u.unit < p.n_units) u.it = items[u.unit / p.num_kv_heads];
+            if (u.unit < u_end) u.it = units[u.unit];
         };
         auto load_idx = [&](Unit& u) {
             u.win = u.nxt = 0;
-            if (u.unit >= 0 && u.unit < p.n_units) {
-                const int32_t* idx = p.indices + u.it.idx_begin;
-                if (lane < u.it.n_pages) u.win = __ldg(idx + lane);
-                if (32 + lane < u.it.n_pages) u.nxt = __ldg(idx + 32 + lane);
+            if (u.unit < u_end) {
+                const int32_t* idx = p.indices + u.it.x;
+                const int n = pages_of(u.it);
+                if (lane < n) u.win = __ldg(idx + lane);
+                if (32 + lane < n) u.nxt = __ldg(idx + 32 + lane);
             }
         };
-        auto valid_unit = [&](int u) { return u >= 0 && u < p.n_units; };
         int g = 0;  // ring position
         bool ok = true;
         Unit cur;
-        cur.unit = blockIdx.x;
+        cur.unit = cta_begin[blockIdx.x];
         load_item(cur);
         load_idx(cur);
-        while (valid_unit(cur.unit)) {
+        while (cur.unit < u_end) {
             Unit nx;
-            nx.unit = 0;
-            if (lane == 0) nx.unit = static_cast<int>(gridDim.x) + atomicAdd(p.work_counter, 1);
+            nx.unit = cur.unit + 1;
             bool nx_item = false, nx_idx = false;
-            const int hkv = cur.unit - (cur.unit / p.num_kv_heads) * p.num_kv_heads;
-            const WorkItem it = cur.it;
-            const int b = it.b, n_pages = it.n_pages;
+            const int4 it = cur.it;
+            const int n_pages = pages_of(it);
+            const int last_len = (it.y >> kUnitPagesBits) & 0x7f;  // 0: not the last page
+            const bool first_page = it.y < 0;                         // bit 31
+            const int b = it.z & ((1 << kUnitBBits) - 1);
+            const int row0 = ((it.z >> kUnitBBits) & 1) * 16;  // second 16-row half of a group
+            const int nrows = min(G - row0, C::kMma ? 16 : G);
+            const int hkv = static_cast<int>(static_cast<uint32_t>(it.z) >> (kUnitBBits + 1));
+            const int valid = last_len ? (n_pages - 1) * ps + last_len : n_pages * ps;
             const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
             int ip0 = 0, ip1 = 0, lst = 0;
             if (lane == 0) {
-                ip0 = p.indptr[b];
-                ip1 = p.indptr[b + 1];
-                lst = p.last_page_len[b];
+                if (first_page) ip0 = p.indptr[b];
+                if (last_len) {
+                    ip1 = p.indptr[b + 1];
+                    lst = p.last_page_len[b];
+                }
             }
             // An index outside [0, num_pages) is recorded and replaced by page
             // 0, so every copy stays inside the pool.
-            const int32_t* idx = p.indices + it.idx_begin;
+            const int32_t* idx = p.indices + it.x;
             int win = cur.win, nxt = cur.nxt;
             int win_base = 0;
             bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
-            if (__any_sync(0xffffffffu, bad) && lane == 0)
-                record_status(p.status, kDeviceBadPage);
+            if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(p.status, p.epoch, kDeviceBadPage);
             win = bad ? 0 : win;
             for (int s = 0; s < n_stages; ++s, ++g) {
                 const int slot = g % C::kStages;
@@ -690,7 +721,7 @@ __global__ void __launch_bounds__(C::kThreads)
                     nxt = win_base + 32 + lane < n_pages ? __ldg(idx + win_base + 32 + lane) : 0;
                     bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
                     if (__any_sync(0xffffffffu, bad) && lane == 0)
-                        record_status(p.status, kDeviceBadPage);
+                        record_status(p.status, p.epoch, kDeviceBadPage);
                     win = bad ? 0 : win;
                 }
                 int okw = 1;
@@ -704,16 +735,19 @@ __global__ void __launch_bounds__(C::kThreads)
                     StageRec* r = sm.rec(slot);
                     r->b = b;
                     r->hkv = hkv;
-                    r->valid = it.valid;
+                    r->valid = valid;
                     r->n_stages = n_stages;
                     r->s = s;
-                    r->slot = it.slot;
-                    const uint32_t qbytes = s == 0 ? static_cast<uint32_t>(G * kHeadDim * 2) : 0u;
+                    r->slot = it.w;
+                    r->row0 = row0;
+                    r->nrows = nrows;
+                    const uint32_t qbytes =
+                        s == 0 ? static_cast<uint32_t>(nrows * kHeadDim * 2) : 0u;
                     mbar_arrive_expect_tx(sm.full(slot), npg * ps * kHeadDim * 2 * 2 + qbytes);
                     if (s == 0)
                         bulk_load(sm.qbuf(slot),
-                                  p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * G) *
-                                            kHeadDim,
+                                  p.q + (static_cast<size_t>(b) * p.num_qo_heads + hkv * G +
+                                         row0) * kHeadDim,
                                   qbytes, sm.full(slot));
                 }
                 const uint32_t tk = sm.ring(slot);
@@ -734,7 +768,6 @@ __global__ void __launch_bounds__(C::kThreads)
                 }
                 if (lane == 0) sm.issued()[slot] += 1;
                 if (s == 0) {
-                    nx.unit = __shfl_sync(0xffffffffu, nx.unit, 0);
                     load_item(nx);
                     nx_item = true;
                 } else if (s == 1) {
@@ -743,13 +776,11 @@ __global__ void __launch_bounds__(C::kThreads)
                 }
             }
             if (!ok) break;
-            if (!nx_item) {
-                nx.unit = __shfl_sync(0xffffffffu, nx.unit, 0);
-                load_item(nx);
-            }
+            if (!nx_item) load_item(nx);
             if (!nx_idx) load_idx(nx);
-            if (lane == 0 && (ip0 != it.indptr_b || ip1 != it.indptr_b1 || lst != it.last))
-                record_status(p.status, kDevicePlanMismatch);
+            if (lane == 0 && ((first_page && ip0 != it.x) ||
+                              (last_len && (ip1 != it.x + n_pages || lst != last_len))))
+                record_status(p.status, p.epoch, kDevicePlanMismatch);
             cur = nx;
         }
         if (ok) {
@@ -770,7 +801,7 @@ __global__ void __launch_bounds__(C::kThreads)
         }
         if (!ok && lane == 0) {
             flags[0] = 1;
-            record_status(p.status, kDeviceWaitTimeout);
+            record_status(p.status, p.epoch, kDeviceWaitTimeout);
         }
     } else {
         // ================================================ consumer warps
@@ -791,7 +822,7 @@ __global__ void __launch_bounds__(C::kThreads)
             }
             const StageRec r = *sm.rec(slot);
             if (r.s < 0) break;
-            if (r.s == 0) cs.init(sm.qbuf(slot), G, mt, lane);
+            if (r.s == 0) cs.init(sm.qbuf(slot), r.nrows, mt, lane);
             const int t0 = slice * kSliceTokens;
             const int u0 = r.s * C::kStageTokens + t0;
             if (u0 < r.valid) {
@@ -806,11 +837,11 @@ __global__ void __launch_bounds__(C::kThreads)
                 float* red_m = sm.red_m();
                 float* red_l = sm.red_l();
                 consumer_sync(C::kConsumerThreads);  // every warp is done reading K/V here
-                const int hq0 = r.hkv * G;
+                const int hq0 = r.hkv * G + r.row0;
                 for (int round = 0; round < C::kMtiles; ++round) {
                     if (mt == round) cs.dump(red_m, red_l, dump, slice, lane);
                     consumer_sync(C::kConsumerThreads);
-                    const int rows = min(16, G - round * 16);
+                    const int rows = min(16, r.nrows - round * 16);
                     for (int i = ctid; i < rows * (kHeadDim / 4); i += C::kConsumerThreads) {
                         const int rr = i / (kHeadDim / 4);
                         const int d4 = i - rr * (kHeadDim / 4);
@@ -850,7 +881,9 @@ __global__ void __launch_bounds__(C::kThreads)
                             *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
                             if (d4 == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
                         } else {
-                            const size_t row = static_cast<size_t>(r.slot) * p.num_qo_heads + hq;
+                            // partial states are [slot][G][128]
+                            const size_t row =
+                                static_cast<size_t>(r.slot) * G + r.row0 + round * 16 + rr;
                             *reinterpret_cast<float4*>(p.part_o + row * kHeadDim + d4 * 4) = o;
                             if (d4 == 0) p.part_lse[row] = lse2;
                         }
@@ -863,7 +896,7 @@ __global__ void __launch_bounds__(C::kThreads)
         }
         if (!ok && lane == 0) {
             flags[0] = 1;
-            record_status(p.status, kDeviceWaitTimeout);
+            record_status(p.status, p.epoch, kDeviceWaitTimeout);
         }
     }
     __syncthreads();  // every warp has left its loop
@@ -892,7 +925,7 @@ cudaError_t ensure_smem_attribute() {
 
 template <class C>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                   const InlineWork& w, int grid, cudaStream_t stream) {
+                   const WorkList& w, int grid, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attribute<C>();
     if (e != cudaSuccess) return e;
     paged_decode_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p, w);
@@ -920,7 +953,7 @@ VariantShape variant_shape(int variant) {
         case kVariantFmaG2: return shape_of<CfgFmaG2>();
         case kVariantMma8: return shape_of<CfgMma8>();
         case kVariantMma16: return shape_of<CfgMma16>();
-        default: return shape_of<CfgMma32>();
+        default: return shape_of<CfgMma16>();  // kVariantMma32: two 16-row CTAs per piece
     }
 }
 
@@ -930,19 +963,19 @@ cudaError_t variant_occupancy(int variant, int* n) {
         case kVariantFmaG2: return occupancy_of<CfgFmaG2>(n);
         case kVariantMma8: return occupancy_of<CfgMma8>(n);
         case kVariantMma16: return occupancy_of<CfgMma16>(n);
-        default: return occupancy_of<CfgMma32>(n);
+        default: return occupancy_of<CfgMma16>(n);
     }
 }
 
 cudaError_t launch_decode(int variant, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, const InlineWork& w, int grid,
+                          const DecodeParams& p, const WorkList& w, int grid,
                           cudaStream_t stream) {
     switch (variant) {
         case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, w, grid, stream);
         case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, w, grid, stream);
         case kVariantMma8: return launch<CfgMma8>(tk, tv, p, w, grid, stream);
         case kVariantMma16: return launch<CfgMma16>(tk, tv, p, w, grid, stream);
-        default: return launch<CfgMma32>(tk, tv, p, w, grid, stream);
+        default: return launch<CfgMma16>(tk, tv, p, w, grid, stream);
     }
 }
 

@@ -3,10 +3,9 @@
 // Lifecycle from the "Oxide Infer" README, "One execution model": the plan
 // fixes the kernel variant, the chunking of every request's pages, the launch
 // shape and the workspace contract; a run only checks operands and enqueues
-// a 16-byte memset of the workspace header (status word, work counter), the
-// decode kernel, whose work list rides in its parameter buffer (long lists
-// are copied into the workspace first), and, when some request was split, a
-// merge kernel launched right behind it. "Providers": checked span, alignment, alias and capacity rules;
+// the decode kernel, whose work list rides in its parameter buffer (long
+// lists are copied into the workspace first), and, when some stream was
+// split, a merge kernel launched right behind it. "Providers": checked span, alignment, alias and capacity rules;
 // explicit workspace; caller stream; typed device status.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -44,10 +43,10 @@ struct oxd_plan_s {
     int64_t total_tokens;
     int grid;
     bool upload;  // work list or split table too long for the parameter buffers
-    size_t off_items, off_split, off_part_o, off_part_lse;
+    size_t off_units, off_cta, off_split, off_part_o, off_part_lse;
     size_t meta_bytes, ws_bytes;
-    InlineWork* inline_work;
-    InlineSplits* inline_splits;
+    WorkList* work;
+    SplitList* splits;
     void* meta;
     bool pinned;
     cudaEvent_t ev_before;
@@ -56,11 +55,19 @@ struct oxd_plan_s {
 
 namespace {
 
-// Planner cost model (microseconds; GB300 HBM measured at about 6.8 TB/s).
-constexpr double kHbmBytesPerUs = 6.8e6;
-constexpr double kUnitOverheadUs = 1.0;       // prologue/epilogue not hidden by prefetch
-constexpr double kSplitOverheadUs = 0.5;      // partial write + counter
-constexpr double kMergeKernelUs = 2.0;        // the merge launch behind the decode
+
+// Run epochs: never 0 and increasing over the process, so a status word left
+// in a workspace by an earlier run never passes for a later run's.
+std::atomic<uint32_t> g_epoch{0};
+uint32_t next_epoch() {
+    uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    while (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    return e;
+}
+
+// Start-up cost of one work unit (prologue, epilogue, refill), in tokens of
+// streaming at a CTA's share of HBM bandwidth (about 2 us).
+constexpr double kUnitOverheadTokens = 96.0;
 
 std::mutex g_plans_mu;
 std::unordered_set<oxd_plan> g_plans;
@@ -177,12 +184,11 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
         return OXD_ERR_UNSUPPORTED;
     if (d->num_qo_heads / d->num_kv_heads > kMaxGroup) return OXD_ERR_UNSUPPORTED;
     if (d->num_pages >= (int64_t{1} << 31)) return OXD_ERR_UNSUPPORTED;
+    if (d->batch >= (1 << kUnitBBits) || d->num_kv_heads >= (1 << (31 - kUnitBBits)))
+        return OXD_ERR_UNSUPPORTED;
     return OXD_OK;
 }
 
-struct Item {
-    int idx_begin, n_pages, valid, b, slot, slot_base, n_chunks;  // host-side view
-};
 
 }  // namespace
 
@@ -252,184 +258,207 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     }
     if (ctas_per_sm < 1) ctas_per_sm = estimate_ctas_per_sm(vs);
 
-    // ---- chunking
+    // ---- partition the work
+    // Work is the page streams of all (request, KV head) pairs, request-major
+    // (CTAs that run at the same time then read neighbouring heads of the
+    // same pages). A piece is a run of consecutive pages of one stream; a
+    // stream cut into several pieces is "split" and gets one partial-state
+    // slot per piece.
     const int pps = std::max(1, vs.stage_tokens / ps);  // pages per pipeline stage
-    const int64_t resident = static_cast<int64_t>(num_sms) * ctas_per_sm;
-    // Items of one request for chunk length `cb` pages (0 = whole request).
-    auto chunks_of = [&](int P, int cb) {
-        std::vector<std::pair<int, int>> ranges;  // [p0, p1)
-        if (d.force_splits > 0) {
-            const int n = std::min(d.force_splits, P);
-            for (int c = 0; c < n; ++c)
-                ranges.push_back({static_cast<int>(static_cast<int64_t>(P) * c / n),
-                                  static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
-            return ranges;
-        }
-        if (cb == 0 || P <= cb) {
-            ranges.push_back({0, P});
-            return ranges;
-        }
-        int n = (P + cb - 1) / cb;
-        if (d.max_splits > 0) n = std::min(n, d.max_splits);
-        int len = (P + n - 1) / n;
-        len = (len + pps - 1) / pps * pps;
-        for (int p0 = 0; p0 < P; p0 += len) ranges.push_back({p0, std::min(P, p0 + len)});
-        return ranges;
+    const int H = d.num_kv_heads;
+    // Groups of more than 16 query heads run every piece on a pair of CTAs,
+    // one per 16-row half, side by side (the second read of each page is
+    // then served by L2); the partition below is over CTA pairs.
+    const int copies = variant == kVariantMma32 ? 2 : 1;
+    const int64_t resident = static_cast<int64_t>(num_sms) * ctas_per_sm / copies;
+    auto tokens_to = [&](int b, int k) {  // tokens in pages [0, k) of request b
+        const int P = indptr[b + 1] - indptr[b];
+        return k >= P ? static_cast<int64_t>(P - 1) * ps + last[b] : static_cast<int64_t>(k) * ps;
     };
-    auto build_items = [&](int cb, std::vector<Item>& items, int& n_slots, int& n_split,
-                           int& max_chunks) {
-        items.clear();
-        n_slots = n_split = 0;
-        max_chunks = 1;
+    struct Piece {
+        int b, h, p0, p1;
+    };
+    std::vector<Piece> pieces;
+    std::vector<int> cta_of;  // CTA index of each piece, non-decreasing after ordering
+    int grid = 0;
+    if (d.force_splits == 0 && d.max_splits == 0) {
+        // Balanced line partition: cut the concatenated streams at the token
+        // positions (c+1) * T / grid, snapped to page boundaries; no piece is
+        // shorter than one pipeline stage unless its stream is.
+        const double T0 = static_cast<double>(total_tokens) * H;
+        const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
+        grid = static_cast<int>(std::max<int64_t>(
+            1, std::min<int64_t>(resident, static_cast<int64_t>(T0 / min_tokens))));
+        // Every piece also costs a unit's start-up; count the streams' first
+        // pieces and one cut per CTA.
+        const double T = T0 + kUnitOverheadTokens * (static_cast<double>(B) * H + grid);
+        const double share = T / grid;
+        double pos = 0.0;  // tokens before the current page on the line
+        int c = 0;
+        double cut = share;
         for (int b = 0; b < B; ++b) {
             const int P = indptr[b + 1] - indptr[b];
-            const int L = (P - 1) * ps + last[b];
-            const auto ranges = chunks_of(P, cb);
-            const int n = static_cast<int>(ranges.size());
-            max_chunks = std::max(max_chunks, n);
-            const int slot_base = n > 1 ? n_slots : -1;
-            if (n > 1) {
-                n_slots += n;
-                ++n_split;
-            }
-            for (int c = 0; c < n; ++c) {
-                const int p0 = ranges[c].first, p1 = ranges[c].second;
-                Item it;
-                it.idx_begin = indptr[b] + p0;
-                it.n_pages = p1 - p0;
-                it.valid = std::min((p1 - p0) * ps, L - p0 * ps);
-                it.b = b;
-                it.slot = n > 1 ? slot_base + c : -1;
-                it.slot_base = slot_base;
-                it.n_chunks = n;
-                items.push_back(it);
-            }
-        }
-        // Longest items first, so the short tails fill in behind them.
-        std::stable_sort(items.begin(), items.end(),
-                         [](const Item& a, const Item& x) { return a.n_pages > x.n_pages; });
-    };
-    // Simulated completion time (us) of the persistent grid pulling the sorted
-    // units from its queue: each unit streams its KV bytes at the CTA's share
-    // of HBM bandwidth plus a fixed per-unit cost; split units add their
-    // partial write, and the plan pays its merge.
-    auto makespan = [&](const std::vector<Item>& items, int max_chunks) {
-        const double cta_bytes_per_us = kHbmBytesPerUs / static_cast<double>(resident);
-        const int64_t units = static_cast<int64_t>(items.size()) * d.num_kv_heads;
-        const int64_t lanes = std::min<int64_t>(units, resident);
-        std::vector<double> finish(static_cast<size_t>(lanes), 0.0);
-        std::make_heap(finish.begin(), finish.end(), std::greater<double>());
-        for (const Item& it : items) {
-            const double t = it.valid * 512.0 / cta_bytes_per_us + kUnitOverheadUs +
-                             (it.n_chunks > 1 ? kSplitOverheadUs : 0.0);
-            for (int h = 0; h < d.num_kv_heads; ++h) {
-                std::pop_heap(finish.begin(), finish.end(), std::greater<double>());
-                finish.back() += t;
-                std::push_heap(finish.begin(), finish.end(), std::greater<double>());
+            for (int h = 0; h < H; ++h) {
+                int p = 0;
+                while (p < P) {
+                    int k = P;
+                    pos += kUnitOverheadTokens;  // the piece's start-up
+                    const double rest = static_cast<double>(tokens_to(b, P) - tokens_to(b, p));
+                    const double room = cut - pos;
+                    if (c < grid - 1 && room < rest - 0.5 * ps) {
+                        k = p + static_cast<int>(std::llround(std::max(0.0, room) / ps));
+                        if (k - p < pps) k = p + pps;          // no piece under a stage
+                        if (P - k < pps) k = P;                // no tail under a stage
+                        k = std::min(k, P);
+                    }
+                    pieces.push_back({b, h, p, k});
+                    cta_of.push_back(c);
+                    pos += static_cast<double>(tokens_to(b, k) - tokens_to(b, p));
+                    p = k;
+                    while (c < grid - 1 && pos >= cut - 0.5 * ps) {
+                        ++c;
+                        cut = share * (c + 1);
+                    }
+                }
             }
         }
-        double end = *std::max_element(finish.begin(), finish.end());
-        if (max_chunks > 1) end += kMergeKernelUs;
-        return end;
-    };
-    std::vector<Item> items;
-    int n_slots = 0, n_split = 0, max_chunks = 1;
-    int chunk_pages = 0;
-    int max_pages = 0;
-    for (int b = 0; b < B; ++b) max_pages = std::max(max_pages, indptr[b + 1] - indptr[b]);
-    if (d.force_splits == 0 && d.max_splits != 1) {
-        // Candidate chunk lengths: whole stages, roughly geometric, up to the
-        // longest request; keep the one with the smallest simulated time
-        // (ties go to the longer chunk, i.e. fewer partial states).
-        std::vector<int> cand;
-        for (double c = pps; c < max_pages + pps; c *= 1.18) {
-            int cb = (static_cast<int>(c) + pps - 1) / pps * pps;
-            if (cand.empty() || cb != cand.back()) cand.push_back(cb);
+        grid = cta_of.empty() ? 1 : cta_of.back() + 1;
+    } else {
+        // Fixed splitting (force_splits, or at most max_splits pieces per
+        // stream, 1 = never split): equal pieces, assigned longest first to
+        // the least-loaded CTA.
+        for (int b = 0; b < B; ++b) {
+            const int P = indptr[b + 1] - indptr[b];
+            int n = 1;
+            if (d.force_splits > 0) {
+                n = std::min(d.force_splits, P);
+            } else if (d.max_splits > 1) {
+                const double T = static_cast<double>(total_tokens) * H;
+                const double share_pages = T / static_cast<double>(resident) / ps;
+                n = static_cast<int>(std::ceil(P / std::max(1.0, share_pages)));
+                n = std::max(1, std::min({n, d.max_splits, P}));
+            }
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < n; ++c)
+                    pieces.push_back({b, h, static_cast<int>(static_cast<int64_t>(P) * c / n),
+                                      static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
         }
-        std::vector<std::pair<int, double>> tried;
-        std::vector<Item> trial;
-        int ns, nsp, mc;
-        for (int cb : cand) {
-            build_items(cb, trial, ns, nsp, mc);
-            // beyond ~64 units per resident CTA the per-unit cost dominates
-            if (static_cast<int64_t>(trial.size()) * d.num_kv_heads > 64 * resident) continue;
-            tried.push_back({cb, makespan(trial, mc)});
+        grid = static_cast<int>(std::min<int64_t>(resident, static_cast<int64_t>(pieces.size())));
+        std::vector<int> order(pieces.size());
+        for (size_t i = 0; i < order.size(); ++i) order[i] = static_cast<int>(i);
+        auto cost = [&](const Piece& x) { return tokens_to(x.b, x.p1) - tokens_to(x.b, x.p0); };
+        std::stable_sort(order.begin(), order.end(),
+                         [&](int a, int x) { return cost(pieces[a]) > cost(pieces[x]); });
+        std::vector<std::pair<int64_t, int>> heap;  // (load, cta), min-heap
+        for (int c = 0; c < grid; ++c) heap.push_back({0, c});
+        std::vector<int> assigned(pieces.size(), 0);
+        for (int i : order) {
+            std::pop_heap(heap.begin(), heap.end(), std::greater<std::pair<int64_t, int>>());
+            heap.back().first += cost(pieces[i]) + 64;  // + a stage of per-unit overhead
+            assigned[i] = heap.back().second;
+            std::push_heap(heap.begin(), heap.end(), std::greater<std::pair<int64_t, int>>());
         }
-        int best_cb = max_pages;
-        if (!tried.empty()) {
-            double best = tried[0].second;
-            for (const auto& t : tried) best = std::min(best, t.second);
-            for (const auto& t : tried)
-                if (t.second <= best * 1.01) best_cb = t.first;  // longest near-best chunk
+        std::vector<int> by_cta(order.size());
+        for (size_t i = 0; i < by_cta.size(); ++i) by_cta[i] = static_cast<int>(i);
+        std::stable_sort(by_cta.begin(), by_cta.end(),
+                         [&](int a, int x) { return assigned[a] < assigned[x]; });
+        std::vector<Piece> sorted;
+        for (int i : by_cta) {
+            sorted.push_back(pieces[i]);
+            cta_of.push_back(assigned[i]);
         }
-        chunk_pages = best_cb >= max_pages ? 0 : best_cb;
+        pieces.swap(sorted);
     }
-    build_items(chunk_pages, items, n_slots, n_split, max_chunks);
-    const int64_t n_units = static_cast<int64_t>(items.size()) * d.num_kv_heads;
-    if (n_units > 0x7fffffff) return OXD_ERR_UNSUPPORTED;
-    // Persistent grid: at most the resident CTAs of the device.
-    const int64_t grid = std::min<int64_t>(n_units, resident);
-    // Split requests are merged by a kernel behind the decode that spreads the
-    // merge over every SM.
+    // Slots for split streams (consecutive per stream) and the merge entries.
+    const int n_pieces = static_cast<int>(pieces.size());
+    std::vector<int> slot(pieces.size(), -1);
     std::vector<int4> split_tab;
+    int n_slots = 0, max_chunks = 1;
     {
-        std::vector<char> seen(static_cast<size_t>(B), 0);
-        for (const Item& it : items)
-            if (it.n_chunks > 1 && !seen[it.b]) {
-                seen[it.b] = 1;
-                split_tab.push_back(make_int4(it.b, it.slot_base, it.n_chunks, 0));
-            }
-        std::sort(split_tab.begin(), split_tab.end(),
-                  [](const int4& a, const int4& x) { return a.x < x.x; });
+        std::vector<std::vector<int>> of_stream(static_cast<size_t>(B) * H);
+        for (int i = 0; i < n_pieces; ++i)
+            of_stream[static_cast<size_t>(pieces[i].b) * H + pieces[i].h].push_back(i);
+        for (size_t st = 0; st < of_stream.size(); ++st) {
+            auto& v = of_stream[st];
+            max_chunks = std::max(max_chunks, static_cast<int>(v.size()));
+            if (v.size() < 2) continue;
+            std::sort(v.begin(), v.end(),
+                      [&](int a, int x) { return pieces[a].p0 < pieces[x].p0; });
+            const int b = static_cast<int>(st / H), h = static_cast<int>(st % H);
+            split_tab.push_back(make_int4(b * d.num_qo_heads + h * G, n_slots,
+                                          static_cast<int>(v.size()), 0));
+            for (int i : v) slot[i] = n_slots++;
+        }
+    }
+    const int n_split = static_cast<int>(split_tab.size());
+    // Units: each piece once per 16-row half, on CTAs copies*c + half.
+    const int n_units = n_pieces * copies;
+    grid *= copies;
+    std::vector<int4> units;
+    std::vector<int32_t> cta_begin(static_cast<size_t>(grid) + 1, 0);
+    {
+        std::vector<std::vector<int4>> per_cta(static_cast<size_t>(grid));
+        for (int i = 0; i < n_pieces; ++i) {
+            const Piece& x = pieces[i];
+            const int P = indptr[x.b + 1] - indptr[x.b];
+            uint32_t y = static_cast<uint32_t>(x.p1 - x.p0);
+            if (x.p1 == P) y |= static_cast<uint32_t>(last[x.b]) << kUnitPagesBits;
+            if (x.p0 == 0) y |= 1u << 31;
+            for (int half = 0; half < copies; ++half)
+                per_cta[static_cast<size_t>(cta_of[i]) * copies + half].push_back(
+                    make_int4(indptr[x.b] + x.p0, static_cast<int>(y),
+                              x.b | (half << kUnitBBits) | (x.h << (kUnitBBits + 1)), slot[i]));
+        }
+        for (int c = 0; c < grid; ++c) {
+            cta_begin[c] = static_cast<int32_t>(units.size());
+            units.insert(units.end(), per_cta[c].begin(), per_cta[c].end());
+        }
+        cta_begin[grid] = static_cast<int32_t>(units.size());
     }
 
-    // ---- workspace layout
+    // ---- plan object and workspace layout
     oxd_plan P = new (std::nothrow) oxd_plan_s();
     if (P == nullptr) return OXD_ERR_NO_MEMORY;
     P->desc = d;
     P->device = plan_device;
     P->group = G;
     P->variant = variant;
-    P->n_items = static_cast<int>(items.size());
+    P->n_items = n_units;
     P->n_slots = n_slots;
     P->n_split = n_split;
     P->max_chunks = max_chunks;
-    P->chunk_pages = chunk_pages;
+    P->chunk_pages = static_cast<int>(
+        std::llround(static_cast<double>(total_tokens) * H * copies / grid / ps));
     P->ctas_per_sm = ctas_per_sm;
     P->num_sms = num_sms;
-    P->grid = static_cast<int>(grid);
-    P->upload = static_cast<int>(items.size()) > kInlineItems ||
-                static_cast<int>(split_tab.size()) > kInlineSplits;
+    P->grid = grid;
+    P->upload = n_units > WorkList::kUnits || grid > WorkList::kCtas ||
+                n_split > SplitList::kEntries;
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
-    P->off_items = sizeof(WsHeader);
-    P->off_split = align_up(P->off_items + sizeof(WorkItem) * items.size(), 256);
+    P->off_units = sizeof(WsHeader);
+    P->off_cta = align_up(P->off_units + 16 * static_cast<size_t>(n_units), 256);
+    P->off_split = align_up(P->off_cta + 4 * (static_cast<size_t>(grid) + 1), 256);
     P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
     P->off_part_o = P->meta_bytes;
-    P->off_part_lse = align_up(
-        P->off_part_o + static_cast<size_t>(n_slots) * d.num_qo_heads * kHeadDim * 4, 256);
-    P->ws_bytes =
-        align_up(P->off_part_lse + static_cast<size_t>(n_slots) * d.num_qo_heads * 4, 256);
+    P->off_part_lse =
+        align_up(P->off_part_o + static_cast<size_t>(n_slots) * G * kHeadDim * 4, 256);
+    P->ws_bytes = align_up(P->off_part_lse + static_cast<size_t>(n_slots) * G * 4, 256);
 
-    P->inline_work = new (std::nothrow) InlineWork();
-    P->inline_splits = new (std::nothrow) InlineSplits();
+    P->work = new (std::nothrow) WorkList();
+    P->splits = new (std::nothrow) SplitList();
     P->meta = nullptr;
     P->pinned = false;
-    if (P->inline_work == nullptr || P->inline_splits == nullptr) {
-        delete P->inline_work;
-        delete P->inline_splits;
+    if (P->work == nullptr || P->splits == nullptr) {
+        delete P->work;
+        delete P->splits;
         delete P;
         return OXD_ERR_NO_MEMORY;
     }
-    std::vector<WorkItem> wl(items.size());
-    for (size_t i = 0; i < items.size(); ++i) {
-        const Item& it = items[i];
-        wl[i] = WorkItem{it.idx_begin, it.n_pages, it.valid, it.b, it.slot, indptr[it.b],
-                         indptr[it.b + 1], last[it.b]};
-    }
     if (!P->upload) {
-        std::copy(wl.begin(), wl.end(), P->inline_work->item);
-        std::copy(split_tab.begin(), split_tab.end(), P->inline_splits->split);
+        std::copy(units.begin(), units.end(), P->work->unit);
+        std::copy(cta_begin.begin(), cta_begin.end(), P->work->cta_begin);
+        std::copy(split_tab.begin(), split_tab.end(), P->splits->entry);
     } else {
         // Too long for the parameter buffers: a page-locked copy is uploaded
         // into the workspace by every run.
@@ -439,14 +468,15 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             P->meta = std::malloc(P->meta_bytes);
         }
         if (P->meta == nullptr) {
-            delete P->inline_work;
-            delete P->inline_splits;
+            delete P->work;
+            delete P->splits;
             delete P;
             return OXD_ERR_NO_MEMORY;
         }
         uint8_t* m = static_cast<uint8_t*>(P->meta);
         std::memset(m, 0, P->meta_bytes);
-        std::memcpy(m + P->off_items, wl.data(), sizeof(WorkItem) * wl.size());
+        std::memcpy(m + P->off_units, units.data(), 16 * units.size());
+        std::memcpy(m + P->off_cta, cta_begin.data(), 4 * cta_begin.size());
         std::memcpy(m + P->off_split, split_tab.data(), 16 * split_tab.size());
     }
     P->ev_before = nullptr;
@@ -476,7 +506,7 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.launches_per_run = plan->n_split > 0 ? 2 : 1;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.upload_bytes =
-        plan->upload ? static_cast<int64_t>(plan->meta_bytes - plan->off_items) : 0;
+        plan->upload ? static_cast<int64_t>(plan->meta_bytes - plan->off_units) : 0;
     r.total_kv_tokens = plan->total_tokens;
     *info = r;
     return OXD_OK;
@@ -500,8 +530,8 @@ oxd_status oxd_plan_destroy(oxd_plan plan) {
         cudaFreeHost(plan->meta);
     else
         std::free(plan->meta);
-    delete plan->inline_work;
-    delete plan->inline_splits;
+    delete plan->work;
+    delete plan->splits;
     delete plan;
     return OXD_OK;
 }
@@ -552,11 +582,9 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    // The status word and the work counter start every run at zero.
-    if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return OXD_ERR_CUDA;
     if (plan->upload &&
-        cudaMemcpyAsync(ws + plan->off_items, static_cast<uint8_t*>(plan->meta) + plan->off_items,
-                        plan->meta_bytes - plan->off_items, cudaMemcpyHostToDevice,
+        cudaMemcpyAsync(ws + plan->off_units, static_cast<uint8_t*>(plan->meta) + plan->off_units,
+                        plan->meta_bytes - plan->off_units, cudaMemcpyHostToDevice,
                         s) != cudaSuccess)
         return OXD_ERR_CUDA;
 
@@ -567,23 +595,24 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.indptr = indptr;
     p.indices = indices;
     p.last_page_len = last_page_len;
-    p.items = plan->upload ? reinterpret_cast<const WorkItem*>(ws + plan->off_items) : nullptr;
+    p.units = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_units) : nullptr;
+    p.cta_begin = plan->upload ? reinterpret_cast<const int32_t*>(ws + plan->off_cta) : nullptr;
     p.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
     p.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
-    p.status = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, status));
-    p.work_counter = reinterpret_cast<int32_t*>(ws + offsetof(WsHeader, work_counter));
+    p.status = reinterpret_cast<unsigned long long*>(ws + offsetof(WsHeader, status));
+    p.last_epoch = reinterpret_cast<uint32_t*>(ws + offsetof(WsHeader, last_epoch));
+    p.epoch = next_epoch();
     p.num_qo_heads = d.num_qo_heads;
     p.num_kv_heads = d.num_kv_heads;
     p.group = plan->group;
     p.page_size = d.page_size;
     p.layout = d.layout;
-    p.n_units = plan->n_items * d.num_kv_heads;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_decode(plan->variant, tk, tv, p, *plan->inline_work, plan->grid, s) !=
+    if (launch_decode(plan->variant, tk, tv, p, *plan->work, plan->grid, s) !=
         cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
@@ -594,17 +623,16 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         mp.s = p.part_lse;
         mp.out = p.out;
         mp.lse = lse;
-        mp.split = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_split) : nullptr;
-        mp.split_mode = 1;
+        mp.entries = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_split) : nullptr;
+        mp.uniform = 0;
         mp.n = plan->n_split;
         mp.S = 0;
-        mp.H = d.num_qo_heads;
+        mp.R = plan->group;
         mp.D = kHeadDim;
         mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
         // With timing events the decode kernel must end before ev_after, so
         // the merge is then launched without the early-start attribute.
-        if (launch_split_merge(mp, *plan->inline_splits, s, plan->ev_after == nullptr) !=
-            cudaSuccess)
+        if (launch_split_merge(mp, *plan->splits, s, plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;
     }
     return OXD_OK;
@@ -628,13 +656,13 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
     mp.s = s;
     mp.out = static_cast<uint16_t*>(v_out);
     mp.lse = s_out;
-    mp.split = nullptr;
-    mp.split_mode = 0;
-    mp.s_to_ln = 1.0f;
+    mp.entries = nullptr;
+    mp.uniform = 1;
     mp.n = N;
     mp.S = S;
-    mp.H = H;
+    mp.R = H;
     mp.D = D;
+    mp.s_to_ln = 1.0f;
     if (launch_merge(mp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OXD_ERR_CUDA;
     return OXD_OK;
@@ -643,11 +671,15 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
 oxd_status oxd_read_device_status(const void* workspace, void* stream, int32_t* code) {
     if (workspace == nullptr || code == nullptr) return OXD_ERR_INVALID_ARGUMENT;
     if (!aligned(workspace, 256)) return OXD_ERR_ALIGNMENT;
-    int32_t c = 0;
+    WsHeader h;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(&c, workspace, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (cudaMemcpyAsync(&h, workspace, 16, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return OXD_ERR_CUDA;
+    // A code counts only if the last run that started recorded it.
+    const int32_t c = static_cast<uint32_t>(h.status >> 32) == h.last_epoch
+                          ? static_cast<int32_t>(static_cast<uint32_t>(h.status))
+                          : OXD_DEVICE_OK;
     *code = c;
     return c == OXD_DEVICE_OK ? OXD_OK : OXD_ERR_DEVICE_STATUS;
 }

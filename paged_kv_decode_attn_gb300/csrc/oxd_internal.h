@@ -19,7 +19,7 @@ enum Variant : int {
     kVariantFmaG2 = 1,   // CUDA-core FMA, G = 2
     kVariantMma8 = 2,    // mma.sync m16n8k16, 3 <= G <= 8 (rows 8..15 of the tile idle)
     kVariantMma16 = 3,   // mma.sync, 9 <= G <= 16
-    kVariantMma32 = 4,   // mma.sync, two 16-row tiles, 17 <= G <= 32
+    kVariantMma32 = 4,   // 17 <= G <= 32: each piece runs on a pair of 16-row CTAs
     kNumVariants = 5
 };
 
@@ -30,46 +30,46 @@ struct VariantShape {
     int smem_bytes;     // dynamic shared memory per CTA
 };
 
-// One work item: consecutive pages of one request, processed once per KV
-// head (a work unit is an (item, KV head) pair; unit u = item u / Hkv, head
-// u % Hkv). The planned indptr/last_page_len of the request ride along so the
-// kernel can check the device block tables against the plan.
-struct WorkItem {
-    int32_t idx_begin;   // absolute offset of the item's first page in `indices`
-    int32_t n_pages;
-    int32_t valid;       // valid tokens in the item (the last page may be partial)
-    int32_t b;           // request
-    int32_t slot;        // partial-state slot, or -1: the item is its whole request
-    int32_t indptr_b;    // planned indptr[b], indptr[b+1], last_page_len[b]
-    int32_t indptr_b1;
-    int32_t last;
-};
-static_assert(sizeof(WorkItem) == 32, "work item is 32 bytes");
+// One work unit: consecutive pages of one request for one KV head.
+//   x: absolute offset of the unit's first page in `indices`
+//   y: pages (bits 0..23); bits 24..30: the request's last_page_len when the
+//      unit ends at the request's last page, else 0; bit 31: the unit starts
+//      at the request's first page
+//   z: request b (bits 0..18) | second 16-row half of a G > 16 group (bit 19)
+//      | KV head (bits 20..31)
+//   w: partial-state slot, or -1 when the unit is its whole (request, head)
+// The planner cuts the concatenation of all (request, KV head) page streams
+// into one contiguous share per CTA; CTA c runs units
+// [cta_begin[c], cta_begin[c+1]) in order.
+constexpr int kUnitPagesBits = 24;
+constexpr int kUnitBBits = 19;
 
-// Work lists up to this length travel in the decode kernel's parameter
-// buffer; longer ones are copied into the workspace.
-constexpr int kInlineItems = 448;
-struct InlineWork {
-    WorkItem item[kInlineItems];
+struct WorkList {
+    static constexpr int kUnits = 1728;  // units carried in the parameter buffer
+    static constexpr int kCtas = 600;    // CTA ranges carried in the parameter buffer
+    int4 unit[kUnits];
+    int32_t cta_begin[kCtas + 1];
 };
 
-// Split requests, {b, first slot, slots, 0}; same rule for the merge kernel.
-constexpr int kInlineSplits = 1024;
-struct InlineSplits {
-    int4 split[kInlineSplits];
+// Per split (request, KV head): x = first output row (b*Hq + hkv*G),
+// y = first slot, z = slots, w = 0.
+struct SplitList {
+    static constexpr int kEntries = 1024;
+    int4 entry[kEntries];
 };
 
 // Workspace layout (byte offsets, each 256-aligned):
-//   [0, 256)     header: int32 status word, int32 work counter (the run
-//                zeroes both with a 16-byte memset before the decode kernel)
-//   items        WorkItem[n_items]   (written by the run only when too long
-//   split        int4[n_split]        for the parameter buffers)
-//   part_o       f32[n_slots][Hq][128]
-//   part_lse     f32[n_slots][Hq]  (log2 domain)
+//   [0, 256)     header: status word {epoch, code} of the last run that
+//                recorded an error, and the epoch of the last run that started
+//   units        int4[n_units]        \ written by the run only when they do
+//   cta_begin    int32[grid + 1]       > not fit the kernels' parameter
+//   splits       int4[n_split]        /  buffers
+//   part_o       f32[n_slots][G][128]
+//   part_lse     f32[n_slots][G]  (log2 domain)
 struct WsHeader {
-    int32_t status;
-    int32_t work_counter;
-    int32_t pad[62];
+    unsigned long long status;
+    uint32_t last_epoch;
+    uint32_t pad[61];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -80,32 +80,36 @@ struct DecodeParams {
     const int32_t* indptr;
     const int32_t* indices;
     const int32_t* last_page_len;
-    const WorkItem* items;        // nullptr: the work list is the InlineWork parameter
+    const int4* units;            // nullptr: the WorkList parameter holds the units
+    const int32_t* cta_begin;     //          and the CTA ranges
     float* part_o;
     float* part_lse;
-    int32_t* status;
-    int32_t* work_counter;
+    unsigned long long* status;
+    uint32_t* last_epoch;
+    uint32_t epoch;               // this run's epoch (never 0)
     int32_t num_qo_heads;
     int32_t num_kv_heads;
     int32_t group;                // G
     int32_t page_size;
     int32_t layout;               // 0 NHD, 1 HND
-    int32_t n_units;              // n_items * num_kv_heads
     int64_t num_pages;
     float scale_log2;             // sm_scale * log2(e)
 };
 
+// Merge of R-row states. Entry n: output rows first_row + r, r < R, from
+// states (first + i) * R + r, i < count (state-major [.][R][D] layout).
 struct MergeParams {
-    const float* v;               // states [.][H][D], state-major
-    const float* s;               // [.][H]
-    uint16_t* out;                // bf16 [rows][H][D]
-    float* lse;                   // [rows][H] natural log, or nullptr
-    const int4* split;            // split table in memory; nullptr: inline (split mode)
-    int32_t split_mode;           // 1: row n is split[n] = {row, first state, count, 0};
-                                  // 0: row n uses states [n*S, n*S + S)
-    int32_t n;                    // rows to merge
-    int32_t S;                    // states per row when split_mode == 0
-    int32_t H;
+    const float* v;               // states [.][R][D]
+    const float* s;               // [.][R]
+    uint16_t* out;                // bf16 rows of D
+    float* lse;                   // per output row, natural log, or nullptr
+    const int4* entries;          // {first_row, first, count, 0}; nullptr: the
+                                  // SplitList parameter (split mode) or, in
+                                  // uniform mode, entry n = {n*R, n*S, S}
+    int32_t uniform;              // 1: entries implicit from S
+    int32_t n;                    // entries
+    int32_t S;                    // states per entry in uniform mode
+    int32_t R;                    // rows per entry
     int32_t D;
     float s_to_ln;                // factor taking s to natural log (1, or ln 2 for log2)
 };
@@ -114,14 +118,14 @@ struct MergeParams {
 VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                          const DecodeParams& p, const InlineWork& work, int grid,
+                          const DecodeParams& p, const WorkList& work, int grid,
                           cudaStream_t stream);
 // Uniform-state merge (the public entry point).
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
-// Merge of the split requests of a decode run, launched behind the decode
-// kernel with programmatic dependent launch when `early` (it waits for the
-// decode grid before reading anything).
-cudaError_t launch_split_merge(const MergeParams& p, const InlineSplits& splits,
+// Merge of the split (request, KV head) streams of a decode run, launched
+// behind the decode kernel with programmatic dependent launch when `early`
+// (it waits for the decode grid before reading anything).
+cudaError_t launch_split_merge(const MergeParams& p, const SplitList& splits,
                                cudaStream_t stream, bool early);
 
 }  // namespace oxd

@@ -58,8 +58,8 @@ extern "C" oxd_status oxd_paged_decode_run_static_workspace(
     if (cudaGetDevice(&device) != cudaSuccess) return OXD_ERR_CUDA;
     void* ws = nullptr;
     if (static_workspace_address(device, &ws) != cudaSuccess) return OXD_ERR_CUDA;
-    // Each run first zeroes the part that must start at zero (the status word
-    // and the work counter); everything else it reads is written by this run.
+    // Nothing in the array has to start at zero: a run writes everything it
+    // reads, and its status word is tagged with the run's epoch.
     return oxd_paged_decode_run(plan, q, k_pages, v_pages, indptr, indices, last_page_len,
                                 sm_scale, out, lse, ws, kStaticWorkspaceBytes, stream);
 }

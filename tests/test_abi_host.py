@@ -62,20 +62,20 @@ def host_plan(lengths, Hq=32, Hkv=8, ps=16, layout="NHD", num_pages=None, **kw):
 
 # ------------------------------------------------------------------ planning
 
-def test_planner_chunks_long_requests_and_sizes_workspace():
+def test_balanced_partition_spreads_work_over_the_grid():
     plan, indptr, _ = host_plan([4096] * 32)
     info = plan.info
     assert info.kernel_variant == 2                       # G = 4: tensor-core variant
-    assert info.num_split_requests == 32 and info.max_chunks > 1
-    assert info.chunk_pages % 4 == 0                      # whole 64-token stages at ps 16
-    assert info.num_work_items == 32 * info.max_chunks
-    # persistent grid: never more CTAs than units, nor than resident slots
-    assert info.grid_ctas == min(info.num_work_items * 8, 152 * info.ctas_per_sm)
-    assert info.num_slots == info.num_work_items
-    part = info.num_slots * 32 * 128 * 4 + info.num_slots * 32 * 4
-    assert info.workspace_bytes >= part + info.upload_bytes
+    assert info.grid_ctas == 152 * info.ctas_per_sm       # every resident CTA gets a share
+    total_pages = int(indptr[-1]) * 8
+    assert abs(info.chunk_pages - total_pages / info.grid_ctas) <= 1  # share per CTA, pages
+    assert info.num_work_items >= info.grid_ctas
+    assert info.num_split_requests > 0 and info.max_chunks > 1
+    # partial states: one [G][128] f32 block + [G] lse per split piece
+    part = info.num_slots * 4 * 128 * 4 + info.num_slots * 4 * 4
+    assert info.workspace_bytes >= part
     assert info.workspace_bytes == plan.workspace_bytes
-    assert info.launches_per_run == 2          # decode + merge of the split requests
+    assert info.launches_per_run == 2          # decode + merge of the split streams
     assert info.upload_bytes == 0              # the work list fits the parameter buffer
     assert info.total_kv_tokens == 32 * 4096
 
@@ -83,9 +83,16 @@ def test_planner_chunks_long_requests_and_sizes_workspace():
 def test_short_batch_is_not_split_when_splitting_is_off():
     plan, _, _ = host_plan([100, 5000, 17], max_splits=1)
     info = plan.info
-    assert info.num_split_requests == 0 and info.num_work_items == 3
+    assert info.num_split_requests == 0 and info.num_work_items == 3 * 8
     assert info.launches_per_run == 1 and info.num_slots == 0
     assert info.grid_ctas == 3 * 8
+
+
+def test_tiny_batch_uses_one_stage_per_cta_at_least():
+    plan, _, _ = host_plan([512], Hq=8, Hkv=8)   # 8 streams of 32 pages
+    info = plan.info
+    assert 32 <= info.grid_ctas <= 8 * 32 // 4    # at least one 64-token stage per CTA
+    assert info.num_work_items >= info.grid_ctas
 
 
 @pytest.mark.parametrize("force", [1, 2, 3, 7])
@@ -95,15 +102,16 @@ def test_forced_splits(force):
     pages = np.diff(indptr)
     chunks = np.minimum(force, pages)
     info = plan.info
-    assert info.num_work_items == chunks.sum()
-    assert info.num_split_requests == int((chunks > 1).sum())
-    assert info.num_slots == int(chunks[chunks > 1].sum())
+    assert info.num_work_items == chunks.sum() * 8
+    assert info.num_split_requests == int((chunks > 1).sum()) * 8   # split (request, head) streams
+    assert info.num_slots == int(chunks[chunks > 1].sum()) * 8
+    assert info.max_chunks == chunks.max()
 
 
 def test_long_work_lists_are_uploaded():
     plan, _, _ = host_plan([64] * 600, Hq=8, Hkv=8, max_splits=1)
     info = plan.info
-    assert info.num_work_items == 600 and info.upload_bytes >= 600 * 32
+    assert info.num_work_items == 600 * 8 and info.upload_bytes >= 600 * 8 * 16
     assert info.launches_per_run == 1
 
 
