@@ -68,6 +68,8 @@ def parse_args(argv=None):
                     help="target wall time of the oracle baseline sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="wall-time budget of a whole --impl reference run")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run only the workload's first N requests (smaller profiling cases)")
     return ap.parse_args(argv)
 
 
@@ -250,7 +252,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = W.CONFIGS[args.config]
-    case = W.make_case(cfg, device="cpu")
+    case = W.make_case(cfg, device="cpu", batch=args.batch)
     import oracle
 
     oracle.build()
@@ -295,6 +297,7 @@ def config_block(cfg, case):
             "kv_tokens": int(case.tables.lengths.sum()), "kv_bytes_per_step": case.kv_bytes(),
             "unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "shared_prefix_tokens": cfg.shared_prefix_tokens,
+            "requests_run": case.batch,
             "l2": "flushed before every timed step, outside its events: 512 MiB write, "
                   "then a 512 MiB read of another buffer"}
 
@@ -316,7 +319,7 @@ def run_oxd(args):
 
     oxd.build()
     cfg = shard_config(W.CONFIGS[args.config], rank)
-    case = W.make_case(cfg, device=dev)
+    case = W.make_case(cfg, device=dev, batch=args.batch)
     t = case.tables
     desc = oxd.make_desc(case.batch, case.num_qo_heads, case.num_kv_heads, case.page_size,
                          case.layout, t.num_pages)
