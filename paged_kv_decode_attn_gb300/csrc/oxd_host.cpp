@@ -282,44 +282,50 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     std::vector<int> cta_of;  // CTA index of each piece, non-decreasing after ordering
     int grid = 0;
     if (d.force_splits == 0 && d.max_splits == 0) {
-        // Balanced line partition: cut the concatenated streams at the token
-        // positions (c+1) * T / grid, snapped to page boundaries; no piece is
-        // shorter than one pipeline stage unless its stream is.
+        // Balanced line partition: walk the concatenated streams and give each
+        // CTA, when it starts, the average of what remains (tokens plus the
+        // start-up cost of the pieces still to come), cutting streams at page
+        // boundaries. A CTA whose remaining room cannot hold a piece's
+        // start-up and half a stage passes the next piece on.
         const double T0 = static_cast<double>(total_tokens) * H;
         const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
         grid = static_cast<int>(std::max<int64_t>(
             1, std::min<int64_t>(resident, static_cast<int64_t>(T0 / min_tokens))));
-        // Every piece also costs a unit's start-up; count the streams' first
-        // pieces and one cut per CTA.
-        const double T = T0 + kUnitOverheadTokens * (static_cast<double>(B) * H + grid);
-        const double share = T / grid;
-        double pos = 0.0;  // tokens before the current page on the line
+        double done = 0.0;                      // tokens assigned so far
+        int64_t streams_left = static_cast<int64_t>(B) * H;
+        auto budget_for = [&](int c) {
+            const double rest =
+                (T0 - done) + kUnitOverheadTokens * static_cast<double>(streams_left + grid - c - 1);
+            return rest / (grid - c);
+        };
         int c = 0;
-        double cut = share;
+        double budget = budget_for(0), used = 0.0;
         for (int b = 0; b < B; ++b) {
             const int P = indptr[b + 1] - indptr[b];
             for (int h = 0; h < H; ++h) {
                 int p = 0;
                 while (p < P) {
+                    if (c < grid - 1 && budget - used - kUnitOverheadTokens < 0.5 * min_tokens) {
+                        ++c;
+                        budget = budget_for(c);
+                        used = 0.0;
+                    }
+                    used += kUnitOverheadTokens;  // the piece's start-up
                     int k = P;
-                    pos += kUnitOverheadTokens;  // the piece's start-up
                     const double rest = static_cast<double>(tokens_to(b, P) - tokens_to(b, p));
-                    const double room = cut - pos;
+                    const double room = budget - used;
                     if (c < grid - 1 && room < rest - 0.5 * ps) {
-                        k = p + static_cast<int>(std::llround(std::max(0.0, room) / ps));
-                        if (k - p < pps) k = p + pps;          // no piece under a stage
-                        if (P - k < pps) k = P;                // no tail under a stage
-                        k = std::min(k, P);
+                        k = p + std::max(1, static_cast<int>(std::llround(room / ps)));
+                        if (k >= P) k = P;
                     }
                     pieces.push_back({b, h, p, k});
                     cta_of.push_back(c);
-                    pos += static_cast<double>(tokens_to(b, k) - tokens_to(b, p));
+                    const double dt = static_cast<double>(tokens_to(b, k) - tokens_to(b, p));
+                    used += dt;
+                    done += dt;
                     p = k;
-                    while (c < grid - 1 && pos >= cut - 0.5 * ps) {
-                        ++c;
-                        cut = share * (c + 1);
-                    }
                 }
+                --streams_left;
             }
         }
         grid = cta_of.empty() ? 1 : cta_of.back() + 1;
