@@ -1,8 +1,11 @@
 """Benchmark of batched paged-KV decode attention on GB300.
 
-One step = one ``oxd_paged_decode_run`` (work-list upload, decode kernel and,
-when a request is split, the merge kernel) over one batch of the workload,
-with the plan already built. Metric: KV-read GB/s (logical KV bytes
+One step = one ``oxd_paged_decode_run`` (decode kernel and, when a request is
+split, the merge kernel) over one batch of the workload, with the plan built
+and bound to its workspace beforehand (``oxd_plan_bind_workspace`` copies the
+work list into the workspace once, as a server does once per batch and then
+reuses for every layer; ``--work-list params`` runs unbound instead, the list
+riding in the kernels' parameter buffers or copied by every run). Metric: KV-read GB/s (logical KV bytes
 sum_b L_b * Hkv * D * 2 (K, V) * 2 B per step over the step time) and us per
 step.
 
@@ -70,6 +73,9 @@ def parse_args(argv=None):
                     help="wall-time budget of a whole --impl reference run")
     ap.add_argument("--batch", type=int, default=None,
                     help="run only the workload's first N requests (smaller profiling cases)")
+    ap.add_argument("--work-list", choices=["bound", "params"], default="bound",
+                    help="bound: the plan is bound to its workspace once before the steps; "
+                         "params: unbound runs")
     return ap.parse_args(argv)
 
 
@@ -333,6 +339,13 @@ def run_oxd(args):
     out = torch.empty_like(case.q)
     lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    bind_us = None
+    if args.work_list == "bound":
+        torch.cuda.synchronize(dev)
+        tb0 = time.perf_counter()
+        oxd.oxd_plan_bind_workspace(plan, ws, plan.workspace_bytes, torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
+        bind_us = (time.perf_counter() - tb0) * 1e6
     flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -480,7 +493,8 @@ def run_oxd(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": K * info.launches_per_run,
             "clocks": clocks,
-            "plan": {"host_us": plan_us, **info.as_dict()},
+            "plan": {"host_us": plan_us, "work_list": args.work_list, "bind_us": bind_us,
+                     **info.as_dict()},
             "wall_s_timed_loop": wall,
         }
         print(json.dumps(line), flush=True)

@@ -161,10 +161,12 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
  *   out           device bf16 [B][Hq][128], 16-byte aligned
  *   lse           device f32 [B][Hq], 4-byte aligned, or NULL
  *   workspace     device scratch of at least the planned size, 256-byte
- *                 aligned, any contents (nothing needs zeroing); holds the
- *                 device status word, the split partial states and, for work
- *                 lists too long for the kernel's parameter buffer, the work
- *                 list; must not be shared by runs that can overlap on the GPU
+ *                 aligned, any contents (nothing needs zeroing) unless it is
+ *                 bound to this plan (oxd_plan_bind_workspace); holds the
+ *                 device status word, the split partial states and, when
+ *                 bound or when the work list is too long for the kernel's
+ *                 parameter buffer, the work list; must not be shared by runs
+ *                 that can overlap on the GPU
  *   stream        cudaStream_t
  *
  * Host-side errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT,
@@ -183,6 +185,43 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
                                 const int32_t* indices, const int32_t* last_page_len,
                                 float sm_scale, void* out, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Bind `workspace` to `plan` ("Oxide Infer" README, "One execution model":
+ * the plan fixes the work decomposition once and every run only enqueues;
+ * "Providers": explicit workspace). Enqueues on `stream` the copy of the
+ * plan's work list (units, per-CTA ranges, split-merge entries) into the
+ * workspace, followed by a 64-bit stamp of the plan in its header.
+ *
+ * Later oxd_paged_decode_run calls of this plan that pass this same
+ * workspace pointer then read the work list from the workspace: the kernels
+ * are launched with small parameter blocks and the run copies nothing. Runs
+ * on any other workspace are unaffected. A plan holds one binding at a time
+ * (binding another workspace replaces it); destroying the plan ends it.
+ *
+ *   workspace       device scratch of at least the planned size, 256-byte
+ *                   aligned, on the plan's device
+ *   workspace_bytes its size
+ *   stream          cudaStream_t; runs on other streams must be ordered
+ *                   after this copy by the caller
+ *
+ * Ownership: from the call on, bytes [0, 256 + list size) of the workspace
+ * belong to the binding. Anything else written there (another plan's run or
+ * binding on the same workspace, a memset, handing the memory to another
+ * user) ends it on the device: each kernel checks the stamp before it uses
+ * the list, and on a mismatch computes nothing and records
+ * OXD_DEVICE_PLAN_MISMATCH (read with oxd_read_device_status). Every unit
+ * read from a bound list is also bounds-checked against the plan's batch,
+ * heads, page count and slot count, so a damaged list is reported the same
+ * way and never leads the kernels outside the caller's buffers. After the
+ * memory was reused, bind again.
+ *
+ * Errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT (NULL),
+ * OXD_ERR_ALIGNMENT, OXD_ERR_WORKSPACE_TOO_SMALL, OXD_ERR_PLAN_MISMATCH
+ * (destroyed or host-only plan, or another current device), OXD_ERR_CUDA.
+ */
+oxd_status oxd_plan_bind_workspace(oxd_plan plan, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /*
  * oxd_paged_decode_run without a caller-provided workspace. The source pages

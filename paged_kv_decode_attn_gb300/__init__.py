@@ -9,7 +9,7 @@ every call raises :class:`LibraryNotBuilt`.
 The functions keep the C names:
 
 * :func:`oxd_paged_decode_plan` -> :class:`Plan` (owns the opaque handle)
-* :func:`oxd_paged_decode_run`
+* :func:`oxd_paged_decode_run`, :func:`oxd_plan_bind_workspace`
 * :func:`oxd_merge_states`
 * :func:`oxd_plan_get_info`, :func:`oxd_plan_set_timing_events`,
   :func:`oxd_plan_destroy`, :func:`oxd_read_device_status`,
@@ -34,7 +34,7 @@ from .build import build
 __all__ = [
     "OXD_OK", "OXD_LAYOUT_NHD", "OXD_LAYOUT_HND", "OxdError", "LibraryNotBuilt", "Desc",
     "PlanInfo", "Plan", "build", "lib", "oxd_paged_decode_plan", "oxd_paged_decode_run",
-    "oxd_paged_decode_run_static_workspace",
+    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace",
     "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
     "oxd_read_device_status", "oxd_status_string", "oxd_device_status_string", "oxd_version",
     "EXPORTED_SYMBOLS",
@@ -63,7 +63,7 @@ EXPORTED_SYMBOLS = (
     "oxd_paged_decode_plan", "oxd_paged_decode_run", "oxd_merge_states", "oxd_plan_get_info",
     "oxd_plan_set_timing_events", "oxd_plan_destroy", "oxd_read_device_status",
     "oxd_status_string", "oxd_device_status_string", "oxd_version",
-    "oxd_paged_decode_run_static_workspace",
+    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace",
 )
 
 
@@ -132,12 +132,13 @@ def lib():
             L.oxd_merge_states.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
             L.oxd_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
             L.oxd_plan_set_timing_events.argtypes = [vp, vp, vp]
+            L.oxd_plan_bind_workspace.argtypes = [vp, vp, sz, vp]
             L.oxd_plan_destroy.argtypes = [vp]
             L.oxd_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
             for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run",
                       "oxd_paged_decode_run_static_workspace", "oxd_merge_states",
                       "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
-                      "oxd_read_device_status"):
+                      "oxd_read_device_status", "oxd_plan_bind_workspace"):
                 getattr(L, f).restype = ctypes.c_int
             L.oxd_status_string.argtypes = [ctypes.c_int]
             L.oxd_status_string.restype = ctypes.c_char_p
@@ -262,6 +263,17 @@ def oxd_paged_decode_run(plan, q, k_pages, v_pages, indptr, indices, last_page_l
         _addr(last_page_len), float(sm_scale), _addr(out), _addr(lse), _addr(workspace),
         int(workspace_bytes), _stream(stream, q))
     _check("oxd_paged_decode_run", st)
+
+
+def oxd_plan_bind_workspace(plan, workspace, workspace_bytes=None, stream=None) -> None:
+    """Enqueue the copy of the plan's work list into ``workspace``; later runs of
+    the plan on that workspace copy nothing and launch with small parameter
+    blocks (see ``oxd_plan_bind_workspace`` in include/oxd.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib().oxd_plan_bind_workspace(_handle(plan), _addr(workspace), int(workspace_bytes),
+                                       _stream(stream, workspace))
+    _check("oxd_plan_bind_workspace", st)
 
 
 def oxd_paged_decode_run_static_workspace(plan, q, k_pages, v_pages, indptr, indices,

@@ -384,13 +384,17 @@ struct MmaConsumer {
         } else {
             s[0][2] = s[0][3] = s[1][2] = s[1][3] = 0.f;
         }
+        // The accumulator only needs rescaling when some row's running max
+        // rose (alpha < 1); after the first tiles that is rare.
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            acc[n][0] *= al0;
-            acc[n][1] *= al0;
-            if constexpr (C::kHiRows) {
-                acc[n][2] *= al1;
-                acc[n][3] *= al1;
+            for (int n = 0; n < 16; ++n) {
+                acc[n][0] *= al0;
+                acc[n][1] *= al0;
+                if constexpr (C::kHiRows) {
+                    acc[n][2] *= al1;
+                    acc[n][3] *= al1;
+                }
             }
         }
         // ---- O += P V: P (bf16) is the A operand, built from the S fragments
@@ -608,12 +612,12 @@ struct Smem {
 
 // ------------------------------------------------------------------ the kernel
 
-template <class C>
+template <class C, class WL>
 __global__ void __launch_bounds__(C::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ DecodeParams p,
-                        const __grid_constant__ WorkList work) {
+                        const __grid_constant__ WL work) {
     extern __shared__ uint8_t smem_raw[];
     const Smem<C> sm{reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))};
@@ -625,9 +629,16 @@ __global__ void __launch_bounds__(C::kThreads)
     const int half_bytes = ps * 128;
     const int pages_per_stage = C::kStageTokens / ps;
     const int G = p.group;
-    // The work list sits in the parameter buffer unless it was too long.
-    const int4* units = p.units != nullptr ? p.units : work.unit;
-    const int32_t* cta_begin = p.cta_begin != nullptr ? p.cta_begin : work.cta_begin;
+    // The work list sits in the parameter buffer, unless it was too long or
+    // the workspace is bound (then it is in the workspace).
+    const int4* units = p.units;
+    const int32_t* cta_begin = p.cta_begin;
+    if constexpr (std::is_same<WL, WorkList>::value) {
+        if (units == nullptr) {
+            units = work.unit;
+            cta_begin = work.cta_begin;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -661,14 +672,29 @@ __global__ void __launch_bounds__(C::kThreads)
             int4 it;
             int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
         };
-        const int u_end = cta_begin[blockIdx.x + 1];
+        // A bound workspace is used only while it still carries this plan's
+        // stamp; every unit is bounds-checked before it is used.
+        bool usable = true;
+        if (p.ws_stamp != nullptr) {
+            int ok_stamp = 1;
+            if (lane == 0) ok_stamp = *p.ws_stamp == p.stamp ? 1 : 0;
+            usable = __shfl_sync(0xffffffffu, ok_stamp, 0) != 0;
+            if (!usable && lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+        }
+        int u_end = usable ? cta_begin[blockIdx.x + 1] : 0;
+        int u_begin = usable ? cta_begin[blockIdx.x] : 0;
+        if (u_begin < 0 || u_end > p.n_units || u_begin > u_end) {
+            if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+            u_begin = u_end = 0;
+        }
         auto pages_of = [](const int4& it) { return it.y & ((1 << kUnitPagesBits) - 1); };
         auto load_item = [&](Unit& u) {
             if (u.unit < u_end) u.it = units[u.unit];
         };
         auto load_idx = [&](Unit& u) {
             u.win = u.nxt = 0;
-            if (u.unit < u_end) {
+            if (u.unit < u_end && u.it.x >= 0 &&
+                static_cast<int64_t>(u.it.x) + pages_of(u.it) <= p.nnz) {
                 const int32_t* idx = p.indices + u.it.x;
                 const int n = pages_of(u.it);
                 if (lane < n) u.win = __ldg(idx + lane);
@@ -678,7 +704,7 @@ __global__ void __launch_bounds__(C::kThreads)
         int g = 0;  // ring position
         bool ok = true;
         Unit cur;
-        cur.unit = cta_begin[blockIdx.x];
+        cur.unit = u_begin;
         load_item(cur);
         load_idx(cur);
         while (cur.unit < u_end) {
@@ -694,9 +720,18 @@ __global__ void __launch_bounds__(C::kThreads)
             const int nrows = min(G - row0, C::kMma ? 16 : G);
             const int hkv = static_cast<int>(static_cast<uint32_t>(it.z) >> (kUnitBBits + 1));
             const int valid = last_len ? (n_pages - 1) * ps + last_len : n_pages * ps;
-            const int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+            int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+            const bool unit_ok = n_pages >= 1 && it.x >= 0 &&
+                                 static_cast<int64_t>(it.x) + n_pages <= p.nnz && b < p.batch &&
+                                 hkv < p.num_kv_heads && row0 < G && it.w >= -1 &&
+                                 it.w < p.n_slots && last_len <= ps;
+            if (!unit_ok) {
+                // not a unit of this plan: skip it (its outputs stay unwritten)
+                if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+                n_stages = 0;
+            }
             int ip0 = 0, ip1 = 0, lst = 0;
-            if (lane == 0) {
+            if (lane == 0 && unit_ok) {
                 if (first_page) ip0 = p.indptr[b];
                 if (last_len) {
                     ip1 = p.indptr[b + 1];
@@ -778,7 +813,7 @@ __global__ void __launch_bounds__(C::kThreads)
             if (!ok) break;
             if (!nx_item) load_item(nx);
             if (!nx_idx) load_idx(nx);
-            if (lane == 0 && ((first_page && ip0 != it.x) ||
+            if (lane == 0 && unit_ok && ((first_page && ip0 != it.x) ||
                               (last_len && (ip1 != it.x + n_pages || lst != last_len))))
                 record_status(p.status, p.epoch, kDevicePlanMismatch);
             cur = nx;
@@ -909,7 +944,7 @@ __global__ void __launch_bounds__(C::kThreads)
 }
 
 // cudaFuncSetAttribute is per device; remember which devices are set up.
-template <class C>
+template <class C, class WL>
 cudaError_t ensure_smem_attribute() {
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -917,18 +952,26 @@ cudaError_t ensure_smem_attribute() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_decode_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(paged_decode_kernel<C, WL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
 
 template <class C>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                   const WorkList& w, int grid, cudaStream_t stream) {
-    cudaError_t e = ensure_smem_attribute<C>();
-    if (e != cudaSuccess) return e;
-    paged_decode_kernel<C><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p, w);
+                   const WorkList* w, int grid, cudaStream_t stream) {
+    if (w != nullptr) {
+        cudaError_t e = ensure_smem_attribute<C, WorkList>();
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<C, WorkList><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p,
+                                                                                      *w);
+    } else {
+        cudaError_t e = ensure_smem_attribute<C, NoList>();
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<C, NoList><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+            tk, tv, p, NoList{0});
+    }
     return cudaGetLastError();
 }
 
@@ -939,10 +982,10 @@ VariantShape shape_of() {
 
 template <class C>
 cudaError_t occupancy_of(int* n) {
-    cudaError_t e = ensure_smem_attribute<C>();
+    cudaError_t e = ensure_smem_attribute<C, WorkList>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, paged_decode_kernel<C>, C::kThreads,
-                                                         C::kSmemBytes);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, paged_decode_kernel<C, WorkList>,
+                                                         C::kThreads, C::kSmemBytes);
 }
 
 }  // namespace
@@ -968,7 +1011,7 @@ cudaError_t variant_occupancy(int variant, int* n) {
 }
 
 cudaError_t launch_decode(int variant, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, const WorkList& w, int grid,
+                          const DecodeParams& p, const WorkList* w, int grid,
                           cudaStream_t stream) {
     switch (variant) {
         case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, w, grid, stream);

@@ -4,8 +4,9 @@
 // fixes the kernel variant, the chunking of every request's pages, the launch
 // shape and the workspace contract; a run only checks operands and enqueues
 // the decode kernel, whose work list rides in its parameter buffer (long
-// lists are copied into the workspace first), and, when some stream was
-// split, a merge kernel launched right behind it. "Providers": checked span, alignment, alias and capacity rules;
+// lists are copied into the workspace first) or, once the plan has been
+// bound to the workspace, is read from it, and, when some stream was split,
+// a merge kernel launched right behind it. "Providers": checked span, alignment, alias and capacity rules;
 // explicit workspace; caller stream; typed device status.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -19,6 +20,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <random>
 #include <unordered_set>
 #include <vector>
 
@@ -47,8 +49,10 @@ struct oxd_plan_s {
     size_t meta_bytes, ws_bytes;
     WorkList* work;
     SplitList* splits;
-    void* meta;
+    void* meta;   // host image of workspace bytes [0, meta_bytes), then the stamp
     bool pinned;
+    unsigned long long stamp;             // identifies the plan in a bound workspace
+    std::atomic<const void*> bound_ws;    // workspace bound by oxd_plan_bind_workspace
     cudaEvent_t ev_before;
     cudaEvent_t ev_after;
 };
@@ -68,6 +72,20 @@ uint32_t next_epoch() {
 // Start-up cost of one work unit (prologue, epilogue, refill), in tokens of
 // streaming at a CTA's share of HBM bandwidth (about 2 us).
 constexpr double kUnitOverheadTokens = 96.0;
+
+// Plan stamps: a per-process random high half and a counter, never 0, so a
+// stamp left in reused memory by another process or an earlier plan is not
+// taken for a live plan's.
+unsigned long long next_stamp() {
+    static const unsigned long long hi = [] {
+        std::random_device rd;
+        return (static_cast<unsigned long long>(rd()) << 32);
+    }();
+    static std::atomic<uint32_t> counter{0};
+    uint32_t c = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    while (c == 0) c = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    return hi | c;
+}
 
 std::mutex g_plans_mu;
 std::unordered_set<oxd_plan> g_plans;
@@ -465,26 +483,32 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         std::copy(units.begin(), units.end(), P->work->unit);
         std::copy(cta_begin.begin(), cta_begin.end(), P->work->cta_begin);
         std::copy(split_tab.begin(), split_tab.end(), P->splits->entry);
-    } else {
-        // Too long for the parameter buffers: a page-locked copy is uploaded
-        // into the workspace by every run.
-        P->pinned = cudaHostAlloc(&P->meta, P->meta_bytes, cudaHostAllocDefault) == cudaSuccess;
-        if (!P->pinned) {
-            cudaGetLastError();  // a host-only plan on a machine without a GPU lands here
-            P->meta = std::malloc(P->meta_bytes);
-        }
-        if (P->meta == nullptr) {
-            delete P->work;
-            delete P->splits;
-            delete P;
-            return OXD_ERR_NO_MEMORY;
-        }
+    }
+    // Workspace image of the list (header stamp 0), for uploads and binds.
+    // Lists too long for the parameter buffers are uploaded by every unbound
+    // run, so their image is page-locked.
+    const size_t image_bytes = P->meta_bytes + 256;
+    if (P->upload) {
+        P->pinned = cudaHostAlloc(&P->meta, image_bytes, cudaHostAllocDefault) == cudaSuccess;
+        if (!P->pinned) cudaGetLastError();  // a host-only plan on a machine without a GPU
+    }
+    if (P->meta == nullptr) P->meta = std::malloc(image_bytes);
+    if (P->meta == nullptr) {
+        delete P->work;
+        delete P->splits;
+        delete P;
+        return OXD_ERR_NO_MEMORY;
+    }
+    {
         uint8_t* m = static_cast<uint8_t*>(P->meta);
-        std::memset(m, 0, P->meta_bytes);
+        std::memset(m, 0, image_bytes);
         std::memcpy(m + P->off_units, units.data(), 16 * units.size());
         std::memcpy(m + P->off_cta, cta_begin.data(), 4 * cta_begin.size());
         std::memcpy(m + P->off_split, split_tab.data(), 16 * split_tab.size());
+        P->stamp = next_stamp();
+        std::memcpy(m + P->meta_bytes, &P->stamp, sizeof(P->stamp));
     }
+    P->bound_ws.store(nullptr);
     P->ev_before = nullptr;
     P->ev_after = nullptr;
     {
@@ -523,6 +547,30 @@ oxd_status oxd_plan_set_timing_events(oxd_plan plan, void* before, void* after) 
     if ((before == nullptr) != (after == nullptr)) return OXD_ERR_INVALID_ARGUMENT;
     plan->ev_before = static_cast<cudaEvent_t>(before);
     plan->ev_after = static_cast<cudaEvent_t>(after);
+    return OXD_OK;
+}
+
+oxd_status oxd_plan_bind_workspace(oxd_plan plan, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (plan == nullptr || !plan_alive(plan)) return OXD_ERR_PLAN_MISMATCH;
+    if (workspace == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256)) return OXD_ERR_ALIGNMENT;
+    if (workspace_bytes < plan->ws_bytes) return OXD_ERR_WORKSPACE_TOO_SMALL;
+    if (plan->device < 0) return OXD_ERR_PLAN_MISMATCH;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
+    if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* m = static_cast<const uint8_t*>(plan->meta);
+    // The list first, then the stamp that makes it valid.
+    if (cudaMemcpyAsync(ws + plan->off_units, m + plan->off_units,
+                        plan->meta_bytes - plan->off_units, cudaMemcpyHostToDevice,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + offsetof(WsHeader, stamp), m + plan->meta_bytes,
+                        sizeof(unsigned long long), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return OXD_ERR_CUDA;
+    plan->bound_ws.store(workspace);
     return OXD_OK;
 }
 
@@ -588,9 +636,14 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if (plan->upload &&
-        cudaMemcpyAsync(ws + plan->off_units, static_cast<uint8_t*>(plan->meta) + plan->off_units,
-                        plan->meta_bytes - plan->off_units, cudaMemcpyHostToDevice,
+    const bool bound = plan->bound_ws.load() == workspace;
+    // An unbound run with a long list uploads it together with a zero stamp,
+    // which also ends any binding of another plan to this workspace.
+    const bool in_ws = bound || plan->upload;
+    constexpr size_t kStampOff = offsetof(WsHeader, stamp);
+    if (!bound && plan->upload &&
+        cudaMemcpyAsync(ws + kStampOff, static_cast<uint8_t*>(plan->meta) + kStampOff,
+                        plan->meta_bytes - kStampOff, cudaMemcpyHostToDevice,
                         s) != cudaSuccess)
         return OXD_ERR_CUDA;
 
@@ -601,8 +654,14 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.indptr = indptr;
     p.indices = indices;
     p.last_page_len = last_page_len;
-    p.units = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_units) : nullptr;
-    p.cta_begin = plan->upload ? reinterpret_cast<const int32_t*>(ws + plan->off_cta) : nullptr;
+    p.units = in_ws ? reinterpret_cast<const int4*>(ws + plan->off_units) : nullptr;
+    p.cta_begin = in_ws ? reinterpret_cast<const int32_t*>(ws + plan->off_cta) : nullptr;
+    p.ws_stamp = bound ? reinterpret_cast<const unsigned long long*>(ws + kStampOff) : nullptr;
+    p.stamp = plan->stamp;
+    p.n_units = plan->n_items;
+    p.n_slots = plan->n_slots;
+    p.batch = d.batch;
+    p.nnz = plan->nnz;
     p.part_o = reinterpret_cast<float*>(ws + plan->off_part_o);
     p.part_lse = reinterpret_cast<float*>(ws + plan->off_part_lse);
     p.status = reinterpret_cast<unsigned long long*>(ws + offsetof(WsHeader, status));
@@ -618,7 +677,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_decode(plan->variant, tk, tv, p, *plan->work, plan->grid, s) !=
+    if (launch_decode(plan->variant, tk, tv, p, in_ws ? nullptr : plan->work, plan->grid, s) !=
         cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
@@ -629,7 +688,11 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         mp.s = p.part_lse;
         mp.out = p.out;
         mp.lse = lse;
-        mp.entries = plan->upload ? reinterpret_cast<const int4*>(ws + plan->off_split) : nullptr;
+        mp.entries = in_ws ? reinterpret_cast<const int4*>(ws + plan->off_split) : nullptr;
+        mp.ws_stamp = p.ws_stamp;
+        mp.stamp = p.stamp;
+        mp.n_rows = static_cast<int64_t>(d.batch) * d.num_qo_heads;
+        mp.n_states = static_cast<int64_t>(plan->n_slots) * plan->group;
         mp.uniform = 0;
         mp.n = plan->n_split;
         mp.S = 0;
@@ -638,7 +701,8 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
         // With timing events the decode kernel must end before ev_after, so
         // the merge is then launched without the early-start attribute.
-        if (launch_split_merge(mp, *plan->splits, s, plan->ev_after == nullptr) != cudaSuccess)
+        if (launch_split_merge(mp, in_ws ? nullptr : plan->splits, s,
+                               plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;
     }
     return OXD_OK;

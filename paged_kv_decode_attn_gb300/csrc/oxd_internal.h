@@ -60,7 +60,10 @@ struct SplitList {
 
 // Workspace layout (byte offsets, each 256-aligned):
 //   [0, 256)     header: status word {epoch, code} of the last run that
-//                recorded an error, and the epoch of the last run that started
+//                recorded an error, the epoch of the last run that started,
+//                and the stamp of the plan bound to the workspace
+//   (a bound workspace holds the units, CTA ranges and merge entries for
+//   good; runs on it pass no work list and copy nothing)
 //   units        int4[n_units]        \ written by the run only when they do
 //   cta_begin    int32[grid + 1]       > not fit the kernels' parameter
 //   splits       int4[n_split]        /  buffers
@@ -69,7 +72,9 @@ struct SplitList {
 struct WsHeader {
     unsigned long long status;
     uint32_t last_epoch;
-    uint32_t pad[61];
+    uint32_t pad0;
+    unsigned long long stamp;      // plan stamp of a bound workspace (oxd_plan_bind_workspace)
+    uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -82,6 +87,13 @@ struct DecodeParams {
     const int32_t* last_page_len;
     const int4* units;            // nullptr: the WorkList parameter holds the units
     const int32_t* cta_begin;     //          and the CTA ranges
+    const unsigned long long* ws_stamp;  // bound workspace: its stamp word, else nullptr
+    unsigned long long stamp;            // the plan's stamp
+    int32_t n_units;              // bounds every unit is checked against
+    int32_t n_slots;
+    int32_t batch;
+    int32_t pad0;
+    int64_t nnz;
     float* part_o;
     float* part_lse;
     unsigned long long* status;
@@ -103,6 +115,10 @@ struct MergeParams {
     const float* s;               // [.][R]
     uint16_t* out;                // bf16 rows of D
     float* lse;                   // per output row, natural log, or nullptr
+    const unsigned long long* ws_stamp;  // bound workspace: its stamp word, else nullptr
+    unsigned long long stamp;
+    int64_t n_rows;               // output rows (entries are checked against it)
+    int64_t n_states;             // states available (likewise)
     const int4* entries;          // {first_row, first, count, 0}; nullptr: the
                                   // SplitList parameter (split mode) or, in
                                   // uniform mode, entry n = {n*R, n*S, S}
@@ -117,15 +133,22 @@ struct MergeParams {
 // Implemented in oxd_decode.cu / oxd_merge.cu.
 VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
+// `work` == nullptr: the units live in memory (p.units), and the kernel is
+// launched with a small parameter block.
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                          const DecodeParams& p, const WorkList& work, int grid,
+                          const DecodeParams& p, const WorkList* work, int grid,
                           cudaStream_t stream);
 // Uniform-state merge (the public entry point).
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 // Merge of the split (request, KV head) streams of a decode run, launched
 // behind the decode kernel with programmatic dependent launch when `early`
 // (it waits for the decode grid before reading anything).
-cudaError_t launch_split_merge(const MergeParams& p, const SplitList& splits,
+cudaError_t launch_split_merge(const MergeParams& p, const SplitList* splits,
                                cudaStream_t stream, bool early);
+
+// Empty stand-in for the parameter-buffer lists of a bound run.
+struct NoList {
+    int32_t unused;
+};
 
 }  // namespace oxd

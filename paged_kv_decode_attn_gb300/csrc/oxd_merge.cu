@@ -13,6 +13,8 @@
 // the decode kernel, it first waits for that grid to complete).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "oxd_internal.h"
 
 namespace oxd {
@@ -39,6 +41,10 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, const int4* entr
         row0 = e.x;
         first = e.y;
         count = e.z;
+        // entries of a bound workspace are checked before use
+        if (row0 < 0 || row0 + p.R > p.n_rows || first < 0 || count < 0 ||
+            (first + count) * p.R > p.n_states)
+            return;
     }
     const float* s = p.s + first * p.R + r;     // state i at s[i * R]
     const float* v = p.v + (first * p.R + r) * p.D;  // state i at v[i * R * D]
@@ -83,12 +89,18 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
     merge_row(p, nullptr);
 }
 
+template <class SL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    split_merge_kernel(const MergeParams p, const __grid_constant__ SplitList inl) {
+    split_merge_kernel(const MergeParams p, const __grid_constant__ SL inl) {
     // Behind the decode kernel this waits for its grid to complete and its
     // writes to be visible; launched on its own it returns at once.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    merge_row(p, p.entries != nullptr ? p.entries : inl.entry);
+    if (p.ws_stamp != nullptr && *p.ws_stamp != p.stamp) return;  // not this plan's entries
+    const int4* entries = p.entries;
+    if constexpr (std::is_same<SL, SplitList>::value) {
+        if (entries == nullptr) entries = inl.entry;
+    }
+    merge_row(p, entries);
 }
 
 unsigned blocks_for(const MergeParams& p) {
@@ -106,7 +118,7 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_split_merge(const MergeParams& p, const SplitList& splits,
+cudaError_t launch_split_merge(const MergeParams& p, const SplitList* splits,
                                cudaStream_t stream, bool early) {
     const unsigned blocks = blocks_for(p);
     if (blocks == 0) return cudaErrorInvalidConfiguration;
@@ -120,7 +132,8 @@ cudaError_t launch_split_merge(const MergeParams& p, const SplitList& splits,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, split_merge_kernel, p, splits);
+    if (splits != nullptr) return cudaLaunchKernelEx(&cfg, split_merge_kernel<SplitList>, p, *splits);
+    return cudaLaunchKernelEx(&cfg, split_merge_kernel<NoList>, p, NoList{0});
 }
 
 }  // namespace oxd

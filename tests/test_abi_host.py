@@ -289,6 +289,23 @@ def test_destroyed_plan_is_refused():
     assert L.oxd_plan_get_info(h, ctypes.byref(info)) == oxd.OXD_ERR_PLAN_MISMATCH
 
 
+def test_bind_workspace_checks_arguments_before_any_cuda_call():
+    plan, _, _ = host_plan([300, 50], Hq=32, Hkv=8)
+    L = oxd.lib()
+    ws = BASE
+    big = plan.workspace_bytes
+    assert L.oxd_plan_bind_workspace(plan.handle, None, big, None) == \
+        oxd.OXD_ERR_INVALID_ARGUMENT
+    assert L.oxd_plan_bind_workspace(plan.handle, ws + 16, big, None) == oxd.OXD_ERR_ALIGNMENT
+    assert L.oxd_plan_bind_workspace(plan.handle, ws, big - 1, None) == \
+        oxd.OXD_ERR_WORKSPACE_TOO_SMALL
+    # a plan made for no device (num_sms given) cannot be bound to device memory
+    assert L.oxd_plan_bind_workspace(plan.handle, ws, big, None) == oxd.OXD_ERR_PLAN_MISMATCH
+    h = plan.handle
+    plan.destroy()
+    assert L.oxd_plan_bind_workspace(h, ws, big, None) == oxd.OXD_ERR_PLAN_MISMATCH
+
+
 def test_timing_events_must_come_in_pairs():
     plan, _, _ = host_plan([40], Hq=8, Hkv=8)
     L = oxd.lib()
