@@ -258,6 +258,12 @@ struct Cfg {
     static constexpr bool kMma = kMma_;
     static constexpr int kFmaGroup = kFmaGroup_;   // G of the CUDA-core variant
     static constexpr int kConsumerWarps = kMma ? kSlices * kMtiles : kSlices;
+    // Register budget: two CTAs of five warps share an SM, so one of its four
+    // register files holds three warps, which fits at most 168 registers a
+    // thread. The 16-row tensor-core and the CUDA-core variants run faster
+    // with all 168; the 8-row variant runs faster with the compiler's own
+    // choice under the launch bound.
+    static constexpr bool kRegs168 = !kMma || kHiRows;
     static constexpr int kConsumerThreads = kConsumerWarps * 32;
     static constexpr int kThreads = kConsumerThreads + 32;
     static constexpr int kStageTokens = kSlices * kSliceTokens;
@@ -270,10 +276,16 @@ struct Cfg {
     static constexpr int kRecOffset = kQOffset + kStages * kQBytes;
     static constexpr int kBarOffset = kRecOffset + kStages * 32;
     static constexpr int kIssuedOffset = kBarOffset + 2 * kStages * 8;
-    static constexpr int kFlagOffset = kIssuedOffset + kStages * 4;
+    static constexpr int kFlagOffset = (kIssuedOffset + kStages * 4 + 15) / 16 * 16;
     static constexpr int kRedOffset = kFlagOffset + 16;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRedOffset +
                                       2 * kConsumerWarps * 16 * 4;
+    // alignment each region's accesses need (the base is 1024-aligned)
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 128-byte swizzle atoms aligned");
+    static_assert(kQOffset % 128 == 0 && kQBytes % 128 == 0, "query rows: bulk copy, ldmatrix");
+    static_assert(kRecOffset % 16 == 0, "stage records");
+    static_assert(kBarOffset % 8 == 0, "mbarriers");
+    static_assert(kFlagOffset % 16 == 0 && kRedOffset % 16 == 0, "flags, reductions");
 };
 
 using CfgFmaG1 = Cfg<1, false, 4, 3, false, 1>;
@@ -613,11 +625,8 @@ struct Smem {
 // ------------------------------------------------------------------ the kernel
 
 template <class C, class WL>
-__global__ void __launch_bounds__(C::kThreads)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v,
-                        const __grid_constant__ DecodeParams p,
-                        const __grid_constant__ WL work) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                            const DecodeParams& p, const WL& work) {
     extern __shared__ uint8_t smem_raw[];
     const Smem<C> sm{reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023))};
@@ -648,7 +657,11 @@ __global__ void __launch_bounds__(C::kThreads)
         }
         flags[0] = 0;
         fence_mbar_init();
-        if (blockIdx.x == 0) *p.last_epoch = p.epoch;  // whose status the word may hold
+        if (blockIdx.x == 0) {
+            *p.last_epoch = p.epoch;  // whose status the word may hold
+            // an unbound run ends any binding of the workspace it writes
+            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
+        }
     }
     if (warp == C::kConsumerWarps && lane == 0) {
         prefetch_tmap(&tmap_k);
@@ -673,16 +686,19 @@ __global__ void __launch_bounds__(C::kThreads)
             int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
         };
         // A bound workspace is used only while it still carries this plan's
-        // stamp; every unit is bounds-checked before it is used.
-        bool usable = true;
+        // stamp; every unit is bounds-checked before it is used. The CTA's
+        // range is read together with the stamp (both lie inside the
+        // workspace) and used only if the stamp matches.
+        int u_begin = cta_begin[blockIdx.x];
+        int u_end = cta_begin[blockIdx.x + 1];
         if (p.ws_stamp != nullptr) {
             int ok_stamp = 1;
             if (lane == 0) ok_stamp = *p.ws_stamp == p.stamp ? 1 : 0;
-            usable = __shfl_sync(0xffffffffu, ok_stamp, 0) != 0;
-            if (!usable && lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+            if (!__shfl_sync(0xffffffffu, ok_stamp, 0)) {
+                if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+                u_begin = u_end = 0;
+            }
         }
-        int u_end = usable ? cta_begin[blockIdx.x + 1] : 0;
-        int u_begin = usable ? cta_begin[blockIdx.x] : 0;
         if (u_begin < 0 || u_end > p.n_units || u_begin > u_end) {
             if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
             u_begin = u_end = 0;
@@ -943,6 +959,34 @@ __global__ void __launch_bounds__(C::kThreads)
     }
 }
 
+// The decode kernel, in its two register budgets (Cfg::kRegs168).
+template <class C, class WL>
+__global__ void __launch_bounds__(C::kThreads)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ DecodeParams p,
+                        const __grid_constant__ WL work) {
+    decode_body<C, WL>(tmap_k, tmap_v, p, work);
+}
+
+template <class C, class WL>
+__global__ void __maxnreg__(168)
+    paged_decode_kernel_r168(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v,
+                             const __grid_constant__ DecodeParams p,
+                             const __grid_constant__ WL work) {
+    decode_body<C, WL>(tmap_k, tmap_v, p, work);
+}
+
+template <class C, class WL>
+using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const DecodeParams, const WL);
+
+template <class C, class WL>
+KernelFn<C, WL> kernel_of() {
+    if constexpr (C::kRegs168) return paged_decode_kernel_r168<C, WL>;
+    else return paged_decode_kernel<C, WL>;
+}
+
 // cudaFuncSetAttribute is per device; remember which devices are set up.
 template <class C, class WL>
 cudaError_t ensure_smem_attribute() {
@@ -952,8 +996,8 @@ cudaError_t ensure_smem_attribute() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(paged_decode_kernel<C, WL>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(kernel_of<C, WL>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
@@ -964,13 +1008,12 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodePar
     if (w != nullptr) {
         cudaError_t e = ensure_smem_attribute<C, WorkList>();
         if (e != cudaSuccess) return e;
-        paged_decode_kernel<C, WorkList><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p,
-                                                                                      *w);
+        kernel_of<C, WorkList>()<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p, *w);
     } else {
         cudaError_t e = ensure_smem_attribute<C, NoList>();
         if (e != cudaSuccess) return e;
-        paged_decode_kernel<C, NoList><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-            tk, tv, p, NoList{0});
+        kernel_of<C, NoList>()<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p,
+                                                                            NoList{0});
     }
     return cudaGetLastError();
 }
@@ -984,7 +1027,7 @@ template <class C>
 cudaError_t occupancy_of(int* n) {
     cudaError_t e = ensure_smem_attribute<C, WorkList>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, paged_decode_kernel<C, WorkList>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kernel_of<C, WorkList>(),
                                                          C::kThreads, C::kSmemBytes);
 }
 

@@ -425,6 +425,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         for (int i = 0; i < n_pieces; ++i) {
             const Piece& x = pieces[i];
             const int P = indptr[x.b + 1] - indptr[x.b];
+            if (x.p1 - x.p0 >= (1 << kUnitPagesBits)) return OXD_ERR_UNSUPPORTED;
             uint32_t y = static_cast<uint32_t>(x.p1 - x.p0);
             if (x.p1 == P) y |= static_cast<uint32_t>(last[x.b]) << kUnitPagesBits;
             if (x.p0 == 0) y |= 1u << 31;
@@ -658,6 +659,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.cta_begin = in_ws ? reinterpret_cast<const int32_t*>(ws + plan->off_cta) : nullptr;
     p.ws_stamp = bound ? reinterpret_cast<const unsigned long long*>(ws + kStampOff) : nullptr;
     p.stamp = plan->stamp;
+    p.clear_stamp = bound ? nullptr : reinterpret_cast<unsigned long long*>(ws + kStampOff);
     p.n_units = plan->n_items;
     p.n_slots = plan->n_slots;
     p.batch = d.batch;

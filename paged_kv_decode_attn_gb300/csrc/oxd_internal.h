@@ -89,6 +89,7 @@ struct DecodeParams {
     const int32_t* cta_begin;     //          and the CTA ranges
     const unsigned long long* ws_stamp;  // bound workspace: its stamp word, else nullptr
     unsigned long long stamp;            // the plan's stamp
+    unsigned long long* clear_stamp;     // unbound run: the workspace's stamp word, set to 0
     int32_t n_units;              // bounds every unit is checked against
     int32_t n_slots;
     int32_t batch;

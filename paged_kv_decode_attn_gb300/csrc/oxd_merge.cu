@@ -2,30 +2,22 @@
 // "Domain coverage": attention state and cascade, state merge; and the merge
 // step of the "Single decode split-K" row of "Admitted attention matrix").
 //
-// For one output row it combines states (v_i, s_i):
-//   M = max_i s_i, w_i = exp(s_i - M), v = sum w_i v_i / sum w_i,
-//   s = M + ln sum w_i,
-// with -inf states weighing nothing and an all -inf row giving v = 0,
-// s = -inf. One warp per output row; each lane owns 4 consecutive columns
-// (16-byte loads); the states are visited in order, so the result is
-// deterministic. The same kernel serves oxd_merge_states (uniform state
-// counts) and the decode run's split streams (an entry list; launched behind
-// the decode kernel, it first waits for that grid to complete).
+// One warp per output row merges its states with merge_states_row
+// (oxd_merge_row.cuh). The same kernel serves oxd_merge_states (uniform state
+// counts) and the decode run's split streams with more pieces than the
+// decode kernel merges itself (an entry list; launched behind the decode
+// kernel, it first waits for that grid to complete).
 #include <cuda_bf16.h>
 
 #include <type_traits>
 
 #include "oxd_internal.h"
+#include "oxd_merge_row.cuh"
 
 namespace oxd {
 namespace {
 
 constexpr int kWarpsPerBlock = 4;
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
 
 __device__ __forceinline__ void merge_row(const MergeParams& p, const int4* entries) {
     const int lane = threadIdx.x & 31;
@@ -46,43 +38,11 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, const int4* entr
             (first + count) * p.R > p.n_states)
             return;
     }
-    const float* s = p.s + first * p.R + r;     // state i at s[i * R]
-    const float* v = p.v + (first * p.R + r) * p.D;  // state i at v[i * R * D]
-    // pass 1: maximum LSE over the states (lanes stride over them)
-    float M = -INFINITY;
-    for (int i = lane; i < count; i += 32) M = fmaxf(M, s[static_cast<size_t>(i) * p.R] * p.s_to_ln);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float W = 0.f;
-    if (M != -INFINITY) {
-        for (int i = lane; i < count; i += 32)
-            W += expf(s[static_cast<size_t>(i) * p.R] * p.s_to_ln - M);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-    }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    const size_t vstride = static_cast<size_t>(p.R) * p.D;
-    // pass 2: weighted sum, states in order
-    for (int c = lane * 4; c < p.D; c += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int i = 0; i < count; ++i) {
-                const float w = expf(s[static_cast<size_t>(i) * p.R] * p.s_to_ln - M);
-                const float4 x = *reinterpret_cast<const float4*>(v + i * vstride + c);
-                acc.x = fmaf(w, x.x, acc.x);
-                acc.y = fmaf(w, x.y, acc.y);
-                acc.z = fmaf(w, x.z, acc.z);
-                acc.w = fmaf(w, x.w, acc.w);
-            }
-        }
-        uint2 packed;
-        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row0 + r) * p.D + c) = packed;
-    }
-    if (lane == 0 && p.lse != nullptr)
-        p.lse[row0 + r] = W > 0.f ? M + logf(W) : -INFINITY;
+    // state i of row r: s[(first + i) * R + r], v[((first + i) * R + r) * D]
+    merge_states_row(p.s + first * p.R + r, static_cast<size_t>(p.R),
+                     p.v + (first * p.R + r) * p.D, static_cast<size_t>(p.R) * p.D, count, p.D,
+                     p.s_to_ln, p.out + static_cast<size_t>(row0 + r) * p.D,
+                     p.lse != nullptr ? p.lse + row0 + r : nullptr, lane);
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {

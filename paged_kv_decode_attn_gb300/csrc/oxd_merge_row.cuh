@@ -1,0 +1,75 @@
+// One warp merges the attention states of one output row ("FlashInfer parity
+// matrix" page, "Domain coverage": attention state and cascade, state merge).
+//
+// State i has the log-sum s[i * s_stride] (times s_to_ln it is a natural
+// log) and the normalised value row v[i * v_stride + c], c < D:
+//   M = max_i s_i, w_i = exp(s_i - M),
+//   out = sum_i w_i v_i / sum_i w_i (rounded once to bf16),
+//   lse = M + ln sum_i w_i.
+// -inf states weigh nothing; a row whose states are all -inf gets out = 0 and
+// lse = -inf. Each lane owns 4 consecutive columns; the weighted sum visits
+// the states in order, so every caller (the merge kernels and the decode
+// kernel's in-place merge of split streams) gets bitwise the same result.
+// Loads go through L2 (ld.global.cg): the states may have been written by
+// other CTAs of a still-running grid.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace oxd {
+
+__device__ __forceinline__ uint32_t merge_pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride, const float* v,
+                                                 size_t v_stride, int count, int D,
+                                                 float s_to_ln, uint16_t* out_row,
+                                                 float* lse_out, int lane) {
+    // pass 1: maximum over the states (lanes stride over them), then the
+    // sum of weights; with at most 32 states lane i keeps state i's weight
+    float M = -INFINITY;
+    for (int i = lane; i < count; i += 32)
+        M = fmaxf(M, __ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float W = 0.f, w_lane = 0.f;
+    if (M != -INFINITY) {
+        for (int i = lane; i < count; i += 32) {
+            const float w = expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
+            if (i == lane) w_lane = w;
+            W += w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    // pass 2: weighted sum, states in order
+    for (int c = lane * 4; c < D; c += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll 8
+            for (int i = 0; i < count; ++i) {
+                const float w =
+                    count <= 32
+                        ? __shfl_sync(0xffffffffu, w_lane, i & 31)
+                        : expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(
+                    v + static_cast<size_t>(i) * v_stride + c));
+                acc.x = fmaf(w, x.x, acc.x);
+                acc.y = fmaf(w, x.y, acc.y);
+                acc.z = fmaf(w, x.z, acc.z);
+                acc.w = fmaf(w, x.w, acc.w);
+            }
+        }
+        uint2 packed;
+        packed.x = merge_pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = merge_pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(out_row + c) = packed;
+    }
+    if (lane == 0 && lse_out != nullptr) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+}  // namespace oxd

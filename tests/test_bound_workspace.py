@@ -132,6 +132,29 @@ def test_unbound_upload_run_of_another_plan_ends_the_binding():
     assert bool(torch.isnan(out_a.float()).all())
 
 
+def test_unbound_run_of_another_plan_ends_the_binding():
+    # the other plan's list rides in its kernels' parameters, but its run
+    # still writes partial states over the bound list: the binding ends
+    case_a, _ = _case("long_list")
+    case_b, kw_b = _case("forced_splits")
+    plan_a, plan_b = plan_case(case_a, max_splits=1), plan_case(case_b, **kw_b)
+    assert plan_b.info.upload_bytes == 0
+    tab_a, tab_b = DeviceTables(case_a), DeviceTables(case_b)
+    ref_a, _, _, _ = run_decode(case_a, plan=plan_a, tables=tab_a)
+    nbytes = max(plan_a.workspace_bytes, plan_b.workspace_bytes)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    oxd.oxd_plan_bind_workspace(plan_a, ws)
+    run_decode(case_b, plan=plan_b, tables=tab_b, workspace=ws)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    out_a, _ = _bound_run(case_a, plan_a, tab_a, ws)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_PLAN_MISMATCH
+    assert bool(torch.isnan(out_a.float()).all())
+    oxd.oxd_plan_bind_workspace(plan_a, ws)
+    out_a, _ = _bound_run(case_a, plan_a, tab_a, ws)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    assert torch.equal(out_a.view(torch.int16), ref_a.view(torch.int16))
+
+
 @pytest.mark.parametrize("region", ["units", "everything_after_header"])
 def test_damaged_list_is_reported_not_followed(region):
     # Every unit becomes 0x7f7f7f7f in each field: its first page lies far

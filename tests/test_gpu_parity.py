@@ -55,11 +55,20 @@ def test_forced_splits_agree(G):
     case = small_case(G, "NHD", 16, lengths=[1000, 333, 64, 1, 129], seed=3)
     ref_out, ref_lse = oracle_ref(case)
     outs = []
-    for force in (1, 2, 3, 7, 64):
+    for force in (1, 2, 3, 7, 8, 9, 64):
         out, lse, plan, _ = run_decode(case, force_splits=force)
         assert plan.info.max_chunks == min(force, 63)
+        assert plan.info.launches_per_run == (2 if force > 1 else 1)
         assert_parity(out, ref_out, lse, ref_lse, f"force {force}")
         outs.append(out.float())
+        # the same plan on a bound workspace: bitwise the same, run after run
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        oxd.oxd_plan_bind_workspace(plan, ws)
+        for _ in range(2):
+            out_b, lse_b, _, _ = run_decode(case, plan=plan, workspace=ws)
+            assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+            assert torch.equal(out_b.view(torch.int16), out.view(torch.int16)), f"bound {force}"
+            assert torch.equal(lse_b.view(torch.int32), lse.view(torch.int32))
     for o in outs[1:]:
         d = (o - outs[0]).abs()
         assert (d <= 1.5e-2 + 1e-2 * outs[0].abs()).all()
@@ -301,7 +310,11 @@ def test_merge_of_split_partials_equals_decode():
 def test_full_size_workloads_on_sampled_heads(name):
     cfg = W.CONFIGS[name]
     case = W.make_case(cfg, device="cuda")
-    out, lse, plan, ws = run_decode(case)   # the benchmark's launch configuration
+    # the benchmark's launch configuration: the plan bound to its workspace
+    plan = plan_case(case)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    oxd.oxd_plan_bind_workspace(plan, ws)
+    out, lse, plan, ws = run_decode(case, plan=plan, workspace=ws)
     assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     rng = np.random.default_rng(cfg.seed)
