@@ -641,7 +641,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
     // The work list sits in the parameter buffer, unless it was too long or
     // the workspace is bound (then it is in the workspace).
     const int4* units = p.units;
-    const int32_t* cta_begin = p.cta_begin;
+    const int32_t* cta_begin = nullptr;
     if constexpr (std::is_same<WL, WorkList>::value) {
         if (units == nullptr) {
             units = work.unit;
@@ -676,7 +676,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
 
     if (warp == C::kConsumerWarps) {
         // ================================================ producer warp
-        // This CTA's share of the work is units [cta_begin[c], cta_begin[c+1]).
+        // This CTA's share of the work is units [u_begin, u_end), in order.
         // The next unit's entry is read after the current unit's first stage
         // is issued and its first page indices after the second, so these
         // dependent loads overlap the current unit's streaming.
@@ -687,10 +687,21 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         };
         // A bound workspace is used only while it still carries this plan's
         // stamp; every unit is bounds-checked before it is used. The CTA's
-        // range is read together with the stamp (both lie inside the
-        // workspace) and used only if the stamp matches.
-        int u_begin = cta_begin[blockIdx.x];
-        int u_end = cta_begin[blockIdx.x + 1];
+        // range (and, from a list in memory, its first unit) is read together
+        // with the stamp (all lie inside the workspace) and used only if the
+        // stamp matches.
+        int u_begin, u_end;
+        int4 first_it = make_int4(0, 0, 0, 0);
+        const bool rec_first = cta_begin == nullptr;
+        if (rec_first) {
+            const int4 r0 = __ldg(p.cta_rec + 2 * blockIdx.x);
+            first_it = __ldg(p.cta_rec + 2 * blockIdx.x + 1);
+            u_begin = r0.x;
+            u_end = r0.y;
+        } else {
+            u_begin = cta_begin[blockIdx.x];
+            u_end = cta_begin[blockIdx.x + 1];
+        }
         if (p.ws_stamp != nullptr) {
             int ok_stamp = 1;
             if (lane == 0) ok_stamp = *p.ws_stamp == p.stamp ? 1 : 0;
@@ -721,7 +732,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         bool ok = true;
         Unit cur;
         cur.unit = u_begin;
-        load_item(cur);
+        if (rec_first)
+            cur.it = first_it;
+        else
+            load_item(cur);
         load_idx(cur);
         while (cur.unit < u_end) {
             Unit nx;

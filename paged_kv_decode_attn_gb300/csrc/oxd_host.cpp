@@ -69,9 +69,18 @@ uint32_t next_epoch() {
     return e;
 }
 
-// Start-up cost of one work unit (prologue, epilogue, refill), in tokens of
-// streaming at a CTA's share of HBM bandwidth (about 2 us).
-constexpr double kUnitOverheadTokens = 96.0;
+// Cost of one more work unit on a CTA (its epilogue and the refill of the
+// pipeline behind it), in tokens of streaming at a CTA's share of HBM
+// bandwidth, per kernel variant; measured from per-CTA timelines (about
+// 1.2 us for the 8-row tensor-core variant, 3 to 5 us for the paired 16-row
+// CTAs, whose epilogue writes 16 rows of partial state).
+double unit_overhead_tokens(int variant) {
+    switch (variant) {
+        case kVariantMma16: return 96.0;
+        case kVariantMma32: return 320.0;
+        default: return 64.0;
+    }
+}
 
 // Plan stamps: a per-process random high half and a counter, never 0, so a
 // stamp left in reused memory by another process or an earlier plan is not
@@ -306,6 +315,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         // boundaries. A CTA whose remaining room cannot hold a piece's
         // start-up and half a stage passes the next piece on.
         const double T0 = static_cast<double>(total_tokens) * H;
+        const double unit_ovh = unit_overhead_tokens(variant);
         const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
         grid = static_cast<int>(std::max<int64_t>(
             1, std::min<int64_t>(resident, static_cast<int64_t>(T0 / min_tokens))));
@@ -313,7 +323,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         int64_t streams_left = static_cast<int64_t>(B) * H;
         auto budget_for = [&](int c) {
             const double rest =
-                (T0 - done) + kUnitOverheadTokens * static_cast<double>(streams_left + grid - c - 1);
+                (T0 - done) + unit_ovh * static_cast<double>(streams_left + grid - c - 1);
             return rest / (grid - c);
         };
         int c = 0;
@@ -323,12 +333,12 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             for (int h = 0; h < H; ++h) {
                 int p = 0;
                 while (p < P) {
-                    if (c < grid - 1 && budget - used - kUnitOverheadTokens < 0.5 * min_tokens) {
+                    if (c < grid - 1 && budget - used - unit_ovh < 0.5 * min_tokens) {
                         ++c;
                         budget = budget_for(c);
                         used = 0.0;
                     }
-                    used += kUnitOverheadTokens;  // the piece's start-up
+                    used += unit_ovh;  // the piece's start-up
                     int k = P;
                     const double rest = static_cast<double>(tokens_to(b, P) - tokens_to(b, p));
                     const double room = budget - used;
@@ -463,7 +473,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->total_tokens = total_tokens;
     P->off_units = sizeof(WsHeader);
     P->off_cta = align_up(P->off_units + 16 * static_cast<size_t>(n_units), 256);
-    P->off_split = align_up(P->off_cta + 4 * (static_cast<size_t>(grid) + 1), 256);
+    P->off_split = align_up(P->off_cta + 32 * static_cast<size_t>(grid), 256);
     P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
     P->off_part_o = P->meta_bytes;
     P->off_part_lse =
@@ -504,7 +514,12 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         uint8_t* m = static_cast<uint8_t*>(P->meta);
         std::memset(m, 0, image_bytes);
         std::memcpy(m + P->off_units, units.data(), 16 * units.size());
-        std::memcpy(m + P->off_cta, cta_begin.data(), 4 * cta_begin.size());
+        int4* rec = reinterpret_cast<int4*>(m + P->off_cta);
+        for (int c = 0; c < grid; ++c) {
+            rec[2 * c] = make_int4(cta_begin[c], cta_begin[c + 1], 0, 0);
+            rec[2 * c + 1] = cta_begin[c] < cta_begin[c + 1] ? units[cta_begin[c]]
+                                                              : make_int4(0, 0, 0, 0);
+        }
         std::memcpy(m + P->off_split, split_tab.data(), 16 * split_tab.size());
         P->stamp = next_stamp();
         std::memcpy(m + P->meta_bytes, &P->stamp, sizeof(P->stamp));
@@ -656,7 +671,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.indices = indices;
     p.last_page_len = last_page_len;
     p.units = in_ws ? reinterpret_cast<const int4*>(ws + plan->off_units) : nullptr;
-    p.cta_begin = in_ws ? reinterpret_cast<const int32_t*>(ws + plan->off_cta) : nullptr;
+    p.cta_rec = in_ws ? reinterpret_cast<const int4*>(ws + plan->off_cta) : nullptr;
     p.ws_stamp = bound ? reinterpret_cast<const unsigned long long*>(ws + kStampOff) : nullptr;
     p.stamp = plan->stamp;
     p.clear_stamp = bound ? nullptr : reinterpret_cast<unsigned long long*>(ws + kStampOff);

@@ -64,9 +64,11 @@ struct SplitList {
 //                and the stamp of the plan bound to the workspace
 //   (a bound workspace holds the units, CTA ranges and merge entries for
 //   good; runs on it pass no work list and copy nothing)
-//   units        int4[n_units]        \ written by the run only when they do
-//   cta_begin    int32[grid + 1]       > not fit the kernels' parameter
-//   splits       int4[n_split]        /  buffers
+//   units        int4[n_units]        \ written by oxd_plan_bind_workspace, or
+//   cta_rec      int4[grid][2]         > by an unbound run whose list does not
+//   splits       int4[n_split]        /  fit the kernels' parameter buffers
+// cta_rec[c] = {first unit, end unit, 0, 0}, then a copy of the CTA's first
+// unit, so one 32-byte load starts the CTA.
 //   part_o       f32[n_slots][G][128]
 //   part_lse     f32[n_slots][G]  (log2 domain)
 struct WsHeader {
@@ -86,7 +88,7 @@ struct DecodeParams {
     const int32_t* indices;
     const int32_t* last_page_len;
     const int4* units;            // nullptr: the WorkList parameter holds the units
-    const int32_t* cta_begin;     //          and the CTA ranges
+    const int4* cta_rec;          //          and the CTA ranges
     const unsigned long long* ws_stamp;  // bound workspace: its stamp word, else nullptr
     unsigned long long stamp;            // the plan's stamp
     unsigned long long* clear_stamp;     // unbound run: the workspace's stamp word, set to 0

@@ -155,25 +155,40 @@ def test_unbound_run_of_another_plan_ends_the_binding():
     assert torch.equal(out_a.view(torch.int16), ref_a.view(torch.int16))
 
 
-@pytest.mark.parametrize("region", ["units", "everything_after_header"])
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("region", ["unit_array", "cta_records", "everything_after_header"])
 def test_damaged_list_is_reported_not_followed(region):
-    # Every unit becomes 0x7f7f7f7f in each field: its first page lies far
-    # beyond the index array, so the kernel rejects it before reading any
-    # index. Damaging everything after the header also puts 0x7f7f7f7f in
-    # every CTA range (beyond the unit count) and every merge entry (beyond
-    # the output rows), which are rejected the same way.
-    case, kw = _case("mqa32_pairs")
-    plan = plan_case(case, max_splits=1)
-    assert plan.info.num_split_requests == 0
+    # The workspace list: a 256-byte header, the unit array (16 bytes a
+    # unit), then at the next 256-byte boundary one 32-byte record per CTA
+    # (its unit range and a copy of its first unit). Damaged bytes read
+    # 0x7f7f7f7f in every field: a unit's first page then lies far beyond the
+    # index array, a CTA range beyond the unit count, a merge entry beyond the
+    # output rows, and the kernels reject each before any access it governs.
+    case, kw = _case("long_list")                 # about 16 units a CTA
+    plan = plan_case(case, **kw)
+    info = plan.info
+    assert info.num_split_requests == 0
     tables = DeviceTables(case)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     oxd.oxd_plan_bind_workspace(plan, ws)
-    n_units = plan.info.num_work_items
-    end = HEADER + 16 * n_units if region == "units" else plan.workspace_bytes
-    ws[HEADER:end].fill_(0x7F)
+    units_end = HEADER + 16 * info.num_work_items
+    rec_begin = _align256(units_end)
+    rec_end = rec_begin + 32 * info.grid_ctas
+    lo, hi = {"unit_array": (HEADER, units_end), "cta_records": (rec_begin, rec_end),
+              "everything_after_header": (HEADER, plan.workspace_bytes)}[region]
+    ws[lo:hi].fill_(0x7F)
     out, lse = _bound_run(case, plan, tables, ws)
     assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_PLAN_MISMATCH
-    assert bool(torch.isnan(out.float()).all()) and bool(torch.isnan(lse).all())
+    nan = torch.isnan(out.float())
+    if region == "unit_array":
+        # each CTA's first unit comes from its intact record; the rest are
+        # rejected
+        assert bool(nan.any()) and not bool(nan.all())
+    else:
+        assert bool(nan.all()) and bool(torch.isnan(lse).all())
 
 
 def test_runs_on_another_workspace_are_unaffected_by_a_binding():
