@@ -76,6 +76,8 @@ def parse_args(argv=None):
     ap.add_argument("--work-list", choices=["bound", "params"], default="bound",
                     help="bound: the plan is bound to its workspace once before the steps; "
                          "params: unbound runs")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one run in a CUDA graph and time its replays")
     return ap.parse_args(argv)
 
 
@@ -357,9 +359,25 @@ def run_oxd(args):
         flush_w.zero_()
         flush_r.sum()
 
-    def step():
+    def run_once(s):
         oxd.oxd_paged_decode_run(plan, case.q, case.k, case.v, indptr, indices, last,
-                                 case.sm_scale, out, lse, ws, plan.workspace_bytes, stream)
+                                 case.sm_scale, out, lse, ws, plan.workspace_bytes, s)
+
+    graph = None
+    if args.graph:
+        # one run captured with every pointer fixed; replays re-read the
+        # buffers' current contents
+        run_once(stream)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run_once(torch.cuda.current_stream(dev))
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            run_once(stream)
 
     K, Wm = args.steps, args.warmup
     for _ in range(Wm):
@@ -408,7 +426,7 @@ def run_oxd(args):
     for k in range(Kk):
         flush()
         oxd.oxd_plan_set_timing_events(plan, kev[k][0], kev[k][1])
-        step()
+        run_once(stream)  # direct runs: the events are recorded by the run itself
     torch.cuda.synchronize(dev)
     oxd.oxd_plan_set_timing_events(plan, None, None)
     kern_ms = [a.elapsed_time(b) for a, b in kev]
@@ -494,6 +512,7 @@ def run_oxd(args):
             "gpu_launches": K * info.launches_per_run,
             "clocks": clocks,
             "plan": {"host_us": plan_us, "work_list": args.work_list, "bind_us": bind_us,
+                     "cuda_graph": bool(args.graph),
                      **info.as_dict()},
             "wall_s_timed_loop": wall,
         }
