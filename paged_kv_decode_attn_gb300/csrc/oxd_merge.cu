@@ -19,48 +19,63 @@ namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
-__device__ __forceinline__ void merge_row(const MergeParams& p, const int4* entries) {
-    const int lane = threadIdx.x & 31;
+// The output row this warp merges: its first output row, first state and
+// state count; false when the warp has none (or its entry is out of range).
+struct RowJob {
+    long long row0, first;
+    int r, count;
+};
+
+__device__ __forceinline__ bool locate_row(const MergeParams& p, const int4* entries, RowJob* j) {
     const long long gw = static_cast<long long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (gw >= static_cast<long long>(p.n) * p.R) return;
+    if (gw >= static_cast<long long>(p.n) * p.R) return false;
     const int n = static_cast<int>(gw / p.R);
-    const int r = static_cast<int>(gw - static_cast<long long>(n) * p.R);
-    long long row0 = static_cast<long long>(n) * p.R;
-    long long first = static_cast<long long>(n) * p.S;
-    int count = p.S;
+    j->r = static_cast<int>(gw - static_cast<long long>(n) * p.R);
+    j->row0 = static_cast<long long>(n) * p.R;
+    j->first = static_cast<long long>(n) * p.S;
+    j->count = p.S;
     if (!p.uniform) {
         const int4 e = entries[n];
-        row0 = e.x;
-        first = e.y;
-        count = e.z;
+        j->row0 = e.x;
+        j->first = e.y;
+        j->count = e.z;
         // entries of a bound workspace are checked before use
-        if (row0 < 0 || row0 + p.R > p.n_rows || first < 0 || count < 0 ||
-            (first + count) * p.R > p.n_states)
-            return;
+        if (e.x < 0 || j->row0 + p.R > p.n_rows || e.y < 0 || e.z < 0 ||
+            (j->first + e.z) * p.R > p.n_states)
+            return false;
     }
+    return true;
+}
+
+__device__ __forceinline__ void merge_row(const MergeParams& p, const RowJob& j) {
     // state i of row r: s[(first + i) * R + r], v[((first + i) * R + r) * D]
-    merge_states_row(p.s + first * p.R + r, static_cast<size_t>(p.R),
-                     p.v + (first * p.R + r) * p.D, static_cast<size_t>(p.R) * p.D, count, p.D,
-                     p.s_to_ln, p.out + static_cast<size_t>(row0 + r) * p.D,
-                     p.lse != nullptr ? p.lse + row0 + r : nullptr, lane);
+    merge_states_row(p.s + j.first * p.R + j.r, static_cast<size_t>(p.R),
+                     p.v + (j.first * p.R + j.r) * p.D, static_cast<size_t>(p.R) * p.D, j.count,
+                     p.D, p.s_to_ln, p.out + static_cast<size_t>(j.row0 + j.r) * p.D,
+                     p.lse != nullptr ? p.lse + j.row0 + j.r : nullptr, threadIdx.x & 31);
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {
-    merge_row(p, nullptr);
+    RowJob j;
+    if (locate_row(p, nullptr, &j)) merge_row(p, j);
 }
 
 template <class SL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     split_merge_kernel(const MergeParams p, const __grid_constant__ SL inl) {
-    // Behind the decode kernel this waits for its grid to complete and its
-    // writes to be visible; launched on its own it returns at once.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (p.ws_stamp != nullptr && *p.ws_stamp != p.stamp) return;  // not this plan's entries
+    // The entry list and the stamp were written before the decode kernel
+    // started, so they are read first; behind the decode kernel the warp
+    // then waits for its grid to complete and its writes to be visible
+    // (launched on its own, the wait returns at once).
     const int4* entries = p.entries;
     if constexpr (std::is_same<SL, SplitList>::value) {
         if (entries == nullptr) entries = inl.entry;
     }
-    merge_row(p, entries);
+    RowJob j;
+    const bool have = (p.ws_stamp == nullptr || *p.ws_stamp == p.stamp) &&  // this plan's entries
+                      locate_row(p, entries, &j);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (have) merge_row(p, j);
 }
 
 unsigned blocks_for(const MergeParams& p) {

@@ -28,8 +28,21 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
                                                  size_t v_stride, int count, int D,
                                                  float s_to_ln, uint16_t* out_row,
                                                  float* lse_out, int lane) {
-    // pass 1: maximum over the states (lanes stride over them), then the
-    // sum of weights; with at most 32 states lane i keeps state i's weight
+    // Values are read kChunk states at a time; the first chunk of a row that
+    // fits one 128-column pass is requested together with the log-sums, so
+    // a row of up to kChunk states costs one round trip to memory.
+    constexpr int kChunk = 16;
+    const bool one_pass = D <= 128;
+    float4 x[kChunk];
+    if (one_pass && lane * 4 < D) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+            if (i < count)
+                x[i] = __ldcg(reinterpret_cast<const float4*>(v + static_cast<size_t>(i) * v_stride +
+                                                              lane * 4));
+    }
+    // maximum over the states (lanes stride over them), then the sum of
+    // weights; with at most 32 states lane i keeps state i's weight
     float M = -INFINITY;
     for (int i = lane; i < count; i += 32)
         M = fmaxf(M, __ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln);
@@ -46,22 +59,32 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
         for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
-    // pass 2: weighted sum, states in order
+    // weighted sum, states in order
     for (int c = lane * 4; c < D; c += 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (M != -INFINITY) {
-#pragma unroll 8
-            for (int i = 0; i < count; ++i) {
-                const float w =
-                    count <= 32
-                        ? __shfl_sync(0xffffffffu, w_lane, i & 31)
-                        : expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(
-                    v + static_cast<size_t>(i) * v_stride + c));
-                acc.x = fmaf(w, x.x, acc.x);
-                acc.y = fmaf(w, x.y, acc.y);
-                acc.z = fmaf(w, x.z, acc.z);
-                acc.w = fmaf(w, x.w, acc.w);
+            for (int base = 0; base < count; base += kChunk) {
+                if (!(one_pass && base == 0)) {
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i)
+                        if (base + i < count)
+                            x[i] = __ldcg(reinterpret_cast<const float4*>(
+                                v + static_cast<size_t>(base + i) * v_stride + c));
+                }
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    if (base + i < count) {
+                        const int j = base + i;
+                        const float w =
+                            count <= 32
+                                ? __shfl_sync(0xffffffffu, w_lane, j & 31)
+                                : expf(__ldcg(s + static_cast<size_t>(j) * s_stride) * s_to_ln - M);
+                        acc.x = fmaf(w, x[i].x, acc.x);
+                        acc.y = fmaf(w, x[i].y, acc.y);
+                        acc.z = fmaf(w, x[i].z, acc.z);
+                        acc.w = fmaf(w, x[i].w, acc.w);
+                    }
+                }
             }
         }
         uint2 packed;
