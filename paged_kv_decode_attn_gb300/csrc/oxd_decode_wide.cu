@@ -1,0 +1,761 @@
+// Paged-KV decode for large query groups (17..32 query heads per KV head,
+// MQA-like) on the 5th-generation tensor cores of sm_103a.
+//
+// Operation: "FlashInfer parity matrix" page, "Admitted attention matrix",
+// row "Paged batch decode" (MQA/GQA), with the F32 online softmax every
+// attention row there fixes and the split partitions + F32 partial workspace
+// of the "Single decode split-K" row. Same work list, stage records, checks,
+// status words and partial-state format as paged_decode_kernel; only the
+// arithmetic moves from mma.sync to tcgen05.
+//
+// One CTA serves all rows of a group (up to 32), three warps:
+//   * producer (warp 2): TMA copies of each stage's K and V pages (64 tokens,
+//     two 64-column halves of 128-byte swizzled rows each) into a ring of
+//     three stages, and of the group's query rows into a query tile on a
+//     unit's first stage;
+//   * MMA warp (warp 1, one thread): S = Q K^T into one of two TMEM score
+//     buffers (M = 128 rows, the group's rows first, N = 64 tokens, K = 128),
+//     then, once the softmax has written P, O += P V with P read from TMEM
+//     as the A operand and V as an MN-major B operand (N = 128 dims, K = 64
+//     tokens); each MMA is issued as soon as its inputs are ready, so the
+//     score MMA of the next stage runs while the softmax works;
+//   * softmax warp (warp 0): lane r owns query row r (TMEM lane r): it reads
+//     the stage's 64 scores, updates the running maximum and denominator,
+//     writes P as bf16 over its scores, rescales O in TMEM only when the
+//     maximum grew by more than 2^8 (otherwise the stale maximum is kept,
+//     so P stays below 256), and at a unit's end writes out/lse or the F32
+//     partial state.
+// The query tile holds only the group's 32 rows; the score MMA's rows 32..127
+// read whatever follows in shared memory and their results are never read.
+// V rows of tokens past the end of a unit are zeroed before its last PV, so
+// stale or NaN pool slots never reach O.
+// Every mbarrier wait gives up after about a second (OXD_DEVICE_WAIT_TIMEOUT);
+// before the CTA returns, the MMAs and copies already issued are drained and
+// the tensor memory is released.
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <type_traits>
+
+#include "oxd_internal.h"
+#include "oxd_ptx.cuh"
+
+namespace oxd {
+namespace {
+
+constexpr int kWRows = 32;                       // query rows a CTA serves
+constexpr int kWStageTokens = 64;
+constexpr int kWStages = 3;
+constexpr int kWThreads = 96;
+constexpr int kWHalf = kWStageTokens * 128;      // one 64-column half of K or V: 8 KB
+constexpr int kWStageBytes = 4 * kWHalf;         // K halves, then V halves: 32 KB
+constexpr int kWQHalf = kWRows * 128;            // 4 KB
+constexpr int kWQOff = 0;                        // query tile: two halves
+constexpr int kWRingOff = 2 * kWQHalf;           // 8 KB
+constexpr int kWCtlOff = kWRingOff + kWStages * kWStageBytes;
+constexpr uint32_t kWTmemCols = 256;             // O [0,128), S0 [128,192), S1 [192,256)
+static_assert(kWRingOff % 1024 == 0 && kWStageBytes % 1024 == 0, "swizzle atoms aligned");
+// The score MMA reads 128 rows (16 KB) from each query half: both spans must
+// lie inside the CTA's shared memory.
+static_assert(kWQOff + kWQHalf + 16 * 1024 <= kWCtlOff, "query-tile MMA rows in bounds");
+
+struct WStageRec {
+    int b, hkv, valid, n_stages, s, slot, row0, nrows;
+};
+
+struct WCtl {
+    WStageRec rec[kWStages];
+    uint64_t full[kWStages];
+    uint64_t empty[kWStages];
+    uint64_t s_ready[2];
+    uint64_t p_ready[2];
+    uint64_t o_ready;
+    uint64_t q_free;
+    uint64_t mma_done;
+    int issued[kWStages];
+    uint32_t tmem;
+    int flags[4];  // [0] abort
+};
+constexpr int kWSmemBytes = 1024 /* alignment slack */ + kWCtlOff + static_cast<int>(sizeof(WCtl));
+
+// ------------------------------------------------------------------ tcgen05 wrappers
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16) |
+           (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: F32 accumulator, bf16 A and B, A
+// K-major, B K-major (b_mn = 0) or MN-major (1), N / 8 and M / 16.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 64 consecutive 32-bit columns; thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,"
+        "%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,"
+        "%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+          "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]),
+          "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]),
+          "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Generic-proxy shared-memory writes made visible to the tensor core.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <class WL>
+__global__ void __launch_bounds__(kWThreads)
+    paged_decode_wide_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v,
+                             const __grid_constant__ CUtensorMap tmap_q,
+                             const __grid_constant__ DecodeParams p,
+                             const __grid_constant__ WL work) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    WCtl& ctl = *reinterpret_cast<WCtl*>(sm + kWCtlOff);
+    volatile int* flags = ctl.flags;
+    const uint32_t s_base = smem_addr(sm);
+    const uint32_t s_q = s_base + kWQOff;
+    auto ring_k = [&](int slot) { return s_base + kWRingOff + slot * kWStageBytes; };
+    auto ring_v = [&](int slot) { return s_base + kWRingOff + slot * kWStageBytes + 2 * kWHalf; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ps = p.page_size;
+    const int pages_per_stage = kWStageTokens / ps;
+    const int G = p.group;
+    const int4* units = p.units;
+    const int32_t* cta_begin = nullptr;
+    if constexpr (std::is_same<WL, WorkList>::value) {
+        if (units == nullptr) {
+            units = work.unit;
+            cta_begin = work.cta_begin;
+        }
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], 1);
+            ctl.issued[s] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl.s_ready[i], 1);
+            mbar_init(&ctl.p_ready[i], 1);
+        }
+        mbar_init(&ctl.o_ready, 1);
+        mbar_init(&ctl.q_free, 1);
+        mbar_init(&ctl.mma_done, 1);
+        flags[0] = 0;
+        fence_mbar_init();
+        if (blockIdx.x == 0) {
+            *p.last_epoch = p.epoch;  // whose status the word may hold
+            // an unbound run ends any binding of the workspace it writes
+            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
+        }
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_addr(&ctl.tmem)),
+            "r"(kWTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 2 && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        prefetch_tmap(&tmap_q);
+    }
+    // The merge kernel, when the plan has one, may be scheduled now; it waits
+    // for this grid to complete before it reads anything.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem;
+    const uint32_t t_o = tmem;
+    auto t_s = [&](int buf) { return tmem + 128u + 64u * static_cast<uint32_t>(buf); };
+
+    if (warp == 2) {
+        // ================================================ producer warp
+        struct Unit {
+            int unit;
+            int4 it;
+            int win, nxt;  // page indices [0, 32) and [32, 64) of the unit, by lane
+        };
+        // A bound workspace is used only while it still carries this plan's
+        // stamp; every unit is bounds-checked before it is used.
+        int u_begin, u_end;
+        int4 first_it = make_int4(0, 0, 0, 0);
+        const bool rec_first = cta_begin == nullptr;
+        if (rec_first) {
+            const int4 r0 = __ldg(p.cta_rec + 2 * blockIdx.x);
+            first_it = __ldg(p.cta_rec + 2 * blockIdx.x + 1);
+            u_begin = r0.x;
+            u_end = r0.y;
+        } else {
+            u_begin = cta_begin[blockIdx.x];
+            u_end = cta_begin[blockIdx.x + 1];
+        }
+        if (p.ws_stamp != nullptr) {
+            int ok_stamp = 1;
+            if (lane == 0) ok_stamp = *p.ws_stamp == p.stamp ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok_stamp, 0)) {
+                if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+                u_begin = u_end = 0;
+            }
+        }
+        if (u_begin < 0 || u_end > p.n_units || u_begin > u_end) {
+            if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+            u_begin = u_end = 0;
+        }
+        auto pages_of = [](const int4& it) { return it.y & ((1 << kUnitPagesBits) - 1); };
+        auto load_item = [&](Unit& u) {
+            if (u.unit < u_end) u.it = units[u.unit];
+        };
+        auto load_idx = [&](Unit& u) {
+            u.win = u.nxt = 0;
+            if (u.unit < u_end && u.it.x >= 0 &&
+                static_cast<int64_t>(u.it.x) + pages_of(u.it) <= p.nnz) {
+                const int32_t* idx = p.indices + u.it.x;
+                const int n = pages_of(u.it);
+                if (lane < n) u.win = __ldg(idx + lane);
+                if (32 + lane < n) u.nxt = __ldg(idx + 32 + lane);
+            }
+        };
+        int g = 0;        // ring position
+        int started = 0;  // units whose stages were issued
+        bool ok = true;
+        Unit cur;
+        cur.unit = u_begin;
+        if (rec_first)
+            cur.it = first_it;
+        else
+            load_item(cur);
+        load_idx(cur);
+        while (cur.unit < u_end) {
+            Unit nx;
+            nx.unit = cur.unit + 1;
+            bool nx_item = false, nx_idx = false;
+            const int4 it = cur.it;
+            const int n_pages = pages_of(it);
+            const int last_len = (it.y >> kUnitPagesBits) & 0x7f;  // 0: not the last page
+            const bool first_page = it.y < 0;                         // bit 31
+            const int b = it.z & ((1 << kUnitBBits) - 1);
+            const bool half_bit = ((it.z >> kUnitBBits) & 1) != 0;   // never set for this kernel
+            const int hkv = static_cast<int>(static_cast<uint32_t>(it.z) >> (kUnitBBits + 1));
+            const int valid = last_len ? (n_pages - 1) * ps + last_len : n_pages * ps;
+            int n_stages = (n_pages + pages_per_stage - 1) / pages_per_stage;
+            const bool unit_ok = n_pages >= 1 && it.x >= 0 &&
+                                 static_cast<int64_t>(it.x) + n_pages <= p.nnz && b < p.batch &&
+                                 hkv < p.num_kv_heads && !half_bit && it.w >= -1 &&
+                                 it.w < p.n_slots && last_len <= ps;
+            if (!unit_ok) {
+                // not a unit of this plan: skip it (its outputs stay unwritten)
+                if (lane == 0) record_status(p.status, p.epoch, kDevicePlanMismatch);
+                n_stages = 0;
+            }
+            int ip0 = 0, ip1 = 0, lst = 0;
+            if (lane == 0 && unit_ok) {
+                if (first_page) ip0 = p.indptr[b];
+                if (last_len) {
+                    ip1 = p.indptr[b + 1];
+                    lst = p.last_page_len[b];
+                }
+            }
+            // An index outside [0, num_pages) is recorded and replaced by page
+            // 0, so every copy stays inside the pool.
+            const int32_t* idx = p.indices + it.x;
+            int win = cur.win, nxt = cur.nxt;
+            int win_base = 0;
+            bool bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+            if (__any_sync(0xffffffffu, bad) && lane == 0)
+                record_status(p.status, p.epoch, kDeviceBadPage);
+            win = bad ? 0 : win;
+            for (int s = 0; s < n_stages; ++s, ++g) {
+                const int slot = g % kWStages;
+                const int pg0 = s * pages_per_stage;
+                const int npg = min(pages_per_stage, n_pages - pg0);
+                if (pg0 >= win_base + 32) {
+                    win = nxt;
+                    win_base += 32;
+                    nxt = win_base + 32 + lane < n_pages ? __ldg(idx + win_base + 32 + lane) : 0;
+                    bad = win < 0 || static_cast<int64_t>(win) >= p.num_pages;
+                    if (__any_sync(0xffffffffu, bad) && lane == 0)
+                        record_status(p.status, p.epoch, kDeviceBadPage);
+                    win = bad ? 0 : win;
+                }
+                int okw = 1;
+                if (lane == 0) {
+                    if (g >= kWStages)
+                        okw = mbar_wait(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags) ? 1 : 0;
+                    // the query tile is rewritten only after the previous
+                    // unit's last score MMA has read it
+                    if (okw && s == 0 && started > 0)
+                        okw = mbar_wait(&ctl.q_free, (started - 1) & 1, flags) ? 1 : 0;
+                }
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    WStageRec* r = &ctl.rec[slot];
+                    r->b = b;
+                    r->hkv = hkv;
+                    r->valid = valid;
+                    r->n_stages = n_stages;
+                    r->s = s;
+                    r->slot = it.w;
+                    r->row0 = 0;
+                    r->nrows = G;
+                    const uint32_t qbytes = s == 0 ? 2u * kWQHalf : 0u;
+                    mbar_arrive_expect_tx(&ctl.full[slot],
+                                          npg * ps * kHeadDim * 2 * 2 + qbytes);
+                    if (s == 0) {
+                        const int qrow = b * p.num_qo_heads + hkv * G;
+                        tma_load_2d(s_q, &tmap_q, &ctl.full[slot], 0, qrow);
+                        tma_load_2d(s_q + kWQHalf, &tmap_q, &ctl.full[slot], 64, qrow);
+                    }
+                }
+                const uint32_t tk = ring_k(slot);
+                const uint32_t tv = ring_v(slot);
+                const int ca = p.layout == 0 ? hkv : 0;  // coordinates (d, A, B, page):
+                const int cb = p.layout == 0 ? 0 : hkv;  // NHD (d, head, token, page)
+                for (int j = 0; j < npg; ++j) {          // HND (d, token, head, page)
+                    const int page = __shfl_sync(0xffffffffu, win, pg0 - win_base + j);
+                    if (lane == 0) {
+                        const uint32_t off = j * ps * 128;
+                        tma_load_4d(tk + off, &tmap_k, &ctl.full[slot], 0, ca, cb, page);
+                        tma_load_4d(tk + kWHalf + off, &tmap_k, &ctl.full[slot], 64, ca, cb, page);
+                        tma_load_4d(tv + off, &tmap_v, &ctl.full[slot], 0, ca, cb, page);
+                        tma_load_4d(tv + kWHalf + off, &tmap_v, &ctl.full[slot], 64, ca, cb, page);
+                    }
+                }
+                if (lane == 0) ctl.issued[slot] += 1;
+                if (s == 0) {
+                    load_item(nx);
+                    nx_item = true;
+                } else if (s == 1) {
+                    load_idx(nx);
+                    nx_idx = true;
+                }
+            }
+            if (!ok) break;
+            if (n_stages > 0) ++started;
+            if (!nx_item) load_item(nx);
+            if (!nx_idx) load_idx(nx);
+            if (lane == 0 && unit_ok &&
+                ((first_page && ip0 != it.x) ||
+                 (last_len && (ip1 != it.x + n_pages || lst != last_len))))
+                record_status(p.status, p.epoch, kDevicePlanMismatch);
+            cur = nx;
+        }
+        if (ok) {
+            // End marker: a stage whose record says s = -1, completed by a
+            // plain arrive (no bytes).
+            const int slot = g % kWStages;
+            int okw = 1;
+            if (lane == 0) {
+                if (g >= kWStages)
+                    okw = mbar_wait(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags) ? 1 : 0;
+                if (okw) {
+                    ctl.rec[slot].s = -1;
+                    mbar_arrive(&ctl.full[slot]);
+                    ctl.issued[slot] += 1;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, okw, 0) != 0;
+        }
+        if (!ok && lane == 0) {
+            flags[0] = 1;
+            record_status(p.status, p.epoch, kDeviceWaitTimeout);
+        }
+    } else if (warp == 1) {
+        // ================================================ MMA warp
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = umma_idesc(128, kWStageTokens, 0);
+            constexpr uint32_t kIdPV = umma_idesc(128, kHeadDim, 1);
+            // Two kinds of work, issued as soon as each is ready: the score
+            // MMA of stage gq (once its K/V have landed and its score buffer
+            // is free, i.e. the PV of stage gq - 2 was issued) and the PV of
+            // stage gp (once the softmax has written its P).
+            int gq = 0, gp = 0;
+            int slot_even = 0, slot_odd = 0;    // ring slot of the pending stages,
+            bool first_even = false, first_odd = false;  // by stage parity
+            bool ended = false, ok = true, issued_any = false;
+            uint64_t idle_since = global_ns();
+            while (!(ended && gp == gq)) {
+                bool progress = false;
+                if (!ended && gq < gp + 2 &&
+                    mbar_try_wait(&ctl.full[gq % kWStages], (gq / kWStages) & 1)) {
+                    const int slot = gq % kWStages;
+                    const WStageRec rec = ctl.rec[slot];
+                    if (rec.s < 0) {
+                        ended = true;
+                    } else {
+                        tc_fence_after();
+                        // S = Q K^T: K = 128 in steps of 16 (32 bytes of a
+                        // 128-byte swizzled row; columns 64..127 in the other
+                        // half)
+                        const uint32_t k0 = ring_k(slot);
+                        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                            const uint32_t h = static_cast<uint32_t>(ks >> 2), kk = ks & 3;
+                            const uint64_t ad = umma_sdesc(s_q + h * kWQHalf + kk * 32, 16, 1024);
+                            const uint64_t bd = umma_sdesc(k0 + h * kWHalf + kk * 32, 16, 1024);
+                            umma_ss(t_s(gq & 1), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
+                        }
+                        issued_any = true;
+                        umma_commit(&ctl.s_ready[gq & 1]);
+                        if (rec.s == rec.n_stages - 1) umma_commit(&ctl.q_free);
+                        if (gq & 1) {
+                            slot_odd = slot;
+                            first_odd = rec.s == 0;
+                        } else {
+                            slot_even = slot;
+                            first_even = rec.s == 0;
+                        }
+                        ++gq;
+                    }
+                    progress = true;
+                }
+                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1)) {
+                    tc_fence_after();
+                    // O += P V: 16 tokens a step = two 8-row groups (1024 B
+                    // apart); the two 64-column halves of V are kWHalf apart
+                    const int slot = (gp & 1) ? slot_odd : slot_even;
+                    const bool first = (gp & 1) ? first_odd : first_even;
+                    const uint32_t v0 = ring_v(slot);
+                    for (int ks = 0; ks < kWStageTokens / 16; ++ks) {
+                        const uint64_t bd = umma_sdesc(v0 + ks * 2048, kWHalf, 1024);
+                        umma_ts(t_o, t_s(gp & 1) + 8u * ks, bd, kIdPV,
+                                (ks > 0 || !first) ? 1u : 0u);
+                    }
+                    umma_commit(&ctl.empty[slot]);  // K and V of the slot are consumed
+                    umma_commit(&ctl.o_ready);
+                    ++gp;
+                    progress = true;
+                }
+                if (progress) {
+                    idle_since = global_ns();
+                } else if (flags[0] ||
+                           global_ns() - idle_since > static_cast<uint64_t>(kWaitTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) {
+                flags[0] = 1;
+                record_status(p.status, p.epoch, kDeviceWaitTimeout);
+            }
+            if (issued_any) {
+                // every MMA completes before the tensor memory is released
+                umma_commit(&ctl.mma_done);
+                mbar_wait(&ctl.mma_done, 0, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================================================ softmax warp
+        // Lane r owns query row r, which is TMEM lane r. Every lane waits on
+        // each barrier itself; the results are AND-ed over the warp so the
+        // lanes always take the same path through the collective TMEM
+        // instructions.
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, flags));
+        };
+        const float sc = p.scale_log2;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int g = 0;; ++g) {
+            const int slot = g % kWStages;
+            if (!wait_all(&ctl.full[slot], (g / kWStages) & 1)) {
+                ok = false;
+                break;
+            }
+            const WStageRec rec = ctl.rec[slot];
+            if (rec.s < 0) break;
+            if (!wait_all(&ctl.s_ready[g & 1], (g >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[64];
+            tmem_ld64(t_s(g & 1), sr);
+            const int nvalid = min(kWStageTokens, rec.valid - rec.s * kWStageTokens);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float x = j < nvalid ? __uint_as_float(sr[j]) * sc : -INFINITY;
+                sr[j] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const bool first = rec.s == 0;
+            float alpha = 1.f;
+            bool rescale = false;
+            if (first) {
+                m_ref = mx;
+                l = 0.f;
+            } else if (mx > m_ref + 8.f && lane < rec.nrows) {
+                alpha = fast_exp2(m_ref - mx);
+                m_ref = mx;
+                l *= alpha;
+                rescale = true;
+            }
+            uint32_t pk[32];
+            float ls = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_ref);
+                const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_ref);
+                ls += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l += ls;
+            tmem_st32(t_s(g & 1), pk);
+            tmem_wait_st();
+            // PV of the previous stage is done before O is touched (and this
+            // barrier's phases are followed one by one)
+            if (g > 0) {
+                if (!wait_all(&ctl.o_ready, (g - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
+                    uint32_t o[64];
+                    tmem_ld64(t_o + c0, o);
+                    uint32_t w0[32], w1[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        w0[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        w1[j] = __float_as_uint(__uint_as_float(o[32 + j]) * alpha);
+                    }
+                    tmem_st32(t_o + c0, w0);
+                    tmem_st32(t_o + c0 + 32, w1);
+                }
+                tmem_wait_st();
+            }
+            const bool last = rec.s == rec.n_stages - 1;
+            if (last && nvalid < kWStageTokens) {
+                // zero V rows past the unit's end (whole 128-byte rows, so the
+                // swizzle does not matter)
+                uint8_t* v0 = sm + kWRingOff + slot * kWStageBytes + 2 * kWHalf;
+                const int n16 = (kWStageTokens - nvalid) * 16;
+                for (int i = lane; i < n16; i += 32) {
+                    const int row = nvalid + (i >> 4), c = i & 15;
+                    *reinterpret_cast<uint4*>(v0 + (c >> 3) * kWHalf + row * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.p_ready[g & 1]);
+            if (last) {
+                // ---- unit epilogue: O / l
+                if (!wait_all(&ctl.o_ready, g & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float inv = 1.f / l;
+                const float lse2 = m_ref + __log2f(l);
+                const bool row_ok = lane < rec.nrows;
+                const int hq = rec.hkv * G + lane;
+                for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
+                    uint32_t o[64];
+                    tmem_ld64(t_o + c0, o);
+                    if (!row_ok) continue;
+                    if (rec.slot < 0) {
+                        uint16_t* dst = p.out +
+                                        (static_cast<size_t>(rec.b) * p.num_qo_heads + hq) *
+                                            kHeadDim + c0;
+#pragma unroll
+                        for (int j = 0; j < 64; j += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[j]) * inv,
+                                              __uint_as_float(o[j + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv,
+                                              __uint_as_float(o[j + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv,
+                                              __uint_as_float(o[j + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv,
+                                              __uint_as_float(o[j + 7]) * inv);
+                            *reinterpret_cast<uint4*>(dst + j) = w;
+                        }
+                    } else {
+                        // partial states are [slot][G][128]
+                        float* dst = p.part_o +
+                                     (static_cast<size_t>(rec.slot) * G + lane) * kHeadDim + c0;
+#pragma unroll
+                        for (int j = 0; j < 64; j += 4)
+                            *reinterpret_cast<float4*>(dst + j) =
+                                make_float4(__uint_as_float(o[j]) * inv,
+                                            __uint_as_float(o[j + 1]) * inv,
+                                            __uint_as_float(o[j + 2]) * inv,
+                                            __uint_as_float(o[j + 3]) * inv);
+                    }
+                }
+                if (row_ok) {
+                    if (rec.slot < 0) {
+                        if (p.lse != nullptr)
+                            p.lse[static_cast<size_t>(rec.b) * p.num_qo_heads + hq] = lse2 * kLn2;
+                    } else {
+                        p.part_lse[static_cast<size_t>(rec.slot) * G + lane] = lse2;
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            flags[0] = 1;
+            record_status(p.status, p.epoch, kDeviceWaitTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();  // every warp has left its loop; the MMAs have completed
+
+    if (flags[0] && threadIdx.x == 0) {
+        // Aborted: wait (bounded) for the copies already issued, then leave.
+        for (int s = 0; s < kWStages; ++s)
+            if (ctl.issued[s] > 0)
+                mbar_wait(&ctl.full[s], (ctl.issued[s] - 1) & 1, nullptr);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kWTmemCols)
+                     : "memory");
+    }
+}
+
+template <class WL>
+cudaError_t ensure_wide_attribute() {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(paged_decode_wide_kernel<WL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
+
+}  // namespace
+
+VariantShape wide_shape() { return {kWThreads, kWStageTokens, kWStages, kWSmemBytes}; }
+
+// Resident CTAs per SM from shared memory, threads and tensor-memory columns.
+// The occupancy query answers 1 for any kernel that uses tcgen05; two of
+// these CTAs (256 TMEM columns each) do run side by side on one SM.
+cudaError_t wide_occupancy(int* n) {
+    cudaError_t e = ensure_wide_attribute<WorkList>();
+    if (e != cudaSuccess) return e;
+    int dev = 0, smem_sm = 0, reserved = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+        cudaSuccess)
+        return e;
+    const int by_smem = smem_sm / (kWSmemBytes + reserved);
+    const int by_tmem = 512 / static_cast<int>(kWTmemCols);
+    const int by_threads = 2048 / kWThreads;
+    *n = max(1, min(by_smem, min(by_tmem, by_threads)));
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_wide(const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tq, const DecodeParams& p, const WorkList* w,
+                               int grid, cudaStream_t stream) {
+    if (w != nullptr) {
+        cudaError_t e = ensure_wide_attribute<WorkList>();
+        if (e != cudaSuccess) return e;
+        paged_decode_wide_kernel<WorkList><<<grid, kWThreads, kWSmemBytes, stream>>>(tk, tv, tq,
+                                                                                     p, *w);
+    } else {
+        cudaError_t e = ensure_wide_attribute<NoList>();
+        if (e != cudaSuccess) return e;
+        paged_decode_wide_kernel<NoList><<<grid, kWThreads, kWSmemBytes, stream>>>(
+            tk, tv, tq, p, NoList{0});
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace oxd

@@ -78,6 +78,7 @@ double unit_overhead_tokens(int variant) {
     switch (variant) {
         case kVariantMma16: return 96.0;
         case kVariantMma32: return 320.0;
+        case kVariantWide: return 96.0;
         default: return 64.0;
     }
 }
@@ -126,7 +127,7 @@ int choose_variant(int G) {
     if (G == 2) return kVariantFmaG2;
     if (G <= 8) return kVariantMma8;
     if (G <= 16) return kVariantMma16;
-    return kVariantMma32;
+    return kVariantWide;
 }
 
 // Resident CTAs per SM without a device: limited by shared memory (228 KB
@@ -191,6 +192,24 @@ bool encode_pool(CUtensorMap* map, const void* pool, const oxd_paged_decode_desc
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
                      strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D map over q as [B*Hq rows][128] for the tcgen05 variant: a box is 32
+// rows x 64 columns with the 128-byte swizzle its score MMA reads; rows past
+// the end read as zeros.
+bool encode_q(CUtensorMap* map, const void* q, const oxd_paged_decode_desc& d) {
+    EncodeTiledFn enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                                static_cast<cuuint64_t>(d.batch) * d.num_qo_heads};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t elem[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims,
+                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -647,8 +666,9 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
         if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
     }
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq;
     if (!encode_pool(&tk, k_pages, d) || !encode_pool(&tv, v_pages, d)) return OXD_ERR_CUDA;
+    if (plan->variant == kVariantWide && !encode_q(&tq, q, d)) return OXD_ERR_CUDA;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -694,9 +714,12 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_decode(plan->variant, tk, tv, p, in_ws ? nullptr : plan->work, plan->grid, s) !=
-        cudaSuccess)
-        return OXD_ERR_CUDA;
+    const WorkList* inline_list = in_ws ? nullptr : plan->work;
+    const cudaError_t le =
+        plan->variant == kVariantWide
+            ? launch_decode_wide(tk, tv, tq, p, inline_list, plan->grid, s)
+            : launch_decode(plan->variant, tk, tv, p, inline_list, plan->grid, s);
+    if (le != cudaSuccess) return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->n_split > 0) {

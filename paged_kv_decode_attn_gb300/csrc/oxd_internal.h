@@ -20,7 +20,8 @@ enum Variant : int {
     kVariantMma8 = 2,    // mma.sync m16n8k16, 3 <= G <= 8 (rows 8..15 of the tile idle)
     kVariantMma16 = 3,   // mma.sync, 9 <= G <= 16
     kVariantMma32 = 4,   // 17 <= G <= 32: each piece runs on a pair of 16-row CTAs
-    kNumVariants = 5
+    kVariantWide = 5,    // 17 <= G <= 32: tcgen05 (TMEM accumulators), one CTA per piece
+    kNumVariants = 6
 };
 
 struct VariantShape {
@@ -141,6 +142,13 @@ cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           const DecodeParams& p, const WorkList* work, int grid,
                           cudaStream_t stream);
+// The tcgen05 variant for groups of 17..32 query heads (oxd_decode_wide.cu);
+// `tq` maps q as [B*Hq rows][128] with the 128-byte swizzle.
+VariantShape wide_shape();
+cudaError_t wide_occupancy(int* ctas_per_sm);
+cudaError_t launch_decode_wide(const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tq, const DecodeParams& p, const WorkList* w,
+                               int grid, cudaStream_t stream);
 // Uniform-state merge (the public entry point).
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 // Merge of the split (request, KV head) streams of a decode run, launched

@@ -121,7 +121,7 @@ def test_max_splits_caps_chunks():
 
 
 @pytest.mark.parametrize("G,variant", [(1, 0), (2, 1), (3, 2), (8, 2), (9, 3), (16, 3),
-                                       (17, 4), (32, 4)])
+                                       (17, 5), (32, 5)])
 def test_variant_follows_group_size(G, variant):
     plan, _, _ = host_plan([64], Hq=G * 2, Hkv=2)
     assert plan.info.kernel_variant == variant
