@@ -92,7 +92,10 @@ typedef struct {
     int32_t max_splits;     /* 0 = planner's choice; 1 = never split; n = at most n per request */
     int32_t force_splits;   /* 0 = off; n > 0: split every request into min(n, P_b) chunks */
     int32_t num_sms;        /* 0 = query the device; > 0 = plan for that many SMs */
-    int32_t reserved[3];    /* must be zero */
+    int32_t tensor_path;    /* groups of 17..32 query heads: 0 = tcgen05 (TMEM accumulators,
+                               one CTA per piece), 1 = mma.sync (pairs of 16-row CTAs);
+                               other groups ignore it */
+    int32_t reserved[2];    /* must be zero */
 } oxd_paged_decode_desc;
 
 typedef struct {

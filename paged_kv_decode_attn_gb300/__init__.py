@@ -88,7 +88,7 @@ class Desc(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
         ("force_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("tensor_path", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -326,9 +326,9 @@ def oxd_read_device_status(workspace, stream=None) -> int:
 
 
 def make_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages, head_dim=128,
-              max_splits=0, force_splits=0, num_sms=0) -> Desc:
+              max_splits=0, force_splits=0, num_sms=0, tensor_path=0) -> Desc:
     """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return Desc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
-                max_splits, force_splits, num_sms, (ctypes.c_int32 * 3)(0, 0, 0))
+                max_splits, force_splits, num_sms, tensor_path, (ctypes.c_int32 * 2)(0, 0))

@@ -122,12 +122,12 @@ bool overlap(const Span& a, const Span& b) {
     return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
 }
 
-int choose_variant(int G) {
+int choose_variant(int G, int tensor_path) {
     if (G == 1) return kVariantFmaG1;
     if (G == 2) return kVariantFmaG2;
     if (G <= 8) return kVariantMma8;
     if (G <= 16) return kVariantMma16;
-    return kVariantWide;
+    return tensor_path == 1 ? kVariantMma32 : kVariantWide;
 }
 
 // Resident CTAs per SM without a device: limited by shared memory (228 KB
@@ -223,7 +223,8 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->max_splits < 0 || d->force_splits < 0 || d->num_sms < 0)
         return OXD_ERR_INVALID_ARGUMENT;
-    if (d->reserved[0] != 0 || d->reserved[1] != 0 || d->reserved[2] != 0)
+    if (d->tensor_path != 0 && d->tensor_path != 1) return OXD_ERR_INVALID_ARGUMENT;
+    if (d->reserved[0] != 0 || d->reserved[1] != 0)
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
     if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
@@ -289,7 +290,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     }
 
     const int G = d.num_qo_heads / d.num_kv_heads;
-    const int variant = choose_variant(G);
+    const int variant = choose_variant(G, d.tensor_path);
     const VariantShape vs = variant_shape(variant);
     int num_sms = d.num_sms, ctas_per_sm = 0, plan_device = -1;
     if (num_sms == 0) {

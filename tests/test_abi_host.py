@@ -125,6 +125,9 @@ def test_max_splits_caps_chunks():
 def test_variant_follows_group_size(G, variant):
     plan, _, _ = host_plan([64], Hq=G * 2, Hkv=2)
     assert plan.info.kernel_variant == variant
+    # the mma.sync path for large groups: pairs of 16-row CTAs
+    plan, _, _ = host_plan([64], Hq=G * 2, Hkv=2, tensor_path=1)
+    assert plan.info.kernel_variant == (4 if G > 16 else variant)
 
 
 BAD_DESC = {
@@ -137,6 +140,7 @@ BAD_DESC = {
     "num_pages0": dict(num_pages=0),
     "reserved": "reserved",
     "negative_splits": dict(max_splits=-1),
+    "tensor_path": dict(tensor_path=2),
 }
 
 

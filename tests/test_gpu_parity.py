@@ -50,6 +50,20 @@ def test_parity_small(G, layout, ps):
     assert_parity(out1, ref_out, lse1, ref_lse, f"G{G} {layout} ps{ps} unsplit")
 
 
+@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("G", [17, 32])
+def test_both_tensor_paths_for_large_groups(G, layout, ps):
+    # groups over 16 heads: tcgen05 (default) and mma.sync on paired CTAs
+    case = small_case(G, layout, ps)
+    ref_out, ref_lse = oracle_ref(case)
+    for path in (0, 1):
+        for force in (0, 3):
+            out, lse, plan, _ = run_decode(case, tensor_path=path, force_splits=force)
+            assert plan.info.kernel_variant == (5 if path == 0 else 4)
+            assert_parity(out, ref_out, lse, ref_lse, f"G{G} {layout} ps{ps} path {path}")
+
+
 @pytest.mark.parametrize("G", [1, 4, 32])
 def test_forced_splits_agree(G):
     case = small_case(G, "NHD", 16, lengths=[1000, 333, 64, 1, 129], seed=3)
