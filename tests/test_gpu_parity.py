@@ -64,6 +64,26 @@ def test_both_tensor_paths_for_large_groups(G, layout, ps):
             assert_parity(out, ref_out, lse, ref_lse, f"G{G} {layout} ps{ps} path {path}")
 
 
+@pytest.mark.parametrize("G,force", [(32, 0), (32, 2), (4, 0), (1, 0)])
+def test_scores_growing_along_the_sequence(G, force):
+    # Keys grow with their position, so each row's running maximum keeps
+    # rising by many units of log2 from stage to stage: the online softmax
+    # rescales again and again (the tcgen05 path only when the rise exceeds
+    # 2^8, which this case forces every few stages).
+    Hkv = 1 if G == 32 else 8
+    case = small_case(G, "NHD", 16, lengths=[1500, 700, 129], Hkv=Hkv, seed=12,
+                      sm_scale=0.5)
+    t = case.tables
+    ps = case.page_size
+    for b in range(case.batch):
+        for lp in range(int(t.indptr[b + 1] - t.indptr[b])):
+            phys = int(t.indices[t.indptr[b] + lp])
+            case.k[phys] *= 1.0 + lp * ps / 64.0
+    ref_out, ref_lse = oracle_ref(case)
+    out, lse, plan, _ = run_decode(case, force_splits=force)
+    assert_parity(out, ref_out, lse, ref_lse, f"growing scores G{G} force {force}")
+
+
 @pytest.mark.parametrize("G", [1, 4, 32])
 def test_forced_splits_agree(G):
     case = small_case(G, "NHD", 16, lengths=[1000, 333, 64, 1, 129], seed=3)
