@@ -84,6 +84,21 @@ def test_scores_growing_along_the_sequence(G, force):
     assert_parity(out, ref_out, lse, ref_lse, f"growing scores G{G} force {force}")
 
 
+@pytest.mark.parametrize("path", [0, 1])
+def test_many_short_units_per_cta_large_group(path):
+    # 600 MQA requests of 1..300 tokens, planned for one SM: every CTA runs
+    # hundreds of units back to back (query tile reloads, per-unit epilogues,
+    # split and whole units interleaved)
+    rng = np.random.default_rng(5)
+    lengths = [int(x) for x in rng.integers(1, 301, 600)]
+    case = small_case(32, "NHD", 16, lengths=lengths, Hkv=1, seed=6)
+    ref_out, ref_lse = oracle_ref(case)
+    out, lse, plan, ws = run_decode(case, num_sms=1, tensor_path=path)
+    assert plan.info.grid_ctas <= 4 and plan.info.num_work_items >= 600
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    assert_parity(out, ref_out, lse, ref_lse, f"many units path {path}")
+
+
 @pytest.mark.parametrize("G", [1, 4, 32])
 def test_forced_splits_agree(G):
     case = small_case(G, "NHD", 16, lengths=[1000, 333, 64, 1, 129], seed=3)
