@@ -710,16 +710,16 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
                 const uint32_t tv = tk + C::kStageBytes / 2;
                 const int ca = p.layout == 0 ? hkv : 0;  // coordinates (d, A, B, page):
                 const int cb = p.layout == 0 ? 0 : hkv;  // NHD (d, head, token, page)
-                for (int j = 0; j < npg; ++j) {          // HND (d, token, head, page)
-                    const int page = __shfl_sync(0xffffffffu, win, pg0 - win_base + j);
-                    if (lane == 0) {
-                        const uint32_t off = j * ps * 256;
-                        tma_load_4d(tk + off, &tmap_k, sm.full(slot), 0, ca, cb, page);
-                        tma_load_4d(tk + off + half_bytes, &tmap_k, sm.full(slot), 64, ca, cb,
-                                    page);
-                        tma_load_4d(tv + off, &tmap_v, sm.full(slot), 0, ca, cb, page);
-                        tma_load_4d(tv + off + half_bytes, &tmap_v, sm.full(slot), 64, ca, cb,
-                                    page);
+                {                                        // HND (d, token, head, page)
+                    // One copy per (page, tensor, 64-column half), one lane each,
+                    // so the whole stage is issued by one warp instruction:
+                    // lane 4j + 2t + h copies half h of tensor t (K, V) of page j.
+                    const int j = lane >> 2;
+                    const int page = __shfl_sync(0xffffffffu, win, (pg0 - win_base + j) & 31);
+                    if (lane < 4 * npg) {
+                        const uint32_t off = j * ps * 256 + ((lane & 1) ? half_bytes : 0);
+                        tma_load_4d(((lane & 2) ? tv : tk) + off, (lane & 2) ? &tmap_v : &tmap_k,
+                                    sm.full(slot), (lane & 1) * 64, ca, cb, page);
                     }
                 }
                 if (lane == 0) sm.issued()[slot] += 1;
