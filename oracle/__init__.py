@@ -67,6 +67,13 @@ def bind(path: str):
     lib.oracle_partial_state_f64.restype = i32
     lib.oracle_merge_states_f64.argtypes = [i32, i32, p, p, p, p]
     lib.oracle_merge_states_f64.restype = None
+    lib.oracle_rope_f64.argtypes = [i32, i32, p, p, f64, p]
+    lib.oracle_rope_f64.restype = None
+    lib.oracle_f64_to_bf16.argtypes = [f64]
+    lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_rope_append.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, p, p, p, p, p, p,
+                                       p, p, f64, p, p, p, p]
+    lib.oracle_rope_append.restype = i32
     return lib
 
 
@@ -187,3 +194,59 @@ def merge_states_batched(v, s):
         for h in range(H):
             out[n, h], lse[n, h] = merge_states(v[n, :, h, :], s[n, :, h])
     return out, lse
+
+
+# ------------------------------------------------------------------ RoPE and paged append
+
+APPEND_WRITTEN = 0
+APPEND_SHARED_PAGE = 1
+APPEND_BAD_POSITION = 2
+APPEND_BAD_PAGE = 3
+
+
+def rope(x, positions, theta=10000.0, lib=None):
+    """f64 split-half rotary embedding of the rows of x ([n, D] float64) at
+    positions ([n] int32); returns [n, D] float64 (see ``oxd_oracle.h``)."""
+    L = _load(lib)
+    x = _as(x, np.float64)
+    n, D = x.shape
+    pos = _as(positions, np.int32)
+    if pos.shape != (n,):
+        raise ValueError("one position per row")
+    y = np.empty_like(x)
+    L.oracle_rope_f64(n, D, _ptr(x), _ptr(pos), float(theta), _ptr(y))
+    return y
+
+
+def f64_to_bf16(x, lib=None):
+    """Nearest bfloat16 (ties to even) of each element, as uint16 bit patterns."""
+    L = _load(lib)
+    a = np.asarray(x, np.float64)
+    return np.array([L.oracle_f64_to_bf16(float(v)) for v in a.ravel()],
+                    np.uint16).reshape(a.shape)
+
+
+def rope_append(q, k, v, token_request, positions, indptr, indices, refcount, k_pages,
+                v_pages, *, page_size, layout, theta=10000.0, lib=None):
+    """Fused RoPE + paged append on copies of the pools.
+
+    q: [T, Hq, D], k, v: [T, Hkv, D] bf16 bits; pools as for ``paged_decode``.
+    Returns (q_out bits, k_pages bits, v_pages bits, status [T] int32)."""
+    L = _load(lib)
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    kp, vp = _bits(k_pages).copy(), _bits(v_pages).copy()
+    num_pages = kp.shape[0]
+    indptr = _as(indptr, np.int32)
+    B = indptr.shape[0] - 1
+    tr, pos = _as(token_request, np.int32), _as(positions, np.int32)
+    idx, rc = _as(indices, np.int32), _as(refcount, np.int32)
+    q_out = np.empty_like(q)
+    status = np.empty(T, np.int32)
+    r = L.oracle_rope_append(T, B, Hq, Hkv, D, page_size, layout, num_pages, _ptr(q), _ptr(k),
+                             _ptr(v), _ptr(tr), _ptr(pos), _ptr(indptr), _ptr(idx), _ptr(rc),
+                             float(theta), _ptr(q_out), _ptr(kp), _ptr(vp), _ptr(status))
+    if r < 0:
+        raise OracleError(f"oracle_rope_append failed ({r})")
+    return q_out, kp, vp, status

@@ -235,3 +235,100 @@ void oracle_merge_states_f64(int S, int D, const double* v, const double* s, dou
     }
     *lse = M + log(W);
 }
+
+/* ------------------------------------------------------------------ RoPE and append */
+
+void oracle_rope_f64(int n, int D, const double* x, const int32_t* pos, double theta, double* y) {
+    const int h = D / 2;
+    for (int r = 0; r < n; ++r) {
+        const double* xr = x + (size_t)r * (size_t)D;
+        double* yr = y + (size_t)r * (size_t)D;
+        for (int i = 0; i < h; ++i) {
+            const double f = pow(theta, -2.0 * (double)i / (double)D);
+            const double a = (double)pos[r] * f;
+            const double c = cos(a), s = sin(a);
+            yr[i] = xr[i] * c - xr[i + h] * s;
+            yr[i + h] = xr[i + h] * c + xr[i] * s;
+        }
+    }
+}
+
+uint16_t oracle_f64_to_bf16(double x) {
+    /* bfloat16 keeps 8 significant bits: round the f64 to 8 bits, ties to
+     * even (the default rounding mode of nearbyint), then the result is exact
+     * in f32 and its upper 16 bits are the bf16 pattern. */
+    if (x == 0.0 || isnan(x) || isinf(x)) {
+        float f = (float)x;
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        return (uint16_t)(u >> 16);
+    }
+    int e;
+    const double m = frexp(x, &e);             /* x = m * 2^e, 0.5 <= |m| < 1 */
+    const double r = nearbyint(ldexp(m, 8));   /* 8 significant bits */
+    const float f = (float)ldexp(r, e - 8);
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+int oracle_rope_append(int T, int B, int Hq, int Hkv, int D, int page_size, int layout,
+                       int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* v, const int32_t* token_request, const int32_t* positions,
+                       const int32_t* indptr, const int32_t* indices, const int32_t* refcount,
+                       double theta, uint16_t* q_out, uint16_t* k_pages, uint16_t* v_pages,
+                       int32_t* status) {
+    if (T < 0 || B < 1 || Hq < 1 || Hkv < 1 || D < 2 || (D & 1) || page_size < 1 ||
+        (layout != ORACLE_LAYOUT_NHD && layout != ORACLE_LAYOUT_HND) || num_pages < 1)
+        return ORACLE_EINVAL;
+    double* xr = (double*)malloc(sizeof(double) * (size_t)D);
+    double* yr = (double*)malloc(sizeof(double) * (size_t)D);
+    if (xr == NULL || yr == NULL) {
+        free(xr);
+        free(yr);
+        return ORACLE_ENOMEM;
+    }
+    int not_written = 0;
+    for (int t = 0; t < T; ++t) {
+        const int32_t p = positions[t];
+        /* q_out: every query head of the token, whatever happens to its KV */
+        for (int hq = 0; hq < Hq; ++hq) {
+            const size_t off = ((size_t)t * (size_t)Hq + (size_t)hq) * (size_t)D;
+            for (int d = 0; d < D; ++d) xr[d] = bf16_to_f64(q[off + (size_t)d]);
+            oracle_rope_f64(1, D, xr, &p, theta, yr);
+            for (int d = 0; d < D; ++d) q_out[off + (size_t)d] = oracle_f64_to_bf16(yr[d]);
+        }
+        const int b = token_request[t];
+        int st = ORACLE_APPEND_WRITTEN;
+        int64_t page = -1;
+        if (b < 0 || b >= B || p < 0 ||
+            (int64_t)p >= ((int64_t)indptr[b + 1] - indptr[b]) * (int64_t)page_size) {
+            st = ORACLE_APPEND_BAD_POSITION;
+        } else {
+            page = indices[indptr[b] + p / page_size];
+            if (page < 0 || page >= num_pages)
+                st = ORACLE_APPEND_BAD_PAGE;
+            else if (refcount[page] != 1)
+                st = ORACLE_APPEND_SHARED_PAGE;
+        }
+        status[t] = st;
+        if (st != ORACLE_APPEND_WRITTEN) {
+            ++not_written;
+            continue;
+        }
+        const int slot = p % page_size;
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t src = ((size_t)t * (size_t)Hkv + (size_t)h) * (size_t)D;
+            const size_t dst = pool_offset(layout, page, slot, h, 0, page_size, Hkv, D);
+            for (int d = 0; d < D; ++d) xr[d] = bf16_to_f64(k[src + (size_t)d]);
+            oracle_rope_f64(1, D, xr, &p, theta, yr);
+            for (int d = 0; d < D; ++d) {
+                k_pages[dst + (size_t)d] = oracle_f64_to_bf16(yr[d]);
+                v_pages[dst + (size_t)d] = v[src + (size_t)d];
+            }
+        }
+    }
+    free(xr);
+    free(yr);
+    return not_written;
+}

@@ -24,6 +24,9 @@
  * with the readings listed in the design notes (consecutive query heads share
  * a KV head; CSR block tables with last_page_len in [1, page_size]).
  *
+ * The RoPE and paged-append functions at the end follow the same page's rows
+ * "Standard RoPE" and "Fused RoPE plus paged append".
+ *
  * Parity status: every function below is pinned by the not-gpu tests
  * (closed forms, invariants, brute force); none is "parity unpinned".
  */
@@ -93,6 +96,54 @@ void oracle_merge_states_f64(int S, int D, const double* v, const double* s, dou
 
 /* Logical token count of request b: (P_b - 1) * page_size + last_page_len[b]. */
 int64_t oracle_kv_len(const int32_t* indptr, const int32_t* last_page_len, int page_size, int b);
+
+/*
+ * Standard rotary position embedding, split-half ("NeoX") pairing: the
+ * "FlashInfer parity matrix" page, "Admitted attention matrix", row "Standard
+ * RoPE" (D128 NeoX split-half with explicit int32 positions). For each of the
+ * n rows x[D] (D even) at position pos[r], with h = D/2 and the frequencies
+ * f_i = theta^(-2i/D), i < h:
+ *     y_i     = x_i     cos(pos f_i) - x_{i+h} sin(pos f_i)
+ *     y_{i+h} = x_{i+h} cos(pos f_i) + x_i     sin(pos f_i)
+ * all in f64. `theta` is the frequency base (10000 in the standard variant).
+ */
+void oracle_rope_f64(int n, int D, const double* x, const int32_t* pos, double theta, double* y);
+
+/* Round to the nearest bfloat16 (ties to even), returned as its bit pattern. */
+uint16_t oracle_f64_to_bf16(double x);
+
+/* Per-token outcome of oracle_rope_append. */
+#define ORACLE_APPEND_WRITTEN 0
+#define ORACLE_APPEND_SHARED_PAGE 1   /* target page's reference count is not one */
+#define ORACLE_APPEND_BAD_POSITION 2  /* request outside [0, B) or position past its pages */
+#define ORACLE_APPEND_BAD_PAGE 3      /* target page index outside [0, num_pages) */
+
+/*
+ * Fused RoPE and paged append: the "Admitted attention matrix" row "Fused
+ * RoPE plus paged append" and the section "Paged KV ownership difference"
+ * (decode may read shared pages; the append writes only to pages whose
+ * reference count is one, and the pager makes a target private first).
+ *
+ * Token t (t < T) belongs to request b = token_request[t] at logical
+ * position p = positions[t]; its KV rows go to page
+ * indices[indptr[b] + p / page_size], slot p % page_size (the request's
+ * block table already covers the position). For every KV head, the K row is
+ * written as bf16(RoPE(k_t, p)) and the V row as v_t unchanged; for every
+ * query head, q_out = bf16(RoPE(q_t, p)) (one rounding, ties to even).
+ * A token whose target page has a reference count other than one, whose
+ * request is outside [0, B), whose position is negative or past the
+ * request's pages, or whose page index is outside [0, num_pages) writes
+ * nothing to the pools (its q_out is still written); status[t] says which.
+ *   q, q_out  bf16 bits [T][Hq][D];  k, v bf16 bits [T][Hkv][D]
+ *   k_pages, v_pages  bf16 bits, pools in `layout`, updated in place
+ * Returns the number of tokens not written, or ORACLE_EINVAL for bad shapes.
+ */
+int oracle_rope_append(int T, int B, int Hq, int Hkv, int D, int page_size, int layout,
+                       int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* v, const int32_t* token_request, const int32_t* positions,
+                       const int32_t* indptr, const int32_t* indices, const int32_t* refcount,
+                       double theta, uint16_t* q_out, uint16_t* k_pages, uint16_t* v_pages,
+                       int32_t* status);
 
 #ifdef __cplusplus
 }
