@@ -78,6 +78,8 @@ typedef enum {
 #define OXD_DEVICE_BAD_PAGE 1       /* a listed page index is outside [0, num_pages) */
 #define OXD_DEVICE_PLAN_MISMATCH 2  /* device indptr/last_page_len differ from the plan's */
 #define OXD_DEVICE_WAIT_TIMEOUT 3   /* an internal pipeline wait gave up (about 1 s) */
+#define OXD_DEVICE_SHARED_PAGE 4    /* an append targeted a page whose reference count is not 1 */
+#define OXD_DEVICE_BAD_POSITION 5   /* an append's request or position lies outside its table */
 
 typedef struct oxd_plan_s* oxd_plan; /* opaque, host-owned, immutable after planning */
 
@@ -276,6 +278,73 @@ oxd_status oxd_paged_decode_run_static_workspace(oxd_plan plan, const void* q,
  */
 oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S, int32_t H,
                             int32_t D, void* v_out, float* s_out, void* stream);
+
+/*
+ * Fused rotary embedding and paged KV append ("FlashInfer parity matrix",
+ * "Admitted attention matrix", rows "Standard RoPE" -- D128 NeoX split-half
+ * with explicit int32 positions -- and "Fused RoPE plus paged append";
+ * "Paged KV ownership difference": decode may read shared pages, the append
+ * writes only to pages whose reference count is one, and the pager makes a
+ * target page private and remaps the request before enqueue).
+ *
+ * Token t (t < T) belongs to request b = token_request[t] at logical
+ * position p = positions[t]. With h = 64 and f_i = rope_theta^(-2i/128):
+ *   RoPE(x, p)_i      = x_i cos(p f_i) - x_{i+h} sin(p f_i)
+ *   RoPE(x, p)_{i+h}  = x_{i+h} cos(p f_i) + x_i sin(p f_i),   i < h
+ * For every query head q_out[t] = bf16(RoPE(q[t], p)); for every KV head the
+ * K row bf16(RoPE(k[t], p)) and the V row v[t] (unchanged) are written to
+ * page indices[indptr[b] + p / page_size], slot p % page_size, of the pools
+ * (the block table must already cover the position). The rotation runs in
+ * float with the angle formed in double; out-of-order tokens, several tokens
+ * of one request and tokens of different requests may share a call; two
+ * tokens must not target the same (page, slot).
+ *
+ *   desc          shapes; num_tokens >= 1, head_dim 128, page_size in
+ *                 {8, 16, 32, 64}, rope_theta finite and > 1
+ *   q, q_out      device bf16 [T][Hq][128], 16-byte aligned; q_out may be q
+ *                 itself (in place) but must not overlap it otherwise
+ *   k, v          device bf16 [T][Hkv][128], 16-byte aligned
+ *   token_request, positions  device int32 [T]
+ *   indptr, indices           device int32 block tables (as for decode); indices
+ *                 holds desc->num_indices entries
+ *   page_refcount device int32 [num_pages]: the caller's authoritative
+ *                 snapshot of each page's reference count
+ *   k_pages, v_pages  device bf16 pools (desc layout), written in place
+ *   workspace     device, >= 256 bytes, 256-byte aligned, any contents: the
+ *                 status word, read with oxd_read_device_status
+ *   stream        cudaStream_t
+ * Host-side errors (nothing enqueued): OXD_ERR_INVALID_ARGUMENT,
+ * OXD_ERR_UNSUPPORTED, OXD_ERR_ALIGNMENT, OXD_ERR_ALIAS (an output overlaps
+ * an input or another output, other than q_out == q),
+ * OXD_ERR_WORKSPACE_TOO_SMALL, OXD_ERR_CUDA. Device-side: a token whose
+ * request or position lies outside the block table
+ * (OXD_DEVICE_BAD_POSITION), whose page index lies outside the pool
+ * (OXD_DEVICE_BAD_PAGE) or whose page is shared (OXD_DEVICE_SHARED_PAGE)
+ * writes no K/V row; the other tokens are written, and every q_out row is. A
+ * request whose indptr entries are negative, decreasing or past num_indices
+ * counts as OXD_DEVICE_BAD_POSITION.
+ */
+typedef struct {
+    int32_t num_tokens;     /* T */
+    int32_t batch;          /* B: requests in the block tables */
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;       /* 128 */
+    int32_t page_size;      /* 8, 16, 32 or 64 */
+    int32_t layout;         /* oxd_kv_layout */
+    int32_t num_indices;    /* entries of `indices` (indptr[B]); the device refuses tables
+                               that point past it */
+    int64_t num_pages;      /* pages in each pool and in page_refcount */
+    double rope_theta;      /* frequency base (10000 in the standard variant) */
+    int32_t reserved[2];    /* must be zero */
+} oxd_rope_append_desc;
+
+oxd_status oxd_rope_append(const oxd_rope_append_desc* desc, const void* q, const void* k,
+                           const void* v, const int32_t* token_request, const int32_t* positions,
+                           const int32_t* indptr, const int32_t* indices,
+                           const int32_t* page_refcount, void* q_out, void* k_pages,
+                           void* v_pages, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* Planner decisions of a plan (host only). */
 oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info);

@@ -11,6 +11,7 @@ The functions keep the C names:
 * :func:`oxd_paged_decode_plan` -> :class:`Plan` (owns the opaque handle)
 * :func:`oxd_paged_decode_run`, :func:`oxd_plan_bind_workspace`
 * :func:`oxd_merge_states`
+* :func:`oxd_rope_append` (fused rotary embedding + paged KV append)
 * :func:`oxd_plan_get_info`, :func:`oxd_plan_set_timing_events`,
   :func:`oxd_plan_destroy`, :func:`oxd_read_device_status`,
   :func:`oxd_status_string`, :func:`oxd_device_status_string`, :func:`oxd_version`
@@ -37,7 +38,7 @@ __all__ = [
     "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace",
     "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
     "oxd_read_device_status", "oxd_status_string", "oxd_device_status_string", "oxd_version",
-    "EXPORTED_SYMBOLS",
+    "oxd_rope_append", "RopeAppendDesc", "make_rope_append_desc", "EXPORTED_SYMBOLS",
 ]
 
 OXD_OK = 0
@@ -58,12 +59,14 @@ OXD_DEVICE_OK = 0
 OXD_DEVICE_BAD_PAGE = 1
 OXD_DEVICE_PLAN_MISMATCH = 2
 OXD_DEVICE_WAIT_TIMEOUT = 3
+OXD_DEVICE_SHARED_PAGE = 4
+OXD_DEVICE_BAD_POSITION = 5
 
 EXPORTED_SYMBOLS = (
     "oxd_paged_decode_plan", "oxd_paged_decode_run", "oxd_merge_states", "oxd_plan_get_info",
     "oxd_plan_set_timing_events", "oxd_plan_destroy", "oxd_read_device_status",
     "oxd_status_string", "oxd_device_status_string", "oxd_version",
-    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace",
+    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace", "oxd_rope_append",
 )
 
 
@@ -113,6 +116,29 @@ _lock = threading.Lock()
 _lib = None
 
 
+class RopeAppendDesc(ctypes.Structure):
+    """``oxd_rope_append_desc``."""
+
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32), ("batch", ctypes.c_int32),
+        ("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("layout", ctypes.c_int32), ("num_indices", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64), ("rope_theta", ctypes.c_double),
+        ("reserved", ctypes.c_int32 * 2),
+    ]
+
+
+def make_rope_append_desc(num_tokens, batch, num_qo_heads, num_kv_heads, page_size, layout,
+                          num_pages, num_indices, rope_theta=10000.0,
+                          head_dim=128) -> RopeAppendDesc:
+    if isinstance(layout, str):
+        layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
+    return RopeAppendDesc(num_tokens, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                          layout, num_indices, num_pages, rope_theta,
+                          (ctypes.c_int32 * 2)(0, 0))
+
+
 def lib():
     """The loaded liboxd.so with its signatures declared."""
     global _lib
@@ -133,12 +159,13 @@ def lib():
             L.oxd_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
             L.oxd_plan_set_timing_events.argtypes = [vp, vp, vp]
             L.oxd_plan_bind_workspace.argtypes = [vp, vp, sz, vp]
+            L.oxd_rope_append.argtypes = [ctypes.POINTER(RopeAppendDesc)] + [vp] * 12 + [sz, vp]
             L.oxd_plan_destroy.argtypes = [vp]
             L.oxd_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
             for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run",
                       "oxd_paged_decode_run_static_workspace", "oxd_merge_states",
                       "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
-                      "oxd_read_device_status", "oxd_plan_bind_workspace"):
+                      "oxd_read_device_status", "oxd_plan_bind_workspace", "oxd_rope_append"):
                 getattr(L, f).restype = ctypes.c_int
             L.oxd_status_string.argtypes = [ctypes.c_int]
             L.oxd_status_string.restype = ctypes.c_char_p
@@ -332,3 +359,18 @@ def make_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages, h
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return Desc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
                 max_splits, force_splits, num_sms, tensor_path, (ctypes.c_int32 * 2)(0, 0))
+
+
+def oxd_rope_append(desc: RopeAppendDesc, q, k, v, token_request, positions, indptr, indices,
+                    page_refcount, q_out, k_pages, v_pages, workspace, workspace_bytes=None,
+                    stream=None) -> None:
+    """Enqueue a fused rotary embedding + paged KV append (see ``oxd_rope_append``
+    in include/oxd.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib().oxd_rope_append(ctypes.byref(desc), _addr(q), _addr(k), _addr(v),
+                               _addr(token_request), _addr(positions), _addr(indptr),
+                               _addr(indices), _addr(page_refcount), _addr(q_out),
+                               _addr(k_pages), _addr(v_pages), _addr(workspace),
+                               int(workspace_bytes), _stream(stream, q))
+    _check("oxd_rope_append", st)

@@ -18,7 +18,7 @@ LIB = os.path.join(LIBDIR, "liboxd.so")
 HEADERS = [os.path.join(ROOT, "include", "oxd.h"), os.path.join(CSRC, "oxd_internal.h"),
            os.path.join(CSRC, "oxd_merge_row.cuh"), os.path.join(CSRC, "oxd_ptx.cuh")]
 SOURCES = ["oxd_host.cpp", "oxd_decode.cu", "oxd_decode_wide.cu", "oxd_merge.cu",
-           "oxd_noalloc.cu"]
+           "oxd_noalloc.cu", "oxd_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

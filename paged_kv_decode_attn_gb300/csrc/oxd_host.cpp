@@ -239,6 +239,10 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
 
 }  // namespace
 
+namespace oxd {
+uint32_t next_run_epoch() { return next_epoch(); }
+}  // namespace oxd
+
 extern "C" {
 
 const char* oxd_version(void) { return "oxd 0.1.0 sm_103a"; }
@@ -265,6 +269,8 @@ const char* oxd_device_status_string(int32_t code) {
         case OXD_DEVICE_BAD_PAGE: return "page index outside the pool";
         case OXD_DEVICE_PLAN_MISMATCH: return "device block tables differ from the plan";
         case OXD_DEVICE_WAIT_TIMEOUT: return "pipeline wait timed out";
+        case OXD_DEVICE_SHARED_PAGE: return "append target page is shared (reference count not 1)";
+        case OXD_DEVICE_BAD_POSITION: return "append position outside the request's block table";
     }
     return "unknown device status";
 }
@@ -796,3 +802,90 @@ oxd_status oxd_read_device_status(const void* workspace, void* stream, int32_t* 
 }
 
 }  // extern "C"
+
+extern "C" oxd_status oxd_rope_append(const oxd_rope_append_desc* desc, const void* q,
+                                      const void* k, const void* v,
+                                      const int32_t* token_request, const int32_t* positions,
+                                      const int32_t* indptr, const int32_t* indices,
+                                      const int32_t* page_refcount, void* q_out, void* k_pages,
+                                      void* v_pages, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    if (desc == nullptr || q == nullptr || k == nullptr || v == nullptr ||
+        token_request == nullptr || positions == nullptr || indptr == nullptr ||
+        indices == nullptr || page_refcount == nullptr || q_out == nullptr ||
+        k_pages == nullptr || v_pages == nullptr || workspace == nullptr)
+        return OXD_ERR_INVALID_ARGUMENT;
+    const oxd_rope_append_desc& d = *desc;
+    if (d.num_tokens < 1 || d.batch < 1 || d.num_qo_heads < 1 || d.num_kv_heads < 1 ||
+        d.num_pages < 1 || d.num_indices < 1 || d.reserved[0] != 0 || d.reserved[1] != 0 ||
+        (d.layout != OXD_LAYOUT_NHD && d.layout != OXD_LAYOUT_HND) ||
+        !(std::isfinite(d.rope_theta) && d.rope_theta > 1.0))
+        return OXD_ERR_INVALID_ARGUMENT;
+    if (d.head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
+    if (d.page_size != 8 && d.page_size != 16 && d.page_size != 32 && d.page_size != 64)
+        return OXD_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(d.num_tokens) * (d.num_qo_heads + d.num_kv_heads) >
+        (int64_t{1} << 33))
+        return OXD_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) ||
+        !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(token_request, 4) ||
+        !aligned(positions, 4) || !aligned(indptr, 4) || !aligned(indices, 4) ||
+        !aligned(page_refcount, 4) || !aligned(workspace, 256))
+        return OXD_ERR_ALIGNMENT;
+    if (workspace_bytes < sizeof(WsHeader)) return OXD_ERR_WORKSPACE_TOO_SMALL;
+    const size_t T = static_cast<size_t>(d.num_tokens);
+    const size_t qbytes = T * d.num_qo_heads * kHeadDim * 2;
+    const size_t kvbytes = T * d.num_kv_heads * kHeadDim * 2;
+    const size_t pool = static_cast<size_t>(d.num_pages) * d.page_size * d.num_kv_heads *
+                        kHeadDim * 2;
+    const Span in[] = {span(k, kvbytes), span(v, kvbytes), span(token_request, T * 4),
+                       span(positions, T * 4),
+                       span(indptr, (static_cast<size_t>(d.batch) + 1) * 4),
+                       span(indices, static_cast<size_t>(d.num_indices) * 4),
+                       span(page_refcount, static_cast<size_t>(d.num_pages) * 4)};
+    const Span qin = span(q, qbytes);
+    const Span outs[] = {span(q_out, qbytes), span(k_pages, pool), span(v_pages, pool),
+                         span(workspace, sizeof(WsHeader))};
+    for (const Span& o : outs) {
+        for (const Span& i : in)
+            if (overlap(o, i)) return OXD_ERR_ALIAS;
+    }
+    // q_out may be q exactly (each row is read before it is written, by the
+    // same warp); any other overlap with q is refused
+    if (q_out != q && overlap(outs[0], qin)) return OXD_ERR_ALIAS;
+    for (int i = 1; i < 4; ++i)
+        if (overlap(outs[i], qin)) return OXD_ERR_ALIAS;
+    for (int i = 0; i < 4; ++i)
+        for (int j = i + 1; j < 4; ++j)
+            if (overlap(outs[i], outs[j])) return OXD_ERR_ALIAS;
+
+    AppendParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.token_request = token_request;
+    p.positions = positions;
+    p.indptr = indptr;
+    p.indices = indices;
+    p.refcount = page_refcount;
+    p.q_out = static_cast<uint16_t*>(q_out);
+    p.k_pages = static_cast<uint16_t*>(k_pages);
+    p.v_pages = static_cast<uint16_t*>(v_pages);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.status = reinterpret_cast<unsigned long long*>(ws + offsetof(WsHeader, status));
+    p.last_epoch = reinterpret_cast<uint32_t*>(ws + offsetof(WsHeader, last_epoch));
+    p.epoch = next_run_epoch();
+    p.T = d.num_tokens;
+    p.B = d.batch;
+    p.Hq = d.num_qo_heads;
+    p.Hkv = d.num_kv_heads;
+    p.page_size = d.page_size;
+    p.layout = d.layout;
+    p.num_indices = d.num_indices;
+    p.num_pages = d.num_pages;
+    for (int i = 0; i < kHeadDim / 2; ++i)
+        p.freq[i] = std::pow(d.rope_theta, -2.0 * static_cast<double>(i) / kHeadDim);
+    if (launch_rope_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return OXD_ERR_CUDA;
+    return OXD_OK;
+}

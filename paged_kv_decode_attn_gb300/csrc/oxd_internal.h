@@ -134,6 +134,30 @@ struct MergeParams {
     float s_to_ln;                // factor taking s to natural log (1, or ln 2 for log2)
 };
 
+// Fused RoPE + paged append (oxd_append.cu).
+struct AppendParams {
+    const uint16_t* q;            // bf16 [T][Hq][128]
+    const uint16_t* k;            // bf16 [T][Hkv][128]
+    const uint16_t* v;
+    const int32_t* token_request; // [T]
+    const int32_t* positions;     // [T]
+    const int32_t* indptr;        // [B+1]
+    const int32_t* indices;
+    const int32_t* refcount;      // [num_pages]
+    uint16_t* q_out;              // bf16 [T][Hq][128]
+    uint16_t* k_pages;
+    uint16_t* v_pages;
+    unsigned long long* status;
+    uint32_t* last_epoch;
+    uint32_t epoch;
+    int32_t T, B, Hq, Hkv, page_size, layout, num_indices;
+    int64_t num_pages;
+    double freq[kHeadDim / 2];    // theta^(-2i/128)
+};
+cudaError_t launch_rope_append(const AppendParams& p, cudaStream_t stream);
+// Run epochs (oxd_host.cpp): never 0, increasing over the process.
+uint32_t next_run_epoch();
+
 // Implemented in oxd_decode.cu / oxd_merge.cu.
 VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);

@@ -345,3 +345,87 @@ def test_merge_rejects_bad_operands(case, expect):
         so = o + 16
     st = oxd.lib().oxd_merge_states(v, s, N, S, H, D, o, so, None)
     assert st == expect
+
+
+# ------------------------------------------------------------------ rope + append
+
+def _append_args(T=4, B=2, Hq=8, Hkv=2, num_pages=16):
+    """Fake, far-apart device addresses for every operand of oxd_rope_append."""
+    names = ["q", "k", "v", "token_request", "positions", "indptr", "indices",
+             "page_refcount", "q_out", "k_pages", "v_pages", "workspace"]
+    return {n: BASE + (i + 1) * (1 << 36) for i, n in enumerate(names)}
+
+
+def _append_status(desc, a, ws_bytes=256):
+    L = oxd.lib()
+    return L.oxd_rope_append(ctypes.byref(desc), a["q"], a["k"], a["v"], a["token_request"],
+                             a["positions"], a["indptr"], a["indices"], a["page_refcount"],
+                             a["q_out"], a["k_pages"], a["v_pages"], a["workspace"], ws_bytes,
+                             None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("no_tokens", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("theta_one", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("theta_nan", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("reserved", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("no_indices", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("indices_over_pool", oxd.OXD_ERR_ALIAS),
+    ("head_dim", oxd.OXD_ERR_UNSUPPORTED),
+    ("page_size", oxd.OXD_ERR_UNSUPPORTED),
+    ("q_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("workspace_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("workspace_small", oxd.OXD_ERR_WORKSPACE_TOO_SMALL),
+    ("q_out_over_k", oxd.OXD_ERR_ALIAS),
+    ("q_out_inside_q", oxd.OXD_ERR_ALIAS),
+    ("pool_over_refcount", oxd.OXD_ERR_ALIAS),
+    ("k_pool_is_v_pool", oxd.OXD_ERR_ALIAS),
+    ("null_indices", oxd.OXD_ERR_INVALID_ARGUMENT),
+])
+def test_rope_append_rejects_bad_operands(case, expect):
+    desc = oxd.make_rope_append_desc(4, 2, 8, 2, 16, "NHD", 16, 8)
+    a = _append_args()
+    ws_bytes = 256
+    if case == "no_tokens":
+        desc.num_tokens = 0
+    elif case == "theta_one":
+        desc.rope_theta = 1.0
+    elif case == "theta_nan":
+        desc.rope_theta = float("nan")
+    elif case == "reserved":
+        desc.reserved[0] = 1
+    elif case == "no_indices":
+        desc.num_indices = 0
+    elif case == "head_dim":
+        desc.head_dim = 64
+    elif case == "page_size":
+        desc.page_size = 12
+    elif case == "q_misaligned":
+        a["q"] += 8
+    elif case == "workspace_misaligned":
+        a["workspace"] += 16
+    elif case == "workspace_small":
+        ws_bytes = 255
+    elif case == "q_out_over_k":
+        a["q_out"] = a["k"]
+    elif case == "q_out_inside_q":
+        a["q_out"] = a["q"] + 256
+    elif case == "pool_over_refcount":
+        a["k_pages"] = a["page_refcount"]
+    elif case == "k_pool_is_v_pool":
+        a["v_pages"] = a["k_pages"]
+    elif case == "null_indices":
+        a["indices"] = None
+    elif case == "indices_over_pool":
+        a["k_pages"] = a["indices"]
+    assert _append_status(desc, a, ws_bytes) == expect
+
+
+def test_rope_append_accepts_in_place_query():
+    # q_out == q passes every host check (the call then fails only for want
+    # of a device on this machine)
+    desc = oxd.make_rope_append_desc(4, 2, 8, 2, 16, "HND", 16, 8)
+    a = _append_args()
+    a["q_out"] = a["q"]
+    assert _append_status(desc, a) not in (oxd.OXD_ERR_ALIAS, oxd.OXD_ERR_ALIGNMENT,
+                                           oxd.OXD_ERR_INVALID_ARGUMENT)
