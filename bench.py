@@ -78,6 +78,11 @@ def parse_args(argv=None):
                          "params: unbound runs")
     ap.add_argument("--graph", action="store_true",
                     help="capture one run in a CUDA graph and time its replays")
+    ap.add_argument("--op", choices=["decode", "rope_append"], default="decode",
+                    help="rope_append: time the fused RoPE + paged append on the workload's "
+                         "tables instead of the decode step")
+    ap.add_argument("--tokens-per-request", type=int, default=1,
+                    help="rope_append: tokens appended per request in one call (1..64)")
     return ap.parse_args(argv)
 
 
@@ -200,9 +205,14 @@ def gpu_id_for_smi(torch, dev):
 
 
 def source_hash():
+    """Hash of the sources that decide a decode launch's DRAM traffic (the
+    planner, the decode and merge kernels); the append kernel's file is left
+    out, it never runs in a decode step."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_attn_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name == "oxd_append.cu":
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -523,10 +533,92 @@ def run_oxd(args):
     return 0
 
 
+def run_rope_append(args):
+    """Fused RoPE + paged append on the workload's shapes: every request gets
+    `tokens_per_request` new tokens (its block table already covers them).
+    Metric: bytes the operation must move (q read and written, k and v read,
+    K and V rows written) per second."""
+    import torch
+
+    import paged_kv_decode_attn_gb300 as oxd
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    oxd.build()
+    cfg = W.CONFIGS[args.config]
+    n_new = args.tokens_per_request
+    t0 = W.make_tables(cfg, batch=args.batch)
+    lengths = t0.lengths
+    case = W.custom_case([int(L) + n_new for L in lengths], num_qo_heads=cfg.num_qo_heads,
+                         num_kv_heads=cfg.num_kv_heads, page_size=cfg.page_size,
+                         layout=cfg.layout, seed=cfg.seed, device=dev)
+    t = case.tables
+    B, Hq, Hkv = case.batch, case.num_qo_heads, case.num_kv_heads
+    tok = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(n_new)
+    pos = (torch.as_tensor(lengths, device=dev).to(torch.int32).repeat_interleave(n_new) +
+           torch.arange(n_new, dtype=torch.int32, device=dev).repeat(B))
+    T = B * n_new
+    g = torch.Generator(device=dev).manual_seed(cfg.seed)
+    q = torch.randn(T, Hq, 128, generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn(T, Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+    q_out = torch.empty_like(q)
+    indptr = torch.as_tensor(t.indptr, device=dev)
+    indices = torch.as_tensor(t.indices, device=dev)
+    refcount = torch.ones(t.num_pages, dtype=torch.int32, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    desc = oxd.make_rope_append_desc(T, B, Hq, Hkv, case.page_size, case.layout, t.num_pages,
+                                     int(t.indptr[-1]))
+    stream = torch.cuda.current_stream(dev)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def step():
+        oxd.oxd_rope_append(desc, q, k, v, tok, pos, indptr, indices, refcount, q_out, case.k,
+                            case.v, ws, 256, stream)
+
+    for _ in range(args.warmup):
+        flush_w.zero_()
+        flush_r.sum()
+        step()
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error in the append")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        flush_w.zero_()
+        flush_r.sum()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    moved = T * (2 * Hq + 4 * Hkv) * 128 * 2
+    peak, peak_kind = measured_peaks()
+    gbs = moved / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "impl": "oxd", "op": "rope_append",
+        "metric": "fused RoPE + paged KV append: bytes moved GB/s, us per call",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "us_per_call": ms * 1e3, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": B, "tokens_per_request": n_new, "tokens": T,
+                   "num_qo_heads": Hq, "num_kv_heads": Hkv, "page_size": case.page_size,
+                   "layout": case.layout, "bytes_moved_per_call": moved,
+                   "l2": "flushed before every call, outside its events"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "peak_source": peak_kind},
+    }), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "rope_append":
+        return run_rope_append(args)
     return run_oxd(args)
 
 

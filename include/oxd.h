@@ -294,8 +294,9 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
  * For every query head q_out[t] = bf16(RoPE(q[t], p)); for every KV head the
  * K row bf16(RoPE(k[t], p)) and the V row v[t] (unchanged) are written to
  * page indices[indptr[b] + p / page_size], slot p % page_size, of the pools
- * (the block table must already cover the position). The rotation runs in
- * float with the angle formed in double; out-of-order tokens, several tokens
+ * (the block table must already cover the position; positions are below
+ * 2^24). The rotation runs in float with the angle carried as a two-float
+ * number of turns; out-of-order tokens, several tokens
  * of one request and tokens of different requests may share a call; two
  * tokens must not target the same (page, slot).
  *
@@ -321,8 +322,9 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
  * (OXD_DEVICE_BAD_POSITION), whose page index lies outside the pool
  * (OXD_DEVICE_BAD_PAGE) or whose page is shared (OXD_DEVICE_SHARED_PAGE)
  * writes no K/V row; the other tokens are written, and every q_out row is. A
- * request whose indptr entries are negative, decreasing or past num_indices
- * counts as OXD_DEVICE_BAD_POSITION.
+ * request whose indptr entries are negative, decreasing or past num_indices,
+ * or a position outside [0, 2^24), counts as OXD_DEVICE_BAD_POSITION; such a
+ * token's q_out rows are rotated at position p & (2^24 - 1).
  */
 typedef struct {
     int32_t num_tokens;     /* T */

@@ -883,8 +883,13 @@ extern "C" oxd_status oxd_rope_append(const oxd_rope_append_desc* desc, const vo
     p.layout = d.layout;
     p.num_indices = d.num_indices;
     p.num_pages = d.num_pages;
-    for (int i = 0; i < kHeadDim / 2; ++i)
-        p.freq[i] = std::pow(d.rope_theta, -2.0 * static_cast<double>(i) / kHeadDim);
+    for (int i = 0; i < kHeadDim / 2; ++i) {
+        // frequency in turns per position, f / (2 pi), split into two floats
+        const double g = std::pow(d.rope_theta, -2.0 * static_cast<double>(i) / kHeadDim) /
+                         6.283185307179586476925286766559;
+        p.turns_hi[i] = static_cast<float>(g);
+        p.turns_lo[i] = static_cast<float>(g - static_cast<double>(p.turns_hi[i]));
+    }
     if (launch_rope_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OXD_ERR_CUDA;
     return OXD_OK;

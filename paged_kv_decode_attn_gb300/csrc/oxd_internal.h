@@ -152,7 +152,8 @@ struct AppendParams {
     uint32_t epoch;
     int32_t T, B, Hq, Hkv, page_size, layout, num_indices;
     int64_t num_pages;
-    double freq[kHeadDim / 2];    // theta^(-2i/128)
+    float turns_hi[kHeadDim / 2];  // theta^(-2i/128) / (2 pi) as hi + lo floats
+    float turns_lo[kHeadDim / 2];
 };
 cudaError_t launch_rope_append(const AppendParams& p, cudaStream_t stream);
 // Run epochs (oxd_host.cpp): never 0, increasing over the process.
