@@ -9,7 +9,9 @@ What it computes (the definition stated in ``oxd_oracle.h``) follows the
 "FlashInfer parity matrix" page, sections "Admitted attention matrix" and
 "Domain coverage": one query token per request attends, with full (non-causal)
 softmax attention, over the tokens its block table lists, for MHA, GQA and MQA
-head groupings, over NHD or HND pages.
+head groupings, over NHD or HND pages. ``paged_prefill`` restates the same
+page's "Paged causal prefill" row: several query tokens per request, the last
+of its cached tokens, each attending causally up to its own position.
 
 Inputs are numpy arrays: bf16 tensors as ``uint16`` bit patterns, block tables
 as ``int32``. Outputs are float64.
@@ -67,6 +69,9 @@ def bind(path: str):
     lib.oracle_partial_state_f64.restype = i32
     lib.oracle_merge_states_f64.argtypes = [i32, i32, p, p, p, p]
     lib.oracle_merge_states_f64.restype = None
+    lib.oracle_paged_prefill_f64.argtypes = [
+        i32, i32, i32, i32, i32, i32, i64, p, p, p, p, p, p, p, f64, p, i32, p, p, i32]
+    lib.oracle_paged_prefill_f64.restype = i32
     lib.oracle_rope_f64.argtypes = [i32, i32, p, p, f64, p]
     lib.oracle_rope_f64.restype = None
     lib.oracle_f64_to_bf16.argtypes = [f64]
@@ -145,6 +150,50 @@ def paged_decode(q, k_pages, v_pages, indptr, indices, last_page_len, *, num_kv_
         None if hl is None else _ptr(hl), n, _ptr(out), _ptr(lse), int(nthreads))
     if rc != 0:
         raise OracleError(f"oracle_paged_decode_f64 returned {rc}")
+    return out, lse
+
+
+def paged_prefill(q, k_pages, v_pages, qo_indptr, indptr, indices, last_page_len, *,
+                  num_kv_heads, page_size, layout, sm_scale, rows=None, nthreads=0, lib=None):
+    """f64 causal prefill attention over paged KV.
+
+    q: [Nq, Hq, D] bf16 bits, Nq = qo_indptr[-1]; request b's query tokens are
+    its last qo_indptr[b+1] - qo_indptr[b] cached tokens. Pools and block
+    tables as for ``paged_decode``. rows: optional sequence of (token, hq)
+    pairs; then out is [n, D], lse [n]. Returns (out, lse) as float64 arrays.
+    """
+    lib = _load(lib)
+    q = _bits(q)
+    k = _bits(k_pages)
+    v = _bits(v_pages)
+    Nq, Hq, D = q.shape
+    qo = _as(qo_indptr, np.int32)
+    indptr = _as(indptr, np.int32)
+    indices = _as(indices, np.int32)
+    last = _as(last_page_len, np.int32)
+    B = last.shape[0]
+    if indptr.shape != (B + 1,) or qo.shape != (B + 1,) or int(qo[-1]) != Nq:
+        raise ValueError("qo_indptr and indptr must be [B+1], qo_indptr[B] = q.shape[0]")
+    per_page = page_size * num_kv_heads * D
+    if k.size % per_page or v.size != k.size:
+        raise ValueError("K/V pools must hold whole pages of equal count")
+    num_pages = k.size // per_page
+    if rows is None:
+        rl = None
+        out = np.empty((Nq, Hq, D), np.float64)
+        lse = np.empty((Nq, Hq), np.float64)
+        n = Nq * Hq
+    else:
+        rl = _as(rows, np.int32).reshape(-1, 2)
+        n = rl.shape[0]
+        out = np.empty((n, D), np.float64)
+        lse = np.empty((n,), np.float64)
+    rc = lib.oracle_paged_prefill_f64(
+        B, Hq, num_kv_heads, D, page_size, layout, num_pages, _ptr(q), _ptr(k), _ptr(v),
+        _ptr(qo), _ptr(indptr), _ptr(indices), _ptr(last), float(sm_scale),
+        None if rl is None else _ptr(rl), n, _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise OracleError(f"oracle_paged_prefill_f64 returned {rc}")
     return out, lse
 
 

@@ -236,6 +236,143 @@ void oracle_merge_states_f64(int S, int D, const double* v, const double* s, dou
     *lse = M + log(W);
 }
 
+/* ------------------------------------------------------------------ causal prefill */
+
+/*
+ * State of one query row `qrow` (D values) against logical tokens [0, t1) of
+ * request b through KV head h: the same definition as head_state, with the
+ * query row given directly.
+ */
+static int row_state(const problem* P, const uint16_t* qrow, int b, int h, int64_t t1, double* o,
+                     double* lse) {
+    for (int d = 0; d < P->D; ++d) o[d] = 0.0;
+    if (t1 <= 0) {
+        *lse = -INFINITY;
+        return ORACLE_OK;
+    }
+    double* s = (double*)malloc((size_t)t1 * sizeof(double));
+    if (!s) return ORACLE_ENOMEM;
+    for (int64_t j = 0; j < t1; ++j) {
+        int64_t page = P->indices[P->indptr[b] + j / P->page_size];
+        int t = (int)(j % P->page_size);
+        double dot = 0.0;
+        for (int d = 0; d < P->D; ++d)
+            dot += bf16_to_f64(qrow[d]) *
+                   bf16_to_f64(P->k[pool_offset(P->layout, page, t, h, d, P->page_size,
+                                                P->Hkv, P->D)]);
+        s[j] = P->sm_scale * dot;
+    }
+    double M = -INFINITY;
+    for (int64_t j = 0; j < t1; ++j)
+        if (s[j] > M) M = s[j];
+    double Z = 0.0;
+    for (int64_t j = 0; j < t1; ++j) Z += exp(s[j] - M);
+    for (int64_t j = 0; j < t1; ++j) {
+        double w = exp(s[j] - M) / Z;
+        int64_t page = P->indices[P->indptr[b] + j / P->page_size];
+        int t = (int)(j % P->page_size);
+        for (int d = 0; d < P->D; ++d)
+            o[d] += w * bf16_to_f64(P->v[pool_offset(P->layout, page, t, h, d, P->page_size,
+                                                     P->Hkv, P->D)]);
+    }
+    *lse = M + log(Z);
+    free(s);
+    return ORACLE_OK;
+}
+
+typedef struct {
+    const problem* P;
+    const int32_t* qo_indptr;
+    const int32_t* rows; /* NULL: every (t, hq) in order */
+    int n_rows;
+    int worker, nworkers;
+    double *out, *lse;
+    int status;
+} prefill_job;
+
+static void* run_prefill_job(void* arg) {
+    prefill_job* J = (prefill_job*)arg;
+    const problem* P = J->P;
+    J->status = ORACLE_OK;
+    for (int i = J->worker; i < J->n_rows; i += J->nworkers) {
+        int t, hq;
+        if (J->rows) {
+            t = J->rows[2 * i];
+            hq = J->rows[2 * i + 1];
+        } else {
+            t = i / P->Hq;
+            hq = i % P->Hq;
+        }
+        /* the request that owns query token t */
+        int b = 0;
+        while (J->qo_indptr[b + 1] <= t) ++b;
+        const int64_t L = oracle_kv_len(P->indptr, P->last_page_len, P->page_size, b);
+        const int64_t q_len = (int64_t)J->qo_indptr[b + 1] - J->qo_indptr[b];
+        const int64_t pos = L - q_len + (t - J->qo_indptr[b]);
+        const int G = P->Hq / P->Hkv;
+        const uint16_t* qrow = P->q + ((size_t)t * (size_t)P->Hq + (size_t)hq) * (size_t)P->D;
+        int rc = row_state(P, qrow, b, hq / G, pos + 1, J->out + (size_t)i * (size_t)P->D,
+                           J->lse + i);
+        if (rc != ORACLE_OK) {
+            J->status = rc;
+            return NULL;
+        }
+    }
+    return NULL;
+}
+
+int oracle_paged_prefill_f64(int B, int Hq, int Hkv, int D, int page_size, int layout,
+                             int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                             const uint16_t* v, const int32_t* qo_indptr, const int32_t* indptr,
+                             const int32_t* indices, const int32_t* last_page_len,
+                             double sm_scale, const int32_t* rows, int n_rows, double* out,
+                             double* lse, int nthreads) {
+    if (check_shape(B, Hq, Hkv, D, page_size, layout) != ORACLE_OK) return ORACLE_EINVAL;
+    if (check_tables(B, page_size, num_pages, indptr, indices, last_page_len) != ORACLE_OK)
+        return ORACLE_EINVAL;
+    if (qo_indptr[0] != 0) return ORACLE_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        const int64_t q_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        if (q_len < 0 || q_len > oracle_kv_len(indptr, last_page_len, page_size, b))
+            return ORACLE_EINVAL;
+    }
+    const int64_t n_tok = qo_indptr[B];
+    if (rows) {
+        for (int i = 0; i < n_rows; ++i)
+            if (rows[2 * i] < 0 || rows[2 * i] >= n_tok || rows[2 * i + 1] < 0 ||
+                rows[2 * i + 1] >= Hq)
+                return ORACLE_EINVAL;
+    } else {
+        if (n_tok * Hq > 0x7fffffff) return ORACLE_EINVAL;
+        n_rows = (int)(n_tok * Hq);
+    }
+    problem P = {B, Hq, Hkv, D, page_size, layout, q, k, v, indptr, indices, last_page_len,
+                 sm_scale};
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n_rows) nthreads = n_rows > 0 ? n_rows : 1;
+    prefill_job* jobs = (prefill_job*)calloc((size_t)nthreads, sizeof(prefill_job));
+    pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) {
+        free(jobs);
+        free(tids);
+        return ORACLE_ENOMEM;
+    }
+    for (int w = 0; w < nthreads; ++w) {
+        jobs[w] = (prefill_job){&P, qo_indptr, rows, n_rows, w, nthreads, out, lse, ORACLE_OK};
+        if (w > 0) pthread_create(&tids[w], NULL, run_prefill_job, &jobs[w]);
+    }
+    run_prefill_job(&jobs[0]);
+    int status = jobs[0].status;
+    for (int w = 1; w < nthreads; ++w) {
+        pthread_join(tids[w], NULL);
+        if (jobs[w].status != ORACLE_OK) status = jobs[w].status;
+    }
+    free(jobs);
+    free(tids);
+    return status;
+}
+
 /* ------------------------------------------------------------------ RoPE and append */
 
 void oracle_rope_f64(int n, int D, const double* x, const int32_t* pos, double theta, double* y) {

@@ -24,7 +24,8 @@
  * with the readings listed in the design notes (consecutive query heads share
  * a KV head; CSR block tables with last_page_len in [1, page_size]).
  *
- * The RoPE and paged-append functions at the end follow the same page's rows
+ * The causal prefill function follows the same page's row "Paged causal
+ * prefill"; the RoPE and paged-append functions at the end follow its rows
  * "Standard RoPE" and "Fused RoPE plus paged append".
  *
  * Parity status: every function below is pinned by the not-gpu tests
@@ -93,6 +94,31 @@ int oracle_partial_state_f64(int B, int Hq, int Hkv, int D, int page_size, int l
  */
 void oracle_merge_states_f64(int S, int D, const double* v, const double* s, double* out,
                              double* lse);
+
+/*
+ * Paged causal prefill attention in f64: the "FlashInfer parity matrix" page,
+ * "Admitted attention matrix", row "Paged causal prefill" (BF16, D128, causal,
+ * over the same NHD/HND pages and block tables as decode). Request b holds
+ * L_b cached tokens and q_len_b = qo_indptr[b+1] - qo_indptr[b] query tokens,
+ * which are its last q_len_b tokens (q_len_b <= L_b): query token i of
+ * request b sits at position p = L_b - q_len_b + i and attends to cached
+ * tokens 0 .. p:
+ *     s_j = sm_scale * sum_d q[d] * k_j[d],   j = 0 .. p
+ *     out = sum_j exp(s_j - M) v_j / Z,  lse = M + ln Z  (M = max s_j, Z = sum exp(s_j - M))
+ * With q_len_b = 1 this is the decode above.
+ *   q, out     [qo_indptr[B]][Hq][D]; lse [qo_indptr[B]][Hq]
+ *   rows       optional list of n_rows (t, hq) pairs (t a global query token
+ *              index), flattened; NULL = every (t, hq), in which case out and
+ *              lse are full size, otherwise out is [n_rows][D], lse [n_rows]
+ * Returns ORACLE_EINVAL for bad tables (as decode), a decreasing qo_indptr,
+ * qo_indptr[0] != 0, or q_len_b > L_b.
+ */
+int oracle_paged_prefill_f64(int B, int Hq, int Hkv, int D, int page_size, int layout,
+                             int64_t num_pages, const uint16_t* q, const uint16_t* k,
+                             const uint16_t* v, const int32_t* qo_indptr, const int32_t* indptr,
+                             const int32_t* indices, const int32_t* last_page_len,
+                             double sm_scale, const int32_t* rows, int n_rows, double* out,
+                             double* lse, int nthreads);
 
 /* Logical token count of request b: (P_b - 1) * page_size + last_page_len[b]. */
 int64_t oracle_kv_len(const int32_t* indptr, const int32_t* last_page_len, int page_size, int b);

@@ -264,3 +264,105 @@ def bf16_bits(t) -> np.ndarray:
     import torch
 
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ causal prefill
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    """A paged causal prefill workload: request b has q_lens[b] new query
+    tokens, the last of its kv_lens[b] cached tokens (the cache already holds
+    the new tokens' K and V)."""
+
+    name: str
+    q_lens: tuple
+    kv_lens: tuple
+    num_qo_heads: int
+    num_kv_heads: int
+    page_size: int = 16
+    layout: str = "NHD"
+    head_dim: int = 128
+    seed: int = 1
+    sigma: float = 1.0
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+PREFILL_CONFIGS = {
+    # the pages' paged-prefill shape: two requests, 32 and 64 new tokens over
+    # 256 and 1024 cached tokens, GQA group of four, D = 128
+    "prefill_gqa4_q32+64_kv256+1024_ps16_nhd": PrefillConfig(
+        "prefill_gqa4_q32+64_kv256+1024_ps16_nhd", (32, 64), (256, 1024), 32, 8, seed=20261301),
+    # a long chunked prefill: eight requests, 2048 new tokens each over 2048
+    # to 16384 cached tokens
+    "prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd": PrefillConfig(
+        "prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd", (2048,) * 8,
+        (2048, 4096, 6144, 8192, 10240, 12288, 14336, 16384), 32, 8, seed=20261302),
+}
+PREFILL_ORDER = list(PREFILL_CONFIGS)
+
+
+@dataclass
+class PrefillCase:
+    """A complete causal prefill problem. q is [Nq, Hq, D]; qo_indptr [B+1]."""
+
+    batch: int
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    layout: str
+    sm_scale: float
+    tables: BlockTables
+    qo_indptr: np.ndarray
+    q: object
+    k: object
+    v: object
+    name: str = "prefill"
+
+    @property
+    def group_size(self):
+        return self.num_qo_heads // self.num_kv_heads
+
+    @property
+    def num_q_tokens(self) -> int:
+        return int(self.qo_indptr[-1])
+
+    def causal_pairs(self) -> int:
+        """(query token, cached token) pairs attended, per query head."""
+        n = 0
+        for b in range(self.batch):
+            ql = int(self.qo_indptr[b + 1] - self.qo_indptr[b])
+            L = int(self.tables.lengths[b])
+            n += ql * (L - ql) + ql * (ql + 1) // 2
+        return n
+
+    def flops(self) -> int:
+        """Multiply-adds of QK^T and PV counted as 2 flops each: 4 D per pair per head."""
+        return 4 * self.head_dim * self.num_qo_heads * self.causal_pairs()
+
+
+def prefill_case(q_lens, kv_lens, num_qo_heads, num_kv_heads, page_size, layout="NHD",
+                 head_dim=128, seed=1, sigma=1.0, device="cpu", sm_scale=None,
+                 permute=True, name="prefill") -> PrefillCase:
+    """Block tables over kv_lens (recipe above), q [sum q_lens, Hq, D], pools."""
+    if len(q_lens) != len(kv_lens) or any(q > L for q, L in zip(q_lens, kv_lens)):
+        raise ValueError("each request needs q_len <= kv_len")
+    rng = np.random.default_rng(seed)
+    t = build_block_tables(list(kv_lens), page_size, rng, 0, 1, permute)
+    qo = np.zeros(len(q_lens) + 1, np.int32)
+    qo[1:] = np.cumsum(np.asarray(q_lens, np.int64))
+    q, k, v = make_values(int(qo[-1]), num_qo_heads, num_kv_heads, head_dim, t.num_pages,
+                          page_size, layout, seed, sigma, device)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(head_dim)
+    return PrefillCase(len(q_lens), num_qo_heads, num_kv_heads, head_dim, page_size, layout,
+                       sm_scale, t, qo, q, k, v, name)
+
+
+def make_prefill_case(cfg: PrefillConfig, device="cpu") -> PrefillCase:
+    return prefill_case(cfg.q_lens, cfg.kv_lens, cfg.num_qo_heads, cfg.num_kv_heads,
+                        cfg.page_size, cfg.layout, cfg.head_dim, cfg.seed, cfg.sigma, device,
+                        cfg.sm_scale, name=cfg.name)
