@@ -204,15 +204,18 @@ def gpu_id_for_smi(torch, dev):
         return None
 
 
+DECODE_SOURCES = ("oxd_decode.cu", "oxd_decode_wide.cu", "oxd_host.cpp", "oxd_host_util.h",
+                  "oxd_internal.h", "oxd_merge.cu", "oxd_merge_row.cuh", "oxd_ptx.cuh",
+                  "oxd_tcgen05.cuh")
+
+
 def source_hash():
-    """Hash of the sources that decide a decode launch's DRAM traffic (the
-    planner, the decode and merge kernels); the append kernel's file is left
-    out, it never runs in a decode step."""
+    """Hash of the sources that decide a decode launch's DRAM traffic: the
+    planner, the decode and merge kernels and their headers (the append and
+    prefill files never run in a decode step)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_attn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name == "oxd_append.cu":
-            continue
+    for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

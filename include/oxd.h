@@ -348,6 +348,115 @@ oxd_status oxd_rope_append(const oxd_rope_append_desc* desc, const void* q, cons
                            void* v_pages, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/*
+ * Paged causal prefill ("FlashInfer parity matrix" page, "Admitted attention
+ * matrix", row "Paged causal prefill": BF16, D128, causal, over the same
+ * NHD/HND pages and block tables as decode, long ranges split into pieces
+ * with a caller-owned F32 workspace; "Domain coverage", "Prefill attention").
+ *
+ * Request b has L_b cached tokens (its block table, as for decode) and
+ * q_len_b = qo_indptr[b+1] - qo_indptr[b] query tokens, which are the last
+ * q_len_b of its cached tokens (their K and V are already in the pages, e.g.
+ * written by oxd_rope_append). Query token i of request b (global index
+ * qo_indptr[b] + i) sits at position p = L_b - q_len_b + i and, for each
+ * query head hq (KV head hq / G, G = Hq / Hkv), computes
+ *   s_j = sm_scale * q . k_j (j = 0 .. p),  out = softmax(s) V,
+ *   lse = ln sum_j exp(s_j).
+ * Numerics as for decode: F32 softmax state, QK^T and PV on the tensor cores
+ * with BF16 operands (P rounded to BF16), out rounded once to BF16.
+ *
+ * Lifecycle as for decode ("Oxide Infer" README, "One execution model"): a
+ * host-side plan fixes the tiles (up to 128 / G query tokens of one request
+ * with the G heads of one KV head), the pieces of long tiles and the
+ * workspace size; runs only check operands and enqueue.
+ */
+typedef struct oxd_prefill_plan_s* oxd_prefill_plan;
+
+typedef struct {
+    int32_t batch;          /* B requests */
+    int32_t num_qo_heads;   /* Hq */
+    int32_t num_kv_heads;   /* Hkv; Hq % Hkv == 0, Hq / Hkv <= 128 */
+    int32_t head_dim;       /* 128 */
+    int32_t page_size;      /* 8, 16, 32 or 64 */
+    int32_t layout;         /* oxd_kv_layout */
+    int64_t num_pages;      /* pages in each pool */
+    int32_t max_splits;     /* 0: the planner splits long tiles to fill the GPU;
+                               1: never split; n > 1: at most n pieces per tile */
+    int32_t num_sms;        /* 0: plan for the device; > 0: host-only plan for that
+                               many SMs (runs refused) */
+    int32_t reserved[2];    /* must be zero */
+} oxd_paged_prefill_desc;
+
+typedef struct {
+    int32_t tile_tokens;        /* query tokens per tile: 128 / G */
+    int32_t num_tiles;
+    int32_t num_units;          /* CTAs per run: pieces of all tiles */
+    int32_t num_split_tiles;
+    int32_t max_pieces;
+    int32_t num_merge_rows;     /* output rows merged from pieces (0: one launch) */
+    int32_t launches_per_run;   /* 1, or 2 with the merge */
+    int32_t ctas_per_sm;
+    int32_t num_sms;
+    int32_t reserved0;
+    int64_t workspace_bytes;
+    int64_t total_q_tokens;
+    int64_t total_kv_tokens;
+    int64_t causal_pairs;       /* (query token, cached token) pairs per query head */
+} oxd_prefill_plan_info;
+
+/*
+ * Plan a prefill over host copies of the tables.
+ *   qo_indptr      host int32 [B+1], qo_indptr[0] = 0, non-decreasing
+ *   indptr         host int32 [B+1] (at least one page per request)
+ *   last_page_len  host int32 [B], in [1, page_size]
+ *   device         CUDA device the plan is for (ignored for a host-only plan)
+ * q_len_b must not exceed L_b; a request with q_len_b = 0 adds no work, but
+ * the batch needs at least one query token.
+ * Writes the plan and its workspace size. Errors: OXD_ERR_INVALID_ARGUMENT,
+ * OXD_ERR_UNSUPPORTED (head_dim, page size, group size), OXD_ERR_CUDA,
+ * OXD_ERR_NO_MEMORY.
+ */
+oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int32_t* qo_indptr,
+                                  const int32_t* indptr, const int32_t* last_page_len,
+                                  int device, oxd_prefill_plan* plan_out,
+                                  size_t* workspace_bytes);
+
+/*
+ * Enqueue one prefill on `stream`.
+ *   q              device bf16 [Nq][Hq][128], Nq = qo_indptr[B], 16-byte aligned
+ *   k_pages, v_pages  device bf16 pools (desc layout), 16-byte aligned
+ *   qo_indptr, indptr, indices, last_page_len  device int32 tables equal to
+ *                  the ones planned (indices may differ: page contents are
+ *                  read through them at run time)
+ *   sm_scale       finite
+ *   out            device bf16 [Nq][Hq][128], 16-byte aligned
+ *   lse            device f32 [Nq][Hq] or NULL
+ *   workspace      device scratch of the planned size, 256-byte aligned
+ * Unless the workspace is bound to the plan (oxd_prefill_plan_bind_workspace),
+ * the run first copies the plan's work list into it. Errors (nothing
+ * enqueued): OXD_ERR_INVALID_ARGUMENT, OXD_ERR_ALIGNMENT, OXD_ERR_ALIAS,
+ * OXD_ERR_WORKSPACE_TOO_SMALL, OXD_ERR_PLAN_MISMATCH (destroyed or host-only
+ * plan, other device), OXD_ERR_CUDA. Device-side: an out-of-range page index
+ * (read as page 0), device tables that differ from the plan's, a damaged
+ * bound list or a wait timeout are recorded in the workspace status word.
+ */
+oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const void* k_pages,
+                                 const void* v_pages, const int32_t* qo_indptr,
+                                 const int32_t* indptr, const int32_t* indices,
+                                 const int32_t* last_page_len, float sm_scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* As oxd_plan_bind_workspace, for a prefill plan: later runs on this
+ * workspace read the work list from it and copy nothing. */
+oxd_status oxd_prefill_plan_bind_workspace(oxd_prefill_plan plan, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+/* As oxd_plan_set_timing_events: events recorded around the prefill kernel. */
+oxd_status oxd_prefill_plan_set_timing_events(oxd_prefill_plan plan, void* event_before,
+                                              void* event_after);
+oxd_status oxd_prefill_plan_get_info(oxd_prefill_plan plan, oxd_prefill_plan_info* info);
+oxd_status oxd_prefill_plan_destroy(oxd_prefill_plan plan);
+
 /* Planner decisions of a plan (host only). */
 oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info);
 

@@ -39,6 +39,10 @@ __all__ = [
     "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
     "oxd_read_device_status", "oxd_status_string", "oxd_device_status_string", "oxd_version",
     "oxd_rope_append", "RopeAppendDesc", "make_rope_append_desc", "EXPORTED_SYMBOLS",
+    "PrefillDesc", "PrefillPlanInfo", "PrefillPlan", "make_prefill_desc",
+    "oxd_paged_prefill_plan", "oxd_paged_prefill_run", "oxd_prefill_plan_bind_workspace",
+    "oxd_prefill_plan_get_info", "oxd_prefill_plan_set_timing_events",
+    "oxd_prefill_plan_destroy",
 ]
 
 OXD_OK = 0
@@ -67,6 +71,9 @@ EXPORTED_SYMBOLS = (
     "oxd_plan_set_timing_events", "oxd_plan_destroy", "oxd_read_device_status",
     "oxd_status_string", "oxd_device_status_string", "oxd_version",
     "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace", "oxd_rope_append",
+    "oxd_paged_prefill_plan", "oxd_paged_prefill_run", "oxd_prefill_plan_bind_workspace",
+    "oxd_prefill_plan_get_info", "oxd_prefill_plan_set_timing_events",
+    "oxd_prefill_plan_destroy",
 )
 
 
@@ -129,6 +136,44 @@ class RopeAppendDesc(ctypes.Structure):
     ]
 
 
+class PrefillDesc(ctypes.Structure):
+    """``oxd_paged_prefill_desc``."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("layout", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+    ]
+
+
+class PrefillPlanInfo(ctypes.Structure):
+    """``oxd_prefill_plan_info``."""
+
+    _fields_ = [
+        ("tile_tokens", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+        ("num_units", ctypes.c_int32), ("num_split_tiles", ctypes.c_int32),
+        ("max_pieces", ctypes.c_int32), ("num_merge_rows", ctypes.c_int32),
+        ("launches_per_run", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64), ("total_q_tokens", ctypes.c_int64),
+        ("total_kv_tokens", ctypes.c_int64), ("causal_pairs", ctypes.c_int64),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved0"}
+
+
+def make_prefill_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages,
+                      head_dim=128, max_splits=0, num_sms=0) -> PrefillDesc:
+    """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1."""
+    if isinstance(layout, str):
+        layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
+    return PrefillDesc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
+                       max_splits, num_sms, (ctypes.c_int32 * 2)(0, 0))
+
+
 def make_rope_append_desc(num_tokens, batch, num_qo_heads, num_kv_heads, page_size, layout,
                           num_pages, num_indices, rope_theta=10000.0,
                           head_dim=128) -> RopeAppendDesc:
@@ -161,11 +206,21 @@ def lib():
             L.oxd_plan_bind_workspace.argtypes = [vp, vp, sz, vp]
             L.oxd_rope_append.argtypes = [ctypes.POINTER(RopeAppendDesc)] + [vp] * 12 + [sz, vp]
             L.oxd_plan_destroy.argtypes = [vp]
+            L.oxd_paged_prefill_plan.argtypes = [ctypes.POINTER(PrefillDesc), vp, vp, vp,
+                                                 ctypes.c_int, vp, vp]
+            L.oxd_paged_prefill_run.argtypes = [vp] * 8 + [ctypes.c_float, vp, vp, vp, sz, vp]
+            L.oxd_prefill_plan_bind_workspace.argtypes = [vp, vp, sz, vp]
+            L.oxd_prefill_plan_get_info.argtypes = [vp, ctypes.POINTER(PrefillPlanInfo)]
+            L.oxd_prefill_plan_set_timing_events.argtypes = [vp, vp, vp]
+            L.oxd_prefill_plan_destroy.argtypes = [vp]
             L.oxd_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
             for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run",
                       "oxd_paged_decode_run_static_workspace", "oxd_merge_states",
                       "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
-                      "oxd_read_device_status", "oxd_plan_bind_workspace", "oxd_rope_append"):
+                      "oxd_read_device_status", "oxd_plan_bind_workspace", "oxd_rope_append",
+                      "oxd_paged_prefill_plan", "oxd_paged_prefill_run",
+                      "oxd_prefill_plan_bind_workspace", "oxd_prefill_plan_get_info",
+                      "oxd_prefill_plan_set_timing_events", "oxd_prefill_plan_destroy"):
                 getattr(L, f).restype = ctypes.c_int
             L.oxd_status_string.argtypes = [ctypes.c_int]
             L.oxd_status_string.restype = ctypes.c_char_p
@@ -262,7 +317,7 @@ class Plan:
 
 
 def _handle(plan):
-    return plan.handle if isinstance(plan, Plan) else plan
+    return plan.handle if isinstance(plan, (Plan, PrefillPlan)) else plan
 
 
 def oxd_paged_decode_plan(desc: Desc, indptr_host, last_page_len_host, device: int = 0) -> Plan:
@@ -374,3 +429,92 @@ def oxd_rope_append(desc: RopeAppendDesc, q, k, v, token_request, positions, ind
                                _addr(k_pages), _addr(v_pages), _addr(workspace),
                                int(workspace_bytes), _stream(stream, q))
     _check("oxd_rope_append", st)
+
+
+# ------------------------------------------------------------------ causal prefill
+
+class PrefillPlan:
+    """Owns an ``oxd_prefill_plan`` handle (destroyed on :meth:`destroy` or garbage collection)."""
+
+    def __init__(self, handle: int, workspace_bytes: int, desc: PrefillDesc):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+        self.desc = desc
+
+    @property
+    def info(self) -> PrefillPlanInfo:
+        return oxd_prefill_plan_get_info(self)
+
+    def destroy(self):
+        if self.handle:
+            _check("oxd_prefill_plan_destroy", lib().oxd_prefill_plan_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle:
+                lib().oxd_prefill_plan_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+def oxd_paged_prefill_plan(desc: PrefillDesc, qo_indptr_host, indptr_host, last_page_len_host,
+                           device: int = 0) -> PrefillPlan:
+    """Plan a causal prefill from host tables; returns a :class:`PrefillPlan`."""
+    qo = np.ascontiguousarray(np.asarray(qo_indptr_host), dtype=np.int32)
+    indptr = np.ascontiguousarray(np.asarray(indptr_host), dtype=np.int32)
+    last = np.ascontiguousarray(np.asarray(last_page_len_host), dtype=np.int32)
+    if (qo.shape != (desc.batch + 1,) or indptr.shape != (desc.batch + 1,)
+            or last.shape != (desc.batch,)):
+        raise OxdError("oxd_paged_prefill_plan", OXD_ERR_INVALID_ARGUMENT,
+                       "qo_indptr and indptr must be [batch+1], last_page_len [batch]")
+    h = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = lib().oxd_paged_prefill_plan(ctypes.byref(desc), qo.ctypes.data, indptr.ctypes.data,
+                                      last.ctypes.data, int(device), ctypes.byref(h),
+                                      ctypes.byref(ws))
+    _check("oxd_paged_prefill_plan", st)
+    return PrefillPlan(h.value, ws.value, desc)
+
+
+def oxd_paged_prefill_run(plan, q, k_pages, v_pages, qo_indptr, indptr, indices, last_page_len,
+                          sm_scale, out, lse, workspace, workspace_bytes=None,
+                          stream=None) -> None:
+    """Enqueue one causal prefill (see ``oxd_paged_prefill_run`` in include/oxd.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib().oxd_paged_prefill_run(
+        _handle(plan), _addr(q), _addr(k_pages), _addr(v_pages), _addr(qo_indptr),
+        _addr(indptr), _addr(indices), _addr(last_page_len), float(sm_scale), _addr(out),
+        _addr(lse), _addr(workspace), int(workspace_bytes), _stream(stream, q))
+    _check("oxd_paged_prefill_run", st)
+
+
+def oxd_prefill_plan_bind_workspace(plan, workspace, workspace_bytes=None, stream=None) -> None:
+    """Enqueue the copy of the prefill plan's work list into ``workspace``."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = lib().oxd_prefill_plan_bind_workspace(_handle(plan), _addr(workspace),
+                                               int(workspace_bytes), _stream(stream, workspace))
+    _check("oxd_prefill_plan_bind_workspace", st)
+
+
+def oxd_prefill_plan_get_info(plan) -> PrefillPlanInfo:
+    info = PrefillPlanInfo()
+    _check("oxd_prefill_plan_get_info",
+           lib().oxd_prefill_plan_get_info(_handle(plan), ctypes.byref(info)))
+    return info
+
+
+def oxd_prefill_plan_set_timing_events(plan, event_before, event_after) -> None:
+    _check("oxd_prefill_plan_set_timing_events",
+           lib().oxd_prefill_plan_set_timing_events(_handle(plan), _event(event_before),
+                                                    _event(event_after)))
+
+
+def oxd_prefill_plan_destroy(plan) -> None:
+    if isinstance(plan, PrefillPlan):
+        plan.destroy()
+    else:
+        _check("oxd_prefill_plan_destroy", lib().oxd_prefill_plan_destroy(plan))

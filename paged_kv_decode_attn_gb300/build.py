@@ -15,10 +15,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "liboxd.so")
-HEADERS = [os.path.join(ROOT, "include", "oxd.h"), os.path.join(CSRC, "oxd_internal.h"),
-           os.path.join(CSRC, "oxd_merge_row.cuh"), os.path.join(CSRC, "oxd_ptx.cuh")]
+HEADERS = [os.path.join(ROOT, "include", "oxd.h")] + [
+    os.path.join(CSRC, h) for h in ("oxd_internal.h", "oxd_merge_row.cuh", "oxd_ptx.cuh",
+                                    "oxd_tcgen05.cuh", "oxd_prefill.h", "oxd_host_util.h")]
 SOURCES = ["oxd_host.cpp", "oxd_decode.cu", "oxd_decode_wide.cu", "oxd_merge.cu",
-           "oxd_noalloc.cu", "oxd_append.cu"]
+           "oxd_noalloc.cu", "oxd_append.cu", "oxd_prefill.cu", "oxd_prefill_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

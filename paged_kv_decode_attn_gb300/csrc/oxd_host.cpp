@@ -25,6 +25,7 @@
 #include <vector>
 
 #include "../../include/oxd.h"
+#include "oxd_host_util.h"
 #include "oxd_internal.h"
 
 using namespace oxd;
@@ -105,23 +106,6 @@ bool plan_alive(oxd_plan p) {
     return g_plans.count(p) != 0;
 }
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-struct Span {
-    uintptr_t lo, hi;  // [lo, hi)
-};
-
-Span span(const void* p, size_t bytes) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    return {a, a + bytes};
-}
-
-bool overlap(const Span& a, const Span& b) {
-    return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi;
-}
-
 int choose_variant(int G, int tensor_path) {
     if (G == 1) return kVariantFmaG1;
     if (G == 2) return kVariantFmaG2;
@@ -157,43 +141,8 @@ EncodeTiledFn get_encoder() {
     return fn;
 }
 
-// 4-D map over a K or V pool: (d, A, B, page) with (A, B) = (head, token)
-// for NHD and (token, head) for HND; the box is 64 columns x all page_size
-// tokens of one head, stored with the 128-byte swizzle.
 bool encode_pool(CUtensorMap* map, const void* pool, const oxd_paged_decode_desc& d) {
-    EncodeTiledFn enc = get_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t D = static_cast<cuuint64_t>(d.head_dim);
-    const cuuint64_t ps = static_cast<cuuint64_t>(d.page_size);
-    const cuuint64_t H = static_cast<cuuint64_t>(d.num_kv_heads);
-    cuuint64_t dims[4], strides[3];
-    cuuint32_t box[4];
-    const cuuint32_t elem[4] = {1, 1, 1, 1};
-    dims[0] = D;
-    dims[3] = static_cast<cuuint64_t>(d.num_pages);
-    if (d.layout == OXD_LAYOUT_NHD) {
-        dims[1] = H;
-        dims[2] = ps;
-        strides[0] = D * 2;
-        strides[1] = H * D * 2;
-        box[1] = 1;
-        box[2] = static_cast<cuuint32_t>(ps);
-    } else {
-        dims[1] = ps;
-        dims[2] = H;
-        strides[0] = D * 2;
-        strides[1] = ps * D * 2;
-        box[1] = static_cast<cuuint32_t>(ps);
-        box[2] = 1;
-    }
-    strides[2] = ps * H * D * 2;
-    box[0] = 64;
-    box[3] = 1;
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
-                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_kv_pool(map, pool, d.layout, d.page_size, d.num_kv_heads, d.num_pages);
 }
 
 // 2-D map over q as [B*Hq rows][128] for the tcgen05 variant: a box is 32
@@ -241,6 +190,64 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
 
 namespace oxd {
 uint32_t next_run_epoch() { return next_epoch(); }
+
+unsigned long long next_plan_stamp() { return next_stamp(); }
+
+bool encode_kv_pool(CUtensorMap* map, const void* pool, int layout, int page_size,
+                    int num_kv_heads, int64_t num_pages) {
+    EncodeTiledFn enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t D = static_cast<cuuint64_t>(kHeadDim);
+    const cuuint64_t ps = static_cast<cuuint64_t>(page_size);
+    const cuuint64_t H = static_cast<cuuint64_t>(num_kv_heads);
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    dims[0] = D;
+    dims[3] = static_cast<cuuint64_t>(num_pages);
+    if (layout == OXD_LAYOUT_NHD) {
+        dims[1] = H;
+        dims[2] = ps;
+        strides[0] = D * 2;
+        strides[1] = H * D * 2;
+        box[1] = 1;
+        box[2] = static_cast<cuuint32_t>(ps);
+    } else {
+        dims[1] = ps;
+        dims[2] = H;
+        strides[0] = D * 2;
+        strides[1] = ps * D * 2;
+        box[1] = static_cast<cuuint32_t>(ps);
+        box[2] = 1;
+    }
+    strides[2] = ps * H * D * 2;
+    box[0] = 64;
+    box[3] = 1;
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
+                     strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
+    EncodeTiledFn enc = get_encoder();
+    if (enc == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], elem[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        elem[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                     const_cast<void*>(base), d, st, bx, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 }  // namespace oxd
 
 extern "C" {
