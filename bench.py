@@ -78,9 +78,14 @@ def parse_args(argv=None):
                          "params: unbound runs")
     ap.add_argument("--graph", action="store_true",
                     help="capture one run in a CUDA graph and time its replays")
-    ap.add_argument("--op", choices=["decode", "rope_append"], default="decode",
+    ap.add_argument("--op", choices=["decode", "rope_append", "prefill"], default="decode",
                     help="rope_append: time the fused RoPE + paged append on the workload's "
-                         "tables instead of the decode step")
+                         "tables instead of the decode step; prefill: time the paged causal "
+                         "prefill of --prefill-config")
+    ap.add_argument("--prefill-config", default="prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd",
+                    choices=W.PREFILL_ORDER)
+    ap.add_argument("--max-splits", type=int, default=0,
+                    help="prefill: at most this many pieces per tile (0: the planner decides)")
     ap.add_argument("--tokens-per-request", type=int, default=1,
                     help="rope_append: tokens appended per request in one call (1..64)")
     return ap.parse_args(argv)
@@ -616,12 +621,134 @@ def run_rope_append(args):
     return 0
 
 
+def run_prefill(args):
+    """Paged causal prefill of one prefill workload. A step is one
+    oxd_paged_prefill_run on the bound workspace (the prefill kernel and, when
+    tiles were split, the merge behind it). Metric: causal attention flops
+    (4 D per attended (query token, cached token) pair per query head) per
+    second; the roofline is the prefill kernel alone against the measured
+    bf16 tensor peak."""
+    import torch
+
+    import paged_kv_decode_attn_gb300 as oxd
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    oxd.build()
+    cfg = W.PREFILL_CONFIGS[args.prefill_config]
+    case = W.make_prefill_case(cfg, device=dev)
+    t = case.tables
+    desc = oxd.make_prefill_desc(case.batch, case.num_qo_heads, case.num_kv_heads,
+                                 case.page_size, case.layout, t.num_pages,
+                                 max_splits=args.max_splits)
+    h0 = time.perf_counter()
+    plan = oxd.oxd_paged_prefill_plan(desc, case.qo_indptr, t.indptr, t.last_page_len)
+    host_us = (time.perf_counter() - h0) * 1e6
+    info = plan.info
+    qo = torch.as_tensor(case.qo_indptr, device=dev)
+    indptr = torch.as_tensor(t.indptr, device=dev)
+    indices = torch.as_tensor(t.indices, device=dev)
+    last = torch.as_tensor(t.last_page_len, device=dev)
+    out = torch.empty_like(case.q)
+    lse = torch.empty(case.q.shape[:2], device=dev)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    oxd.oxd_prefill_plan_bind_workspace(plan, ws, stream=stream)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
+
+    def step():
+        oxd.oxd_paged_prefill_run(plan, case.q, case.k, case.v, qo, indptr, indices, last,
+                                  case.sm_scale, out, lse, ws, stream=stream)
+
+    W_ = max(3, args.warmup)
+    for _ in range(W_):
+        flush()
+        step()
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error in the prefill warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev))
+    sampler.start()
+    torch.cuda.synchronize(dev)
+    sampler.mark_start()
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error during the timed steps")
+    # the prefill kernel alone (events the library records around its launch)
+    Kk = max(3, min(K, 200))
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Kk)]
+    for a, b in kev:  # materialise the events so their handles exist
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    for a, b in kev:
+        flush()
+        oxd.oxd_prefill_plan_set_timing_events(plan, a, b)
+        step()
+    torch.cuda.synchronize(dev)
+    oxd.oxd_prefill_plan_set_timing_events(plan, None, None)
+    kern = [a.elapsed_time(b) for a, b in kev]
+    ms = statistics.mean(step_ms)
+    k_ms = statistics.mean(kern)
+    flops = case.flops()
+    tfs = flops / (ms * 1e-3) / 1e12
+    k_tfs = flops / (k_ms * 1e-3) / 1e12
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peak = float(json.load(f)["bf16_tflops"])
+    line = {
+        "impl": "oxd", "op": "prefill",
+        "metric": "paged causal prefill: attention TFLOP/s (4 D flops per attended pair per "
+                  "query head), us per call",
+        "value": tfs, "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": W_,
+        "ms_per_step": ms, "us_per_call": ms * 1e3,
+        "us_p10_p90": [float(np.percentile(step_ms, 10)) * 1e3,
+                       float(np.percentile(step_ms, 90)) * 1e3],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": case.batch, "q_lens": list(cfg.q_lens),
+                   "kv_lens": list(cfg.kv_lens), "num_qo_heads": case.num_qo_heads,
+                   "num_kv_heads": case.num_kv_heads, "page_size": case.page_size,
+                   "layout": case.layout, "flops_per_call": flops,
+                   "causal_pairs_per_head": case.causal_pairs(),
+                   "l2": "flushed before every call, outside its events"},
+        "plan": dict(info.as_dict(), host_us=host_us),
+        "roofline": {"bound": "tensor", "achieved": k_tfs, "peak": peak, "unit": "TFLOP/s",
+                     "frac": k_tfs / peak, "kernel_us": k_ms * 1e3,
+                     "peak_source": "measured bf16 burst"},
+        "gpu_launches": K * info.launches_per_run,
+        "clocks": clocks,
+    }
+    if cfg.name.startswith("prefill_gqa4_q32+64"):
+        line["context"] = {"pages_h20_us": {"oxide": 46.60, "flashinfer": 23.21},
+                           "note": "other hardware (H20): context, not a target"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "rope_append":
         return run_rope_append(args)
+    if args.op == "prefill":
+        return run_prefill(args)
     return run_oxd(args)
 
 
