@@ -23,8 +23,10 @@
 //     lane r). Per stage it loads the row's 64 scores, masks the tokens past
 //     its position (and past the piece), keeps a running maximum that is
 //     raised only when a score exceeds it by more than 2^8 (then O is
-//     rescaled in TMEM), writes P as bf16 over its scores, and at the end
-//     writes out/lse, or the F32 partial state of the piece.
+//     rescaled in TMEM, after the previous PV), writes P as bf16 over its
+//     scores and publishes it without waiting for the previous PV (the MMAs
+//     run in issue order), and at the end writes out/lse, or the F32 partial
+//     state of the piece.
 // V rows past the piece's last cached token are zeroed before its last PV.
 // Every wait is bounded (OXD_DEVICE_WAIT_TIMEOUT); on abort the MMAs and
 // copies in flight are drained before the tensor memory is released.
@@ -40,61 +42,73 @@
 namespace oxd {
 namespace {
 
-constexpr int kPStages = 2;
-constexpr int kPThreads = 192;
+constexpr int kPKStages = 3;     // K ring: a slot is free once its score MMA is done
+constexpr int kPVStages = 2;     // V ring: a slot is free once its PV is done
+constexpr int kPThreads = 224;   // 4 softmax warps, MMA warp, K producer, V producer
 constexpr int kPSoftmaxThreads = 128;
 constexpr int kPHalf = kPrefillStageTokens * 128;  // one 64-column half of K or V: 8 KB
-constexpr int kPStageBytes = 4 * kPHalf;           // K halves, then V halves: 32 KB
+constexpr int kPSlotBytes = 2 * kPHalf;            // K or V of one stage: 16 KB
 constexpr int kPQHalf = kPrefillRows * 128;        // 16 KB
 constexpr int kPQOff = 0;
-constexpr int kPRingOff = 2 * kPQHalf;
-constexpr int kPCtlOff = kPRingOff + kPStages * kPStageBytes;
+constexpr int kPKOff = 2 * kPQHalf;
+constexpr int kPVOff = kPKOff + kPKStages * kPSlotBytes;
+constexpr int kPCtlOff = kPVOff + kPVStages * kPSlotBytes;  // 112 KB of operands
 constexpr uint32_t kPTmemCols = 256;  // O [0,128), S0 [128,192), S1 [192,256)
-static_assert(kPRingOff % 1024 == 0 && kPStageBytes % 1024 == 0, "swizzle atoms aligned");
+static_assert(kPKOff % 1024 == 0 && kPVOff % 1024 == 0 && kPSlotBytes % 1024 == 0,
+              "swizzle atoms aligned");
 
 struct PCtl {
-    uint64_t full[kPStages];
-    uint64_t empty[kPStages];
+    uint64_t kfull[kPKStages];
+    uint64_t kempty[kPKStages];
+    uint64_t vfull[kPVStages];
+    uint64_t vempty[kPVStages];
     uint64_t s_ready[2];
     uint64_t p_ready[2];
-    uint64_t o_ready;
+    uint64_t o_ready[4];  // PV(g) completes phase g / 4 of o_ready[g % 4]
     uint64_t mma_done;
-    int issued[kPStages];
+    int kissued[kPKStages];
+    int vissued[kPVStages];
     uint32_t tmem;
     int flags[4];  // [0] abort, [1] the unit is usable
 };
-constexpr int kPSmemBytes = 1024 /* alignment slack */ + kPCtlOff + static_cast<int>(sizeof(PCtl));
+// The dynamic shared memory starts 1024-byte aligned (checked in the kernel),
+// so no alignment slack: two CTAs fit one SM.
+constexpr int kPSmemBytes = kPCtlOff + static_cast<int>(sizeof(PCtl));
 
 __global__ void __launch_bounds__(kPThreads)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v,
                          const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ PrefillParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw;
     PCtl& ctl = *reinterpret_cast<PCtl*>(sm + kPCtlOff);
     volatile int* flags = ctl.flags;
     const uint32_t s_base = smem_addr(sm);
     const uint32_t s_q = s_base + kPQOff;
-    auto ring_k = [&](int slot) { return s_base + kPRingOff + slot * kPStageBytes; };
-    auto ring_v = [&](int slot) { return s_base + kPRingOff + slot * kPStageBytes + 2 * kPHalf; };
+    auto ring_k = [&](int slot) { return s_base + kPKOff + slot * kPSlotBytes; };
+    auto ring_v = [&](int slot) { return s_base + kPVOff + slot * kPSlotBytes; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ps = p.page_size;
     const int G = p.group;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPStages; ++s) {
-            mbar_init(&ctl.full[s], 1);
-            mbar_init(&ctl.empty[s], 1);
-            ctl.issued[s] = 0;
+        for (int s = 0; s < kPKStages; ++s) {
+            mbar_init(&ctl.kfull[s], 1);
+            mbar_init(&ctl.kempty[s], 1);
+            ctl.kissued[s] = 0;
+        }
+        for (int s = 0; s < kPVStages; ++s) {
+            mbar_init(&ctl.vfull[s], 1);
+            mbar_init(&ctl.vempty[s], 1);
+            ctl.vissued[s] = 0;
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl.s_ready[i], 1);
             mbar_init(&ctl.p_ready[i], 4);  // one arrival per softmax warp
         }
-        mbar_init(&ctl.o_ready, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&ctl.o_ready[i], 1);
         mbar_init(&ctl.mma_done, 1);
         flags[0] = 0;
         fence_mbar_init();
@@ -102,8 +116,9 @@ __global__ void __launch_bounds__(kPThreads)
             *p.last_epoch = p.epoch;
             if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
         }
-        // the unit, checked before anything uses it
-        int ok = p.ws_stamp == nullptr || *p.ws_stamp == p.stamp;
+        // the unit, checked before anything uses it (and the operand
+        // buffers' alignment, which the swizzled copies need)
+        int ok = (p.ws_stamp == nullptr || *p.ws_stamp == p.stamp) && (s_base & 1023u) == 0;
         if (ok && static_cast<int>(blockIdx.x) < p.n_units) {
             const PrefillUnit u = p.units[blockIdx.x];
             const int T = p.tile_tokens;
@@ -155,8 +170,11 @@ __global__ void __launch_bounds__(kPThreads)
     if (usable) u = p.units[blockIdx.x];
     const int n_st = usable ? (u.kv_valid + kPrefillStageTokens - 1) / kPrefillStageTokens : 0;
 
-    if (warp == 5) {
-        // ================================================ producer warp
+    if (warp >= 5) {
+        // ================================================ producer warps
+        // warp 5: the query tile and K; warp 6: V. Lane 2j + h copies half h
+        // of page j of the stage.
+        const bool is_k = warp == 5;
         const int pps = kPrefillStageTokens / ps;  // pages per stage (divides 32)
         const int32_t* idx = p.indices + u.idx_begin;
         int win = 0, nxt = 0, win_base = 0;
@@ -171,9 +189,16 @@ __global__ void __launch_bounds__(kPThreads)
             win = bad ? 0 : win;  // an index outside the pool reads page 0
         };
         if (n_st > 0) check_window();
+        const int n_slots = is_k ? kPKStages : kPVStages;
+        uint64_t* full = is_k ? ctl.kfull : ctl.vfull;
+        uint64_t* empty = is_k ? ctl.kempty : ctl.vempty;
+        int* issued = is_k ? ctl.kissued : ctl.vissued;
+        const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+        const int ca = p.layout == 0 ? u.hkv : 0;  // (d, A, B, page): NHD (d, head, token,
+        const int cb = p.layout == 0 ? 0 : u.hkv;  // page), HND (d, token, head, page)
         bool ok = true;
         for (int s = 0; s < n_st; ++s) {
-            const int slot = s % kPStages;
+            const int slot = s % n_slots;
             const int pg0 = s * pps;
             const int npg = min(pps, u.n_pages - pg0);
             if (pg0 >= win_base + 32) {
@@ -183,37 +208,30 @@ __global__ void __launch_bounds__(kPThreads)
                 check_window();
             }
             int okw = 1;
-            if (lane == 0 && s >= kPStages)
-                okw = mbar_wait(&ctl.empty[slot], ((s / kPStages) + 1) & 1, flags) ? 1 : 0;
+            if (lane == 0 && s >= n_slots)
+                okw = mbar_wait(&empty[slot], ((s / n_slots) + 1) & 1, flags) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, okw, 0)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                const uint32_t qbytes = s == 0 ? 2u * 128u * G * p.tile_tokens : 0u;
-                mbar_arrive_expect_tx(&ctl.full[slot], npg * ps * kHeadDim * 2 * 2 + qbytes);
-                if (s == 0) {
-                    tma_load_3d(s_q, &tmap_q, &ctl.full[slot], 0, u.hkv * G, u.q_begin);
-                    tma_load_3d(s_q + kPQHalf, &tmap_q, &ctl.full[slot], 64, u.hkv * G,
-                                u.q_begin);
+                const uint32_t qbytes = is_k && s == 0 ? 2u * 128u * G * p.tile_tokens : 0u;
+                mbar_arrive_expect_tx(&full[slot], npg * ps * kHeadDim * 2 + qbytes);
+                if (qbytes) {
+                    tma_load_3d(s_q, &tmap_q, &full[slot], 0, u.hkv * G, u.q_begin);
+                    tma_load_3d(s_q + kPQHalf, &tmap_q, &full[slot], 64, u.hkv * G, u.q_begin);
                 }
             }
-            {
-                // lane 4j + 2t + h copies half h of tensor t (K, V) of page j
-                const int ca = p.layout == 0 ? u.hkv : 0;  // (d, A, B, page): NHD (d, head,
-                const int cb = p.layout == 0 ? 0 : u.hkv;  // token, page), HND (d, token, head, page)
-                const int j = lane >> 2;
-                const int page = __shfl_sync(0xffffffffu, win, (pg0 - win_base + j) & 31);
-                if (lane < 4 * npg) {
-                    const uint32_t off = j * ps * 128 + ((lane & 1) ? kPHalf : 0);
-                    tma_load_4d(((lane & 2) ? ring_v(slot) : ring_k(slot)) + off,
-                                (lane & 2) ? &tmap_v : &tmap_k, &ctl.full[slot], (lane & 1) * 64,
-                                ca, cb, page);
-                }
+            const int j = lane >> 1;
+            const int page = __shfl_sync(0xffffffffu, win, (pg0 - win_base + j) & 31);
+            if (lane < 2 * npg) {
+                const uint32_t dst = (is_k ? ring_k(slot) : ring_v(slot)) + j * ps * 128 +
+                                     ((lane & 1) ? kPHalf : 0);
+                tma_load_4d(dst, map, &full[slot], (lane & 1) * 64, ca, cb, page);
             }
-            if (lane == 0) ctl.issued[slot] += 1;
+            if (lane == 0) issued[slot] += 1;
         }
-        if (lane == 0 && usable) {
+        if (is_k && lane == 0 && usable) {
             // the device tables must be the ones the plan was made from
             const int b = u.b;
             const int64_t L = static_cast<int64_t>(p.indptr[b + 1] - p.indptr[b] - 1) * ps +
@@ -236,11 +254,11 @@ __global__ void __launch_bounds__(kPThreads)
             while (gp < n_st) {
                 bool progress = false;
                 if (gq < n_st && gq < gp + 2 &&
-                    mbar_try_wait(&ctl.full[gq % kPStages], (gq / kPStages) & 1)) {
+                    mbar_try_wait(&ctl.kfull[gq % kPKStages], (gq / kPKStages) & 1)) {
                     tc_fence_after();
                     // S = Q K^T: K = 128 in steps of 16 (32 bytes of a 128-byte
                     // swizzled row; columns 64..127 in the other half)
-                    const uint32_t k0 = ring_k(gq % kPStages);
+                    const uint32_t k0 = ring_k(gq % kPKStages);
                     for (int ks = 0; ks < kHeadDim / 16; ++ks) {
                         const uint32_t h = static_cast<uint32_t>(ks >> 2), kk = ks & 3;
                         const uint64_t ad = umma_sdesc(s_q + h * kPQHalf + kk * 32, 16, 1024);
@@ -248,21 +266,23 @@ __global__ void __launch_bounds__(kPThreads)
                         umma_ss(t_s(gq & 1), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
                     }
                     umma_commit(&ctl.s_ready[gq & 1]);
+                    umma_commit(&ctl.kempty[gq % kPKStages]);  // K of the slot is consumed
                     ++gq;
                     progress = true;
                 }
-                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1)) {
+                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1) &&
+                    mbar_try_wait(&ctl.vfull[gp % kPVStages], (gp / kPVStages) & 1)) {
                     tc_fence_after();
                     // O += P V: 16 tokens a step = two 8-row groups (1024 B apart);
                     // the two 64-column halves of V are kPHalf apart
-                    const uint32_t v0 = ring_v(gp % kPStages);
+                    const uint32_t v0 = ring_v(gp % kPVStages);
                     for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks) {
                         const uint64_t bd = umma_sdesc(v0 + ks * 2048, kPHalf, 1024);
                         umma_ts(t_o, t_s(gp & 1) + 8u * ks, bd, kIdPV,
                                 (ks > 0 || gp > 0) ? 1u : 0u);
                     }
-                    umma_commit(&ctl.empty[gp % kPStages]);
-                    umma_commit(&ctl.o_ready);
+                    umma_commit(&ctl.vempty[gp % kPVStages]);
+                    umma_commit(&ctl.o_ready[gp & 3]);
                     ++gp;
                     progress = true;
                 }
@@ -301,9 +321,7 @@ __global__ void __launch_bounds__(kPThreads)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int g = 0; g < n_st; ++g) {
-            const int slot = g % kPStages;
-            if (!wait_all(&ctl.full[slot], (g / kPStages) & 1) ||
-                !wait_all(&ctl.s_ready[g & 1], (g >> 1) & 1)) {
+            if (!wait_all(&ctl.s_ready[g & 1], (g >> 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -312,14 +330,28 @@ __global__ void __launch_bounds__(kPThreads)
             tmem_ld64(t_s(g & 1) + lane_off, sr);
             const int base = u.kv_begin + g * kPrefillStageTokens;
             const int nvalid = min(kPrefillStageTokens, u.kv_valid - g * kPrefillStageTokens);
-            const int lim = min(nvalid, pos - base + 1);  // visible columns of this row
-            float mx = -INFINITY;
+            // A stage that ends at or before the tile's first position is seen
+            // whole by every row (the same for the whole CTA): no mask, the
+            // maximum is taken over the raw scores and the scale is folded
+            // into the exponent's FMA. Otherwise scores are scaled and masked
+            // first.
+            const bool whole = nvalid == kPrefillStageTokens &&
+                               base + kPrefillStageTokens - 1 <= u.p0 && sc > 0.f;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float x = j < lim ? __uint_as_float(sr[j]) * sc : -INFINITY;
-                sr[j] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sr[j]));
+            } else {
+                const int lim = min(nvalid, pos - base + 1);  // visible columns of this row
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float x = j < lim ? __uint_as_float(sr[j]) * sc : -INFINITY;
+                    sr[j] = __float_as_uint(x);
+                    mq[j & 3] = fmaxf(mq[j & 3], x);
+                }
             }
+            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            if (whole) mx *= sc;
             float alpha = 1.f;
             bool rescale = false;
             if (g == 0) {
@@ -332,26 +364,41 @@ __global__ void __launch_bounds__(kPThreads)
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
             uint32_t pk[32];
-            float ls = 0.f;
+            float lq[4] = {0.f, 0.f, 0.f, 0.f};
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_use);
-                const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_use);
-                ls += p0 + p1;
-                pk[j] = pack_bf16x2(p0, p1);
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), sc, -m_use));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), sc, -m_use));
+                    lq[j & 3] += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_use);
+                    const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_use);
+                    lq[j & 3] += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
             }
-            l += ls;
+            l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
             tmem_st32(t_s(g & 1) + lane_off, pk);
             tmem_wait_st();
-            // the previous stage's PV is done before O is touched
-            if (g > 0) {
-                if (!wait_all(&ctl.o_ready, (g - 1) & 1)) {
+            // PV(g - 1) must be done before O is rescaled; without a rescale
+            // P(g) is published at once (PV(g) runs after PV(g - 1) anyway).
+            // Four o_ready barriers keep every parity wait unambiguous: PV
+            // (g + 3) cannot complete before this warp publishes P(g + 3),
+            // and PV(g - 5) is known done from the wait of two stages ago.
+            auto wait_pv = [&](int k) {
+                return wait_all(&ctl.o_ready[k & 3], (k >> 2) & 1);
+            };
+            if (__any_sync(0xffffffffu, rescale)) {
+                if (g > 0 && !wait_pv(g - 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
                 for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
                     uint32_t o[64];
                     tmem_ld64(t_o + lane_off + c0, o);
@@ -368,9 +415,14 @@ __global__ void __launch_bounds__(kPThreads)
             }
             const bool last = g == n_st - 1;
             if (last && nvalid < kPrefillStageTokens) {
-                // zero V rows past the piece (whole 128-byte rows, so the
-                // swizzle does not matter)
-                uint8_t* v0 = sm + kPRingOff + slot * kPStageBytes + 2 * kPHalf;
+                // zero V rows past the piece once its V landed (whole 128-byte
+                // rows, so the swizzle does not matter); PV(g - 2) was issued
+                // (QK(g) was), so this phase of vfull is the one for stage g
+                if (!wait_all(&ctl.vfull[g % kPVStages], (g / kPVStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* v0 = sm + kPVOff + (g % kPVStages) * kPSlotBytes;
                 const int n16 = (kPrefillStageTokens - nvalid) * 16;
                 for (int i = r; i < n16; i += kPSoftmaxThreads) {
                     const int row = nvalid + (i >> 4), c = i & 15;
@@ -382,9 +434,14 @@ __global__ void __launch_bounds__(kPThreads)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.p_ready[g & 1]);
+            // follow the o_ready phases two stages behind, off the critical path
+            if (g >= 2 && !wait_pv(g - 2)) {
+                ok = false;
+                break;
+            }
             if (last) {
-                // ---- epilogue: O / l
-                if (!wait_all(&ctl.o_ready, g & 1)) {
+                // ---- epilogue: O / l, once PV(g) is done
+                if (!wait_pv(g)) {
                     ok = false;
                     break;
                 }
@@ -452,8 +509,10 @@ __global__ void __launch_bounds__(kPThreads)
 
     if (flags[0] && threadIdx.x == 0) {
         // Aborted: wait (bounded) for the copies already issued, then leave.
-        for (int s = 0; s < kPStages; ++s)
-            if (ctl.issued[s] > 0) mbar_wait(&ctl.full[s], (ctl.issued[s] - 1) & 1, nullptr);
+        for (int s = 0; s < kPKStages; ++s)
+            if (ctl.kissued[s] > 0) mbar_wait(&ctl.kfull[s], (ctl.kissued[s] - 1) & 1, nullptr);
+        for (int s = 0; s < kPVStages; ++s)
+            if (ctl.vissued[s] > 0) mbar_wait(&ctl.vfull[s], (ctl.vissued[s] - 1) & 1, nullptr);
     }
     if (warp == 4) {
         tc_fence_after();
