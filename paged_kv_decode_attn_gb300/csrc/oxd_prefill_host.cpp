@@ -355,7 +355,6 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
         workspace == nullptr)
         return OXD_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(sm_scale)) return OXD_ERR_INVALID_ARGUMENT;
-    if (plan->device < 0) return OXD_ERR_PLAN_MISMATCH;
     const oxd_paged_prefill_desc& d = plan->desc;
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(out, 16) ||
         !aligned(qo_indptr, 4) || !aligned(indptr, 4) || !aligned(indices, 4) ||
@@ -380,6 +379,9 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
             if (overlap(o, i)) return OXD_ERR_ALIAS;
     if (overlap(outs[0], outs[1]) || overlap(outs[0], outs[2]) || overlap(outs[1], outs[2]))
         return OXD_ERR_ALIAS;
+    // operands are checked first (so every rejection above needs no GPU);
+    // a host-only plan is never run
+    if (plan->device < 0) return OXD_ERR_PLAN_MISMATCH;
     int cur = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
     if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;

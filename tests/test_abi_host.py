@@ -429,3 +429,135 @@ def test_rope_append_accepts_in_place_query():
     a["q_out"] = a["q"]
     assert _append_status(desc, a) not in (oxd.OXD_ERR_ALIAS, oxd.OXD_ERR_ALIGNMENT,
                                            oxd.OXD_ERR_INVALID_ARGUMENT)
+
+
+# ------------------------------------------------------------------ causal prefill
+
+def prefill_plan(q_lens, kv_lens, Hq=32, Hkv=8, ps=16, num_sms=152, **kw):
+    kv = np.asarray(kv_lens, np.int64)
+    pages = (kv + ps - 1) // ps
+    indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    last = (kv - (pages - 1) * ps).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    desc = oxd.make_prefill_desc(len(kv), Hq, Hkv, ps, kw.pop("layout", "NHD"),
+                                 kw.pop("num_pages", int(pages.sum())), num_sms=num_sms, **kw)
+    return oxd.oxd_paged_prefill_plan(desc, qo, indptr, last), qo, indptr, last
+
+
+def test_prefill_plan_tiles_and_pieces():
+    # the pages' shape: 32 + 64 query tokens, GQA4 -> 32-token tiles, 8 KV heads
+    plan, *_ = prefill_plan((32, 64), (256, 1024))
+    i = plan.info
+    assert i.tile_tokens == 32 and i.num_tiles == (1 + 2) * 8
+    assert i.total_q_tokens == 96 and i.total_kv_tokens == 1280
+    assert i.causal_pairs == 32 * 224 + 32 * 33 // 2 + 64 * 960 + 64 * 65 // 2
+    assert i.num_units > i.num_tiles and i.launches_per_run == 2  # split to fill the GPU
+    assert i.num_merge_rows == i.num_split_tiles * 32 * 4 or i.num_split_tiles < i.num_tiles
+    one, *_ = prefill_plan((32, 64), (256, 1024), max_splits=1)
+    assert one.info.num_units == 24 and one.info.launches_per_run == 1
+    capped, *_ = prefill_plan((32, 64), (256, 1024), max_splits=2)
+    assert capped.info.max_pieces == 2
+    # enough tiles to fill the GPU: no split
+    big, *_ = prefill_plan((2048,) * 8, [4096] * 8)
+    assert big.info.num_split_tiles == 0 and big.info.num_units == 8 * 64 * 8
+
+
+@pytest.mark.parametrize("G,T", [(1, 128), (2, 64), (3, 42), (8, 16), (32, 4), (128, 1)])
+def test_prefill_tile_tokens_follow_group(G, T):
+    plan, *_ = prefill_plan((T * 2 + 1,), (500,), Hq=G, Hkv=1)
+    assert plan.info.tile_tokens == T and plan.info.num_tiles == 3
+
+
+@pytest.mark.parametrize("name", ["q_above_kv", "qo_start", "qo_decreasing", "no_query",
+                                  "group_too_big", "page_size", "head_dim", "reserved",
+                                  "heads_not_divisible"])
+def test_prefill_bad_plans_are_rejected(name):
+    q_lens, kv_lens, kw = (4, 4), (10, 10), {}
+    expect = oxd.OXD_ERR_INVALID_ARGUMENT
+    if name == "q_above_kv":
+        q_lens = (4, 11)
+    elif name == "no_query":
+        q_lens = (0, 0)
+    elif name == "group_too_big":
+        kw = dict(Hq=256, Hkv=1)
+        expect = oxd.OXD_ERR_UNSUPPORTED
+    elif name == "heads_not_divisible":
+        kw = dict(Hq=12, Hkv=8)
+    kv = np.asarray(kv_lens)
+    pages = (kv + 15) // 16
+    indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    last = (kv - (pages - 1) * 16).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    desc = oxd.make_prefill_desc(2, kw.get("Hq", 8), kw.get("Hkv", 2), 16, "NHD", 4, num_sms=152)
+    if name == "qo_start":
+        qo = qo + 1
+    elif name == "qo_decreasing":
+        qo = np.array([0, 5, 4], np.int32)
+    elif name == "page_size":
+        desc.page_size = 12
+        expect = oxd.OXD_ERR_UNSUPPORTED
+    elif name == "head_dim":
+        desc.head_dim = 64
+        expect = oxd.OXD_ERR_UNSUPPORTED
+    elif name == "reserved":
+        desc.reserved[1] = 3
+    with pytest.raises(oxd.OxdError) as e:
+        oxd.oxd_paged_prefill_plan(desc, qo, indptr, last)
+    assert e.value.status == expect
+
+
+def _prefill_status(plan, B, Hq, Hkv, num_pages, nq, ps=16, **over):
+    step = 1 << 36
+    ops = dict(q=BASE, k=BASE + step, v=BASE + 2 * step, qo=BASE + 3 * step,
+               indptr=BASE + 4 * step, indices=BASE + 5 * step, last=BASE + 6 * step,
+               scale=0.088, out=BASE + 7 * step, lse=BASE + 8 * step, ws=BASE + 9 * step,
+               ws_bytes=plan.workspace_bytes)
+    ops.update(over)
+    return oxd.lib().oxd_paged_prefill_run(
+        oxd._handle(plan), ops["q"], ops["k"], ops["v"], ops["qo"], ops["indptr"],
+        ops["indices"], ops["last"], ctypes.c_float(ops["scale"]), ops["out"], ops["lse"],
+        ops["ws"], ops["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("case,expect", [
+    ("q_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("out_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("ws_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("qo_misaligned", oxd.OXD_ERR_ALIGNMENT),
+    ("ws_small", oxd.OXD_ERR_WORKSPACE_TOO_SMALL),
+    ("out_is_q", oxd.OXD_ERR_ALIAS),
+    ("out_in_vpool", oxd.OXD_ERR_ALIAS),
+    ("lse_in_out", oxd.OXD_ERR_ALIAS),
+    ("ws_over_qo", oxd.OXD_ERR_ALIAS),
+    ("null_indices", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("nan_scale", oxd.OXD_ERR_INVALID_ARGUMENT),
+    ("host_only_plan", oxd.OXD_ERR_PLAN_MISMATCH),
+])
+def test_prefill_run_rejects_bad_operands_before_enqueue(case, expect):
+    plan, qo, *_ = prefill_plan((20, 5), (100, 40), Hq=8, Hkv=2)
+    step = 1 << 36
+    over = {
+        "q_misaligned": dict(q=BASE + 8), "out_misaligned": dict(out=BASE + 7 * step + 4),
+        "ws_misaligned": dict(ws=BASE + 9 * step + 128), "qo_misaligned": dict(qo=BASE + 3 * step + 2),
+        "ws_small": dict(ws_bytes=plan.workspace_bytes - 256), "out_is_q": dict(out=BASE),
+        "out_in_vpool": dict(out=BASE + 2 * step + 4096), "lse_in_out": dict(lse=BASE + 7 * step + 256),
+        "ws_over_qo": dict(ws=BASE + 3 * step - 256), "null_indices": dict(indices=0),
+        "nan_scale": dict(scale=float("nan")), "host_only_plan": {},
+    }[case]
+    assert _prefill_status(plan, 2, 8, 2, 9, 25, **over) == expect
+
+
+def test_prefill_plan_lifetime():
+    plan, *_ = prefill_plan((3,), (3,))
+    h = plan.handle
+    ws = (ctypes.c_uint8 * 512)()
+    # a host-only plan cannot be bound (checked before any CUDA call)
+    assert oxd.lib().oxd_prefill_plan_bind_workspace(h, BASE, plan.workspace_bytes, None) == \
+        oxd.OXD_ERR_PLAN_MISMATCH
+    assert oxd.lib().oxd_prefill_plan_set_timing_events(h, BASE, None) == \
+        oxd.OXD_ERR_INVALID_ARGUMENT
+    plan.destroy()
+    assert oxd.lib().oxd_prefill_plan_destroy(h) == oxd.OXD_ERR_PLAN_MISMATCH
+    info = oxd.PrefillPlanInfo()
+    assert oxd.lib().oxd_prefill_plan_get_info(h, ctypes.byref(info)) == oxd.OXD_ERR_PLAN_MISMATCH
+    del ws
