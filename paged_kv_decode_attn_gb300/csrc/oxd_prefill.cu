@@ -42,6 +42,33 @@
 namespace oxd {
 namespace {
 
+// Packed f32x2 arithmetic and a three-input max (sm_100-class): half the
+// issue slots of the scalar forms for the softmax's bulk work, same results
+// (each lane rounds as the scalar instruction does).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a, b) * (s, s) + (c, c)
+__device__ __forceinline__ void fma2(float a, float b, float s, float c, float& x, float& y) {
+    asm("{\n\t.reg .b64 u, v, w, r;\n\t"
+        "mov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %4};\n\tmov.b64 w, {%5, %5};\n\t"
+        "fma.rn.f32x2 r, u, v, w;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(x), "=f"(y)
+        : "f"(a), "f"(b), "f"(s), "f"(c));
+}
+
+// (x, y) += (a, b)
+__device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
+    asm("{\n\t.reg .b64 u, v, r;\n\t"
+        "mov.b64 u, {%0, %1};\n\tmov.b64 v, {%2, %3};\n\t"
+        "add.rn.f32x2 r, u, v;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(a), "f"(b));
+}
+
 constexpr int kPKStages = 3;     // K ring: a slot is free once its score MMA is done
 constexpr int kPVStages = 2;     // V ring: a slot is free once its PV is done
 constexpr int kPThreads = 224;   // 4 softmax warps, MMA warp, K producer, V producer
@@ -340,7 +367,9 @@ __global__ void __launch_bounds__(kPThreads)
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (whole) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], __uint_as_float(sr[j]));
+                for (int j = 0; j < 64; j += 2)
+                    mq[(j >> 1) & 3] = max3(mq[(j >> 1) & 3], __uint_as_float(sr[j]),
+                                            __uint_as_float(sr[j + 1]));
             } else {
                 const int lim = min(nvalid, pos - base + 1);  // visible columns of this row
 #pragma unroll
@@ -368,9 +397,12 @@ __global__ void __launch_bounds__(kPThreads)
             if (whole) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), sc, -m_use));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), sc, -m_use));
-                    lq[j & 3] += p0 + p1;
+                    float x0, x1;
+                    fma2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1]), sc, -m_use,
+                         x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
                     pk[j] = pack_bf16x2(p0, p1);
                 }
             } else {
