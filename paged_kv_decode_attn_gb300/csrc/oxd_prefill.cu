@@ -275,11 +275,32 @@ __global__ void __launch_bounds__(kPThreads)
         if (lane == 0 && n_st > 0) {
             constexpr uint32_t kIdQK = umma_idesc(128, kPrefillStageTokens, 0);
             constexpr uint32_t kIdPV = umma_idesc(128, kHeadDim, 1);
+            // Two kinds of work, each issued as soon as its inputs are ready:
+            // the PV of stage gp (P written, V landed), checked first since it
+            // frees a V slot and the score buffer of stage gp + 2, and the
+            // score MMA of stage gq (K landed, its score buffer free). An idle
+            // poll naps briefly so the softmax warps keep the issue slots.
             int gq = 0, gp = 0;
             bool ok = true;
             uint64_t idle_since = global_ns();
             while (gp < n_st) {
                 bool progress = false;
+                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1) &&
+                    mbar_try_wait(&ctl.vfull[gp % kPVStages], (gp / kPVStages) & 1)) {
+                    tc_fence_after();
+                    // O += P V: 16 tokens a step = two 8-row groups (1024 B apart);
+                    // the two 64-column halves of V are kPHalf apart
+                    const uint32_t v0 = ring_v(gp % kPVStages);
+                    for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks) {
+                        const uint64_t bd = umma_sdesc(v0 + ks * 2048, kPHalf, 1024);
+                        umma_ts(t_o, t_s(gp & 1) + 8u * ks, bd, kIdPV,
+                                (ks > 0 || gp > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&ctl.vempty[gp % kPVStages]);
+                    umma_commit(&ctl.o_ready[gp & 3]);
+                    ++gp;
+                    progress = true;
+                }
                 if (gq < n_st && gq < gp + 2 &&
                     mbar_try_wait(&ctl.kfull[gq % kPKStages], (gq / kPKStages) & 1)) {
                     tc_fence_after();
@@ -297,26 +318,13 @@ __global__ void __launch_bounds__(kPThreads)
                     ++gq;
                     progress = true;
                 }
-                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1) &&
-                    mbar_try_wait(&ctl.vfull[gp % kPVStages], (gp / kPVStages) & 1)) {
-                    tc_fence_after();
-                    // O += P V: 16 tokens a step = two 8-row groups (1024 B apart);
-                    // the two 64-column halves of V are kPHalf apart
-                    const uint32_t v0 = ring_v(gp % kPVStages);
-                    for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks) {
-                        const uint64_t bd = umma_sdesc(v0 + ks * 2048, kPHalf, 1024);
-                        umma_ts(t_o, t_s(gp & 1) + 8u * ks, bd, kIdPV,
-                                (ks > 0 || gp > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&ctl.vempty[gp % kPVStages]);
-                    umma_commit(&ctl.o_ready[gp & 3]);
-                    ++gp;
-                    progress = true;
-                }
                 if (progress) {
                     idle_since = global_ns();
-                } else if (flags[0] ||
-                           global_ns() - idle_since > static_cast<uint64_t>(kWaitTimeoutNs)) {
+                } else {
+                    __nanosleep(32);
+                }
+                if (!progress && (flags[0] ||
+                           global_ns() - idle_since > static_cast<uint64_t>(kWaitTimeoutNs))) {
                     ok = false;
                     break;
                 }
