@@ -82,6 +82,9 @@ def parse_args(argv=None):
                     help="rope_append: time the fused RoPE + paged append on the workload's "
                          "tables instead of the decode step; prefill: time the paged causal "
                          "prefill of --prefill-config")
+    ap.add_argument("--cascade", action="store_true",
+                    help="decode: plan a cascade over the workload's shared prefix (workloads "
+                         "with one: attend each group's prefix once, then the suffixes)")
     ap.add_argument("--prefill-config", default="prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd",
                     choices=W.PREFILL_ORDER)
     ap.add_argument("--max-splits", type=int, default=0,
@@ -347,8 +350,12 @@ def run_oxd(args):
     cfg = shard_config(W.CONFIGS[args.config], rank)
     case = W.make_case(cfg, device=dev, batch=args.batch)
     t = case.tables
+    casc = {}
+    if args.cascade and cfg.shared_prefix_tokens > 0 and cfg.share_group > 1:
+        # the workload declares which requests share which leading pages
+        casc = dict(shared_prefix_tokens=cfg.shared_prefix_tokens, share_group=cfg.share_group)
     desc = oxd.make_desc(case.batch, case.num_qo_heads, case.num_kv_heads, case.page_size,
-                         case.layout, t.num_pages)
+                         case.layout, t.num_pages, **casc)
     tp0 = time.perf_counter()
     plan = oxd.oxd_paged_decode_plan(desc, t.indptr, t.last_page_len, dev.index)
     plan_us = (time.perf_counter() - tp0) * 1e6
@@ -511,7 +518,7 @@ def run_oxd(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_block(cfg, case),
+            "config": dict(config_block(cfg, case), cascade=bool(casc)),
             "us_per_step": ms * 1e3,
             "us_per_step_p10_p50_p90": [srt[len(srt) // 10] * 1e3, srt[len(srt) // 2] * 1e3,
                                         srt[(9 * len(srt)) // 10] * 1e3],

@@ -97,7 +97,19 @@ typedef struct {
     int32_t tensor_path;    /* groups of 17..32 query heads: 0 = tcgen05 (TMEM accumulators,
                                one CTA per piece), 1 = mma.sync (pairs of 16-row CTAs);
                                other groups ignore it */
-    int32_t reserved[2];    /* must be zero */
+    /* Cascade ("Attention state and cascade"; "Paged KV ownership difference":
+     * decode may read shared pages): 0, 0 = off. Otherwise requests
+     * [g*share_group, (g+1)*share_group) share the pages of their first
+     * shared_prefix_tokens cached tokens (the caller guarantees that their first
+     * shared_prefix_tokens / page_size block-table entries are the same pages).
+     * The plan then attends each group's requests to that prefix once (on the
+     * tensor cores, every query row of the group against each prefix page read
+     * once), decodes the rest of every request, and merges the two states;
+     * results equal the plain decode's within rounding. A request whose L_b is
+     * not above shared_prefix_tokens, or that is alone in its group, is decoded
+     * whole. */
+    int32_t shared_prefix_tokens; /* 0, or a positive multiple of page_size */
+    int32_t share_group;          /* 0 (with no prefix), or >= 2 consecutive requests */
 } oxd_paged_decode_desc;
 
 typedef struct {
@@ -115,6 +127,11 @@ typedef struct {
     int64_t upload_bytes;       /* host->device bytes one run copies (0: work list fits the
                                    kernel parameter buffer) */
     int64_t total_kv_tokens;    /* sum_b L_b */
+    int32_t cascade_units;      /* prefix tiles (group chunk x KV head) of a cascade plan, else 0 */
+    int32_t cascade_requests;   /* requests decoded as prefix + suffix */
+    int64_t shared_kv_tokens;   /* cached tokens read once per group instead of once per request
+                                   (sum over cascade requests of shared_prefix_tokens, minus
+                                   one prefix per tile), 0 without cascade */
 } oxd_plan_info;
 
 /*
@@ -138,8 +155,10 @@ typedef struct {
  * workspace asynchronously by each run, so the plan must outlive every run
  * that used it until that run's stream work has completed.
  * Errors: OXD_ERR_INVALID_ARGUMENT (NULL pointer, non-positive sizes,
- * Hq % Hkv != 0, empty request, last_page_len outside [1, page_size], nonzero
- * reserved fields), OXD_ERR_UNSUPPORTED (head_dim != 128, page_size not in
+ * Hq % Hkv != 0, empty request, last_page_len outside [1, page_size], a
+ * shared_prefix_tokens that is negative or not a multiple of page_size, a
+ * share_group below 2 with a prefix, or a share_group without one),
+ * OXD_ERR_UNSUPPORTED (head_dim != 128, page_size not in
  * {8,16,32,64}, G > 32), OXD_ERR_CUDA (device query failed),
  * OXD_ERR_NO_MEMORY.
  */

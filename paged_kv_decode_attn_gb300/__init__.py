@@ -98,7 +98,8 @@ class Desc(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
         ("force_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-        ("tensor_path", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+        ("tensor_path", ctypes.c_int32), ("shared_prefix_tokens", ctypes.c_int32),
+        ("share_group", ctypes.c_int32),
     ]
 
 
@@ -112,7 +113,8 @@ class PlanInfo(ctypes.Structure):
         ("grid_ctas", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
         ("num_sms", ctypes.c_int32), ("launches_per_run", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64), ("upload_bytes", ctypes.c_int64),
-        ("total_kv_tokens", ctypes.c_int64),
+        ("total_kv_tokens", ctypes.c_int64), ("cascade_units", ctypes.c_int32),
+        ("cascade_requests", ctypes.c_int32), ("shared_kv_tokens", ctypes.c_int64),
     ]
 
     def as_dict(self):
@@ -408,12 +410,15 @@ def oxd_read_device_status(workspace, stream=None) -> int:
 
 
 def make_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages, head_dim=128,
-              max_splits=0, force_splits=0, num_sms=0, tensor_path=0) -> Desc:
-    """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1."""
+              max_splits=0, force_splits=0, num_sms=0, tensor_path=0, shared_prefix_tokens=0,
+              share_group=0) -> Desc:
+    """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1. A nonzero
+    ``shared_prefix_tokens`` with ``share_group`` plans a cascade decode."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return Desc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
-                max_splits, force_splits, num_sms, tensor_path, (ctypes.c_int32 * 2)(0, 0))
+                max_splits, force_splits, num_sms, tensor_path, shared_prefix_tokens,
+                share_group)
 
 
 def oxd_rope_append(desc: RopeAppendDesc, q, k, v, token_request, positions, indptr, indices,

@@ -27,6 +27,7 @@
 #include "../../include/oxd.h"
 #include "oxd_host_util.h"
 #include "oxd_internal.h"
+#include "oxd_prefill.h"
 
 using namespace oxd;
 
@@ -46,7 +47,12 @@ struct oxd_plan_s {
     int64_t total_tokens;
     int grid;
     bool upload;  // work list or split table too long for the parameter buffers
-    size_t off_units, off_cta, off_split, off_part_o, off_part_lse;
+    size_t off_units, off_cta, off_split, off_punits, off_part_o, off_part_lse;
+    // cascade: prefix tiles run by the prefill kernel before the decode kernel
+    int casc_units;
+    int casc_requests;
+    int casc_tile_tokens;
+    int64_t shared_kv;
     size_t meta_bytes, ws_bytes;
     WorkList* work;
     SplitList* splits;
@@ -173,7 +179,10 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
     if (d->max_splits < 0 || d->force_splits < 0 || d->num_sms < 0)
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->tensor_path != 0 && d->tensor_path != 1) return OXD_ERR_INVALID_ARGUMENT;
-    if (d->reserved[0] != 0 || d->reserved[1] != 0)
+    if (d->shared_prefix_tokens < 0 || d->share_group < 0) return OXD_ERR_INVALID_ARGUMENT;
+    if (d->shared_prefix_tokens == 0 ? d->share_group != 0
+                                     : (d->share_group < 2 || d->page_size < 1 ||
+                                        d->shared_prefix_tokens % d->page_size != 0))
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
     if (d->page_size != 8 && d->page_size != 16 && d->page_size != 32 && d->page_size != 64)
@@ -318,6 +327,46 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     }
     if (ctas_per_sm < 1) ctas_per_sm = estimate_ctas_per_sm(vs);
 
+    // ---- cascade: requests of a sharing group with more than the shared
+    // prefix attend the prefix together (one prefill-kernel tile per chunk of
+    // up to 128 / G consecutive such requests and KV head) and decode only
+    // their pages after it.
+    const int H = d.num_kv_heads;
+    const int prefix_pages = d.shared_prefix_tokens / ps;  // 0 without cascade
+    std::vector<int> start_page(B, 0);
+    struct Chunk {
+        int b0, n;  // requests [b0, b0 + n)
+    };
+    std::vector<Chunk> chunks;
+    int casc_requests = 0;
+    if (prefix_pages > 0) {
+        const int T = kPrefillRows / G;
+        for (int g0 = 0; g0 < B; g0 += d.share_group) {
+            const int g1 = std::min(B, g0 + d.share_group);
+            std::vector<int> members;
+            for (int b = g0; b < g1; ++b) {
+                const int64_t L = static_cast<int64_t>(indptr[b + 1] - indptr[b] - 1) * ps + last[b];
+                if (L > d.shared_prefix_tokens) members.push_back(b);
+            }
+            if (members.size() < 2) continue;
+            // consecutive runs of members, cut into chunks of at most T
+            // requests (rows of requests in between are computed and unused)
+            for (size_t i = 0; i < members.size();) {
+                const int b0 = members[i];
+                size_t j = i;
+                while (j + 1 < members.size() && members[j + 1] - b0 < T) ++j;
+                chunks.push_back({b0, members[j] - b0 + 1});
+                i = j + 1;
+            }
+            for (int b : members) start_page[b] = prefix_pages;
+            casc_requests += static_cast<int>(members.size());
+        }
+    }
+    auto stream_tokens = [&](int b) {  // tokens the decode kernel streams for request b
+        const int64_t L = static_cast<int64_t>(indptr[b + 1] - indptr[b] - 1) * ps + last[b];
+        return L - static_cast<int64_t>(start_page[b]) * ps;
+    };
+
     // ---- partition the work
     // Work is the page streams of all (request, KV head) pairs, request-major
     // (CTAs that run at the same time then read neighbouring heads of the
@@ -325,7 +374,6 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     // stream cut into several pieces is "split" and gets one partial-state
     // slot per piece.
     const int pps = std::max(1, vs.stage_tokens / ps);  // pages per pipeline stage
-    const int H = d.num_kv_heads;
     // Groups of more than 16 query heads run every piece on a pair of CTAs,
     // one per 16-row half, side by side (the second read of each page is
     // then served by L2); the partition below is over CTA pairs.
@@ -347,7 +395,9 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         // start-up cost of the pieces still to come), cutting streams at page
         // boundaries. A CTA whose remaining room cannot hold a piece's
         // start-up and half a stage passes the next piece on.
-        const double T0 = static_cast<double>(total_tokens) * H;
+        int64_t streamed = 0;
+        for (int b = 0; b < B; ++b) streamed += stream_tokens(b);
+        const double T0 = static_cast<double>(streamed) * H;
         const double unit_ovh = unit_overhead_tokens(variant);
         const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
         grid = static_cast<int>(std::max<int64_t>(
@@ -364,7 +414,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         for (int b = 0; b < B; ++b) {
             const int P = indptr[b + 1] - indptr[b];
             for (int h = 0; h < H; ++h) {
-                int p = 0;
+                int p = start_page[b];
                 while (p < P) {
                     if (c < grid - 1 && budget - used - unit_ovh < 0.5 * min_tokens) {
                         ++c;
@@ -395,7 +445,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         // stream, 1 = never split): equal pieces, assigned longest first to
         // the least-loaded CTA.
         for (int b = 0; b < B; ++b) {
-            const int P = indptr[b + 1] - indptr[b];
+            const int P0 = start_page[b];
+            const int P = indptr[b + 1] - indptr[b] - P0;  // pages the decode kernel streams
             int n = 1;
             if (d.force_splits > 0) {
                 n = std::min(d.force_splits, P);
@@ -407,8 +458,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             }
             for (int h = 0; h < H; ++h)
                 for (int c = 0; c < n; ++c)
-                    pieces.push_back({b, h, static_cast<int>(static_cast<int64_t>(P) * c / n),
-                                      static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
+                    pieces.push_back({b, h, P0 + static_cast<int>(static_cast<int64_t>(P) * c / n),
+                                      P0 + static_cast<int>(static_cast<int64_t>(P) * (c + 1) / n)});
         }
         grid = static_cast<int>(std::min<int64_t>(resident, static_cast<int64_t>(pieces.size())));
         std::vector<int> order(pieces.size());
@@ -437,24 +488,78 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         pieces.swap(sorted);
     }
     // Slots for split streams (consecutive per stream) and the merge entries.
+    // A cascade plan gives every stream a block of K slots, slot (h*B + b)*K
+    // + i: i = 0 holds the prefix state of a cascade request, its suffix
+    // pieces (or a split plain stream's pieces) follow, so each merge entry
+    // and each prefix tile (requests b0.., stride K) addresses its states
+    // contiguously as the kernels expect.
     const int n_pieces = static_cast<int>(pieces.size());
     std::vector<int> slot(pieces.size(), -1);
     std::vector<int4> split_tab;
-    int n_slots = 0, max_chunks = 1;
+    int n_slots = 0, max_chunks = 1, casc_K = 0;
     {
         std::vector<std::vector<int>> of_stream(static_cast<size_t>(B) * H);
         for (int i = 0; i < n_pieces; ++i)
             of_stream[static_cast<size_t>(pieces[i].b) * H + pieces[i].h].push_back(i);
+        if (!chunks.empty()) {
+            size_t most = 1;
+            for (const auto& v : of_stream) most = std::max(most, v.size());
+            casc_K = static_cast<int>(most) + 1;
+            if (static_cast<int64_t>(B) * H * casc_K * G >= (int64_t{1} << 31))
+                return OXD_ERR_UNSUPPORTED;
+        }
         for (size_t st = 0; st < of_stream.size(); ++st) {
             auto& v = of_stream[st];
             max_chunks = std::max(max_chunks, static_cast<int>(v.size()));
-            if (v.size() < 2) continue;
+            const int b = static_cast<int>(st / H), h = static_cast<int>(st % H);
+            const bool casc = start_page[b] > 0;
+            if (v.size() < 2 && !casc) continue;
             std::sort(v.begin(), v.end(),
                       [&](int a, int x) { return pieces[a].p0 < pieces[x].p0; });
-            const int b = static_cast<int>(st / H), h = static_cast<int>(st % H);
-            split_tab.push_back(make_int4(b * d.num_qo_heads + h * G, n_slots,
-                                          static_cast<int>(v.size()), 0));
-            for (int i : v) slot[i] = n_slots++;
+            if (casc_K > 0) {
+                const int blk = (h * B + b) * casc_K;
+                split_tab.push_back(make_int4(b * d.num_qo_heads + h * G, casc ? blk : blk + 1,
+                                              static_cast<int>(v.size()) + (casc ? 1 : 0), 0));
+                int k = blk + 1;
+                for (int i : v) slot[i] = k++;
+            } else {
+                split_tab.push_back(make_int4(b * d.num_qo_heads + h * G, n_slots,
+                                              static_cast<int>(v.size()), 0));
+                for (int i : v) slot[i] = n_slots++;
+            }
+        }
+        if (casc_K > 0) n_slots = B * H * casc_K;
+    }
+    // Prefix tiles of a cascade plan (the prefill kernel's work units): the
+    // chunk's requests as query "tokens" of q [B][Hq][128], every row seeing
+    // the whole prefix (position prefix - 1 for the first), read from the
+    // block table of the chunk's first request.
+    std::vector<PrefillUnit> punits;
+    int64_t shared_kv = 0;
+    for (const Chunk& c : chunks) {
+        const int64_t L0 =
+            static_cast<int64_t>(indptr[c.b0 + 1] - indptr[c.b0] - 1) * ps + last[c.b0];
+        int members = 0;
+        for (int b = c.b0; b < c.b0 + c.n; ++b) members += start_page[b] > 0 ? 1 : 0;
+        shared_kv += static_cast<int64_t>(members - 1) * d.shared_prefix_tokens;
+        for (int h = 0; h < H; ++h) {
+            PrefillUnit u{};
+            u.idx_begin = indptr[c.b0];
+            u.n_pages = prefix_pages;
+            u.kv_begin = 0;
+            u.kv_valid = d.shared_prefix_tokens;
+            u.q_begin = c.b0;
+            u.n_tok = c.n;
+            u.p0 = d.shared_prefix_tokens - 1;
+            u.hkv = h;
+            u.b = c.b0;
+            u.state = (h * B + c.b0) * casc_K;
+            u.n_pieces = casc_K;
+            u.piece = 0;
+            u.qo_b = 0;
+            u.kv_len = static_cast<int32_t>(L0);
+            u.page_base = indptr[c.b0];
+            punits.push_back(u);
         }
     }
     const int n_split = static_cast<int>(split_tab.size());
@@ -500,14 +605,21 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->ctas_per_sm = ctas_per_sm;
     P->num_sms = num_sms;
     P->grid = grid;
+    // the prefix tiles of a cascade plan live in the workspace, so a
+    // cascade plan's unbound runs upload the whole list
     P->upload = n_units > WorkList::kUnits || grid > WorkList::kCtas ||
-                n_split > SplitList::kEntries;
+                n_split > SplitList::kEntries || !punits.empty();
+    P->casc_units = static_cast<int>(punits.size());
+    P->casc_requests = casc_requests;
+    P->casc_tile_tokens = kPrefillRows / G;
+    P->shared_kv = shared_kv;
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
     P->off_units = sizeof(WsHeader);
     P->off_cta = align_up(P->off_units + 16 * static_cast<size_t>(n_units), 256);
     P->off_split = align_up(P->off_cta + 32 * static_cast<size_t>(grid), 256);
-    P->meta_bytes = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
+    P->off_punits = align_up(P->off_split + 16 * std::max<size_t>(split_tab.size(), 1), 256);
+    P->meta_bytes = align_up(P->off_punits + sizeof(PrefillUnit) * punits.size(), 256);
     P->off_part_o = P->meta_bytes;
     P->off_part_lse =
         align_up(P->off_part_o + static_cast<size_t>(n_slots) * G * kHeadDim * 4, 256);
@@ -554,6 +666,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
                                                               : make_int4(0, 0, 0, 0);
         }
         std::memcpy(m + P->off_split, split_tab.data(), 16 * split_tab.size());
+        if (!punits.empty())
+            std::memcpy(m + P->off_punits, punits.data(), sizeof(PrefillUnit) * punits.size());
         P->stamp = next_stamp();
         std::memcpy(m + P->meta_bytes, &P->stamp, sizeof(P->stamp));
     }
@@ -587,6 +701,10 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.upload_bytes =
         plan->upload ? static_cast<int64_t>(plan->meta_bytes - plan->off_units) : 0;
     r.total_kv_tokens = plan->total_tokens;
+    r.cascade_units = plan->casc_units;
+    r.cascade_requests = plan->casc_requests;
+    r.shared_kv_tokens = plan->shared_kv;
+    if (plan->casc_units > 0) r.launches_per_run = 3;
     *info = r;
     return OXD_OK;
 }
@@ -680,9 +798,21 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
         if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
     }
-    CUtensorMap tk, tv, tq;
+    CUtensorMap tk, tv, tq, tq3;
     if (!encode_pool(&tk, k_pages, d) || !encode_pool(&tv, v_pages, d)) return OXD_ERR_CUDA;
     if (plan->variant == kVariantWide && !encode_q(&tq, q, d)) return OXD_ERR_CUDA;
+    if (plan->casc_units > 0) {
+        // q [B][Hq][128] as (d, head, request) for the prefix tiles: a box is
+        // 64 columns x the G heads of one KV head x up to 128 / G requests
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim),
+                                  static_cast<uint64_t>(d.num_qo_heads),
+                                  static_cast<uint64_t>(d.batch)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
+                                     static_cast<uint64_t>(d.num_qo_heads) * kHeadDim * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(plan->group),
+                                 static_cast<uint32_t>(plan->casc_tile_tokens)};
+        if (!encode_bf16_map(&tq3, q, 3, dims, strides, box)) return OXD_ERR_CUDA;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -736,6 +866,45 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     if (le != cudaSuccess) return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
+    if (plan->casc_units > 0) {
+        // the shared prefixes: every prefix tile writes slot i = 0 of its
+        // requests' streams (the decode kernel writes the others). Launched
+        // early behind the decode kernel, its CTAs fill the SMs the decode
+        // CTAs leave; each waits for the decode grid before it exits, so the
+        // merge, which waits for this grid, sees both kernels' states.
+        PrefillParams pp{};
+        pp.q = p.q;
+        pp.indptr = indptr;
+        pp.indices = indices;
+        pp.last_page_len = last_page_len;
+        pp.qo_indptr = nullptr;  // the query rows are the batch's own
+        pp.units = reinterpret_cast<const PrefillUnit*>(ws + plan->off_punits);
+        pp.ws_stamp = p.ws_stamp;
+        pp.stamp = p.stamp;
+        pp.clear_stamp = nullptr;
+        pp.part_o = p.part_o;
+        pp.part_lse = p.part_lse;
+        pp.n_states = static_cast<int64_t>(plan->n_slots) * plan->group;
+        pp.status = p.status;
+        pp.last_epoch = p.last_epoch;
+        pp.epoch = p.epoch;
+        pp.n_units = plan->casc_units;
+        pp.batch = d.batch;
+        pp.n_q_tokens = d.batch;
+        pp.nnz = plan->nnz;
+        pp.num_qo_heads = d.num_qo_heads;
+        pp.num_kv_heads = d.num_kv_heads;
+        pp.group = plan->group;
+        pp.tile_tokens = plan->casc_tile_tokens;
+        pp.page_size = d.page_size;
+        pp.layout = d.layout;
+        pp.num_pages = d.num_pages;
+        pp.scale_log2 = p.scale_log2;
+        pp.wait_prior = 1;
+        if (launch_prefill(tk, tv, tq3, pp, plan->casc_units, s,
+                           plan->ev_after == nullptr) != cudaSuccess)
+            return OXD_ERR_CUDA;
+    }
     if (plan->n_split > 0) {
         MergeParams mp{};
         mp.v = p.part_o;

@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(kPThreads)
             const int b = u.b;
             const int64_t L = static_cast<int64_t>(p.indptr[b + 1] - p.indptr[b] - 1) * ps +
                               p.last_page_len[b];
-            if (p.qo_indptr[b] != u.qo_b || p.indptr[b] != u.page_base || L != u.kv_len)
+            if ((p.qo_indptr != nullptr && p.qo_indptr[b] != u.qo_b) ||
+                p.indptr[b] != u.page_base || L != u.kv_len)
                 record_status(p.status, p.epoch, kDevicePlanMismatch);
         }
         if (!ok && lane == 0) {
@@ -560,6 +561,9 @@ __global__ void __launch_bounds__(kPThreads)
                      "r"(kPTmemCols)
                      : "memory");
     }
+    // Started early behind another grid: that grid completes before this one
+    // does, so a kernel that waits for this grid also sees the other's writes.
+    if (p.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 cudaError_t ensure_prefill_attribute() {
@@ -603,12 +607,21 @@ cudaError_t prefill_occupancy(int* n) {
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, int grid, cudaStream_t stream) {
-    if (grid < 1) return cudaErrorInvalidConfiguration;
+                           const PrefillParams& p, int grid, cudaStream_t stream, bool early) {
+    if (grid < 1 || (early && !p.wait_prior)) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_prefill_attribute();
     if (e != cudaSuccess) return e;
-    paged_prefill_kernel<<<grid, kPThreads, kPSmemBytes, stream>>>(tk, tv, tq, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tk, tv, tq, p);
 }
 
 }  // namespace oxd

@@ -39,7 +39,7 @@ struct PrefillParams {
     const uint16_t* q;              // bf16 [Nq][Hq][128] (read through the tensor map)
     uint16_t* out;                  // bf16 [Nq][Hq][128]
     float* lse;                     // [Nq][Hq] or nullptr
-    const int32_t* qo_indptr;
+    const int32_t* qo_indptr;       // nullptr: rows are not checked against one (cascade)
     const int32_t* indptr;
     const int32_t* indices;
     const int32_t* last_page_len;
@@ -65,13 +65,18 @@ struct PrefillParams {
     int32_t layout;
     int64_t num_pages;
     float scale_log2;
+    int32_t wait_prior;             // 1: launched early behind another grid, which must
+                                    // complete before this one does (griddepcontrol.wait)
 };
 
 cudaError_t prefill_smem_bytes(int* bytes);
 cudaError_t prefill_occupancy(int* ctas_per_sm);
 // tk, tv: the pool maps (as for decode); tq: q as (d, head, token) with a
 // box of 64 x G x tile_tokens and the 128-byte swizzle.
+// early: launched with programmatic dependent launch behind the previous
+// kernel on the stream (then p.wait_prior must be 1).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, int grid, cudaStream_t stream);
+                           const PrefillParams& p, int grid, cudaStream_t stream,
+                           bool early = false);
 
 }  // namespace oxd

@@ -138,7 +138,10 @@ BAD_DESC = {
     "group_64": dict(num_qo_heads=64, num_kv_heads=1),
     "layout": dict(layout=2),
     "num_pages0": dict(num_pages=0),
-    "reserved": "reserved",
+    "group_without_prefix": dict(share_group=4),
+    "prefix_not_page_multiple": dict(shared_prefix_tokens=24, share_group=4),
+    "prefix_group_of_one": dict(shared_prefix_tokens=32, share_group=1),
+    "negative_prefix": dict(shared_prefix_tokens=-16, share_group=2),
     "negative_splits": dict(max_splits=-1),
     "tensor_path": dict(tensor_path=2),
 }
@@ -148,11 +151,8 @@ BAD_DESC = {
 def test_bad_descriptors_are_rejected(name):
     desc = oxd.make_desc(2, 32, 8, 16, "NHD", 10, num_sms=152)
     mod = BAD_DESC[name]
-    if mod == "reserved":
-        desc.reserved[1] = 1
-    else:
-        for k, v in mod.items():
-            setattr(desc, k, v)
+    for k, v in mod.items():
+        setattr(desc, k, v)
     expect = oxd.OXD_ERR_UNSUPPORTED if name in ("head_dim", "page_size", "group_64") \
         else oxd.OXD_ERR_INVALID_ARGUMENT
     indptr = np.array([0, 5, 10], np.int32)
@@ -561,3 +561,28 @@ def test_prefill_plan_lifetime():
     info = oxd.PrefillPlanInfo()
     assert oxd.lib().oxd_prefill_plan_get_info(h, ctypes.byref(info)) == oxd.OXD_ERR_PLAN_MISMATCH
     del ws
+
+
+# ------------------------------------------------------------------ cascade decode planning
+
+def test_cascade_plan_counts_groups_and_shared_tokens():
+    # 3 groups of 4; group 1 has two requests no longer than the prefix, group
+    # 2 has only one longer request (decoded whole)
+    lengths = [300, 500, 129, 1000,  100, 128, 700, 900,  64, 50, 2000, 120]
+    plan, _, _ = host_plan(lengths, Hq=32, Hkv=8, ps=16, shared_prefix_tokens=128,
+                           share_group=4)
+    i = plan.info
+    assert i.cascade_requests == 4 + 2
+    assert i.cascade_units == (1 + 1) * 8          # one chunk per sharing group, x 8 KV heads
+    assert i.shared_kv_tokens == (4 - 1) * 128 + (2 - 1) * 128
+    assert i.launches_per_run == 3
+    plain, _, _ = host_plan(lengths, Hq=32, Hkv=8, ps=16)
+    assert plain.info.cascade_units == 0 and plain.info.shared_kv_tokens == 0
+
+
+def test_cascade_groups_wider_than_a_tile_are_chunked():
+    # G = 8 -> 16 requests per prefix tile; a group of 40 needs three chunks
+    plan, _, _ = host_plan([5000] * 40, Hq=64, Hkv=8, ps=16, shared_prefix_tokens=1024,
+                           share_group=40)
+    assert plan.info.cascade_units == 3 * 8 and plan.info.cascade_requests == 40
+    assert plan.info.shared_kv_tokens == (40 - 3) * 1024
