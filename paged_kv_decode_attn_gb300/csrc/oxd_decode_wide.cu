@@ -70,7 +70,7 @@ struct WCtl {
     uint64_t empty[kWStages];
     uint64_t s_ready[2];
     uint64_t p_ready[2];
-    uint64_t o_ready;
+    uint64_t o_ready[4];  // PV(k) completes phase k / 4 of o_ready[k % 4]
     uint64_t q_free;
     uint64_t mma_done;
     int issued[kWStages];
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kWThreads)
             mbar_init(&ctl.s_ready[i], 1);
             mbar_init(&ctl.p_ready[i], 1);
         }
-        mbar_init(&ctl.o_ready, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&ctl.o_ready[i], 1);
         mbar_init(&ctl.q_free, 1);
         mbar_init(&ctl.mma_done, 1);
         flags[0] = 0;
@@ -411,16 +411,19 @@ __global__ void __launch_bounds__(kWThreads)
                                 (ks > 0 || !first) ? 1u : 0u);
                     }
                     umma_commit(&ctl.empty[slot]);  // K and V of the slot are consumed
-                    umma_commit(&ctl.o_ready);
+                    umma_commit(&ctl.o_ready[gp & 3]);
                     ++gp;
                     progress = true;
                 }
                 if (progress) {
                     idle_since = global_ns();
-                } else if (flags[0] ||
-                           global_ns() - idle_since > static_cast<uint64_t>(kWaitTimeoutNs)) {
-                    ok = false;
-                    break;
+                } else {
+                    __nanosleep(32);  // leave the issue slots to the other warps
+                    if (flags[0] ||
+                        global_ns() - idle_since > static_cast<uint64_t>(kWaitTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
                 }
             }
             if (!ok) {
@@ -462,13 +465,26 @@ __global__ void __launch_bounds__(kWThreads)
             uint32_t sr[64];
             tmem_ld64(t_s(g & 1), sr);
             const int nvalid = min(kWStageTokens, rec.valid - rec.s * kWStageTokens);
-            float mx = -INFINITY;
+            // A full stage (the common case) takes the maximum over the raw
+            // scores and folds the scale into the exponent's FMA; a stage
+            // past the unit's end is scaled and masked first.
+            const bool whole = nvalid == kWStageTokens && sc > 0.f;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float x = j < nvalid ? __uint_as_float(sr[j]) * sc : -INFINITY;
-                sr[j] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < 64; j += 2)
+                    mq[(j >> 1) & 3] = max3(mq[(j >> 1) & 3], __uint_as_float(sr[j]),
+                                            __uint_as_float(sr[j + 1]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float x = j < nvalid ? __uint_as_float(sr[j]) * sc : -INFINITY;
+                    sr[j] = __float_as_uint(x);
+                    mq[j & 3] = fmaxf(mq[j & 3], x);
+                }
             }
+            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            if (whole) mx *= sc;
             const bool first = rec.s == 0;
             float alpha = 1.f;
             bool rescale = false;
@@ -482,27 +498,42 @@ __global__ void __launch_bounds__(kWThreads)
                 rescale = true;
             }
             uint32_t pk[32];
-            float ls = 0.f;
+            float lq[4] = {0.f, 0.f, 0.f, 0.f};
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_ref);
-                const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_ref);
-                ls += p0 + p1;
-                pk[j] = pack_bf16x2(p0, p1);
+                for (int j = 0; j < 32; ++j) {
+                    float x0, x1;
+                    fma2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1]), sc, -m_ref,
+                         x0, x1);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_ref);
+                    const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_ref);
+                    lq[j & 3] += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
             }
-            l += ls;
+            l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
             tmem_st32(t_s(g & 1), pk);
             tmem_wait_st();
-            // PV of the previous stage is done before O is touched (and this
-            // barrier's phases are followed one by one)
-            if (g > 0) {
-                if (!wait_all(&ctl.o_ready, (g - 1) & 1)) {
+            // P(g) is published without waiting for PV(g - 1): MMAs from one
+            // thread run in issue order, so PV(g) follows it anyway. Only an
+            // O rescale waits for PV(g - 1). Parity waits on the four
+            // o_ready barriers are exact: s_ready(g) means every MMA issued
+            // before QK(g), PV(g - 2) included, has completed, so PV(g - 5)
+            // is done, and PV(g + 3) needs P(g + 3), not yet written.
+            if (__any_sync(0xffffffffu, rescale)) {
+                if (!wait_all(&ctl.o_ready[(g - 1) & 3], ((g - 1) >> 2) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
                 for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
                     uint32_t o[64];
                     tmem_ld64(t_o + c0, o);
@@ -534,8 +565,8 @@ __global__ void __launch_bounds__(kWThreads)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl.p_ready[g & 1]);
             if (last) {
-                // ---- unit epilogue: O / l
-                if (!wait_all(&ctl.o_ready, g & 1)) {
+                // ---- unit epilogue: O / l, once PV(g) is done
+                if (!wait_all(&ctl.o_ready[g & 3], (g >> 2) & 1)) {
                     ok = false;
                     break;
                 }

@@ -117,6 +117,33 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed f32x2 arithmetic and a three-input max (sm_100-class): half the
+// issue slots of the scalar forms for the softmax's bulk work, same results
+// (each lane rounds as the scalar instruction does).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a, b) * (s, s) + (c, c)
+__device__ __forceinline__ void fma2(float a, float b, float s, float c, float& x, float& y) {
+    asm("{\n\t.reg .b64 u, v, w, r;\n\t"
+        "mov.b64 u, {%2, %3};\n\tmov.b64 v, {%4, %4};\n\tmov.b64 w, {%5, %5};\n\t"
+        "fma.rn.f32x2 r, u, v, w;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(x), "=f"(y)
+        : "f"(a), "f"(b), "f"(s), "f"(c));
+}
+
+// (x, y) += (a, b)
+__device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
+    asm("{\n\t.reg .b64 u, v, r;\n\t"
+        "mov.b64 u, {%0, %1};\n\tmov.b64 v, {%2, %3};\n\t"
+        "add.rn.f32x2 r, u, v;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "f"(a), "f"(b));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
