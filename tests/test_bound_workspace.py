@@ -14,6 +14,7 @@ damaged list) is reported the same way, with every access kept inside the
 caller's buffers by the kernels' own bounds checks on each unit.
 """
 import numpy as np
+
 import pytest
 import torch
 
@@ -43,6 +44,9 @@ def _case(kind):
     if kind == "mqa32_pairs":
         return W.custom_case([5000, 64, 1], num_qo_heads=32, num_kv_heads=1, page_size=64,
                              layout="NHD", seed=73, device="cuda"), {}
+    if kind == "mqa32_mma_pairs":  # paired 16-row CTAs: two halves publish each piece
+        return W.custom_case([5000, 64, 1], num_qo_heads=32, num_kv_heads=1, page_size=64,
+                             layout="NHD", seed=73, device="cuda"), {"tensor_path": 1}
     if kind == "forced_splits":
         return W.custom_case([3000, 900, 77], num_qo_heads=32, num_kv_heads=8, page_size=16,
                              layout="NHD", seed=74, device="cuda"), {"force_splits": 5}
@@ -60,8 +64,8 @@ def _bound_run(case, plan, tables, ws, fill=float("nan")):
     return out, lse
 
 
-@pytest.mark.parametrize("kind", ["gqa4_nhd", "mha_hnd", "mqa32_pairs", "forced_splits",
-                                  "long_list"])
+@pytest.mark.parametrize("kind", ["gqa4_nhd", "mha_hnd", "mqa32_pairs", "mqa32_mma_pairs",
+                                  "forced_splits", "long_list"])
 def test_bound_runs_equal_unbound_runs_bitwise(kind):
     case, kw = _case(kind)
     plan = plan_case(case, **kw)
