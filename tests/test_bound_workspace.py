@@ -14,7 +14,6 @@ damaged list) is reported the same way, with every access kept inside the
 caller's buffers by the kernels' own bounds checks on each unit.
 """
 import numpy as np
-
 import pytest
 import torch
 
@@ -44,7 +43,7 @@ def _case(kind):
     if kind == "mqa32_pairs":
         return W.custom_case([5000, 64, 1], num_qo_heads=32, num_kv_heads=1, page_size=64,
                              layout="NHD", seed=73, device="cuda"), {}
-    if kind == "mqa32_mma_pairs":  # paired 16-row CTAs: two halves publish each piece
+    if kind == "mqa32_mma_pairs":  # each piece on two 16-row CTAs, one per row half
         return W.custom_case([5000, 64, 1], num_qo_heads=32, num_kv_heads=1, page_size=64,
                              layout="NHD", seed=73, device="cuda"), {"tensor_path": 1}
     if kind == "forced_splits":
