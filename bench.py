@@ -230,7 +230,9 @@ def source_hash():
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per decode launch from the committed ncu summary, if it still applies."""
+    """DRAM bytes per decode launch from the committed ncu summary, if it still applies.
+    A cascade plan's decode kernel streams fewer pages than the plain plan's: its
+    entries are keyed "<workload>+cascade"."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -526,7 +528,7 @@ def run_oxd(args):
             "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": recorded_traffic(cfg.name),
+                         "traffic": recorded_traffic(cfg.name + ("+cascade" if casc else "")),
                          "kernel": f"paged_decode_kernel variant {info.kernel_variant}",
                          "kernel_us": kern * 1e3, "kernel_timed_launches": Kk,
                          "algorithmic_bytes_per_launch": kv_bytes},
