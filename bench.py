@@ -18,7 +18,8 @@ CUDA events on the launching stream; before every step (outside its events)
 L2 (129 MB) is flushed by writing a 512 MiB buffer and then reading another
 512 MiB buffer (so no dirty flush lines are written back during the step).
 The kernel-only time comes from events the library records around the
-decode launch. ``e2e``
+decode launch. ``warm_l2_us_per_step`` is the median of back-to-back steps
+with no flush in between. ``e2e``
 repeats the step through the public API from pinned host buffers: H2D copies
 of q, the K/V pools and the block tables, the run, and the D2H read of out
 and lse, all inside the events. Clocks are sampled with nvidia-smi during
@@ -71,6 +72,9 @@ def parse_args(argv=None):
                     help="target wall time of the oracle baseline sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0,
                     help="wall-time budget of a whole --impl reference run")
+    ap.add_argument("--raw-samples", default=None, metavar="PATH",
+                    help="write every timed step's and kernel launch's microseconds (and the "
+                         "warm-L2 steps') to PATH as JSON")
     ap.add_argument("--batch", type=int, default=None,
                     help="run only the workload's first N requests (smaller profiling cases)")
     ap.add_argument("--work-list", choices=["bound", "params"], default="bound",
@@ -247,21 +251,23 @@ def recorded_traffic(workload):
 
 # ------------------------------------------------------------------ the oracle baseline
 
-def oracle_time(case, heads=None, reps=1):
+def oracle_time(case, heads=None, reps=1, nthreads=0):
     import oracle
 
     args = (W.bf16_bits(case.q), W.bf16_bits(case.k), W.bf16_bits(case.v), case.tables.indptr,
             case.tables.indices, case.tables.last_page_len)
     kw = dict(num_kv_heads=case.num_kv_heads, page_size=case.page_size,
-              layout=0 if case.layout == "NHD" else 1, sm_scale=case.sm_scale, heads=heads)
+              layout=0 if case.layout == "NHD" else 1, sm_scale=case.sm_scale, heads=heads,
+              nthreads=nthreads)
     t0 = time.perf_counter()
     for _ in range(reps):
         oracle.paged_decode(*args, **kw)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(case_host, target_s):
-    """Oracle (as it stands) on the whole batch, repeated to about target_s seconds."""
+def cpu_baseline(case_host, target_s, single_thread=False):
+    """Oracle (as it stands) on the whole batch, repeated to about target_s seconds;
+    with single_thread, also one pass of the batch on one thread."""
     cores = os.cpu_count() or 1
     t1 = oracle_time(case_host)
     reps = max(1, min(1000, int(math.ceil(target_s / max(t1, 1e-6)))) - 1)
@@ -269,11 +275,16 @@ def cpu_baseline(case_host, target_s):
     reps = max(reps, 1)
     per = t / reps
     gbs = case_host.kv_bytes() / per / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"whole workload batch ({case_host.batch} requests, "
-                      f"{case_host.batch * case_host.num_qo_heads} heads), f64 oracle over "
-                      f"{cores} threads, {reps} repetition(s), {per * 1e3:.1f} ms each",
-            "seconds": t}
+    out = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": f"whole workload batch ({case_host.batch} requests, "
+                     f"{case_host.batch * case_host.num_qo_heads} heads), f64 oracle over "
+                     f"{cores} threads, {reps} repetition(s), {per * 1e3:.1f} ms each",
+           "seconds": t}
+    if single_thread:
+        t_st = oracle_time(case_host, nthreads=1)
+        out["single_thread_value"] = case_host.kv_bytes() / t_st / 1e9
+        out["single_thread_ms_per_step"] = t_st * 1e3
+    return out
 
 
 # ------------------------------------------------------------------ reference arm
@@ -441,6 +452,19 @@ def run_oxd(args):
     if oxd.oxd_read_device_status(ws, stream) != 0:
         raise RuntimeError("device status error during the timed steps")
 
+    # ---- back-to-back steps with a warm L2 (no flush): what a loop over a
+    # working set that L2 holds would see
+    Kw = max(3, min(K, 200))
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Kw)]
+    torch.cuda.synchronize(dev)
+    for a, b in wev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = sorted(a.elapsed_time(b) for a, b in wev)
+
     # ---- the decode kernel alone (roofline): events the library records
     # around its launch, in a separate loop so they never perturb the steps
     Kk = max(3, min(K, 200))
@@ -512,7 +536,8 @@ def run_oxd(args):
         host_case = W.Case(case.batch, case.num_qo_heads, case.num_kv_heads, case.head_dim,
                            case.page_size, case.layout, case.sm_scale, case.tables,
                            host["q"], host["k"], host["v"])
-        cpu = cpu_baseline(host_case, args.cpu_seconds)
+        cpu = cpu_baseline(host_case, args.cpu_seconds,
+                           single_thread=cfg.name in ("mha8_b1_l512_ps16_nhd", DEFAULT_CONFIG))
 
     if rank == 0:
         srt = sorted(step_ms)
@@ -524,6 +549,7 @@ def run_oxd(args):
             "us_per_step": ms * 1e3,
             "us_per_step_p10_p50_p90": [srt[len(srt) // 10] * 1e3, srt[len(srt) // 2] * 1e3,
                                         srt[(9 * len(srt)) // 10] * 1e3],
+            "warm_l2_us_per_step": warm_ms[len(warm_ms) // 2] * 1e3,
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -544,6 +570,11 @@ def run_oxd(args):
             "wall_s_timed_loop": wall,
         }
         print(json.dumps(line), flush=True)
+        if args.raw_samples:
+            with open(args.raw_samples, "w") as f:
+                json.dump({"workload": cfg.name, "step_us": [x * 1e3 for x in step_ms],
+                           "kernel_us": [x * 1e3 for x in kern_ms],
+                           "warm_l2_step_us": [x * 1e3 for x in warm_ms]}, f)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
