@@ -217,16 +217,16 @@ def gpu_id_for_smi(torch, dev):
 
 
 DECODE_SOURCES = ("oxd_decode.cu", "oxd_decode_wide.cu", "oxd_host.cpp", "oxd_host_util.h",
-                  "oxd_internal.h", "oxd_merge.cu", "oxd_merge_row.cuh", "oxd_ptx.cuh",
-                  "oxd_tcgen05.cuh")
+                  "oxd_internal.h", "oxd_ptx.cuh", "oxd_tcgen05.cuh")
 
 
-def source_hash():
+def source_hash(csrc=None):
     """Hash of the sources that decide a decode launch's DRAM traffic: the
-    planner, the decode and merge kernels and their headers (the append and
-    prefill files never run in a decode step)."""
+    planner and the decode kernels with their headers (the merge kernel runs
+    in its own launch; the append and prefill files never run in a decode
+    step)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_kv_decode_attn_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_kv_decode_attn_gb300", "csrc")
     for name in DECODE_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())

@@ -33,6 +33,10 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
     // a row of up to kChunk states costs one round trip to memory.
     constexpr int kChunk = 16;
     const bool one_pass = D <= 128;
+    // lane i's first log-sum (state i) is loaded once, before the values,
+    // and kept for the weights
+    const float s_lane =
+        lane < count ? __ldcg(s + static_cast<size_t>(lane) * s_stride) * s_to_ln : -INFINITY;
     float4 x[kChunk];
     if (one_pass && lane * 4 < D) {
 #pragma unroll
@@ -43,18 +47,19 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
     }
     // maximum over the states (lanes stride over them), then the sum of
     // weights; with at most 32 states lane i keeps state i's weight
-    float M = -INFINITY;
-    for (int i = lane; i < count; i += 32)
+    float M = s_lane;
+    for (int i = lane + 32; i < count; i += 32)
         M = fmaxf(M, __ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float W = 0.f, w_lane = 0.f;
     if (M != -INFINITY) {
-        for (int i = lane; i < count; i += 32) {
-            const float w = expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
-            if (i == lane) w_lane = w;
-            W += w;
+        if (lane < count) {
+            w_lane = expf(s_lane - M);
+            W = w_lane;
         }
+        for (int i = lane + 32; i < count; i += 32)
+            W += expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     }
