@@ -922,6 +922,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         mp.R = plan->group;
         mp.D = kHeadDim;
         mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
+        mp.max_count = plan->max_chunks + (plan->casc_units > 0 ? 1 : 0);
         // With timing events the decode kernel must end before ev_after, so
         // the merge is then launched without the early-start attribute.
         if (launch_split_merge(mp, in_ws ? nullptr : plan->splits, s,
@@ -956,6 +957,7 @@ oxd_status oxd_merge_states(const float* v, const float* s, int32_t N, int32_t S
     mp.R = H;
     mp.D = D;
     mp.s_to_ln = 1.0f;
+    mp.max_count = S;
     if (launch_merge(mp, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return OXD_ERR_CUDA;
     return OXD_OK;

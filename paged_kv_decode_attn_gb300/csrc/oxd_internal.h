@@ -132,6 +132,8 @@ struct MergeParams {
     int32_t R;                    // rows per entry
     int32_t D;
     float s_to_ln;                // factor taking s to natural log (1, or ln 2 for log2)
+    int32_t max_count;            // most states of any entry: rows of more than 16 states
+                                  // (D = 128) are merged by two warps, half a row each
 };
 
 // Fused RoPE + paged append (oxd_append.cu).

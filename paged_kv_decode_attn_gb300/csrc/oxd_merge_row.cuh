@@ -100,4 +100,68 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
     if (lane == 0 && lse_out != nullptr) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
+// The same merge for one half of a 128-column row: columns [64 half, 64 half
+// + 64), two per lane, up to 32 states in one pass (the values of 32 states
+// take the registers that 16 states of a whole row take). Per column the
+// arithmetic, the weights and the state order are those of
+// merge_states_row, so the results are bitwise the same. lse_out is written
+// by the half-0 warp.
+__device__ __forceinline__ void merge_states_half_row(const float* s, size_t s_stride,
+                                                      const float* v, size_t v_stride, int count,
+                                                      float s_to_ln, uint16_t* out_row,
+                                                      float* lse_out, int lane, int half) {
+    constexpr int kChunk = 32;
+    const int c = half * 64 + lane * 2;
+    const float s_lane =
+        lane < count ? __ldcg(s + static_cast<size_t>(lane) * s_stride) * s_to_ln : -INFINITY;
+    float2 x[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+        if (i < count)
+            x[i] = __ldcg(reinterpret_cast<const float2*>(v + static_cast<size_t>(i) * v_stride + c));
+    float M = s_lane;
+    for (int i = lane + 32; i < count; i += 32)
+        M = fmaxf(M, __ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float W = 0.f, w_lane = 0.f;
+    if (M != -INFINITY) {
+        if (lane < count) {
+            w_lane = expf(s_lane - M);
+            W = w_lane;
+        }
+        for (int i = lane + 32; i < count; i += 32)
+            W += expf(__ldcg(s + static_cast<size_t>(i) * s_stride) * s_to_ln - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    float2 acc = make_float2(0.f, 0.f);
+    if (M != -INFINITY) {
+        for (int base = 0; base < count; base += kChunk) {
+            if (base > 0) {
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i)
+                    if (base + i < count)
+                        x[i] = __ldcg(reinterpret_cast<const float2*>(
+                            v + static_cast<size_t>(base + i) * v_stride + c));
+            }
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                if (base + i < count) {
+                    const int j = base + i;
+                    const float w =
+                        count <= 32
+                            ? __shfl_sync(0xffffffffu, w_lane, j & 31)
+                            : expf(__ldcg(s + static_cast<size_t>(j) * s_stride) * s_to_ln - M);
+                    acc.x = fmaf(w, x[i].x, acc.x);
+                    acc.y = fmaf(w, x[i].y, acc.y);
+                }
+            }
+        }
+    }
+    *reinterpret_cast<uint32_t*>(out_row + c) = merge_pack_bf16x2(acc.x * inv, acc.y * inv);
+    if (half == 0 && lane == 0 && lse_out != nullptr) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
 }  // namespace oxd

@@ -467,6 +467,7 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
         mp.R = plan->group;
         mp.D = kHeadDim;
         mp.s_to_ln = 0.693147180559945309f;  // partial LSEs are log2
+        mp.max_count = plan->max_pieces;
         if (launch_split_merge(mp, nullptr, s, plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;
     }

@@ -304,7 +304,7 @@ def test_workspace_too_small_is_refused_on_device_run():
 
 # ------------------------------------------------------------------ state merge
 
-@pytest.mark.parametrize("S", [1, 2, 5, 40])
+@pytest.mark.parametrize("S", [1, 2, 5, 16, 17, 32, 40])
 def test_merge_states_matches_oracle(S):
     N, H, D = 3, 4, 128
     g = torch.Generator(device="cuda").manual_seed(S)
