@@ -132,6 +132,10 @@ typedef struct {
     int64_t shared_kv_tokens;   /* cached tokens read once per group instead of once per request
                                    (sum over cascade requests of shared_prefix_tokens, minus
                                    one prefix per tile), 0 without cascade */
+    int32_t cluster_size;       /* > 0: every (request, KV head) stream is cut into this many
+                                   pieces run by one thread-block cluster, whose first CTA
+                                   merges them (one launch per run); 0: no cluster merge */
+    int32_t reserved;
 } oxd_plan_info;
 
 /*

@@ -115,6 +115,7 @@ class PlanInfo(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64), ("upload_bytes", ctypes.c_int64),
         ("total_kv_tokens", ctypes.c_int64), ("cascade_units", ctypes.c_int32),
         ("cascade_requests", ctypes.c_int32), ("shared_kv_tokens", ctypes.c_int64),
+        ("cluster_size", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
     def as_dict(self):

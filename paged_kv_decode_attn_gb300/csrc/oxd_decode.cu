@@ -40,6 +40,7 @@
 #include <type_traits>
 
 #include "oxd_internal.h"
+#include "oxd_merge_row.cuh"
 #include "oxd_ptx.cuh"
 
 namespace oxd {
@@ -62,6 +63,12 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 
@@ -162,15 +169,22 @@ struct Cfg {
     static constexpr int kQRows = kMma ? (kHiRows ? 16 * kMtiles : 8) : kFmaGroup;
     static constexpr int kQBytes = kQRows * kHeadDim * 2;
     static_assert(kSlices * 16 * kHeadDim * 4 <= kStageBytes, "epilogue scratch fits a stage");
-    // ring | q[kStages] | rec[kStages] | full, empty | issued | flags | red_m | red_l
+    // ring | q[kStages] | rec[kStages] | full, empty, cluster | issued | flags | red_m | red_l
     static constexpr int kQOffset = kStages * kStageBytes;
     static constexpr int kRecOffset = kQOffset + kStages * kQBytes;
     static constexpr int kBarOffset = kRecOffset + kStages * 32;
-    static constexpr int kIssuedOffset = kBarOffset + 2 * kStages * 8;
+    static constexpr int kIssuedOffset = kBarOffset + (2 * kStages + 1) * 8;
     static constexpr int kFlagOffset = (kIssuedOffset + kStages * 4 + 15) / 16 * 16;
     static constexpr int kRedOffset = kFlagOffset + 16;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kRedOffset +
                                       2 * kConsumerWarps * 16 * 4;
+    // Cluster launches add a region for the pieces' final states, filled by
+    // the cluster's CTAs in rank 0: [kMaxClusterCtas][kQRows][128] f32 values,
+    // then [kMaxClusterCtas][kQRows] f32 log2-sums.
+    static constexpr int kClusterOff = (kSmemBytes - 1024 + 15) / 16 * 16;
+    static constexpr int kClusterOBytes = kMaxClusterCtas * kQRows * kHeadDim * 4;
+    static constexpr int kSmemBytesCluster =
+        1024 + kClusterOff + kClusterOBytes + kMaxClusterCtas * kQRows * 4;
     // alignment each region's accesses need (the base is 1024-aligned)
     static_assert(kStageBytes % 1024 == 0, "stages keep the 128-byte swizzle atoms aligned");
     static_assert(kQOffset % 128 == 0 && kQBytes % 128 == 0, "query rows: bulk copy, ldmatrix");
@@ -499,6 +513,17 @@ struct Smem {
     __device__ __forceinline__ uint64_t* empty(int slot) const {
         return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + C::kStages + slot;
     }
+    // cluster merge: the pieces' states (written remotely into rank 0)
+    __device__ __forceinline__ uint32_t cluster_o(int rank, int row) const {
+        return smem_addr(base) + C::kClusterOff + (rank * C::kQRows + row) * kHeadDim * 4;
+    }
+    __device__ __forceinline__ uint32_t cluster_s(int rank, int row) const {
+        return smem_addr(base) + C::kClusterOff + C::kClusterOBytes + (rank * C::kQRows + row) * 4;
+    }
+    // every CTA of the cluster arrives here in rank 0
+    __device__ __forceinline__ uint64_t* cluster_bar() const {
+        return reinterpret_cast<uint64_t*>(base + C::kBarOffset) + 2 * C::kStages;
+    }
     __device__ __forceinline__ int* issued() const {
         return reinterpret_cast<int*>(base + C::kIssuedOffset);
     }
@@ -515,7 +540,65 @@ struct Smem {
 
 // ------------------------------------------------------------------ the kernel
 
-template <class C, class WL>
+// Address in cluster rank 0 of the same shared-memory location.
+__device__ __forceinline__ uint32_t map_rank0(uint32_t local) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(local));
+    return remote;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Rank 0 of a cluster merges row g of the cluster's n pieces from its own
+// shared memory (every lane holds all n log2-sums, so no shuffles): the
+// state merge of the "Single decode split-K" row, with natural-log weights
+// as the merge kernel takes them.
+template <class C>
+__device__ __forceinline__ void cluster_merge_row(const Smem<C>& sm, int g, int n, int lane,
+                                                  uint16_t* out_row, float* lse_out) {
+    float sv[kMaxClusterCtas];
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxClusterCtas; ++i) {
+        sv[i] = i < n ? lds_f32(sm.cluster_s(i, g)) * kLn2 : -INFINITY;
+        M = fmaxf(M, sv[i]);
+    }
+    float W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kMaxClusterCtas; ++i) {
+            if (i < n) {
+                const float w = expf(sv[i] - M);
+                W += w;
+                const uint4 x = lds128(sm.cluster_o(i, g) + lane * 16);
+                acc.x = fmaf(w, __uint_as_float(x.x), acc.x);
+                acc.y = fmaf(w, __uint_as_float(x.y), acc.y);
+                acc.z = fmaf(w, __uint_as_float(x.z), acc.z);
+                acc.w = fmaf(w, __uint_as_float(x.w), acc.w);
+            }
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(out_row + lane * 4) = packed;
+    if (lane == 0 && lse_out != nullptr) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+// kCluster: launched as clusters of p.cluster_c CTAs that merge their
+// pieces in rank 0 (a separate instantiation, so the merge code does not
+// weigh on the registers of the kernels launched without clusters).
+template <class C, class WL, bool kCluster>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                                             const DecodeParams& p, const WL& work) {
     extern __shared__ uint8_t smem_raw[];
@@ -546,6 +629,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
             mbar_init(sm.empty(s), C::kConsumerWarps);
             sm.issued()[s] = 0;
         }
+        if constexpr (kCluster) mbar_init(sm.cluster_bar(), static_cast<uint32_t>(p.cluster_c));
         flags[0] = 0;
         fence_mbar_init();
         if (blockIdx.x == 0) {
@@ -562,6 +646,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
     // for this grid to complete before it reads anything.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
+    // A cluster's barrier in rank 0 is initialised before any CTA can arrive.
+    if constexpr (kCluster) cluster_sync_all();
 
     using Consumer = typename std::conditional<C::kMma, MmaConsumer<C>, FmaConsumer<C>>::type;
 
@@ -765,6 +851,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         // always take the same path through it: each stage's wait result is
         // AND-reduced over all of them before anyone acts on it.
         Consumer cs;
+        int own_b = -1, own_hkv = 0, own_slot = -1;  // the CTA's unit (cluster merge)
         const int slice = warp % C::kSlices;
         const int mt = warp / C::kSlices;
         const int ctid = threadIdx.x;  // 0 .. kConsumerThreads-1
@@ -778,7 +865,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
             }
             const StageRec r = *sm.rec(slot);
             if (r.s < 0) break;
-            if (r.s == 0) cs.init(sm.qbuf(slot), r.nrows, mt, lane);
+            if (r.s == 0) {
+                cs.init(sm.qbuf(slot), r.nrows, mt, lane);
+                own_b = r.b;
+                own_hkv = r.hkv;
+                own_slot = r.slot;
+            }
             const int t0 = slice * kSliceTokens;
             const int u0 = r.s * C::kStageTokens + t0;
             if (u0 < r.valid) {
@@ -836,6 +928,15 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
                             packed.y = pack_bf16x2(o.z, o.w);
                             *reinterpret_cast<uint2*>(p.out + row * kHeadDim + d4 * 4) = packed;
                             if (d4 == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
+                        } else if constexpr (kCluster) {
+                            // this piece's state, into rank 0's shared memory
+                            const uint32_t rank = cluster_ctarank();
+                            st_cluster_v4(map_rank0(sm.cluster_o(static_cast<int>(rank), rr) +
+                                                    d4 * 16),
+                                          o);
+                            if (d4 == 0)
+                                st_cluster_f32(map_rank0(sm.cluster_s(static_cast<int>(rank), rr)),
+                                               lse2);
                         } else {
                             // partial states are [slot][G][128]
                             const size_t row =
@@ -854,6 +955,28 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
             flags[0] = 1;
             record_status(p.status, p.epoch, kDeviceWaitTimeout);
         }
+        if constexpr (kCluster) {
+            // ---- cluster merge: this CTA's piece (its partial state is
+            // written: every consumer passed the epilogue's last barrier) is
+            // announced to rank 0, which merges the cluster's pieces.
+            consumer_sync(C::kConsumerThreads);
+            if (ctid == 0) mbar_arrive_remote(sm.cluster_bar(), 0);
+            if (cluster_ctarank() == 0) {
+                const bool got = mbar_wait_cluster(sm.cluster_bar(), 0, 4 * kWaitTimeoutNs);
+                if (consumer_all(C::kConsumerThreads, got)) {
+                    if (own_b >= 0) {
+                        const size_t row0 =
+                            static_cast<size_t>(own_b) * p.num_qo_heads + own_hkv * G;
+                        for (int g = warp; g < G; g += C::kConsumerWarps)
+                            cluster_merge_row(sm, g, p.cluster_c, lane,
+                                              p.out + (row0 + g) * kHeadDim,
+                                              p.lse != nullptr ? p.lse + row0 + g : nullptr);
+                    }
+                } else if (ctid == 0) {
+                    record_status(p.status, p.epoch, kDeviceWaitTimeout);
+                }
+            }
+        }
     }
     __syncthreads();  // every warp has left its loop
 
@@ -865,35 +988,35 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
 }
 
 // The decode kernel, in its two register budgets (Cfg::kRegs168).
-template <class C, class WL>
+template <class C, class WL, bool kCluster>
 __global__ void __launch_bounds__(C::kThreads)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ DecodeParams p,
                         const __grid_constant__ WL work) {
-    decode_body<C, WL>(tmap_k, tmap_v, p, work);
+    decode_body<C, WL, kCluster>(tmap_k, tmap_v, p, work);
 }
 
-template <class C, class WL>
+template <class C, class WL, bool kCluster>
 __global__ void __maxnreg__(168)
     paged_decode_kernel_r168(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v,
                              const __grid_constant__ DecodeParams p,
                              const __grid_constant__ WL work) {
-    decode_body<C, WL>(tmap_k, tmap_v, p, work);
+    decode_body<C, WL, kCluster>(tmap_k, tmap_v, p, work);
 }
 
 template <class C, class WL>
 using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const DecodeParams, const WL);
 
-template <class C, class WL>
+template <class C, class WL, bool kCluster = false>
 KernelFn<C, WL> kernel_of() {
-    if constexpr (C::kRegs168) return paged_decode_kernel_r168<C, WL>;
-    else return paged_decode_kernel<C, WL>;
+    if constexpr (C::kRegs168) return paged_decode_kernel_r168<C, WL, kCluster>;
+    else return paged_decode_kernel<C, WL, kCluster>;
 }
 
 // cudaFuncSetAttribute is per device; remember which devices are set up.
-template <class C, class WL>
+template <class C, class WL, bool kCluster = false>
 cudaError_t ensure_smem_attribute() {
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -901,15 +1024,43 @@ cudaError_t ensure_smem_attribute() {
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
     if (bit != 0 && (done.load(std::memory_order_relaxed) & bit)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel_of<C, WL>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+    e = cudaFuncSetAttribute(kernel_of<C, WL, kCluster>(),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCluster ? C::kSmemBytesCluster : C::kSmemBytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
+}
+
+template <class C, class WL>
+cudaError_t launch_cluster(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                           const WL& w, int grid, cudaStream_t stream) {
+    cudaError_t e = ensure_smem_attribute<C, WL, true>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytesCluster;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster_c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel_of<C, WL, true>(), tk, tv, p, w);
 }
 
 template <class C>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                    const WorkList* w, int grid, cudaStream_t stream) {
+    if (p.cluster_c > 1) {
+        // clusters of p.cluster_c CTAs (CUDA-core variants); grid is a multiple of it
+        if (C::kMma || grid % p.cluster_c != 0 || p.cluster_c > kMaxClusterCtas)
+            return cudaErrorInvalidValue;
+        if (w != nullptr) return launch_cluster<C, WorkList>(tk, tv, p, *w, grid, stream);
+        return launch_cluster<C, NoList>(tk, tv, p, NoList{0}, grid, stream);
+    }
     if (w != nullptr) {
         cudaError_t e = ensure_smem_attribute<C, WorkList>();
         if (e != cudaSuccess) return e;

@@ -50,6 +50,7 @@ struct oxd_plan_s {
     size_t off_units, off_cta, off_split, off_punits, off_part_o, off_part_lse;
     // cascade: prefix tiles run by the prefill kernel before the decode kernel
     int casc_units;
+    int cluster_c;  // > 0: streams cut into this many pieces, merged inside the decode launch
     int casc_requests;
     int casc_tile_tokens;
     int64_t shared_kv;
@@ -389,7 +390,42 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     std::vector<Piece> pieces;
     std::vector<int> cta_of;  // CTA index of each piece, non-decreasing after ordering
     int grid = 0;
-    if (d.force_splits == 0 && d.max_splits == 0) {
+    // Cluster merge (groups of one or two heads, whose pieces' states fit
+    // rank 0's shared memory): when every stream can be cut into C >= 2
+    // pieces (C <= 8, at least a page each) and the whole batch then fits the
+    // resident CTAs, stream k runs on the C CTAs of cluster k, piece r on rank
+    // r; the pieces write their final states into rank 0, which merges them:
+    // no merge launch. Taken when the longest
+    // piece is no longer than a line-partition share plus what the separate
+    // merge costs (about 3 us, some 160 tokens of a CTA's streaming).
+    int cluster_c = 0;
+    if (d.force_splits == 0 && d.max_splits == 0 && prefix_pages == 0 &&
+        (variant == kVariantFmaG1 || variant == kVariantFmaG2)) {
+        int64_t min_pages = INT64_MAX, max_tokens = 0;
+        for (int b = 0; b < B; ++b) {
+            min_pages = std::min<int64_t>(min_pages, indptr[b + 1] - indptr[b]);
+            max_tokens = std::max<int64_t>(max_tokens, stream_tokens(b));
+        }
+        const int64_t n_streams = static_cast<int64_t>(B) * H;
+        const int C = static_cast<int>(std::min<int64_t>(kMaxClusterCtas, min_pages));
+        if (C >= 2 && n_streams * C <= resident) {
+            const double share = static_cast<double>(total_tokens) * H / resident;
+            if ((static_cast<double>(max_tokens) + C - 1) / C <= share + 160.0) cluster_c = C;
+        }
+    }
+    if (cluster_c > 0) {
+        for (int b = 0; b < B; ++b) {
+            const int P = indptr[b + 1] - indptr[b];
+            for (int h = 0; h < H; ++h) {
+                for (int r = 0; r < cluster_c; ++r) {
+                    pieces.push_back({b, h, static_cast<int>(static_cast<int64_t>(P) * r / cluster_c),
+                                      static_cast<int>(static_cast<int64_t>(P) * (r + 1) / cluster_c)});
+                    cta_of.push_back(static_cast<int>(cta_of.size()));
+                }
+            }
+        }
+        grid = static_cast<int>(cta_of.size());
+    } else if (d.force_splits == 0 && d.max_splits == 0) {
         // Balanced line partition: walk the concatenated streams and give each
         // CTA, when it starts, the average of what remains (tokens plus the
         // start-up cost of the pieces still to come), cutting streams at page
@@ -508,7 +544,12 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             if (static_cast<int64_t>(B) * H * casc_K * G >= (int64_t{1} << 31))
                 return OXD_ERR_UNSUPPORTED;
         }
-        for (size_t st = 0; st < of_stream.size(); ++st) {
+        if (cluster_c > 0) {
+            for (int i = 0; i < n_pieces; ++i) slot[i] = i;  // piece r of stream k: k * C + r
+            n_slots = n_pieces;
+            max_chunks = cluster_c;
+        }
+        for (size_t st = 0; st < of_stream.size() && cluster_c == 0; ++st) {
             auto& v = of_stream[st];
             max_chunks = std::max(max_chunks, static_cast<int>(v.size()));
             const int b = static_cast<int>(st / H), h = static_cast<int>(st % H);
@@ -610,6 +651,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->upload = n_units > WorkList::kUnits || grid > WorkList::kCtas ||
                 n_split > SplitList::kEntries || !punits.empty();
     P->casc_units = static_cast<int>(punits.size());
+    P->cluster_c = cluster_c;
     P->casc_requests = casc_requests;
     P->casc_tile_tokens = kPrefillRows / G;
     P->shared_kv = shared_kv;
@@ -704,6 +746,8 @@ oxd_status oxd_plan_get_info(oxd_plan plan, oxd_plan_info* info) {
     r.cascade_units = plan->casc_units;
     r.cascade_requests = plan->casc_requests;
     r.shared_kv_tokens = plan->shared_kv;
+    r.cluster_size = plan->cluster_c;
+    if (plan->cluster_c > 0) r.num_split_requests = plan->n_slots / plan->cluster_c;
     if (plan->casc_units > 0) r.launches_per_run = 3;
     *info = r;
     return OXD_OK;
@@ -855,6 +899,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.layout = d.layout;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
+    p.cluster_c = plan->cluster_c;
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;

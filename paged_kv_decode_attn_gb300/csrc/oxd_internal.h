@@ -12,6 +12,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 32;           // G = Hq / Hkv handled by the decode kernels
 constexpr int kSliceTokens = 16;        // tokens one consumer warp handles per stage
 constexpr long long kWaitTimeoutNs = 1000000000LL;  // bounded waits (1 s)
+constexpr int kMaxClusterCtas = 8;                  // CTAs of a merging cluster (portable size)
 
 // Decode kernel variants (oxd_plan_info.kernel_variant).
 enum Variant : int {
@@ -110,6 +111,10 @@ struct DecodeParams {
     int32_t layout;               // 0 NHD, 1 HND
     int64_t num_pages;
     float scale_log2;             // sm_scale * log2(e)
+    // > 1: launched as clusters of this many CTAs, one stream per cluster,
+    // piece r on rank r (slot = CTA index); rank 0 merges the cluster's
+    // partial states into out/lse. 0: no cluster merge.
+    int32_t cluster_c;
 };
 
 // Merge of R-row states. Entry n: output rows first_row + r, r < R, from

@@ -95,6 +95,33 @@ def test_tiny_batch_uses_one_stage_per_cta_at_least():
     assert info.num_work_items >= info.grid_ctas
 
 
+def test_small_batch_merges_inside_clusters():
+    # 8 streams of 32 pages: each cut into 8 pieces on the 8 CTAs of a cluster,
+    # whose first CTA merges them (no merge launch)
+    plan, _, _ = host_plan([512], Hq=8, Hkv=8)
+    info = plan.info
+    assert info.cluster_size == 8 and info.grid_ctas == 8 * 8
+    assert info.launches_per_run == 1 and info.num_slots == 64
+    assert info.num_split_requests == 8 and info.max_chunks == 8
+    # the shortest stream bounds the cluster size (3 pages: clusters of 3)
+    plan, _, _ = host_plan([40, 300, 129], Hq=4, Hkv=2)
+    assert plan.info.cluster_size == 3 and plan.info.grid_ctas == 3 * 2 * 3
+
+
+@pytest.mark.parametrize("lengths,Hq,Hkv,kw", [
+    ([4096] * 32, 32, 8, {}),                 # many streams: line partition + merge kernel
+    ([32768], 32, 8, {}),                     # few long streams: pieces would be too long
+    ([512, 1, 300], 8, 8, {}),                # a one-page stream: no pieces to spread
+    ([512], 8, 8, {"force_splits": 4}),       # the caller fixed the split
+    ([512], 8, 8, {"max_splits": 2}),
+    ([4000, 4000], 32, 1, {}),                # 32-head groups: other kernels
+    ([512], 32, 8, {}),                       # groups of 4: states do not fit rank 0
+])
+def test_cluster_merge_only_where_it_pays(lengths, Hq, Hkv, kw):
+    plan, _, _ = host_plan(lengths, Hq=Hq, Hkv=Hkv, **kw)
+    assert plan.info.cluster_size == 0
+
+
 @pytest.mark.parametrize("force", [1, 2, 3, 7])
 def test_forced_splits(force):
     lengths = [1, 16, 17, 100, 1000]
