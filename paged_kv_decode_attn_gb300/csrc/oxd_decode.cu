@@ -198,6 +198,13 @@ using CfgFmaG2 = Cfg<1, false, 4, 3, false, 2>;
 using CfgMma8 = Cfg<1, false, 4, 3, true, 0>;
 using CfgMma16 = Cfg<1, true, 4, 3, true, 0>;
 
+// Configuration of a cluster launch. A cluster's pieces are short (a few
+// stages each), so the 8-row tensor-core variant gives up a ring stage to
+// hold the eight pieces' states of its up to 8 rows in rank 0 (about 103 KB
+// a CTA, still two a SM); the CUDA-core variants keep theirs.
+template <class C> struct ClusterCfg { using type = C; };
+template <> struct ClusterCfg<CfgMma8> { using type = Cfg<1, false, 4, 2, true, 0>; };
+
 // What the producer tells the consumers about each stage it fills.
 struct StageRec {
     int b, hkv, valid, n_stages, s, slot, row0, nrows;  // query rows [row0, row0+nrows) of the group
@@ -1055,11 +1062,18 @@ template <class C>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                    const WorkList* w, int grid, cudaStream_t stream) {
     if (p.cluster_c > 1) {
-        // clusters of p.cluster_c CTAs (CUDA-core variants); grid is a multiple of it
-        if (C::kMma || grid % p.cluster_c != 0 || p.cluster_c > kMaxClusterCtas)
-            return cudaErrorInvalidValue;
-        if (w != nullptr) return launch_cluster<C, WorkList>(tk, tv, p, *w, grid, stream);
-        return launch_cluster<C, NoList>(tk, tv, p, NoList{0}, grid, stream);
+        // clusters of p.cluster_c CTAs (CUDA-core and 8-row variants); grid is a
+        // multiple of it
+        if constexpr (C::kMma && C::kHiRows) {
+            return cudaErrorInvalidValue;  // 16-row groups: no cluster merge
+        } else {
+            using CC = typename ClusterCfg<C>::type;
+            static_assert(CC::kSmemBytesCluster <= 113 * 1024, "two cluster CTAs a SM");
+            if (grid % p.cluster_c != 0 || p.cluster_c > kMaxClusterCtas)
+                return cudaErrorInvalidValue;
+            if (w != nullptr) return launch_cluster<CC, WorkList>(tk, tv, p, *w, grid, stream);
+            return launch_cluster<CC, NoList>(tk, tv, p, NoList{0}, grid, stream);
+        }
     }
     if (w != nullptr) {
         cudaError_t e = ensure_smem_attribute<C, WorkList>();

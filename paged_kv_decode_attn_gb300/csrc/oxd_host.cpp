@@ -390,8 +390,8 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     std::vector<Piece> pieces;
     std::vector<int> cta_of;  // CTA index of each piece, non-decreasing after ordering
     int grid = 0;
-    // Cluster merge (groups of one or two heads, whose pieces' states fit
-    // rank 0's shared memory): when every stream can be cut into C >= 2
+    // Cluster merge (groups of up to 8 heads, whose pieces' states fit rank
+    // 0's shared memory): when every stream can be cut into C >= 2
     // pieces (C <= 8, at least a page each) and the whole batch then fits the
     // resident CTAs, stream k runs on the C CTAs of cluster k, piece r on rank
     // r; the pieces write their final states into rank 0, which merges them:
@@ -400,7 +400,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     // merge costs (about 3 us, some 160 tokens of a CTA's streaming).
     int cluster_c = 0;
     if (d.force_splits == 0 && d.max_splits == 0 && prefix_pages == 0 &&
-        (variant == kVariantFmaG1 || variant == kVariantFmaG2)) {
+        (variant == kVariantFmaG1 || variant == kVariantFmaG2 || variant == kVariantMma8)) {
         int64_t min_pages = INT64_MAX, max_tokens = 0;
         for (int b = 0; b < B; ++b) {
             min_pages = std::min<int64_t>(min_pages, indptr[b + 1] - indptr[b]);

@@ -115,7 +115,7 @@ def test_small_batch_merges_inside_clusters():
     ([512], 8, 8, {"force_splits": 4}),       # the caller fixed the split
     ([512], 8, 8, {"max_splits": 2}),
     ([4000, 4000], 32, 1, {}),                # 32-head groups: other kernels
-    ([512], 32, 8, {}),                       # groups of 4: states do not fit rank 0
+    ([512], 96, 8, {}),                       # groups of 12: states do not fit rank 0
 ])
 def test_cluster_merge_only_where_it_pays(lengths, Hq, Hkv, kw):
     plan, _, _ = host_plan(lengths, Hq=Hq, Hkv=Hkv, **kw)

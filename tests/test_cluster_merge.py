@@ -4,7 +4,7 @@ When every (request, KV head) stream of a batch can be cut into C >= 2 pieces
 and the batch then fits the resident CTAs, the plan runs stream k on the C
 CTAs of cluster k and the cluster's first CTA merges the pieces: one launch,
 no merge kernel. These cases check the result against the f64 oracle for
-the kernel variants that take this path (G = 1 and 2), NHD and HND,
+the kernel variants that take this path (G = 1, 2 and 3..8), NHD and HND,
 clusters of 2..8 CTAs, with and without LSE; bitwise equality of bound and
 unbound runs and of repeated runs; a CUDA-graph replay with new inputs; and
 the device status for a bad page index (the merge still ends, no hang).
@@ -33,7 +33,7 @@ def _case(lengths, G, Hkv, layout="NHD", ps=16, seed=1):
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
-@pytest.mark.parametrize("G,Hkv", [(1, 8), (1, 1), (2, 4), (2, 12)])
+@pytest.mark.parametrize("G,Hkv", [(1, 8), (1, 1), (2, 4), (2, 12), (3, 2), (4, 8), (8, 4)])
 def test_cluster_merge_matches_oracle(G, Hkv, layout):
     case = _case([512, 200, 1000], G, Hkv, layout, seed=G)
     ref_out, ref_lse = oracle_ref(case)
@@ -56,7 +56,7 @@ def test_cluster_sizes(lengths, C):
 
 
 def test_cluster_merge_without_lse_and_bound_runs_bitwise():
-    case = _case([512, 400], 2, 8, "HND", seed=11)
+    case = _case([512, 400], 4, 8, "HND", seed=11)
     plan = plan_case(case)
     assert plan.info.cluster_size == 8
     tables = DeviceTables(case)
@@ -76,7 +76,7 @@ def test_cluster_merge_without_lse_and_bound_runs_bitwise():
 
 
 def test_cluster_merge_replays_in_a_cuda_graph():
-    case = _case([512, 300, 96], 1, 8, "NHD", seed=21)
+    case = _case([512, 300, 96], 8, 2, "NHD", seed=21)
     plan = plan_case(case)
     assert plan.info.cluster_size == 6
     tables = DeviceTables(case)
@@ -108,7 +108,7 @@ def test_cluster_merge_replays_in_a_cuda_graph():
 
 
 def test_bad_page_index_in_a_cluster_is_reported():
-    case = _case([512, 256], 1, 8, "NHD", seed=31)
+    case = _case([512, 256], 4, 8, "NHD", seed=31)
     plan = plan_case(case)
     assert plan.info.cluster_size == 8
     tables = DeviceTables(case)
