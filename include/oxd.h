@@ -154,6 +154,13 @@ typedef struct {
  *   plan_out           receives the plan; destroy with oxd_plan_destroy
  *   workspace_bytes_out receives the device workspace size run needs
  *
+ * How the work is cut is the plan's choice (reported by oxd_plan_get_info):
+ * the page streams of all (request, KV head) pairs are laid end to end and
+ * cut into one share per resident CTA, streams cut in two or more being
+ * merged by a second kernel; or, for a small batch of groups of up to 8
+ * heads (every stream at least C >= 2 pages, C <= 8, and B * Hkv * C CTAs
+ * resident at once), each stream is cut into C pieces run by one
+ * thread-block cluster whose first CTA merges them: one launch.
  * A run passes the work list to the kernels in their parameter buffers; a
  * list too long for them is kept page-locked by the plan and copied to the
  * workspace asynchronously by each run, so the plan must outlive every run
