@@ -26,7 +26,10 @@
 //   * after a unit's last stage the consumers merge their states through the
 //     stage's own buffer and write the bf16 output and LSE, or, for a split
 //     request, an F32 partial state that the merge kernel (launched right
-//     behind this one) combines.
+//     behind this one) combines;
+//   * a small batch may instead be launched as thread-block clusters, one
+//     stream per cluster and one piece per CTA: each piece's state goes to
+//     the shared memory of the cluster's first CTA, which merges them.
 // The work list travels in the kernel's parameter buffer when it fits, and
 // the device status word carries the run's epoch, so a run enqueues nothing
 // but its kernels.
