@@ -425,19 +425,47 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             }
         }
         grid = static_cast<int>(cta_of.size());
-    } else if (d.force_splits == 0 && d.max_splits == 0) {
+    }
+    // Whole streams: when every stream can have a CTA of its own and the
+    // longest is no longer than a line-partition share plus what the merge of
+    // split streams would cost (about 160 tokens of a CTA's streaming), each
+    // stream runs whole on its own CTA and nothing needs merging.
+    bool whole_streams = false;
+    if (cluster_c == 0 && d.force_splits == 0 && d.max_splits == 0) {
+        int64_t streamed = 0, live = 0, longest = 0;
+        for (int b = 0; b < B; ++b) {
+            streamed += stream_tokens(b);
+            if (stream_tokens(b) > 0) live += H;
+            longest = std::max<int64_t>(longest, stream_tokens(b));
+        }
+        const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
+        const int64_t line_grid = std::max<int64_t>(
+            1, std::min<int64_t>(resident, std::max<int64_t>(streamed * H / min_tokens, live)));
+        whole_streams = live <= resident &&
+                        static_cast<double>(longest) <=
+                            static_cast<double>(streamed) * H / line_grid + 160.0;
+    }
+    if (cluster_c > 0) {
+    } else if (d.force_splits == 0 && d.max_splits == 0 && !whole_streams) {
         // Balanced line partition: walk the concatenated streams and give each
         // CTA, when it starts, the average of what remains (tokens plus the
         // start-up cost of the pieces still to come), cutting streams at page
         // boundaries. A CTA whose remaining room cannot hold a piece's
         // start-up and half a stage passes the next piece on.
-        int64_t streamed = 0;
-        for (int b = 0; b < B; ++b) streamed += stream_tokens(b);
+        int64_t streamed = 0, live_streams = 0;
+        for (int b = 0; b < B; ++b) {
+            streamed += stream_tokens(b);
+            if (stream_tokens(b) > 0) live_streams += H;
+        }
         const double T0 = static_cast<double>(streamed) * H;
         const double unit_ovh = unit_overhead_tokens(variant);
         const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
+        // At least a stage of tokens a CTA, but at least one CTA a stream while
+        // they last: a stream costs a unit's start-up wherever it runs, so short
+        // streams stacked on few CTAs would queue behind one another.
         grid = static_cast<int>(std::max<int64_t>(
-            1, std::min<int64_t>(resident, static_cast<int64_t>(T0 / min_tokens))));
+            1, std::min<int64_t>(resident, std::max<int64_t>(static_cast<int64_t>(T0 / min_tokens),
+                                                             live_streams))));
         double done = 0.0;                      // tokens assigned so far
         int64_t streams_left = static_cast<int64_t>(B) * H;
         auto budget_for = [&](int c) {
@@ -477,14 +505,17 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         }
         grid = cta_of.empty() ? 1 : cta_of.back() + 1;
     } else {
-        // Fixed splitting (force_splits, or at most max_splits pieces per
+        // Whole streams, or fixed splitting (force_splits, or at most max_splits pieces per
         // stream, 1 = never split): equal pieces, assigned longest first to
         // the least-loaded CTA.
         for (int b = 0; b < B; ++b) {
             const int P0 = start_page[b];
             const int P = indptr[b + 1] - indptr[b] - P0;  // pages the decode kernel streams
+            if (P <= 0) continue;
             int n = 1;
-            if (d.force_splits > 0) {
+            if (whole_streams) {
+                n = 1;
+            } else if (d.force_splits > 0) {
                 n = std::min(d.force_splits, P);
             } else if (d.max_splits > 1) {
                 const double T = static_cast<double>(total_tokens) * H;

@@ -122,6 +122,24 @@ def test_cluster_merge_only_where_it_pays(lengths, Hq, Hkv, kw):
     assert plan.info.cluster_size == 0
 
 
+@pytest.mark.parametrize("lengths,H", [([1], 8), ([1], 32), ([16], 32), ([100] * 4, 32)])
+def test_short_streams_get_a_cta_each_and_need_no_merge(lengths, H):
+    # one-token or one-page contexts: every (request, head) stream on its own
+    # CTA (they used to queue on the few CTAs their token count asked for)
+    plan, _, _ = host_plan(lengths, Hq=H, Hkv=H)
+    info = plan.info
+    assert info.grid_ctas == len(lengths) * H == info.num_work_items
+    assert info.launches_per_run == 1 and info.num_split_requests == 0
+    assert info.cluster_size == 0
+
+
+def test_many_short_streams_share_the_resident_ctas():
+    plan, _, _ = host_plan([40] * 100, Hq=8, Hkv=8)   # 800 streams of 3 pages
+    info = plan.info
+    assert info.grid_ctas == 152 * info.ctas_per_sm and info.num_work_items == 800
+    assert info.launches_per_run == 1
+
+
 @pytest.mark.parametrize("force", [1, 2, 3, 7])
 def test_forced_splits(force):
     lengths = [1, 16, 17, 100, 1000]
