@@ -390,27 +390,51 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     std::vector<Piece> pieces;
     std::vector<int> cta_of;  // CTA index of each piece, non-decreasing after ordering
     int grid = 0;
-    // Cluster merge (groups of up to 8 heads, whose pieces' states fit rank
-    // 0's shared memory): when every stream can be cut into C >= 2
-    // pieces (C <= 8, at least a page each) and the whole batch then fits the
-    // resident CTAs, stream k runs on the C CTAs of cluster k, piece r on rank
-    // r; the pieces write their final states into rank 0, which merges them:
-    // no merge launch. Taken when the longest
-    // piece is no longer than a line-partition share plus what the separate
-    // merge costs (about 3 us, some 160 tokens of a CTA's streaming).
+    // How to cut a batch whose split the planner chooses. Measured on one GPU
+    // (step times of small batches): a stream's pieces cost about a stage of
+    // streaming (~1 us) each when a CTA runs alone, the separate merge about
+    // 2.5 us, merging inside a cluster about 0.3 us.
+    //  * Whole streams: when every stream can have a CTA and the longest is at
+    //    most two stages and within a line-partition share plus what the merge
+    //    would cost (about 160 tokens of a CTA's streaming), each stream runs
+    //    whole on its own CTA: nothing to merge.
+    //  * Cluster merge (groups of up to 8 heads, whose pieces' states fit rank
+    //    0's shared memory): when every stream can be cut into C >= 2 pieces
+    //    (C <= 8, at least a page each, as many as the resident CTAs allow),
+    //    there are at most 64 streams (many small clusters launched slower),
+    //    and a piece is at most four stages (the cluster instance has a
+    //    shorter ring) and within a line share plus 80 tokens, stream k runs on
+    //    the C CTAs of cluster k, piece r on rank r; the pieces write their
+    //    final states into rank 0, which merges them: no merge launch.
+    //  * Otherwise the balanced line partition below, with a merge kernel for
+    //    the streams it cuts.
     int cluster_c = 0;
-    if (d.force_splits == 0 && d.max_splits == 0 && prefix_pages == 0 &&
-        (variant == kVariantFmaG1 || variant == kVariantFmaG2 || variant == kVariantMma8)) {
-        int64_t min_pages = INT64_MAX, max_tokens = 0;
+    bool whole_streams = false;
+    if (d.force_splits == 0 && d.max_splits == 0) {
+        int64_t streamed = 0, live = 0, longest = 0, min_pages = INT64_MAX;
         for (int b = 0; b < B; ++b) {
-            min_pages = std::min<int64_t>(min_pages, indptr[b + 1] - indptr[b]);
-            max_tokens = std::max<int64_t>(max_tokens, stream_tokens(b));
+            const int64_t t = stream_tokens(b);
+            streamed += t;
+            if (t > 0) live += H;
+            longest = std::max<int64_t>(longest, t);
+            min_pages = std::min<int64_t>(min_pages, indptr[b + 1] - indptr[b] - start_page[b]);
         }
+        const int64_t stage_tokens = static_cast<int64_t>(pps) * ps;
+        const int64_t line_grid = std::max<int64_t>(
+            1, std::min<int64_t>(resident, std::max<int64_t>(streamed * H / stage_tokens, live)));
+        const double share = static_cast<double>(streamed) * H / line_grid;
+        whole_streams = live <= resident && longest <= 2 * stage_tokens &&
+                        static_cast<double>(longest) <= share + 160.0;
         const int64_t n_streams = static_cast<int64_t>(B) * H;
-        const int C = static_cast<int>(std::min<int64_t>(kMaxClusterCtas, min_pages));
-        if (C >= 2 && n_streams * C <= resident) {
-            const double share = static_cast<double>(total_tokens) * H / resident;
-            if ((static_cast<double>(max_tokens) + C - 1) / C <= share + 160.0) cluster_c = C;
+        if (!whole_streams && prefix_pages == 0 && n_streams <= 64 &&
+            (variant == kVariantFmaG1 || variant == kVariantFmaG2 || variant == kVariantMma8)) {
+            const int C = static_cast<int>(
+                std::min<int64_t>({kMaxClusterCtas, min_pages, resident / n_streams}));
+            if (C >= 2) {
+                const int64_t piece = (longest + C - 1) / C;
+                if (piece <= 4 * stage_tokens && static_cast<double>(piece) <= share + 80.0)
+                    cluster_c = C;
+            }
         }
     }
     if (cluster_c > 0) {
@@ -425,25 +449,6 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
             }
         }
         grid = static_cast<int>(cta_of.size());
-    }
-    // Whole streams: when every stream can have a CTA of its own and the
-    // longest is no longer than a line-partition share plus what the merge of
-    // split streams would cost (about 160 tokens of a CTA's streaming), each
-    // stream runs whole on its own CTA and nothing needs merging.
-    bool whole_streams = false;
-    if (cluster_c == 0 && d.force_splits == 0 && d.max_splits == 0) {
-        int64_t streamed = 0, live = 0, longest = 0;
-        for (int b = 0; b < B; ++b) {
-            streamed += stream_tokens(b);
-            if (stream_tokens(b) > 0) live += H;
-            longest = std::max<int64_t>(longest, stream_tokens(b));
-        }
-        const int64_t min_tokens = static_cast<int64_t>(pps) * ps;
-        const int64_t line_grid = std::max<int64_t>(
-            1, std::min<int64_t>(resident, std::max<int64_t>(streamed * H / min_tokens, live)));
-        whole_streams = live <= resident &&
-                        static_cast<double>(longest) <=
-                            static_cast<double>(streamed) * H / line_grid + 160.0;
     }
     if (cluster_c > 0) {
     } else if (d.force_splits == 0 && d.max_splits == 0 && !whole_streams) {

@@ -44,8 +44,8 @@ def test_cluster_merge_matches_oracle(G, Hkv, layout):
     assert_parity(out, ref_out, lse, ref_lse, f"cluster G={G} {layout}")
 
 
-@pytest.mark.parametrize("lengths,C", [([33, 100], 3), ([20, 300, 64], 2), ([128] * 3, 8),
-                                       ([16 * 5 + 1] * 2, 6)])
+@pytest.mark.parametrize("lengths,C", [([33, 300], 3), ([20, 250, 64], 2), ([160] * 3, 8),
+                                       ([81, 300], 6)])
 def test_cluster_sizes(lengths, C):
     case = _case(lengths, 1, 4, "NHD", seed=C)
     ref_out, ref_lse = oracle_ref(case)
