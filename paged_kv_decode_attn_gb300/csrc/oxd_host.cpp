@@ -438,6 +438,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         }
     }
     if (cluster_c > 0) {
+        // stream k = b * H + h on CTAs [k C, k C + C), piece r on rank r
         for (int b = 0; b < B; ++b) {
             const int P = indptr[b + 1] - indptr[b];
             for (int h = 0; h < H; ++h) {
@@ -451,6 +452,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
         grid = static_cast<int>(cta_of.size());
     }
     if (cluster_c > 0) {
+        // the cluster pieces are laid out above
     } else if (d.force_splits == 0 && d.max_splits == 0 && !whole_streams) {
         // Balanced line partition: walk the concatenated streams and give each
         // CTA, when it starts, the average of what remains (tokens plus the
