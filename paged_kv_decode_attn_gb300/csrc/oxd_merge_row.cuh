@@ -8,10 +8,11 @@
 //   lse = M + ln sum_i w_i.
 // -inf states weigh nothing; a row whose states are all -inf gets out = 0 and
 // lse = -inf. Each lane owns 4 consecutive columns; the weighted sum visits
-// the states in order, so every caller (the merge kernels and the decode
-// kernel's in-place merge of split streams) gets bitwise the same result.
-// Loads go through L2 (ld.global.cg): the states may have been written by
-// other CTAs of a still-running grid.
+// the states in order. A row of up to 16 states (one pass) is merged with
+// every lane holding all the log-sums; longer rows reduce them across the
+// warp. A given launch always takes the same path for a row, so results are
+// deterministic. Loads go through L2 (ld.global.cg): the states may have been
+// written by other CTAs of a still-running grid.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -33,6 +34,53 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
     // a row of up to kChunk states costs one round trip to memory.
     constexpr int kChunk = 16;
     const bool one_pass = D <= 128;
+    if (one_pass && count <= kChunk) {
+        // Every lane loads all the log-sums (broadcast loads, in the same round
+        // trip as the values) and forms the maximum, the weights and their sum
+        // itself: no shuffles on the way to the output.
+        float sv[kChunk];
+        float4 xv[kChunk];
+        const bool cols = lane * 4 < D;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if (i < count) {
+                sv[i] = __ldcg(s + static_cast<size_t>(i) * s_stride);
+                if (cols)
+                    xv[i] = __ldcg(reinterpret_cast<const float4*>(
+                        v + static_cast<size_t>(i) * v_stride + lane * 4));
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+            if (i < count) M = fmaxf(M, sv[i] * s_to_ln);
+        float W = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                if (i < count) {
+                    const float w = expf(sv[i] * s_to_ln - M);
+                    W += w;
+                    if (cols) {
+                        acc.x = fmaf(w, xv[i].x, acc.x);
+                        acc.y = fmaf(w, xv[i].y, acc.y);
+                        acc.z = fmaf(w, xv[i].z, acc.z);
+                        acc.w = fmaf(w, xv[i].w, acc.w);
+                    }
+                }
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        if (cols) {
+            uint2 packed;
+            packed.x = merge_pack_bf16x2(acc.x * inv, acc.y * inv);
+            packed.y = merge_pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(out_row + lane * 4) = packed;
+        }
+        if (lane == 0 && lse_out != nullptr) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+        return;
+    }
     // lane i's first log-sum (state i) is loaded once, before the values,
     // and kept for the weights
     const float s_lane =
@@ -103,9 +151,9 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
 // The same merge for one half of a 128-column row: columns [64 half, 64 half
 // + 64), two per lane, up to 32 states in one pass (the values of 32 states
 // take the registers that 16 states of a whole row take). Per column the
-// arithmetic, the weights and the state order are those of
-// merge_states_row, so the results are bitwise the same. lse_out is written
-// by the half-0 warp.
+// arithmetic, the weights and the state order are those merge_states_row
+// uses for rows of more than 16 states. lse_out is written by the half-0
+// warp.
 __device__ __forceinline__ void merge_states_half_row(const float* s, size_t s_stride,
                                                       const float* v, size_t v_stride, int count,
                                                       float s_to_ln, uint16_t* out_row,
