@@ -150,16 +150,52 @@ __device__ __forceinline__ void merge_states_row(const float* s, size_t s_stride
 
 // The same merge for one half of a 128-column row: columns [64 half, 64 half
 // + 64), two per lane, up to 32 states in one pass (the values of 32 states
-// take the registers that 16 states of a whole row take). Per column the
-// arithmetic, the weights and the state order are those merge_states_row
-// uses for rows of more than 16 states. lse_out is written by the half-0
-// warp.
+// take the registers that 16 states of a whole row take). A row of up to 32
+// states is merged with every lane holding all the log-sums; longer rows
+// reduce them across the warp, with the arithmetic, weights and state order
+// merge_states_row uses for them. lse_out is written by the half-0 warp.
 __device__ __forceinline__ void merge_states_half_row(const float* s, size_t s_stride,
                                                       const float* v, size_t v_stride, int count,
                                                       float s_to_ln, uint16_t* out_row,
                                                       float* lse_out, int lane, int half) {
     constexpr int kChunk = 32;
     const int c = half * 64 + lane * 2;
+    if (count <= kChunk) {
+        // One pass: every lane loads all the log-sums (broadcast loads, in the
+        // values' round trip) and forms the maximum, the weights and their sum
+        // itself, in state order, as merge_states_row does for up to 16 states.
+        float sv[kChunk];
+        float2 xv[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if (i < count) {
+                sv[i] = __ldcg(s + static_cast<size_t>(i) * s_stride);
+                xv[i] = __ldcg(reinterpret_cast<const float2*>(v + static_cast<size_t>(i) * v_stride + c));
+            }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+            if (i < count) M = fmaxf(M, sv[i] * s_to_ln);
+        float W = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                if (i < count) {
+                    const float w = expf(sv[i] * s_to_ln - M);
+                    W += w;
+                    acc.x = fmaf(w, xv[i].x, acc.x);
+                    acc.y = fmaf(w, xv[i].y, acc.y);
+                }
+            }
+        }
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        *reinterpret_cast<uint32_t*>(out_row + c) = merge_pack_bf16x2(acc.x * inv, acc.y * inv);
+        if (half == 0 && lane == 0 && lse_out != nullptr)
+            *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+        return;
+    }
     const float s_lane =
         lane < count ? __ldcg(s + static_cast<size_t>(lane) * s_stride) * s_to_ln : -INFINITY;
     float2 x[kChunk];
