@@ -631,3 +631,56 @@ def test_cascade_groups_wider_than_a_tile_are_chunked():
                            share_group=40)
     assert plan.info.cascade_units == 3 * 8 and plan.info.cascade_requests == 40
     assert plan.info.shared_kv_tokens == (40 - 3) * 1024
+
+
+# ------------------------------------------------------------------ encoding limits
+# A work unit packs the request index in 19 bits and the KV head in the 12 bits
+# above it (plus one bit for the row half), and page indices are int32: the
+# planner accepts everything up to those limits and refuses the first value past.
+
+def _one_page_each(B):
+    return np.arange(B + 1, dtype=np.int32), np.ones(B, np.int32)
+
+
+def test_largest_batch_is_planned():
+    B = (1 << 19) - 1
+    indptr, last = _one_page_each(B)
+    desc = oxd.make_desc(B, 1, 1, 16, "NHD", B, num_sms=152)
+    plan = oxd.oxd_paged_decode_plan(desc, indptr, last)
+    info = plan.info
+    assert info.total_kv_tokens == B
+    assert info.num_split_requests == 0
+
+
+def test_batch_past_the_unit_encoding_is_refused():
+    B = 1 << 19
+    indptr, last = _one_page_each(B)
+    desc = oxd.make_desc(B, 1, 1, 16, "NHD", B, num_sms=152)
+    with pytest.raises(oxd.OxdError) as e:
+        oxd.oxd_paged_decode_plan(desc, indptr, last)
+    assert e.value.status == oxd.OXD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("hkv,ok", [((1 << 12) - 1, True), (1 << 12, False)])
+def test_kv_head_count_limit(hkv, ok):
+    indptr, last = np.array([0, 2], np.int32), np.array([5], np.int32)
+    desc = oxd.make_desc(1, hkv, hkv, 16, "NHD", 4, num_sms=152)
+    if ok:
+        plan = oxd.oxd_paged_decode_plan(desc, indptr, last)
+        assert plan.info.total_kv_tokens == 21
+    else:
+        with pytest.raises(oxd.OxdError) as e:
+            oxd.oxd_paged_decode_plan(desc, indptr, last)
+        assert e.value.status == oxd.OXD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("num_pages,ok", [((1 << 31) - 1, True), (1 << 31, False)])
+def test_pool_size_limit(num_pages, ok):
+    indptr, last = np.array([0, 3], np.int32), np.array([16], np.int32)
+    desc = oxd.make_desc(1, 8, 8, 16, "NHD", num_pages, num_sms=152)
+    if ok:
+        assert oxd.oxd_paged_decode_plan(desc, indptr, last).info.total_kv_tokens == 48
+    else:
+        with pytest.raises(oxd.OxdError) as e:
+            oxd.oxd_paged_decode_plan(desc, indptr, last)
+        assert e.value.status == oxd.OXD_ERR_UNSUPPORTED
