@@ -376,3 +376,27 @@ def test_full_size_workloads_on_sampled_heads(name):
     ref_out, ref_lse = oracle_ref(case, heads=heads)
     go, gl = gpu_heads(out, lse, heads)
     assert_parity(go, ref_out, gl, ref_lse, name)
+
+
+@pytest.mark.slow
+def test_largest_batch_the_work_units_encode():
+    # 2^19 - 1 requests, the most a work unit's 19-bit request field holds, of
+    # 1..24 tokens each (one to three pages of 8): about 1.05 M pages, 4.3 GB of
+    # K and V. Checked on sampled heads, always including the last requests.
+    B = (1 << 19) - 1
+    lengths = np.random.default_rng(77).integers(1, 25, size=B).tolist()
+    case = W.custom_case(lengths, num_qo_heads=2, num_kv_heads=1, page_size=8, layout="NHD",
+                         seed=77, device="cuda")
+    plan = plan_case(case)
+    assert plan.info.num_work_items == B
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    oxd.oxd_plan_bind_workspace(plan, ws)
+    out, lse, plan, ws = run_decode(case, plan=plan, workspace=ws)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    rng = np.random.default_rng(78)
+    heads = {(int(b), int(h)) for b, h in zip(rng.integers(0, B, 40), rng.integers(0, 2, 40))}
+    heads |= {(0, 0), (B - 1, 0), (B - 1, 1), (B - 2, 1), ((1 << 18), 0)}
+    heads = sorted(heads)
+    ref_out, ref_lse = oracle_ref(case, heads=heads)
+    go, gl = gpu_heads(out, lse, heads)
+    assert_parity(go, ref_out, gl, ref_lse, "largest batch")
