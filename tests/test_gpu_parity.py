@@ -400,3 +400,21 @@ def test_largest_batch_the_work_units_encode():
     ref_out, ref_lse = oracle_ref(case, heads=heads)
     go, gl = gpu_heads(out, lse, heads)
     assert_parity(go, ref_out, gl, ref_lse, "largest batch")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("G", [1, 8, 32])
+def test_one_long_request_split_over_every_cta(G):
+    # One request of 2^21 tokens (32768 pages of 64, 1 GB of K and V) is cut into
+    # one piece a resident CTA (304 states a row), so the merge takes its
+    # multi-pass path for rows of more than 32 states.
+    case = W.custom_case([1 << 21], num_qo_heads=G, num_kv_heads=1, page_size=64, layout="NHD",
+                         seed=80 + G, device="cuda")
+    plan = plan_case(case)
+    assert plan.info.num_split_requests == 1 and plan.info.max_chunks > 32
+    out, lse, plan, ws = run_decode(case, plan=plan)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    heads = [(0, h) for h in (range(G) if G <= 8 else (0, 1, 15, 16, 30, 31))]
+    ref_out, ref_lse = oracle_ref(case, heads=heads)
+    go, gl = gpu_heads(out, lse, heads)
+    assert_parity(go, ref_out, gl, ref_lse, f"one long request G={G}")
