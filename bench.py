@@ -334,7 +334,11 @@ def run_reference(args):
     rng = np.random.default_rng(cfg.seed)
     flat = rng.permutation(n_heads_total)[:n]
     heads = [(int(i // case.num_qo_heads), int(i % case.num_qo_heads)) for i in flat]
-    sample_bytes = sum(int(L[b]) for b, _ in heads) * case.head_dim * 4
+    # The metric counts each KV head's bytes once per step; the G query heads of
+    # a group read the same K and V, so a sampled query head stands for 1/G of
+    # its KV head's bytes.
+    G = case.num_qo_heads // case.num_kv_heads
+    sample_bytes = sum(int(L[b]) for b, _ in heads) * case.head_dim * 4 / G
     for _ in range(args.warmup):
         oracle_time(case, heads=heads)
     times = [oracle_time(case, heads=heads) for _ in range(args.steps)]

@@ -83,3 +83,19 @@ def test_reference_arm_other_ranks_exit_quietly():
         [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
          "--warmup", "1"], capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_counts_each_kv_head_once():
+    # Every query head of a two-request batch sampled: the arm's GB/s must be the
+    # metric's logical KV bytes per step over its time, although the G = 4 query
+    # heads of a group each read their KV head's whole sequence.
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+         "--warmup", "1", "--batch", "2", "--ref-budget-s", "30"],
+        capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["cpu_baseline"]["sample"].startswith("64 of 64 ")
+    kv = d["config"]["kv_bytes_per_step"]
+    assert d["value"] == pytest.approx(kv / (d["ms_per_step"] * 1e-3) / 1e9, rel=1e-9)
