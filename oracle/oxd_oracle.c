@@ -391,19 +391,26 @@ void oracle_rope_f64(int n, int D, const double* x, const int32_t* pos, double t
 }
 
 uint16_t oracle_f64_to_bf16(double x) {
-    /* bfloat16 keeps 8 significant bits: round the f64 to 8 bits, ties to
-     * even (the default rounding mode of nearbyint), then the result is exact
-     * in f32 and its upper 16 bits are the bf16 pattern. */
+    /* bfloat16: a sign bit, 8 exponent bits (bias 127) and 7 fraction bits,
+     * so normal values carry 8 significant bits down to 2^-126 and below that
+     * the numbers are multiples of 2^-133 (the subnormal step). The f64 value
+     * is rounded once, to nearest with ties to even (nearbyint in the default
+     * rounding mode): to 8 significant bits at or above 2^-126, to a multiple
+     * of 2^-133 below it. The rounded value is exact in f32, whose upper 16
+     * bits are then the bf16 pattern; a value that rounds to 2^128 or beyond
+     * is an infinity. */
+    double r;
     if (x == 0.0 || isnan(x) || isinf(x)) {
-        float f = (float)x;
-        uint32_t u;
-        memcpy(&u, &f, 4);
-        return (uint16_t)(u >> 16);
+        r = x;
+    } else if (fabs(x) < ldexp(1.0, -126)) {
+        r = ldexp(nearbyint(ldexp(x, 133)), -133);
+    } else {
+        int e;
+        const double m = frexp(x, &e);           /* x = m * 2^e, 0.5 <= |m| < 1 */
+        r = ldexp(nearbyint(ldexp(m, 8)), e - 8);
     }
-    int e;
-    const double m = frexp(x, &e);             /* x = m * 2^e, 0.5 <= |m| < 1 */
-    const double r = nearbyint(ldexp(m, 8));   /* 8 significant bits */
-    const float f = (float)ldexp(r, e - 8);
+    if (fabs(r) >= ldexp(1.0, 128)) return (uint16_t)(signbit(r) ? 0xFF80u : 0x7F80u);
+    const float f = (float)r;
     uint32_t u;
     memcpy(&u, &f, 4);
     return (uint16_t)(u >> 16);

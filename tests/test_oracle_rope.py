@@ -7,13 +7,19 @@ What pins them, other than the formula itself:
   * invariants of a rotation: each (x_i, x_{i+D/2}) pair keeps its length,
     dot products of a query and a key depend only on the position difference,
     and two rotations compose into one;
-  * the bf16 rounding against torch's float32 -> bfloat16 conversion;
+  * the bf16 rounding against torch's float32 -> bfloat16 conversion, and
+    against bit patterns worked out by hand for f64 inputs that rounding
+    through f32 first would get wrong (1 + 2^-8 + 2^-30 lies above the
+    halfway point between two bf16 neighbours, but its f32 rounding lands
+    exactly on it), for ties, for subnormal results (steps of 2^-133) and
+    for overflow to infinity;
   * the append against a dense logical view of the cache built here with plain
     indexing (no page arithmetic from the oracle), and the write rule (pages
     whose reference count is not one stay untouched);
   * planted mistakes (split-half vs interleaved pairing, sign, frequency
-    exponent, slot arithmetic, the reference-count rule) are each rejected by
-    this battery.
+    exponent, slot arithmetic, the reference-count rule, bf16 rounding through
+    f32, truncated or missing subnormal rounding) are each rejected by this
+    battery.
 """
 import math
 import os
@@ -38,6 +44,44 @@ def _f64(b):
 
 
 # ------------------------------------------------------------------ the pin battery
+
+# f64 value -> bf16 pattern, each worked out by hand. bf16 = sign | 8-bit
+# exponent (bias 127) | 7-bit fraction; the smallest normal is 2^-126 (0x0080),
+# subnormals are k * 2^-133 (pattern k), the largest finite value is
+# (2 - 2^-7) * 2^127 (0x7F7F).
+BF16_GOLDEN = [
+    (1.0, 0x3F80),
+    (1 + 2**-8 + 2**-30, 0x3F81),      # above the 1 | 1 + 2^-7 midpoint: up
+    (-(1 + 2**-8 + 2**-30), 0xBF81),
+    (1 + 2**-8, 0x3F80),               # the midpoint itself: to the even 1.0
+    (1 + 3 * 2**-8, 0x3F82),           # midpoint of 1 + 2^-7, 1 + 2^-6: to even
+    (1 + 3 * 2**-8 - 2**-40, 0x3F81),  # just below that midpoint: down
+    (3.0 * 2**-127, 0x0040 | 0x0080),  # 1.5 * 2^-126 is normal: 0x00C0
+    (2**-133, 0x0001),                 # the smallest subnormal
+    (-(2**-133), 0x8001),
+    (2**-134, 0x0000),                 # half of it: to the even 0
+    (3 * 2**-134, 0x0002),             # 1.5 steps: to the even 2
+    (2**-134 + 2**-150, 0x0001),       # just above half a step: up
+    (127.5 * 2**-133, 0x0080),         # halfway to the smallest normal: to even (128)
+    (126.5 * 2**-133, 0x007E),         # halfway between 126 and 127 steps: to even
+    (5e-324, 0x0000),                  # the smallest f64 subnormal
+    (255 * 2.0**120, 0x7F7F),          # the largest finite bf16
+    ((2 - 2**-8) * 2.0**127, 0x7F80),  # midpoint of the largest and 2^128: to even (inf)
+    ((2 - 2**-8) * 2.0**127 - 2.0**90, 0x7F7F),
+    (1e300, 0x7F80),
+    (-1e300, 0xFF80),
+]
+
+
+def bf16_pins(lib):
+    """The hand-worked rounding cases; returns a list of failures."""
+    bad = []
+    for x, want in BF16_GOLDEN:
+        got = int(oracle.f64_to_bf16(np.array([x]), lib=lib)[0])
+        if got != want:
+            bad.append(f"bf16({x!r}) = {got:#06x}, want {want:#06x}")
+    return bad
+
 
 def rope_pins(lib):
     """Every pin of the embedding; returns a list of failures (empty = pass)."""
@@ -165,6 +209,10 @@ def test_append_pins():
     assert append_pins(None) == []
 
 
+def test_bf16_pins():
+    assert bf16_pins(None) == []
+
+
 def test_bf16_rounding_matches_torch():
     rng = np.random.default_rng(3)
     x = np.concatenate([rng.standard_normal(2000).astype(np.float32),
@@ -181,6 +229,12 @@ ROPE_MUTANTS = {
                            "const double f = pow(theta, -(double)i / (double)D);"),
     "slot_from_page": ("const int slot = p % page_size;", "const int slot = (p + 1) % page_size;"),
     "ignores_refcount": ("else if (refcount[page] != 1)", "else if (refcount[page] < 1)"),
+    # converting to f32 before rounding to bf16 rounds twice
+    "bf16_through_f32": ("const double m = frexp(x, &e);           /* x = m * 2^e, 0.5 <= |m| < 1 */",
+                         "const double m = frexp((double)(float)x, &e);"),
+    "bf16_subnormal_truncated": ("r = ldexp(nearbyint(ldexp(x, 133)), -133);",
+                                 "r = ldexp(trunc(ldexp(x, 133)), -133);"),
+    "bf16_no_subnormal_step": ("} else if (fabs(x) < ldexp(1.0, -126)) {", "} else if (0) {"),
     "pool_past_last_page": (
         "(int64_t)p >= ((int64_t)indptr[b + 1] - indptr[b]) * (int64_t)page_size) {",
         "(int64_t)p > ((int64_t)indptr[b + 1] - indptr[b]) * (int64_t)page_size) {"),
@@ -197,7 +251,7 @@ def test_pins_reject_planted_mistakes(name, tmp_path):
     (tmp_path / "oxd_oracle.h").write_text(open(SRC[:-1] + "h").read())
     lib = oracle.bind(oracle.compile_library(str(mutated), str(tmp_path / f"lib_{name}.so")))
     try:
-        failures = rope_pins(lib) + append_pins(lib)
+        failures = rope_pins(lib) + append_pins(lib) + bf16_pins(lib)
     except Exception as e:  # a mutant may also crash the battery
         failures = [repr(e)]
     assert failures, f"mutant {name} passed every pin"

@@ -4,8 +4,11 @@ Each token's query heads are rotated into q_out and its K (rotated) and V
 rows land in its page slot. The GPU rotates in float with the angle carried
 as a two-float number of turns; the oracle rotates in f64. Both round once
 to bf16, so K and q_out agree bit for bit except where the exact value sits
-next to a
-rounding boundary: every element within one bf16 step, almost all exact.
+next to a rounding boundary. The bound applied to every element: within one
+bf16 step of the oracle, or within the oracle's bf16 step plus 2^-20 of the
+rotated pair's norm, the float arithmetic's own error (about 2.5e-7 of the
+norm) with a margin of four, which matters where a rotated value sits near
+zero; and at least 99 % of the elements bitwise equal.
 V rows are copies and every other pool byte is untouched: both bitwise.
 Tokens aimed at shared pages (reference count not one), past the request's
 pages or at out-of-pool pages write nothing and set the status word; a
