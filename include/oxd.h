@@ -110,6 +110,17 @@ typedef struct {
      * whole. */
     int32_t shared_prefix_tokens; /* 0, or a positive multiple of page_size */
     int32_t share_group;          /* 0 (with no prefix), or >= 2 consecutive requests */
+    int32_t reserved;             /* must be zero */
+    /* How long one pipeline wait inside the kernels may last before the run
+     * gives up ("Providers": typed device-status failures): 0 = about one
+     * second; n > 0 = n nanoseconds. A run whose wait runs out stops its
+     * CTA, records OXD_DEVICE_WAIT_TIMEOUT and returns; before the CTA
+     * leaves it still waits (up to about one second, whatever this limit)
+     * for the copies and tensor-core operations it has already issued.
+     * The outputs of such a run are unspecified; the next run is unaffected.
+     * A limit of a few nanoseconds makes most runs give up (a test of that
+     * path). */
+    int64_t wait_timeout_ns;
 } oxd_paged_decode_desc;
 
 typedef struct {
@@ -281,14 +292,28 @@ oxd_status oxd_plan_bind_workspace(oxd_plan plan, void* workspace, size_t worksp
  * run's epoch, so what an earlier call left is never read as this call's).
  * Calls that can overlap on the GPU (other streams, other threads) race on
  * the array and must be serialised by the caller.
- * The device status word lives in that array, so oxd_read_device_status
- * cannot be used with this entry point.
+ * The device status word lives in that array: read it with
+ * oxd_read_static_workspace_status, not oxd_read_device_status.
  */
 oxd_status oxd_paged_decode_run_static_workspace(oxd_plan plan, const void* q,
                                                  const void* k_pages, const void* v_pages,
                                                  const int32_t* indptr, const int32_t* indices,
                                                  const int32_t* last_page_len, float sm_scale,
                                                  void* out, float* lse, void* stream);
+
+/*
+ * The device status of the last oxd_paged_decode_run_static_workspace call on
+ * the calling thread's current device (the pages have no counterpart; it
+ * completes the allocation-free entry point above, whose status word is in
+ * the library's array). Synchronises `stream`, then reads into *code the
+ * first error that call's kernels recorded (a page index outside the pool,
+ * device tables that differ from the plan's, a wait that ran out), or
+ * OXD_DEVICE_OK. Allocates nothing. Returns OXD_OK when the code is
+ * OXD_DEVICE_OK, OXD_ERR_DEVICE_STATUS otherwise, OXD_ERR_INVALID_ARGUMENT
+ * for a NULL `code`, OXD_ERR_CUDA if a CUDA call failed. Another static-array
+ * call enqueued after the one of interest replaces the status.
+ */
+oxd_status oxd_read_static_workspace_status(void* stream, int32_t* code);
 
 /*
  * Merge attention states ("Attention state and cascade": state merge).
@@ -414,7 +439,8 @@ typedef struct {
                                1: never split; n > 1: at most n pieces per tile */
     int32_t num_sms;        /* 0: plan for the device; > 0: host-only plan for that
                                many SMs (runs refused) */
-    int32_t reserved[2];    /* must be zero */
+    int64_t wait_timeout_ns; /* limit of one pipeline wait, as for decode: 0 = about one
+                                second, n > 0 = n nanoseconds */
 } oxd_paged_prefill_desc;
 
 typedef struct {

@@ -35,8 +35,8 @@ from .build import build
 __all__ = [
     "OXD_OK", "OXD_LAYOUT_NHD", "OXD_LAYOUT_HND", "OxdError", "LibraryNotBuilt", "Desc",
     "PlanInfo", "Plan", "build", "lib", "oxd_paged_decode_plan", "oxd_paged_decode_run",
-    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace",
-    "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
+    "oxd_paged_decode_run_static_workspace", "oxd_read_static_workspace_status",
+    "oxd_plan_bind_workspace", "oxd_merge_states", "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
     "oxd_read_device_status", "oxd_status_string", "oxd_device_status_string", "oxd_version",
     "oxd_rope_append", "RopeAppendDesc", "make_rope_append_desc", "EXPORTED_SYMBOLS",
     "PrefillDesc", "PrefillPlanInfo", "PrefillPlan", "make_prefill_desc",
@@ -70,7 +70,8 @@ EXPORTED_SYMBOLS = (
     "oxd_paged_decode_plan", "oxd_paged_decode_run", "oxd_merge_states", "oxd_plan_get_info",
     "oxd_plan_set_timing_events", "oxd_plan_destroy", "oxd_read_device_status",
     "oxd_status_string", "oxd_device_status_string", "oxd_version",
-    "oxd_paged_decode_run_static_workspace", "oxd_plan_bind_workspace", "oxd_rope_append",
+    "oxd_paged_decode_run_static_workspace", "oxd_read_static_workspace_status",
+    "oxd_plan_bind_workspace", "oxd_rope_append",
     "oxd_paged_prefill_plan", "oxd_paged_prefill_run", "oxd_prefill_plan_bind_workspace",
     "oxd_prefill_plan_get_info", "oxd_prefill_plan_set_timing_events",
     "oxd_prefill_plan_destroy",
@@ -99,7 +100,8 @@ class Desc(ctypes.Structure):
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
         ("force_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("tensor_path", ctypes.c_int32), ("shared_prefix_tokens", ctypes.c_int32),
-        ("share_group", ctypes.c_int32),
+        ("share_group", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("wait_timeout_ns", ctypes.c_int64),
     ]
 
 
@@ -147,7 +149,7 @@ class PrefillDesc(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
         ("page_size", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
-        ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2),
+        ("num_sms", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_int64),
     ]
 
 
@@ -169,12 +171,12 @@ class PrefillPlanInfo(ctypes.Structure):
 
 
 def make_prefill_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages,
-                      head_dim=128, max_splits=0, num_sms=0) -> PrefillDesc:
+                      head_dim=128, max_splits=0, num_sms=0, wait_timeout_ns=0) -> PrefillDesc:
     """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return PrefillDesc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
-                       max_splits, num_sms, (ctypes.c_int32 * 2)(0, 0))
+                       max_splits, num_sms, wait_timeout_ns)
 
 
 def make_rope_append_desc(num_tokens, batch, num_qo_heads, num_kv_heads, page_size, layout,
@@ -217,8 +219,10 @@ def lib():
             L.oxd_prefill_plan_set_timing_events.argtypes = [vp, vp, vp]
             L.oxd_prefill_plan_destroy.argtypes = [vp]
             L.oxd_read_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+            L.oxd_read_static_workspace_status.argtypes = [vp, ctypes.POINTER(i32)]
             for f in ("oxd_paged_decode_plan", "oxd_paged_decode_run",
-                      "oxd_paged_decode_run_static_workspace", "oxd_merge_states",
+                      "oxd_paged_decode_run_static_workspace",
+                      "oxd_read_static_workspace_status", "oxd_merge_states",
                       "oxd_plan_get_info", "oxd_plan_set_timing_events", "oxd_plan_destroy",
                       "oxd_read_device_status", "oxd_plan_bind_workspace", "oxd_rope_append",
                       "oxd_paged_prefill_plan", "oxd_paged_prefill_run",
@@ -374,6 +378,16 @@ def oxd_paged_decode_run_static_workspace(plan, q, k_pages, v_pages, indptr, ind
     _check("oxd_paged_decode_run_static_workspace", st)
 
 
+def oxd_read_static_workspace_status(stream=None) -> int:
+    """Synchronise the stream and return the device status code of the last
+    ``oxd_paged_decode_run_static_workspace`` call on the current device."""
+    code = ctypes.c_int32()
+    st = lib().oxd_read_static_workspace_status(_stream(stream), ctypes.byref(code))
+    if st not in (OXD_OK, OXD_ERR_DEVICE_STATUS):
+        _check("oxd_read_static_workspace_status", st)
+    return code.value
+
+
 def oxd_merge_states(v, s, N, S, H, D, v_out, s_out=None, stream=None) -> None:
     """Enqueue a state merge (see ``oxd_merge_states`` in include/oxd.h)."""
     st = lib().oxd_merge_states(_addr(v), _addr(s), int(N), int(S), int(H), int(D),
@@ -412,14 +426,15 @@ def oxd_read_device_status(workspace, stream=None) -> int:
 
 def make_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages, head_dim=128,
               max_splits=0, force_splits=0, num_sms=0, tensor_path=0, shared_prefix_tokens=0,
-              share_group=0) -> Desc:
+              share_group=0, wait_timeout_ns=0) -> Desc:
     """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1. A nonzero
-    ``shared_prefix_tokens`` with ``share_group`` plans a cascade decode."""
+    ``shared_prefix_tokens`` with ``share_group`` plans a cascade decode;
+    ``wait_timeout_ns`` > 0 shortens the kernels' pipeline-wait limit."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return Desc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
                 max_splits, force_splits, num_sms, tensor_path, shared_prefix_tokens,
-                share_group)
+                share_group, 0, wait_timeout_ns)
 
 
 def oxd_rope_append(desc: RopeAppendDesc, q, k, v, token_request, positions, indptr, indices,

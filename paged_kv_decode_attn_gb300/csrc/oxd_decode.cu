@@ -778,7 +778,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
                 }
                 int okw = 1;
                 if (lane == 0 && g >= C::kStages)
-                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags) ? 1 : 0;
+                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags, p.wait_ns)
+                              ? 1
+                              : 0;
                 if (!__shfl_sync(0xffffffffu, okw, 0)) {
                     ok = false;
                     break;
@@ -842,7 +844,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
             int okw = 1;
             if (lane == 0) {
                 if (g >= C::kStages)
-                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags) ? 1 : 0;
+                    okw = mbar_wait(sm.empty(slot), ((g / C::kStages) + 1) & 1, flags, p.wait_ns)
+                              ? 1
+                              : 0;
                 if (okw) {
                     sm.rec(slot)->s = -1;
                     mbar_arrive(sm.full(slot));
@@ -868,7 +872,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         bool ok = true;
         for (int g = 0;; ++g) {
             const int slot = g % C::kStages;
-            const bool got = mbar_wait(sm.full(slot), (g / C::kStages) & 1, flags);
+            const bool got = mbar_wait(sm.full(slot), (g / C::kStages) & 1, flags, p.wait_ns);
             if (!consumer_all(C::kConsumerThreads, got)) {
                 ok = false;
                 break;
@@ -972,7 +976,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
             consumer_sync(C::kConsumerThreads);
             if (ctid == 0) mbar_arrive_remote(sm.cluster_bar(), 0);
             if (cluster_ctarank() == 0) {
-                const bool got = mbar_wait_cluster(sm.cluster_bar(), 0, 4 * kWaitTimeoutNs);
+                const bool got = mbar_wait_cluster(sm.cluster_bar(), 0, 4 * p.wait_ns);
                 if (consumer_all(C::kConsumerThreads, got)) {
                     if (own_b >= 0) {
                         const size_t row0 =
@@ -989,11 +993,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         }
     }
     __syncthreads();  // every warp has left its loop
+    // No CTA of a cluster leaves before all have passed this point: a piece
+    // stores into rank 0's shared memory and arrives there before it gets
+    // here, so rank 0 (even one whose wait for the pieces gave up) never
+    // exits ahead of a remote store. Every wait before it is bounded, so the
+    // barrier completes.
+    if constexpr (kCluster) cluster_sync_all();
 
     if (flags[0] && threadIdx.x == 0) {
         // Aborted: wait (bounded) for the copies already issued, then leave.
         for (int s = 0; s < C::kStages; ++s)
-            if (sm.issued()[s] > 0) mbar_wait(sm.full(s), (sm.issued()[s] - 1) & 1, nullptr);
+            if (sm.issued()[s] > 0)
+                mbar_wait(sm.full(s), (sm.issued()[s] - 1) & 1, nullptr, kWaitTimeoutNs);
     }
 }
 

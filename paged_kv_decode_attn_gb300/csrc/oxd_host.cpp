@@ -180,6 +180,7 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
     if (d->max_splits < 0 || d->force_splits < 0 || d->num_sms < 0)
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->tensor_path != 0 && d->tensor_path != 1) return OXD_ERR_INVALID_ARGUMENT;
+    if (d->reserved != 0 || d->wait_timeout_ns < 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d->shared_prefix_tokens < 0 || d->share_group < 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d->shared_prefix_tokens == 0 ? d->share_group != 0
                                      : (d->share_group < 2 || d->page_size < 1 ||
@@ -938,6 +939,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
     p.cluster_c = plan->cluster_c;
+    p.wait_ns = d.wait_timeout_ns > 0 ? d.wait_timeout_ns : kWaitTimeoutNs;
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
@@ -984,6 +986,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         pp.num_pages = d.num_pages;
         pp.scale_log2 = p.scale_log2;
         pp.wait_prior = 1;
+        pp.wait_ns = p.wait_ns;
         if (launch_prefill(tk, tv, tq3, pp, plan->casc_units, s,
                            plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;

@@ -115,6 +115,8 @@ struct DecodeParams {
     // piece r on rank r (slot = CTA index); rank 0 merges the cluster's
     // partial states into out/lse. 0: no cluster merge.
     int32_t cluster_c;
+    int32_t pad1;
+    int64_t wait_ns;              // limit of a pipeline wait (> 0)
 };
 
 // Merge of R-row states. Entry n: output rows first_row + r, r < R, from

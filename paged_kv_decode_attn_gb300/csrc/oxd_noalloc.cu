@@ -63,3 +63,14 @@ extern "C" oxd_status oxd_paged_decode_run_static_workspace(
     return oxd_paged_decode_run(plan, q, k_pages, v_pages, indptr, indices, last_page_len,
                                 sm_scale, out, lse, ws, kStaticWorkspaceBytes, stream);
 }
+
+extern "C" oxd_status oxd_read_static_workspace_status(void* stream, int32_t* code) {
+    if (code == nullptr) return OXD_ERR_INVALID_ARGUMENT;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return OXD_ERR_CUDA;
+    void* ws = nullptr;
+    if (static_workspace_address(device, &ws) != cudaSuccess) return OXD_ERR_CUDA;
+    // The status word sits where a caller-provided workspace keeps it, so the
+    // regular reader applies (it synchronises the stream first).
+    return oxd_read_device_status(ws, stream, code);
+}

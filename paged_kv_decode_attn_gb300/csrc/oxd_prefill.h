@@ -67,6 +67,7 @@ struct PrefillParams {
     float scale_log2;
     int32_t wait_prior;             // 1: launched early behind another grid, which must
                                     // complete before this one does (griddepcontrol.wait)
+    int64_t wait_ns;                // limit of a pipeline wait (> 0)
 };
 
 cudaError_t prefill_smem_bytes(int* bytes);

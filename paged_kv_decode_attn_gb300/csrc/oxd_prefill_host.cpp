@@ -72,7 +72,7 @@ oxd_status check_desc(const oxd_paged_prefill_desc& d) {
         return OXD_ERR_INVALID_ARGUMENT;
     if (d.num_qo_heads % d.num_kv_heads != 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d.layout != OXD_LAYOUT_NHD && d.layout != OXD_LAYOUT_HND) return OXD_ERR_INVALID_ARGUMENT;
-    if (d.reserved[0] != 0 || d.reserved[1] != 0) return OXD_ERR_INVALID_ARGUMENT;
+    if (d.wait_timeout_ns < 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d.head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
     if (d.page_size != 8 && d.page_size != 16 && d.page_size != 32 && d.page_size != 64)
         return OXD_ERR_UNSUPPORTED;
@@ -444,6 +444,7 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
     p.layout = d.layout;
     p.num_pages = d.num_pages;
     p.scale_log2 = sm_scale * 1.4426950408889634f;  // log2(e)
+    p.wait_ns = d.wait_timeout_ns > 0 ? d.wait_timeout_ns : kWaitTimeoutNs;
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;

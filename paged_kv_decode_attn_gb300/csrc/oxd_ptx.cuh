@@ -103,16 +103,45 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// Non-blocking test of the phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Limits below this are polled with test_wait: try_wait may suspend the
+// thread for a hardware-chosen time, longer than such a limit.
+constexpr long long kPolledWaitNs = 1000000LL;  // 1 ms
+
 // Waits for the phase with `parity` to complete. Gives up (returns false)
-// after kWaitTimeoutNs, or early once *abort is set by another warp.
+// after limit_ns, or early once *abort is set by another warp. Pipeline
+// waits take the run's limit (DecodeParams / PrefillParams wait_ns); the
+// waits for copies and MMAs already in flight before a CTA leaves take
+// kWaitTimeoutNs, whatever the run's limit, so no CTA exits while the
+// asynchronous units still write its shared memory.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
+                                          const volatile int* abort, long long limit_ns) {
+    if (limit_ns < kPolledWaitNs) {
+        const uint64_t t0 = global_ns();
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (abort != nullptr && *abort) return false;
+            if (global_ns() - t0 > static_cast<uint64_t>(limit_ns)) return false;
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort != nullptr && *abort) return false;
-        if (global_ns() - t0 > static_cast<uint64_t>(kWaitTimeoutNs)) return false;
+        if (global_ns() - t0 > static_cast<uint64_t>(limit_ns)) return false;
     }
 }
 

@@ -189,6 +189,8 @@ BAD_DESC = {
     "negative_prefix": dict(shared_prefix_tokens=-16, share_group=2),
     "negative_splits": dict(max_splits=-1),
     "tensor_path": dict(tensor_path=2),
+    "reserved": dict(reserved=1),
+    "negative_wait": dict(wait_timeout_ns=-5),
 }
 
 
@@ -514,7 +516,7 @@ def test_prefill_tile_tokens_follow_group(G, T):
 
 
 @pytest.mark.parametrize("name", ["q_above_kv", "qo_start", "qo_decreasing", "no_query",
-                                  "group_too_big", "page_size", "head_dim", "reserved",
+                                  "group_too_big", "page_size", "head_dim", "negative_wait",
                                   "heads_not_divisible"])
 def test_prefill_bad_plans_are_rejected(name):
     q_lens, kv_lens, kw = (4, 4), (10, 10), {}
@@ -544,8 +546,8 @@ def test_prefill_bad_plans_are_rejected(name):
     elif name == "head_dim":
         desc.head_dim = 64
         expect = oxd.OXD_ERR_UNSUPPORTED
-    elif name == "reserved":
-        desc.reserved[1] = 3
+    elif name == "negative_wait":
+        desc.wait_timeout_ns = -1
     with pytest.raises(oxd.OxdError) as e:
         oxd.oxd_paged_prefill_plan(desc, qo, indptr, last)
     assert e.value.status == expect
