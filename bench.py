@@ -1,17 +1,26 @@
 """Benchmark of batched paged-KV decode attention on GB300.
 
-One step = one ``oxd_paged_decode_run`` (decode kernel and, when a request is
-split, the merge kernel) over one batch of the workload, with the plan built
-and bound to its workspace beforehand (``oxd_plan_bind_workspace`` copies the
-work list into the workspace once, as a server does once per batch and then
-reuses for every layer; ``--work-list params`` runs unbound instead, the list
-riding in the kernels' parameter buffers or copied by every run). Metric: KV-read GB/s (logical KV bytes
-sum_b L_b * Hkv * D * 2 (K, V) * 2 B per step over the step time) and us per
-step.
+One step = one ``oxd_paged_decode_run`` (the decode kernel; the merge kernel
+when a request is split; for a cascade plan also the prefix tiles) over one
+batch of the workload, with the plan built and bound to its workspace
+beforehand (``oxd_plan_bind_workspace`` copies the work list into the
+workspace once, as a server does once per batch and then reuses for every
+layer; ``--work-list params`` runs unbound instead).
 
-Default workload: GQA4, Hq=32, Hkv=8, D=128, B=32, KV lengths uniform in
-[512, 4096], page size 16, NHD, bf16 ~N(0,1), random page order
-(``--config`` picks another of the five workloads in ``workloads``).
+Default workload: GQA8, Hq=64, Hkv=8, D=128, B=256, KV lengths uniform in
+[128, 16384], page size 16, NHD, bf16 ~N(0, 1.5), the first 1024 tokens'
+pages shared read-only by groups of 8 consecutive requests, random page
+order; out and lse. The workload declares its shared prefixes, so the plan
+is the cascade (each group's prefix attended once; ``--plan plain`` for the
+other). ``--config`` picks another workload; the default run also measures
+the other four (and the default workload on the plain plan) in the same
+process under ``workloads``.
+
+Metric: KV-read GB/s and us per step. ``value`` counts the unique KV bytes a
+step must read (each shared prefix page once: sum over physical pages in use
+of page_size * Hkv * D * 2 (K, V) * 2 B) over the mean step time;
+``logical_gbs`` counts every request's pages (sum_b L_b * Hkv * D * 4 B).
+Both bases are the same for workloads without shared pages.
 
 Timing: W untimed warm-up steps, then K steps, each between its own pair of
 CUDA events on the launching stream; before every step (outside its events)
@@ -19,11 +28,14 @@ L2 (129 MB) is flushed by writing a 512 MiB buffer and then reading another
 512 MiB buffer (so no dirty flush lines are written back during the step).
 The kernel-only time comes from events the library records around the
 decode launch. ``warm_l2_us_per_step`` is the median of back-to-back steps
-with no flush in between. ``e2e``
-repeats the step through the public API from pinned host buffers: H2D copies
-of q, the K/V pools and the block tables, the run, and the D2H read of out
-and lse, all inside the events. Clocks are sampled with nvidia-smi during
-the timed loop.
+with no flush in between. ``e2e`` repeats the step through the public API
+from pinned host buffers: H2D copies of q, the K/V pools and the block
+tables, the run, and the D2H read of out and lse, all inside the events.
+Clocks are sampled with nvidia-smi during the timed loop.
+
+``parity`` compares the timed run's out and lse with the f64 CPU oracle on
+every head (|out - ref| <= 1.5e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3);
+``cpu_baseline`` is that oracle's time on the host cores.
 
 ``--impl reference`` times the f64 CPU oracle (the reference arm) on a
 bounded sample of the same workload on the host cores.
@@ -54,7 +66,7 @@ import numpy as np  # noqa: E402
 import workloads as W  # noqa: E402
 
 METRIC = "paged decode attention: KV-read HBM GB/s (% of GB300 peak), µs per batch step"
-DEFAULT_CONFIG = "gqa4_b32_u512to4096_ps16_nhd"
+DEFAULT_CONFIG = "gqa8_b256_u128to16384_prefix1024x8_ps16_nhd"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
 
@@ -86,9 +98,15 @@ def parse_args(argv=None):
                     help="rope_append: time the fused RoPE + paged append on the workload's "
                          "tables instead of the decode step; prefill: time the paged causal "
                          "prefill of --prefill-config")
-    ap.add_argument("--cascade", action="store_true",
-                    help="decode: plan a cascade over the workload's shared prefix (workloads "
-                         "with one: attend each group's prefix once, then the suffixes)")
+    ap.add_argument("--plan", choices=["auto", "plain", "cascade"], default="auto",
+                    help="decode: auto picks the cascade (each sharing group's prefix "
+                         "attended once, then the suffixes) for a workload that declares "
+                         "shared prefixes, else the plain decode")
+    ap.add_argument("--cascade", action="store_true", help="same as --plan cascade")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the every-head comparison with the f64 oracle")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure only --config (not the other workloads)")
     ap.add_argument("--prefill-config", default="prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd",
                     choices=W.PREFILL_ORDER)
     ap.add_argument("--max-splits", type=int, default=0,
@@ -177,7 +195,10 @@ class ClockSampler:
     def mark_end(self):
         self.t1 = time.time()
 
-    def stop(self):
+    def stop(self, steps=None):
+        """Samples taken during the marked window (within 60 ms of it: the
+        sampling period is 50 ms). With `steps`, also how many timed steps
+        each sample strictly inside the window stands for."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.15)
@@ -204,9 +225,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in used for n, v in zip(names, r[3][1:]) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": used[0][2],
-                "reasons": reasons, "samples": len(used),
-                "samples_in_window": len(inside)}
+        strict = [r for r in rows if self.t0 <= r[0] <= self.t1]
+        res = {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": used[0][2],
+               "reasons": reasons, "samples": len(used), "samples_in_window": len(inside),
+               "samples_strictly_inside": len(strict),
+               "window_ms": (self.t1 - self.t0) * 1e3, "sample_period_ms": 50}
+        if steps:
+            res["steps_per_sample"] = steps / max(1, len(strict))
+        return res
 
 
 def gpu_id_for_smi(torch, dev):
@@ -276,11 +302,11 @@ def recorded_traffic(workload):
 
 # ------------------------------------------------------------------ the oracle baseline
 
-def oracle_time(case, heads=None, reps=1, nthreads=0):
+def oracle_time(case, heads=None, reps=1, nthreads=0, bits=None):
     import oracle
 
-    args = (W.bf16_bits(case.q), W.bf16_bits(case.k), W.bf16_bits(case.v), case.tables.indptr,
-            case.tables.indices, case.tables.last_page_len)
+    bits = bits or (W.bf16_bits(case.q), W.bf16_bits(case.k), W.bf16_bits(case.v))
+    args = (*bits, case.tables.indptr, case.tables.indices, case.tables.last_page_len)
     kw = dict(num_kv_heads=case.num_kv_heads, page_size=case.page_size,
               layout=0 if case.layout == "NHD" else 1, sm_scale=case.sm_scale, heads=heads,
               nthreads=nthreads)
@@ -290,24 +316,28 @@ def oracle_time(case, heads=None, reps=1, nthreads=0):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(case_host, target_s, single_thread=False):
-    """Oracle (as it stands) on the whole batch, repeated to about target_s seconds;
-    with single_thread, also one pass of the batch on one thread."""
+def cpu_baseline(case, bits, target_s, t_first=None, single_thread=False):
+    """Oracle (as it stands) on the whole batch on all host cores, repeated to
+    about target_s seconds (t_first: the time of a pass already made, which
+    counts as the first repetition); with single_thread, also one pass of the
+    batch on one thread. GB/s on the same byte basis as the GPU arm's value
+    (unique KV bytes)."""
     cores = os.cpu_count() or 1
-    t1 = oracle_time(case_host)
-    reps = max(1, min(1000, int(math.ceil(target_s / max(t1, 1e-6)))) - 1)
-    t = oracle_time(case_host, reps=reps) if reps > 0 else t1
-    reps = max(reps, 1)
+    t1 = t_first if t_first is not None else oracle_time(case, bits=bits)
+    more = max(0, min(1000, int(math.ceil(target_s / max(t1, 1e-6)))) - 1)
+    t = t1 + (oracle_time(case, reps=more, bits=bits) if more > 0 else 0.0)
+    reps = more + 1
     per = t / reps
-    gbs = case_host.kv_bytes() / per / 1e9
-    out = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-           "sample": f"whole workload batch ({case_host.batch} requests, "
-                     f"{case_host.batch * case_host.num_qo_heads} heads), f64 oracle over "
+    out = {"value": case.unique_kv_bytes() / per / 1e9, "unit": "GB/s", "cores": cores,
+           "kind": "oracle", "ms_per_step": per * 1e3,
+           "logical_gbs": case.kv_bytes() / per / 1e9,
+           "sample": f"whole workload batch ({case.batch} requests, "
+                     f"{case.batch * case.num_qo_heads} heads), f64 oracle over "
                      f"{cores} threads, {reps} repetition(s), {per * 1e3:.1f} ms each",
            "seconds": t}
     if single_thread:
-        t_st = oracle_time(case_host, nthreads=1)
-        out["single_thread_value"] = case_host.kv_bytes() / t_st / 1e9
+        t_st = oracle_time(case, nthreads=1, bits=bits)
+        out["single_thread_value"] = case.unique_kv_bytes() / t_st / 1e9
         out["single_thread_ms_per_step"] = t_st * 1e3
     return out
 
@@ -326,7 +356,7 @@ def run_reference(args):
     L = case.tables.lengths
     # One step = the oracle over a bounded subset of heads, sized so that the
     # whole run (K + W steps) takes about two minutes.
-    t_one = oracle_time(case, heads=[(0, 0)])
+    t_one = oracle_time(case, heads=[(int(np.argmax(L)), 0)])
     per_head = max(t_one, 1e-5)
     budget = args.ref_budget_s / max(1, args.steps + args.warmup)
     n_heads_total = case.batch * case.num_qo_heads
@@ -339,18 +369,28 @@ def run_reference(args):
     # its KV head's bytes.
     G = case.num_qo_heads // case.num_kv_heads
     sample_bytes = sum(int(L[b]) for b, _ in heads) * case.head_dim * 4 / G
+    bits = (W.bf16_bits(case.q), W.bf16_bits(case.k), W.bf16_bits(case.v))
     for _ in range(args.warmup):
-        oracle_time(case, heads=heads)
-    times = [oracle_time(case, heads=heads) for _ in range(args.steps)]
+        oracle_time(case, heads=heads, bits=bits)
+    times = [oracle_time(case, heads=heads, bits=bits) for _ in range(args.steps)]
     per = statistics.mean(times)
-    gbs = sample_bytes / per / 1e9
+    # A whole batch step at the sampled rate: the sample stands for
+    # sample_bytes of the step's kv_bytes. value is on the GPU arm's basis
+    # (unique KV bytes over the step time).
+    step_s = per * case.kv_bytes() / sample_bytes
+    gbs = case.unique_kv_bytes() / step_s / 1e9
     cores = os.cpu_count() or 1
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_block(cfg, case),
+        "logical_gbs": case.kv_bytes() / step_s / 1e9,
+        "sample_ms_per_step": per * 1e3,
+        "heads_sampled": n, "heads_total": n_heads_total,
+        "ms_per_step_basis": "a whole batch step at the sampled rate: the sampled heads' time "
+                             "times the step's KV bytes over the sample's",
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n} of {n_heads_total} query heads per step (each head's "
                                    "whole KV sequence), f64 oracle"},
@@ -375,26 +415,78 @@ def config_block(cfg, case):
 
 # ------------------------------------------------------------------ our arm
 
-def run_oxd(args):
-    import torch
+ATOL, RTOL, LSE_ATOL = 1.5e-2, 1e-2, 1e-3
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    import paged_kv_decode_attn_gb300 as oxd
+def plan_kind_for(cfg, requested):
+    """The plan a server would pick: the cascade when the workload declares
+    requests that share their leading pages, else the plain decode."""
+    can = cfg.shared_prefix_tokens > 0 and cfg.share_group > 1
+    if requested == "auto":
+        return "cascade" if can else "plain"
+    if requested == "cascade" and not can:
+        return "plain"
+    return requested
 
-    oxd.build()
-    cfg = shard_config(W.CONFIGS[args.config], rank)
-    case = W.make_case(cfg, device=dev, batch=args.batch)
+
+def oracle_inputs(case, host=None):
+    """Host uint16 views of q, K, V for the oracle (from pinned copies when given)."""
+    src = host or {"q": case.q, "k": case.k, "v": case.v}
+    return W.bf16_bits(src["q"]), W.bf16_bits(src["k"]), W.bf16_bits(src["v"])
+
+
+def oracle_full(case, bits, nthreads=0):
+    """The f64 oracle on every head of the batch; returns (out, lse, seconds)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    out, lse = oracle.paged_decode(
+        *bits, case.tables.indptr, case.tables.indices, case.tables.last_page_len,
+        num_kv_heads=case.num_kv_heads, page_size=case.page_size,
+        layout=0 if case.layout == "NHD" else 1, sm_scale=case.sm_scale, nthreads=nthreads)
+    return out, lse, time.perf_counter() - t0
+
+
+def parity_report(out, lse, ref_out, ref_lse):
+    """Element-by-element comparison of a run's out/lse with the f64 oracle on
+    every head: |out - ref| <= 1.5e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3."""
+    o = out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - ref_out)
+    rel = err / (ATOL + RTOL * np.abs(ref_out))
+    lg = lse.float().cpu().numpy().astype(np.float64)
+    lerr = np.abs(lg - ref_lse)
+    ok = bool(np.isfinite(o).all() and np.isfinite(lg).all() and rel.max() <= 1.0 and
+              lerr.max() <= LSE_ATOL)
+    return {"heads_checked": int(o.shape[0] * o.shape[1]),
+            "elements_checked": int(o.size), "max_abs_err": float(err.max()),
+            "max_rel_to_bound": float(rel.max()), "max_lse_err": float(lerr.max()),
+            "tolerance": "out: 1.5e-2 + 1e-2 |ref|; lse: 1e-3 (f64 oracle, every head)",
+            "pass": ok}
+
+
+class Flusher:
+    """Write 512 MiB, then read another 512 MiB: L2 (129 MB) ends up with clean
+    lines of neither the workload nor the written buffer, so no write-back of
+    flush data lands inside the next timed step."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+def measure_decode(oxd, torch, case, cfg, plan_kind, dev, stream, flush, K, Wm,
+                   work_list="bound", graph=False, sampler=None, world=1):
+    """Plan, bind and time one workload: K steps after Wm warm-ups, an L2
+    flush before each (outside its events); then up to 200 back-to-back steps
+    with a warm L2 and the decode kernel alone over up to 200 flushed steps
+    (events the library records around its launch)."""
     t = case.tables
     casc = {}
-    if args.cascade and cfg.shared_prefix_tokens > 0 and cfg.share_group > 1:
-        # the workload declares which requests share which leading pages
+    if plan_kind == "cascade":
         casc = dict(shared_prefix_tokens=cfg.shared_prefix_tokens, share_group=cfg.share_group)
     desc = oxd.make_desc(case.batch, case.num_qo_heads, case.num_kv_heads, case.page_size,
                          case.layout, t.num_pages, **casc)
@@ -409,56 +501,42 @@ def run_oxd(args):
     lse = torch.empty(case.batch, case.num_qo_heads, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     bind_us = None
-    if args.work_list == "bound":
+    if work_list == "bound":
         torch.cuda.synchronize(dev)
         tb0 = time.perf_counter()
-        oxd.oxd_plan_bind_workspace(plan, ws, plan.workspace_bytes, torch.cuda.current_stream(dev))
+        oxd.oxd_plan_bind_workspace(plan, ws, plan.workspace_bytes, stream)
         torch.cuda.synchronize(dev)
         bind_us = (time.perf_counter() - tb0) * 1e6
-    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def flush():
-        # Write 512 MiB, then read another 512 MiB: L2 (129 MB) ends up with
-        # clean lines of neither the workload nor the written buffer, so no
-        # write-back of flush data lands inside the next timed step.
-        flush_w.zero_()
-        flush_r.sum()
 
     def run_once(s):
         oxd.oxd_paged_decode_run(plan, case.q, case.k, case.v, indptr, indices, last,
                                  case.sm_scale, out, lse, ws, plan.workspace_bytes, s)
 
-    graph = None
-    if args.graph:
+    g = None
+    if graph:
         # one run captured with every pointer fixed; replays re-read the
         # buffers' current contents
         run_once(stream)
         torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
             run_once(torch.cuda.current_stream(dev))
 
     def step():
-        if graph is not None:
-            graph.replay()
+        if g is not None:
+            g.replay()
         else:
             run_once(stream)
 
-    K, Wm = args.steps, args.warmup
     for _ in range(Wm):
         flush()
         step()
     if oxd.oxd_read_device_status(ws, stream) != 0:
-        raise RuntimeError("device status error during warm-up")
+        raise RuntimeError(f"{cfg.name}: device status error during warm-up")
 
     # ---- timed steps: the production path, events only around each step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
-    if sampler:
-        sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -477,12 +555,10 @@ def run_oxd(args):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    clocks = sampler.stop() if sampler else None
     if oxd.oxd_read_device_status(ws, stream) != 0:
-        raise RuntimeError("device status error during the timed steps")
+        raise RuntimeError(f"{cfg.name}: device status error during the timed steps")
 
-    # ---- back-to-back steps with a warm L2 (no flush): what a loop over a
-    # working set that L2 holds would see
+    # ---- back-to-back steps with a warm L2 (no flush)
     Kw = max(3, min(K, 200))
     wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(Kw)]
@@ -510,29 +586,108 @@ def run_oxd(args):
     torch.cuda.synchronize(dev)
     oxd.oxd_plan_set_timing_events(plan, None, None)
     kern_ms = [a.elapsed_time(b) for a, b in kev]
+    if oxd.oxd_read_device_status(ws, stream) != 0:
+        raise RuntimeError(f"{cfg.name}: device status error in the kernel-only loop")
 
-    ms = max_over_ranks(statistics.mean(step_ms), dev)
-    kv_bytes = case.kv_bytes()
-    value = whole_job_gbs(kv_bytes, world, ms)
-    kern = statistics.mean(kern_ms)
-    peak, peak_kind = measured_peaks()
     # Bytes the timed decode kernel reads. In a cascade plan the prefill kernel
     # reads the shared-prefix tokens of the cascade requests (once per group)
     # and the decode kernel the rest of each request's cache.
-    kern_bytes = kv_bytes
+    kern_bytes = case.kv_bytes()
     if casc:
         kern_bytes -= (info.cascade_requests * cfg.shared_prefix_tokens * case.num_kv_heads *
                        case.head_dim * 2 * 2)
-    achieved = kern_bytes / (kern * 1e-3) / 1e9
+    return dict(plan=plan, info=info, plan_us=plan_us, bind_us=bind_us, out=out, lse=lse,
+                ws=ws, indptr=indptr, indices=indices, last=last, step_ms=step_ms,
+                warm_ms=warm_ms, kern_ms=kern_ms, kern_launches=Kk, kern_bytes=kern_bytes,
+                wall=wall, run_once=run_once, casc=casc)
+
+
+def summary(case, m, peak, traffic_key, parity):
+    """One workload's figures for the bench line."""
+    ms = statistics.mean(m["step_ms"])
+    kern = statistics.mean(m["kern_ms"])
+    srt = sorted(m["step_ms"])
+    uniq = case.unique_kv_bytes()
+    return {
+        "us_per_step": ms * 1e3,
+        "us_per_step_p10_p50_p90": [srt[len(srt) // 10] * 1e3, srt[len(srt) // 2] * 1e3,
+                                    srt[(9 * len(srt)) // 10] * 1e3],
+        "warm_l2_us_per_step": m["warm_ms"][len(m["warm_ms"]) // 2] * 1e3,
+        "unique_gbs": uniq / (ms * 1e-3) / 1e9,
+        "logical_gbs": case.kv_bytes() / (ms * 1e-3) / 1e9,
+        "pct_of_hbm_peak": 100.0 * uniq / (ms * 1e-3) / 1e9 / peak,
+        "kv_bytes_per_step": case.kv_bytes(), "unique_kv_bytes_per_step": uniq,
+        "kernel_us": kern * 1e3,
+        "kernel_frac": m["kern_bytes"] / (kern * 1e-3) / 1e9 / peak,
+        "kernel_algorithmic_bytes": m["kern_bytes"],
+        "traffic": recorded_traffic(traffic_key),
+        "launches_per_step": m["info"].launches_per_run,
+        "plan_host_us": m["plan_us"],
+        "parity": parity,
+    }
+
+
+def run_oxd(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import paged_kv_decode_attn_gb300 as oxd
+
+    oxd.build()
+    cfg = shard_config(W.CONFIGS[args.config], rank)
+    kind = plan_kind_for(cfg, "cascade" if args.cascade else args.plan)
+    case = W.make_case(cfg, device=dev, batch=args.batch)
+    cfg_block = config_block(cfg, case)
+    stream = torch.cuda.current_stream(dev)
+    flush = Flusher(torch, dev)
+    peak, peak_kind = measured_peaks()
+    solo = rank == 0 and world == 1
+    check = solo and not args.no_parity
+    if check or (solo and not args.no_cpu_baseline):
+        import oracle
+
+        oracle.build()  # compiled on the host before any timed region
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, dev)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    m = measure_decode(oxd, torch, case, cfg, kind, dev, stream, flush, args.steps, args.warmup,
+                       work_list=args.work_list, graph=args.graph, sampler=sampler, world=world)
+    clocks = sampler.stop(steps=args.steps) if sampler else None
+    info, plan, ws, out, lse = m["info"], m["plan"], m["ws"], m["out"], m["lse"]
+    timed_out, timed_lse = out.clone(), lse.clone()  # the timed run's results
+
+    ms = max_over_ranks(statistics.mean(m["step_ms"]), dev)
+    kv_bytes, uniq = case.kv_bytes(), case.unique_kv_bytes()
+    value = whole_job_gbs(uniq, world, ms)
+    kern = statistics.mean(m["kern_ms"])
+    achieved = m["kern_bytes"] / (kern * 1e-3) / 1e9
+    traffic_key = cfg.name + ("+cascade" if kind == "cascade" else "")
+    head = summary(case, m, peak, traffic_key, None)
+    kern_launches, bind_us, wall = m["kern_launches"], m["bind_us"], m["wall"]
+    if args.raw_samples and rank == 0:
+        with open(args.raw_samples, "w") as f:
+            json.dump({"workload": cfg.name, "plan": kind,
+                       "step_us": [x * 1e3 for x in m["step_ms"]],
+                       "kernel_us": [x * 1e3 for x in m["kern_ms"]],
+                       "warm_l2_step_us": [x * 1e3 for x in m["warm_ms"]]}, f)
 
     # ---- end to end through the public API from pinned host buffers
     host = {name: x.cpu().pin_memory() for name, x in
-            (("q", case.q), ("k", case.k), ("v", case.v), ("indptr", indptr),
-             ("indices", indices), ("last", last))}
+            (("q", case.q), ("k", case.k), ("v", case.v), ("indptr", m["indptr"]),
+             ("indices", m["indices"]), ("last", m["last"]))}
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     dq, dk, dv = torch.empty_like(case.q), torch.empty_like(case.k), torch.empty_like(case.v)
-    dind, dptr, dlast = torch.empty_like(indices), torch.empty_like(indptr), torch.empty_like(last)
+    dind, dptr, dlast = (torch.empty_like(m["indices"]), torch.empty_like(m["indptr"]),
+                         torch.empty_like(m["last"]))
     h2d = sum(x.numel() * x.element_size() for x in host.values())
     d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
 
@@ -551,7 +706,7 @@ def run_oxd(args):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize(dev)
-    n_e2e = max(3, min(args.e2e_steps, K))
+    n_e2e = max(3, min(args.e2e_steps, args.steps))
     e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(n_e2e)]
     for a, b in e_ev:
@@ -563,54 +718,90 @@ def run_oxd(args):
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_ev), dev)
     if not torch.equal(out_h, out.cpu()):
         raise RuntimeError("e2e output mismatch")
+    del dq, dk, dv, dind, dptr, dlast
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
+    # ---- parity of the timed run with the f64 oracle on every head, and the
+    # oracle's own time on the host cores (the CPU baseline)
+    cpu, ref = None, None
+    if solo and (check or not args.no_cpu_baseline):
+        bits = oracle_inputs(case, host)
+        ref_out, ref_lse, t_pass = oracle_full(case, bits)
+        ref = (ref_out, ref_lse)
+        if check:
+            head["parity"] = parity_report(timed_out, timed_lse, ref_out, ref_lse)
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline(case, bits, args.cpu_seconds, t_first=t_pass,
+                               single_thread=cfg.name in ("mha8_b1_l512_ps16_nhd",
+                                                          "gqa4_b32_u512to4096_ps16_nhd"))
+        del bits
+    del host, out_h, lse_h
 
-        oracle.build()
-        host_case = W.Case(case.batch, case.num_qo_heads, case.num_kv_heads, case.head_dim,
-                           case.page_size, case.layout, case.sm_scale, case.tables,
-                           host["q"], host["k"], host["v"])
-        cpu = cpu_baseline(host_case, args.cpu_seconds,
-                           single_thread=cfg.name in ("mha8_b1_l512_ps16_nhd", DEFAULT_CONFIG))
+    # ---- the other workloads, measured in the same process (one GPU)
+    others = None
+    if solo and not args.no_workloads and args.batch is None:
+        others = {}
+        if kind == "cascade":
+            # the same batch on the plain plan, for comparison
+            mp = measure_decode(oxd, torch, case, cfg, "plain", dev, stream, flush,
+                                args.steps, args.warmup)
+            par = parity_report(mp["out"], mp["lse"], *ref) if check else None
+            others[cfg.name + "+plain"] = dict(summary(case, mp, peak, cfg.name, par),
+                                               plan="plain")
+            del mp
+        del m, out, lse, timed_out, timed_lse
+        case = None
+        torch.cuda.empty_cache()
+        for name in W.CONFIG_ORDER:
+            if name == cfg.name:
+                continue
+            c2 = W.CONFIGS[name]
+            k2 = plan_kind_for(c2, "auto")
+            case2 = W.make_case(c2, device=dev)
+            m2 = measure_decode(oxd, torch, case2, c2, k2, dev, stream, flush, args.steps,
+                                args.warmup)
+            par = None
+            if check:
+                r_out, r_lse, _ = oracle_full(case2, oracle_inputs(case2))
+                par = parity_report(m2["out"], m2["lse"], r_out, r_lse)
+            key = name + ("+cascade" if k2 == "cascade" else "")
+            others[name] = dict(summary(case2, m2, peak, key, par), plan=k2)
+            del m2, case2
+            torch.cuda.empty_cache()
 
     if rank == 0:
-        srt = sorted(step_ms)
         line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
-            "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(config_block(cfg, case), cascade=bool(casc)),
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg_block,
+            "value_basis": "unique KV bytes read per step (each shared prefix page once) over "
+                           "the mean step time; logical_gbs counts every request's pages",
             "us_per_step": ms * 1e3,
-            "us_per_step_p10_p50_p90": [srt[len(srt) // 10] * 1e3, srt[len(srt) // 2] * 1e3,
-                                        srt[(9 * len(srt)) // 10] * 1e3],
-            "warm_l2_us_per_step": warm_ms[len(warm_ms) // 2] * 1e3,
+            "us_per_step_p10_p50_p90": head["us_per_step_p10_p50_p90"],
+            "warm_l2_us_per_step": head["warm_l2_us_per_step"],
+            "unique_gbs": value, "logical_gbs": whole_job_gbs(kv_bytes, world, ms),
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "traffic": recorded_traffic(cfg.name + ("+cascade" if casc else "")),
+                         "traffic": head["traffic"],
                          "kernel": f"paged_decode_kernel variant {info.kernel_variant}",
-                         "kernel_us": kern * 1e3, "kernel_timed_launches": Kk,
-                         "algorithmic_bytes_per_launch": kern_bytes},
+                         "kernel_us": kern * 1e3, "kernel_timed_launches": kern_launches,
+                         "algorithmic_bytes_per_launch": head["kernel_algorithmic_bytes"]},
+            "parity": head["parity"],
             "cpu_baseline": cpu,
-            "e2e": {"value": whole_job_gbs(kv_bytes, world, e2e_ms), "unit": "GB/s",
+            "e2e": {"value": whole_job_gbs(uniq, world, e2e_ms), "unit": "GB/s",
                     "ms_per_step": e2e_ms, "steps": n_e2e,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": K * info.launches_per_run,
+            "gpu_launches": args.steps * info.launches_per_run,
             "clocks": clocks,
-            "plan": {"host_us": plan_us, "work_list": args.work_list, "bind_us": bind_us,
-                     "cuda_graph": bool(args.graph),
+            "plan": {"kind": kind, "host_us": head["plan_host_us"], "work_list": args.work_list,
+                     "bind_us": bind_us, "cuda_graph": bool(args.graph),
                      **info.as_dict()},
+            "workloads": others,
             "wall_s_timed_loop": wall,
         }
         print(json.dumps(line), flush=True)
-        if args.raw_samples:
-            with open(args.raw_samples, "w") as f:
-                json.dump({"workload": cfg.name, "step_us": [x * 1e3 for x in step_ms],
-                           "kernel_us": [x * 1e3 for x in kern_ms],
-                           "warm_l2_step_us": [x * 1e3 for x in warm_ms]}, f)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()

@@ -65,7 +65,7 @@ def test_reference_arm_prints_one_json_line():
     env = dict(os.environ, RANK="0", WORLD_SIZE="1")
     r = subprocess.run(
         [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
-         "--warmup", "1", "--ref-budget-s", "3"],
+         "--warmup", "1", "--ref-budget-s", "3", "--config", "gqa4_b32_u512to4096_ps16_nhd"],
         capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [line for line in r.stdout.splitlines() if line.strip()]
@@ -92,10 +92,67 @@ def test_reference_arm_counts_each_kv_head_once():
     env = dict(os.environ, RANK="0", WORLD_SIZE="1")
     r = subprocess.run(
         [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-         "--warmup", "1", "--batch", "2", "--ref-budget-s", "30"],
+         "--warmup", "1", "--batch", "2", "--ref-budget-s", "30", "--config",
+         "gqa4_b32_u512to4096_ps16_nhd"],
         capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     d = json.loads(r.stdout.strip().splitlines()[-1])
     assert d["cpu_baseline"]["sample"].startswith("64 of 64 ")
     kv = d["config"]["kv_bytes_per_step"]
     assert d["value"] == pytest.approx(kv / (d["ms_per_step"] * 1e-3) / 1e9, rel=1e-9)
+    assert d["ms_per_step"] == pytest.approx(d["sample_ms_per_step"], rel=1e-9)
+
+
+def test_reference_arm_reports_unique_bytes_and_a_whole_step_on_shared_prefixes():
+    # Nine requests of the GQA8 workload: a group of eight sharing 1024 tokens
+    # and one more. value counts each shared page once, logical_gbs every
+    # request's pages; ms_per_step stands for the whole batch (here all heads
+    # are sampled, so it equals the sample's time).
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+         "--warmup", "1", "--batch", "9", "--ref-budget-s", "60"],
+        capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    c = d["config"]
+    assert c["workload"] == "gqa8_b256_u128to16384_prefix1024x8_ps16_nhd"
+    assert c["unique_kv_bytes_per_step"] < c["kv_bytes_per_step"]
+    assert d["heads_sampled"] == d["heads_total"] == 9 * 64
+    step_s = d["ms_per_step"] * 1e-3
+    assert d["value"] == pytest.approx(c["unique_kv_bytes_per_step"] / step_s / 1e9, rel=1e-9)
+    assert d["logical_gbs"] == pytest.approx(c["kv_bytes_per_step"] / step_s / 1e9, rel=1e-9)
+
+
+def test_default_run_is_the_largest_workload_on_the_cascade_plan():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+
+    args = bench.parse_args([])
+    cfg = W.CONFIGS[args.config]
+    assert args.config == "gqa8_b256_u128to16384_prefix1024x8_ps16_nhd"
+    assert max(W.CONFIGS.values(), key=lambda c: W.make_tables(c).lengths.sum()) is cfg
+    assert bench.plan_kind_for(cfg, args.plan) == "cascade"
+    assert bench.plan_kind_for(W.CONFIGS["gqa4_b32_u512to4096_ps16_nhd"], "auto") == "plain"
+    assert bench.plan_kind_for(W.CONFIGS["mqa32_b16_l32768_ps64_nhd"], "cascade") == "plain"
+
+
+def test_parity_report_flags_an_element_outside_the_bound():
+    import numpy as np
+    import torch
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rng = np.random.default_rng(1)
+    ref = rng.standard_normal((3, 4, 128))
+    ref_lse = rng.standard_normal((3, 4))
+    out = torch.as_tensor(ref, dtype=torch.float32).to(torch.bfloat16)
+    lse = torch.as_tensor(ref_lse, dtype=torch.float32)
+    good = bench.parity_report(out, lse, ref, ref_lse)
+    assert good["pass"] and good["heads_checked"] == 12 and good["max_rel_to_bound"] < 1.0
+    bad = out.clone()
+    bad[2, 3, 7] = float(ref[2, 3, 7]) + 0.05 + 0.02 * abs(float(ref[2, 3, 7]))
+    assert not bench.parity_report(bad, lse, ref, ref_lse)["pass"]
+    assert not bench.parity_report(out, lse + 2e-3, ref, ref_lse)["pass"]
