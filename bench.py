@@ -94,10 +94,14 @@ def parse_args(argv=None):
                          "params: unbound runs")
     ap.add_argument("--graph", action="store_true",
                     help="capture one run in a CUDA graph and time its replays")
-    ap.add_argument("--op", choices=["decode", "rope_append", "prefill"], default="decode",
+    ap.add_argument("--op", choices=["decode", "rope_append", "prefill", "append_decode"],
+                    default="decode",
                     help="rope_append: time the fused RoPE + paged append on the workload's "
                          "tables instead of the decode step; prefill: time the paged causal "
-                         "prefill of --prefill-config")
+                         "prefill of --prefill-config; append_decode: one engine step, the "
+                         "append of each request's new token followed by the decode that reads "
+                         "it, with plain launches and with the decode launched as a "
+                         "programmatic dependent of the append")
     ap.add_argument("--plan", choices=["auto", "plain", "cascade"], default="auto",
                     help="decode: auto picks the cascade (each sharing group's prefix "
                          "attended once, then the suffixes) for a workload that declares "
@@ -888,6 +892,125 @@ def run_rope_append(args):
     return 0
 
 
+def run_append_decode(args):
+    """One engine step of a decode layer: oxd_rope_append writes each request's
+    new token (rotated q, K and V rows in their page slots), then
+    oxd_paged_decode_run attends over the grown cache. Timed four ways, an L2
+    flush before each step: the append alone, the decode alone, the two with
+    plain launches, and the two with the decode launched as a programmatic
+    dependent of the append (plan pdl = 1). Metric as for decode: unique KV
+    bytes per step over the step time."""
+    import torch
+
+    import paged_kv_decode_attn_gb300 as oxd
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    oxd.build()
+    cfg = W.CONFIGS[args.config]
+    kind = plan_kind_for(cfg, "cascade" if args.cascade else args.plan)
+    lengths = W.make_tables(cfg, batch=args.batch).lengths
+    casc = {}
+    if kind == "cascade":
+        casc = dict(shared_prefix_tokens=cfg.shared_prefix_tokens, share_group=cfg.share_group)
+    case = W.custom_case([int(L) + 1 for L in lengths], num_qo_heads=cfg.num_qo_heads,
+                         num_kv_heads=cfg.num_kv_heads, page_size=cfg.page_size,
+                         layout=cfg.layout, seed=cfg.seed, sigma=cfg.sigma, device=dev, **casc)
+    t = case.tables
+    B, Hq, Hkv = case.batch, case.num_qo_heads, case.num_kv_heads
+    g = torch.Generator(device=dev).manual_seed(cfg.seed)
+    q_new = torch.randn(B, Hq, 128, generator=g, device=dev).to(torch.bfloat16)
+    k_new = torch.randn(B, Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn(B, Hkv, 128, generator=g, device=dev).to(torch.bfloat16)
+    tok = torch.arange(B, dtype=torch.int32, device=dev)
+    pos = torch.as_tensor(lengths, device=dev).to(torch.int32)
+    indptr = torch.as_tensor(t.indptr, device=dev)
+    indices = torch.as_tensor(t.indices, device=dev)
+    last = torch.as_tensor(t.last_page_len, device=dev)
+    # each page's reference count is the number of requests that list it: a
+    # token whose slot lies in a page shared with other requests is refused by
+    # the append (the pages' write rule; an engine makes that page private
+    # first), the others are written
+    rc = np.bincount(t.indices, minlength=t.num_pages).astype(np.int32)
+    refcount = torch.as_tensor(rc, device=dev)
+    slot_page = t.indices[t.indptr[:-1] + np.asarray(lengths) // case.page_size]
+    n_shared_slot = int((rc[slot_page] > 1).sum())
+    aws = torch.empty(256, dtype=torch.uint8, device=dev)
+    adesc = oxd.make_rope_append_desc(B, B, Hq, Hkv, case.page_size, case.layout, t.num_pages,
+                                      int(t.indptr[-1]))
+    stream = torch.cuda.current_stream(dev)
+    plans = {}
+    for pdl in (0, 1):
+        desc = oxd.make_desc(B, Hq, Hkv, case.page_size, case.layout, t.num_pages, pdl=pdl,
+                             **casc)
+        plan = oxd.oxd_paged_decode_plan(desc, t.indptr, t.last_page_len, 0)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        oxd.oxd_plan_bind_workspace(plan, ws, plan.workspace_bytes, stream)
+        plans[pdl] = (plan, ws)
+    q = torch.empty_like(q_new)
+    out = torch.empty_like(q_new)
+    lse = torch.empty(B, Hq, device=dev)
+    flush = Flusher(torch, dev)
+
+    def append():
+        oxd.oxd_rope_append(adesc, q_new, k_new, v_new, tok, pos, indptr, indices, refcount, q,
+                            case.k, case.v, aws, 256, stream)
+
+    def decode(pdl):
+        plan, ws = plans[pdl]
+        oxd.oxd_paged_decode_run(plan, q, case.k, case.v, indptr, indices, last, case.sm_scale,
+                                 out, lse, ws, plan.workspace_bytes, stream)
+
+    ways = {"append": append, "decode": lambda: decode(0),
+            "append_then_decode": lambda: (append(), decode(0)),
+            "append_then_decode_pdl": lambda: (append(), decode(1))}
+    times = {}
+    K, Wm = args.steps, max(3, args.warmup)
+    for r in range(2):  # two rounds, alternating order
+        for name in (list(ways) if r == 0 else list(reversed(list(ways)))):
+            fn = ways[name]
+            for _ in range(Wm):
+                flush()
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            torch.cuda.synchronize(dev)
+            for a, b_ in ev:
+                flush()
+                a.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize(dev)
+            times.setdefault(name, []).extend(a.elapsed_time(b_) for a, b_ in ev)
+    want = oxd.OXD_DEVICE_SHARED_PAGE if n_shared_slot else oxd.OXD_DEVICE_OK
+    if oxd.oxd_read_device_status(aws, stream) != want:
+        raise RuntimeError("unexpected device status in the append")
+    for _, ws_ in plans.values():
+        if oxd.oxd_read_device_status(ws_, stream) != 0:
+            raise RuntimeError("device status error in the decode")
+    us = {k: statistics.mean(v) * 1e3 for k, v in times.items()}
+    uniq = case.unique_kv_bytes()
+    step_ms = us["append_then_decode_pdl"] * 1e-3
+    peak, peak_kind = measured_peaks()
+    print(json.dumps({
+        "impl": "oxd", "op": "append_decode",
+        "metric": "append + decode step: unique KV-read GB/s, us per step",
+        "value": uniq / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
+        "steps": K, "warmup": Wm, "ms_per_step": step_ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "plan": kind, "batch": B, "new_tokens": B,
+                   "tokens_refused_shared_page": n_shared_slot,
+                   "kv_bytes_per_step": case.kv_bytes(), "unique_kv_bytes_per_step": uniq,
+                   "l2": "flushed before every step, outside its events"},
+        "us": us,
+        "sum_of_parts_us": us["append"] + us["decode"],
+        "pdl_saves_us": us["append_then_decode"] - us["append_then_decode_pdl"],
+        "pct_of_hbm_peak": 100.0 * uniq / (step_ms * 1e-3) / 1e9 / peak,
+        "gpu_launches": K * (1 + plans[1][0].info.launches_per_run),
+    }), flush=True)
+    return 0
+
+
 def run_prefill(args):
     """Paged causal prefill of one prefill workload. A step is one
     oxd_paged_prefill_run on the bound workspace (the prefill kernel and, when
@@ -1016,6 +1139,8 @@ def main(argv=None):
         return run_rope_append(args)
     if args.op == "prefill":
         return run_prefill(args)
+    if args.op == "append_decode":
+        return run_append_decode(args)
     return run_oxd(args)
 
 

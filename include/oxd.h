@@ -110,7 +110,16 @@ typedef struct {
      * whole. */
     int32_t shared_prefix_tokens; /* 0, or a positive multiple of page_size */
     int32_t share_group;          /* 0 (with no prefix), or >= 2 consecutive requests */
-    int32_t reserved;             /* must be zero */
+    /* 1: launch a run's first kernel as a programmatic dependent of the kernel
+     * before it on the stream (e.g. oxd_rope_append writing this step's q and
+     * K/V rows): its CTAs are scheduled while that kernel finishes, and they
+     * wait for it to complete (griddepcontrol.wait) before they read or write
+     * any memory, so the results are those of a plain launch. The kernel
+     * before it gains from triggering its dependents early
+     * (griddepcontrol.launch_dependents), as oxd_rope_append does; a copy or
+     * event between the two launches makes it a plain launch. Not used while
+     * timing events are set. 0: plain launches. */
+    int32_t pdl;
     /* How long one pipeline wait inside the kernels may last before the run
      * gives up ("Providers": typed device-status failures): 0 = about one
      * second; n > 0 = n nanoseconds. A run whose wait runs out stops its

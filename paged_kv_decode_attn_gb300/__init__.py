@@ -100,7 +100,7 @@ class Desc(ctypes.Structure):
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
         ("force_splits", ctypes.c_int32), ("num_sms", ctypes.c_int32),
         ("tensor_path", ctypes.c_int32), ("shared_prefix_tokens", ctypes.c_int32),
-        ("share_group", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("share_group", ctypes.c_int32), ("pdl", ctypes.c_int32),
         ("wait_timeout_ns", ctypes.c_int64),
     ]
 
@@ -426,15 +426,17 @@ def oxd_read_device_status(workspace, stream=None) -> int:
 
 def make_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages, head_dim=128,
               max_splits=0, force_splits=0, num_sms=0, tensor_path=0, shared_prefix_tokens=0,
-              share_group=0, wait_timeout_ns=0) -> Desc:
+              share_group=0, wait_timeout_ns=0, pdl=0) -> Desc:
     """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1. A nonzero
     ``shared_prefix_tokens`` with ``share_group`` plans a cascade decode;
-    ``wait_timeout_ns`` > 0 shortens the kernels' pipeline-wait limit."""
+    ``wait_timeout_ns`` > 0 shortens the kernels' pipeline-wait limit;
+    ``pdl`` = 1 launches a run's first kernel as a programmatic dependent of
+    the kernel before it on the stream."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return Desc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
                 max_splits, force_splits, num_sms, tensor_path, shared_prefix_tokens,
-                share_group, 0, wait_timeout_ns)
+                share_group, pdl, wait_timeout_ns)
 
 
 def oxd_rope_append(desc: RopeAppendDesc, q, k, v, token_request, positions, indptr, indices,

@@ -69,6 +69,10 @@ __device__ __forceinline__ void rope_store(uint32_t lo, uint32_t hi, uint16_t* d
 // itself, so the compiler could not hoist a later load over an earlier
 // store) and forms the token's angles once.
 __global__ void __launch_bounds__(kAppendWarps * 32) rope_append_kernel(const AppendParams p) {
+    // A decode launched behind this kernel as its programmatic dependent may
+    // be scheduled now; it waits for this grid to complete before it touches
+    // memory, so it still reads the rotated q and the appended rows.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.last_epoch = p.epoch;
     const int lane = threadIdx.x & 31;
     const long long gw = static_cast<long long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);

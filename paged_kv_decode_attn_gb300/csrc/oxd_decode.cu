@@ -642,19 +642,26 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
         if constexpr (kCluster) mbar_init(sm.cluster_bar(), static_cast<uint32_t>(p.cluster_c));
         flags[0] = 0;
         fence_mbar_init();
-        if (blockIdx.x == 0) {
-            *p.last_epoch = p.epoch;  // whose status the word may hold
-            // an unbound run ends any binding of the workspace it writes
-            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
-        }
     }
     if (warp == C::kConsumerWarps && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
-    // The merge kernel, when the plan has one, may be scheduled now; it waits
-    // for this grid to complete before it reads anything.
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream (a plan with pdl = 1), this CTA may start while that kernel is
+    // still running: nothing in global memory is read or written before the
+    // wait. Launched plainly, the wait returns at once.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        if (blockIdx.x == 0) {
+            *p.last_epoch = p.epoch;  // whose status the word may hold
+            // an unbound run ends any binding of the workspace it writes
+            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
+        }
+        // The kernels behind this one (merge, prefix tiles) may be scheduled
+        // now; they wait for this grid before they read its results.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     __syncthreads();
     // A cluster's barrier in rank 0 is initialised before any CTA can arrive.
     if constexpr (kCluster) cluster_sync_all();
@@ -995,10 +1002,17 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tmap_k, const CUt
     __syncthreads();  // every warp has left its loop
     // No CTA of a cluster leaves before all have passed this point: a piece
     // stores into rank 0's shared memory and arrives there before it gets
-    // here, so rank 0 (even one whose wait for the pieces gave up) never
-    // exits ahead of a remote store. Every wait before it is bounded, so the
-    // barrier completes.
-    if constexpr (kCluster) cluster_sync_all();
+    // here, and its arrival releases those operations, so rank 0 (even one
+    // whose wait for the pieces gave up) never exits ahead of a remote store.
+    // Rank 0 orders nothing of its own by this barrier: its arrival is
+    // relaxed (a release there would wait for its output stores, +1.5 us on a
+    // one-request batch). Every wait before it is bounded, so it completes.
+    if constexpr (kCluster) {
+        if (cluster_ctarank() == 0)
+            cluster_sync_relaxed_arrive();
+        else
+            cluster_sync_all();
+    }
 
     if (flags[0] && threadIdx.x == 0) {
         // Aborted: wait (bounded) for the copies already issued, then leave.
@@ -1052,29 +1066,40 @@ cudaError_t ensure_smem_attribute() {
     return e;
 }
 
-template <class C, class WL>
-cudaError_t launch_cluster(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                           const WL& w, int grid, cudaStream_t stream) {
-    cudaError_t e = ensure_smem_attribute<C, WL, true>();
+template <class C, class WL, bool cluster>
+cudaError_t launch_ex(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                      const WL& w, int grid, cudaStream_t stream, bool pdl) {
+    cudaError_t e = ensure_smem_attribute<C, WL, cluster>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytesCluster;
+    cfg.dynamicSmemBytes = cluster ? C::kSmemBytesCluster : C::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster_c);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if constexpr (cluster) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(p.cluster_c);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        // a programmatic dependent of the kernel before it on the stream: it
+        // may start early and waits (griddepcontrol.wait) before touching memory
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel_of<C, WL, true>(), tk, tv, p, w);
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel_of<C, WL, cluster>(), tk, tv, p, w);
 }
 
 template <class C>
 cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                   const WorkList* w, int grid, cudaStream_t stream) {
+                   const WorkList* w, int grid, cudaStream_t stream, bool pdl) {
     if (p.cluster_c > 1) {
         // clusters of p.cluster_c CTAs (CUDA-core and 8-row variants); grid is a
         // multiple of it
@@ -1085,21 +1110,13 @@ cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodePar
             static_assert(CC::kSmemBytesCluster <= 113 * 1024, "two cluster CTAs a SM");
             if (grid % p.cluster_c != 0 || p.cluster_c > kMaxClusterCtas)
                 return cudaErrorInvalidValue;
-            if (w != nullptr) return launch_cluster<CC, WorkList>(tk, tv, p, *w, grid, stream);
-            return launch_cluster<CC, NoList>(tk, tv, p, NoList{0}, grid, stream);
+            if (w != nullptr)
+                return launch_ex<CC, WorkList, true>(tk, tv, p, *w, grid, stream, pdl);
+            return launch_ex<CC, NoList, true>(tk, tv, p, NoList{0}, grid, stream, pdl);
         }
     }
-    if (w != nullptr) {
-        cudaError_t e = ensure_smem_attribute<C, WorkList>();
-        if (e != cudaSuccess) return e;
-        kernel_of<C, WorkList>()<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p, *w);
-    } else {
-        cudaError_t e = ensure_smem_attribute<C, NoList>();
-        if (e != cudaSuccess) return e;
-        kernel_of<C, NoList>()<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p,
-                                                                            NoList{0});
-    }
-    return cudaGetLastError();
+    if (w != nullptr) return launch_ex<C, WorkList, false>(tk, tv, p, *w, grid, stream, pdl);
+    return launch_ex<C, NoList, false>(tk, tv, p, NoList{0}, grid, stream, pdl);
 }
 
 template <class C>
@@ -1141,13 +1158,13 @@ cudaError_t variant_occupancy(int variant, int* n) {
 
 cudaError_t launch_decode(int variant, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, const WorkList* w, int grid,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool pdl) {
     switch (variant) {
-        case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, w, grid, stream);
-        case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, w, grid, stream);
-        case kVariantMma8: return launch<CfgMma8>(tk, tv, p, w, grid, stream);
-        case kVariantMma16: return launch<CfgMma16>(tk, tv, p, w, grid, stream);
-        default: return launch<CfgMma16>(tk, tv, p, w, grid, stream);
+        case kVariantFmaG1: return launch<CfgFmaG1>(tk, tv, p, w, grid, stream, pdl);
+        case kVariantFmaG2: return launch<CfgFmaG2>(tk, tv, p, w, grid, stream, pdl);
+        case kVariantMma8: return launch<CfgMma8>(tk, tv, p, w, grid, stream, pdl);
+        case kVariantMma16: return launch<CfgMma16>(tk, tv, p, w, grid, stream, pdl);
+        default: return launch<CfgMma16>(tk, tv, p, w, grid, stream, pdl);
     }
 }
 

@@ -126,11 +126,6 @@ __global__ void __launch_bounds__(kWThreads)
         mbar_init(&ctl.mma_done, 1);
         flags[0] = 0;
         fence_mbar_init();
-        if (blockIdx.x == 0) {
-            *p.last_epoch = p.epoch;  // whose status the word may hold
-            // an unbound run ends any binding of the workspace it writes
-            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
-        }
     }
     if (warp == 1) {
         asm volatile(
@@ -145,9 +140,19 @@ __global__ void __launch_bounds__(kWThreads)
         prefetch_tmap(&tmap_v);
         prefetch_tmap(&tmap_q);
     }
-    // The merge kernel, when the plan has one, may be scheduled now; it waits
-    // for this grid to complete before it reads anything.
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // A programmatic dependent of the kernel before it (pdl = 1) touches no
+    // global memory before this wait; launched plainly it returns at once.
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        if (blockIdx.x == 0) {
+            *p.last_epoch = p.epoch;  // whose status the word may hold
+            // an unbound run ends any binding of the workspace it writes
+            if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
+        }
+        // The merge kernel, when the plan has one, may be scheduled now; it
+        // waits for this grid to complete before it reads anything.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -686,19 +691,26 @@ cudaError_t wide_occupancy(int* n) {
 
 cudaError_t launch_decode_wide(const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tq, const DecodeParams& p, const WorkList* w,
-                               int grid, cudaStream_t stream) {
+                               int grid, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kWThreads);
+    cfg.dynamicSmemBytes = kWSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    // pdl: a programmatic dependent of the kernel before it on the stream
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     if (w != nullptr) {
         cudaError_t e = ensure_wide_attribute<WorkList>();
         if (e != cudaSuccess) return e;
-        paged_decode_wide_kernel<WorkList><<<grid, kWThreads, kWSmemBytes, stream>>>(tk, tv, tq,
-                                                                                     p, *w);
-    } else {
-        cudaError_t e = ensure_wide_attribute<NoList>();
-        if (e != cudaSuccess) return e;
-        paged_decode_wide_kernel<NoList><<<grid, kWThreads, kWSmemBytes, stream>>>(
-            tk, tv, tq, p, NoList{0});
+        return cudaLaunchKernelEx(&cfg, paged_decode_wide_kernel<WorkList>, tk, tv, tq, p, *w);
     }
-    return cudaGetLastError();
+    cudaError_t e = ensure_wide_attribute<NoList>();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, paged_decode_wide_kernel<NoList>, tk, tv, tq, p, NoList{0});
 }
 
 }  // namespace oxd

@@ -180,7 +180,7 @@ oxd_status check_desc(const oxd_paged_decode_desc* d) {
     if (d->max_splits < 0 || d->force_splits < 0 || d->num_sms < 0)
         return OXD_ERR_INVALID_ARGUMENT;
     if (d->tensor_path != 0 && d->tensor_path != 1) return OXD_ERR_INVALID_ARGUMENT;
-    if (d->reserved != 0 || d->wait_timeout_ns < 0) return OXD_ERR_INVALID_ARGUMENT;
+    if ((d->pdl != 0 && d->pdl != 1) || d->wait_timeout_ns < 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d->shared_prefix_tokens < 0 || d->share_group < 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d->shared_prefix_tokens == 0 ? d->share_group != 0
                                      : (d->share_group < 2 || d->page_size < 1 ||
@@ -944,10 +944,14 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     const WorkList* inline_list = in_ws ? nullptr : plan->work;
+    // A programmatic dependent launch only where the decode kernel directly
+    // follows the caller's previous work on the stream (no copy or timing
+    // event of this run in between).
+    const bool pdl = d.pdl != 0 && plan->ev_before == nullptr && !(!bound && plan->upload);
     const cudaError_t le =
         plan->variant == kVariantWide
-            ? launch_decode_wide(tk, tv, tq, p, inline_list, plan->grid, s)
-            : launch_decode(plan->variant, tk, tv, p, inline_list, plan->grid, s);
+            ? launch_decode_wide(tk, tv, tq, p, inline_list, plan->grid, s, pdl)
+            : launch_decode(plan->variant, tk, tv, p, inline_list, plan->grid, s, pdl);
     if (le != cudaSuccess) return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;

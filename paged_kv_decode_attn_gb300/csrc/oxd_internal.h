@@ -172,17 +172,18 @@ uint32_t next_run_epoch();
 VariantShape variant_shape(int variant);
 cudaError_t variant_occupancy(int variant, int* ctas_per_sm);
 // `work` == nullptr: the units live in memory (p.units), and the kernel is
-// launched with a small parameter block.
+// launched with a small parameter block. pdl: launched as a programmatic
+// dependent of the kernel before it on the stream.
 cudaError_t launch_decode(int variant, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           const DecodeParams& p, const WorkList* work, int grid,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool pdl);
 // The tcgen05 variant for groups of 17..32 query heads (oxd_decode_wide.cu);
 // `tq` maps q as [B*Hq rows][128] with the 128-byte swizzle.
 VariantShape wide_shape();
 cudaError_t wide_occupancy(int* ctas_per_sm);
 cudaError_t launch_decode_wide(const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tq, const DecodeParams& p, const WorkList* w,
-                               int grid, cudaStream_t stream);
+                               int grid, cudaStream_t stream, bool pdl);
 // Uniform-state merge (the public entry point).
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 // Merge of the split (request, KV head) streams of a decode run, launched

@@ -53,6 +53,13 @@ __device__ __forceinline__ void cluster_sync_all() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same barrier, arriving without release semantics (this thread's
+// earlier writes need no ordering before the other CTAs pass it).
+__device__ __forceinline__ void cluster_sync_relaxed_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of
 // the cluster; release at cluster scope (orders this thread's earlier
 // writes, and those it has seen through a barrier, before the arrival).
@@ -180,6 +187,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Waits until the grids this one depends on programmatically have completed
+// and their memory operations are visible (a no-op for a plain launch).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

@@ -189,7 +189,7 @@ BAD_DESC = {
     "negative_prefix": dict(shared_prefix_tokens=-16, share_group=2),
     "negative_splits": dict(max_splits=-1),
     "tensor_path": dict(tensor_path=2),
-    "reserved": dict(reserved=1),
+    "pdl": dict(pdl=2),
     "negative_wait": dict(wait_timeout_ns=-5),
 }
 

@@ -356,26 +356,28 @@ def test_merge_of_split_partials_equals_decode():
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", W.CONFIG_ORDER)
-def test_full_size_workloads_on_sampled_heads(name):
+def test_full_size_workloads_on_every_head(name):
+    # Each of the five workloads at full size, in the benchmark's launch
+    # configuration (the plan bound to its workspace), element by element on
+    # every head (B * Hq rows of 128 and B * Hq LSEs) against the f64 oracle;
+    # a workload that declares shared prefixes also on the cascade plan.
     cfg = W.CONFIGS[name]
     case = W.make_case(cfg, device="cuda")
-    # the benchmark's launch configuration: the plan bound to its workspace
-    plan = plan_case(case)
-    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
-    oxd.oxd_plan_bind_workspace(plan, ws)
-    out, lse, plan, ws = run_decode(case, plan=plan, workspace=ws)
-    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-    rng = np.random.default_rng(cfg.seed)
-    L = case.tables.lengths
-    heads = {(int(b), int(h)) for b, h in zip(rng.integers(0, case.batch, 48),
-                                               rng.integers(0, case.num_qo_heads, 48))}
-    for b in (int(np.argmax(L)), int(np.argmin(L))):
-        heads |= {(b, 0), (b, case.num_qo_heads - 1)}
-    heads = sorted(heads)
-    ref_out, ref_lse = oracle_ref(case, heads=heads)
-    go, gl = gpu_heads(out, lse, heads)
-    assert_parity(go, ref_out, gl, ref_lse, name)
+    ref_out, ref_lse = oracle_ref(case)
+    assert ref_out.shape == (case.batch, case.num_qo_heads, 128)
+    plans = [{}]
+    if cfg.shared_prefix_tokens > 0:
+        plans.append(dict(shared_prefix_tokens=cfg.shared_prefix_tokens,
+                          share_group=cfg.share_group))
+    for kw in plans:
+        plan = plan_case(case, **kw)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        oxd.oxd_plan_bind_workspace(plan, ws)
+        out, lse, plan, ws = run_decode(case, plan=plan, workspace=ws)
+        assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+        if kw:
+            assert plan.info.cascade_units > 0
+        assert_parity(out, ref_out, lse, ref_lse, f"{name} {'cascade' if kw else 'plain'}")
 
 
 @pytest.mark.slow

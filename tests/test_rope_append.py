@@ -257,11 +257,19 @@ def test_decode_after_append_sees_the_new_tokens():
     lengths = [100, 257, 16, 1]
     add = [1, 1, 1, 1]
     case = _grown_case(lengths, add, 4, 2, 16, "NHD", seed=13)
+    k_before, v_before = _bits(case.k), _bits(case.v)
     q, k, v, tr, pos = _append_inputs(lengths, add, 8, 2, seed=8)
     refcount = torch.ones(case.tables.num_pages, dtype=torch.int32, device="cuda")
     q_rot, status = _run_append(case, q, k, v, tr, pos, refcount)
     assert status == oxd.OXD_DEVICE_OK
     case.q.copy_(q_rot)  # one new token per request, in request order
-    ref_out, ref_lse = oracle_ref(case)
+    # the oracle's inputs are the oracle's own append of the same tokens to
+    # host copies of the pools taken before the GPU append
+    rq, rk, rv, st = _oracle_append(case, k_before, v_before, q, k, v, tr, pos, refcount)
+    assert (st == oracle.APPEND_WRITTEN).all()
+    t = case.tables
+    ref_out, ref_lse = oracle.paged_decode(rq, rk, rv, t.indptr, t.indices, t.last_page_len,
+                                           num_kv_heads=2, page_size=16, layout=0,
+                                           sm_scale=case.sm_scale)
     out, lse, _, _ = run_decode(case)
     assert_parity(out, ref_out, lse, ref_lse, "decode after append")
