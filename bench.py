@@ -111,6 +111,13 @@ def parse_args(argv=None):
                     help="skip the every-head comparison with the f64 oracle")
     ap.add_argument("--no-workloads", action="store_true",
                     help="measure only --config (not the other workloads)")
+    ap.add_argument("--record-traffic", nargs=2, metavar=("KEY", "CSV"), default=None,
+                    help="no GPU work: read the DRAM bytes of the first paged_decode launch in "
+                         "an ncu --csv log of this benchmark and store them in "
+                         "profiles/traffic.json under KEY (<workload> or <workload>+cascade), "
+                         "keyed to the current decode sources; with --batch, the capture ran "
+                         "on that many requests and is scaled to the whole workload by the "
+                         "decode kernel's algorithmic bytes")
     ap.add_argument("--prefill-config", default="prefill_gqa4_b8_q2048_kv2048to16384_ps16_nhd",
                     choices=W.PREFILL_ORDER)
     ap.add_argument("--max-splits", type=int, default=0,
@@ -286,6 +293,95 @@ def source_hash(csrc=None):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode() + " ".join(strip_comments(f.read()).split()).encode())
     return h.hexdigest()[:16]
+
+
+def ncu_csv_metrics(path, kernel_regex="paged_decode"):
+    """Metric name -> value (bytes, or us for durations) of the first launch of a
+    kernel matching kernel_regex in an `ncu --csv` log."""
+    import csv
+    import io
+    import re
+
+    txt = open(path).read()
+    rows = list(csv.DictReader(io.StringIO(txt[txt.find('"ID"'):])))
+    first, vals = None, {}
+    for r in rows:
+        if not re.search(kernel_regex, r["Kernel Name"]):
+            continue
+        first = first if first is not None else r["ID"]
+        if r["ID"] != first:
+            break
+        unit, v = r["Metric Unit"], float(r["Metric Value"].replace(",", ""))
+        vals[r["Metric Name"]] = v * {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9,
+                                      "nsecond": 1e-3, "usecond": 1, "msecond": 1e3}.get(unit, 1)
+        vals["kernel"] = r["Kernel Name"]
+    if not vals:
+        raise ValueError(f"no {kernel_regex} launch in {path}")
+    return vals
+
+
+def decode_kernel_bytes(cfg, batch=None):
+    """Algorithmic bytes of one decode-kernel launch: the KV bytes it streams
+    (a cascade plan's decode kernel skips the shared prefixes of the requests
+    it decodes as prefix + suffix; the planner's rule, recomputed on the host)."""
+    t = W.make_tables(cfg, batch=batch)
+    row = cfg.num_kv_heads * cfg.head_dim * 2 * 2
+    return int(t.lengths.sum()) * row
+
+
+def record_traffic(key, csv_path, batch=None):
+    """Store one capture in profiles/traffic.json (see --record-traffic)."""
+    name, _, plan = key.partition("+")
+    cfg = W.CONFIGS[name]
+    v = ncu_csv_metrics(csv_path)
+    rd, wr = v["dram__bytes_read.sum"], v["dram__bytes_write.sum"]
+    entry = {"source_hash": source_hash(), "kernel": v["kernel"][:80],
+             "duration_us_under_ncu": v.get("gpu__time_duration.sum")}
+    if batch:
+        # the capture ran on the first `batch` requests: scale by the bytes the
+        # decode kernel streams (traffic grows with the pages streamed)
+        full, part = decode_kernel_bytes(cfg), decode_kernel_bytes(cfg, batch)
+        if plan == "cascade":
+            full, part = cascade_suffix_bytes(cfg), cascade_suffix_bytes(cfg, batch)
+        s = full / part
+        entry.update(dram_bytes_per_launch=int((rd + wr) * s), dram_read=int(rd * s),
+                     dram_write=int(wr * s), captured_read=int(rd), captured_write=int(wr),
+                     captured_algorithmic_bytes=part, full_algorithmic_bytes=full,
+                     capture=f"first {batch} requests, one launch; bytes scaled to the whole "
+                             f"batch by the decode kernel's algorithmic bytes (x {s:.4f})")
+    else:
+        entry.update(dram_bytes_per_launch=int(rd + wr), dram_read=int(rd), dram_write=int(wr),
+                     capture="full-size workload, one launch")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        d = {}
+    d[key] = entry
+    with open(path, "w") as f:
+        json.dump(d, f, indent=1)
+        f.write("\n")
+    print(json.dumps({key: entry}))
+    return 0
+
+
+def cascade_suffix_bytes(cfg, batch=None):
+    """Bytes a cascade plan's decode kernel streams: every request's pages after
+    the shared prefix when it is decoded as prefix + suffix (longer than the
+    prefix, in a group with at least two such requests), else all of them."""
+    t = W.make_tables(cfg, batch=batch)
+    L = t.lengths
+    P, S = cfg.shared_prefix_tokens, cfg.share_group
+    tok = 0
+    for g0 in range(0, len(L), S):
+        grp = L[g0:g0 + S]
+        members = grp > P
+        if members.sum() >= 2:
+            tok += int((grp[members] - P).sum() + grp[~members].sum())
+        else:
+            tok += int(grp.sum())
+    return tok * cfg.num_kv_heads * cfg.head_dim * 2 * 2
 
 
 def recorded_traffic(workload):
@@ -1133,6 +1229,8 @@ def run_prefill(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.record_traffic:
+        return record_traffic(args.record_traffic[0], args.record_traffic[1], args.batch)
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "rope_append":
