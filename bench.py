@@ -313,7 +313,8 @@ def ncu_csv_metrics(path, kernel_regex="paged_decode"):
             break
         unit, v = r["Metric Unit"], float(r["Metric Value"].replace(",", ""))
         vals[r["Metric Name"]] = v * {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9,
-                                      "nsecond": 1e-3, "usecond": 1, "msecond": 1e3}.get(unit, 1)
+                                      "ns": 1e-3, "nsecond": 1e-3, "us": 1, "usecond": 1,
+                                      "ms": 1e3, "msecond": 1e3}.get(unit, 1)
         vals["kernel"] = r["Kernel Name"]
     if not vals:
         raise ValueError(f"no {kernel_regex} launch in {path}")
