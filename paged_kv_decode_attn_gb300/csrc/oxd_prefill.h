@@ -8,9 +8,7 @@
 
 namespace oxd {
 
-constexpr int kPrefillRows = 256;         // rows of a tile: tile_tokens * G (<= 256), two
-                                          // halves of 128 MMA rows
-constexpr int kMaxPrefillGroup = 128;     // G = Hq / Hkv of a prefill
+constexpr int kPrefillRows = 128;         // MMA rows of a tile: tile_tokens * G (<= 128)
 constexpr int kPrefillStageTokens = 64;   // cached tokens per pipeline stage
 
 // One CTA's work: a piece of the cached-token range of one tile (up to
@@ -38,7 +36,7 @@ struct PrefillUnit {
 static_assert(sizeof(PrefillUnit) == 64, "units are 64 bytes");
 
 struct PrefillParams {
-    const uint16_t* q;              // bf16 [Nq][Hq][128]
+    const uint16_t* q;              // bf16 [Nq][Hq][128] (read through the tensor map)
     uint16_t* out;                  // bf16 [Nq][Hq][128]
     float* lse;                     // [Nq][Hq] or nullptr
     const int32_t* qo_indptr;       // nullptr: rows are not checked against one (cascade)
@@ -74,10 +72,12 @@ struct PrefillParams {
 
 cudaError_t prefill_smem_bytes(int* bytes);
 cudaError_t prefill_occupancy(int* ctas_per_sm);
-// tk, tv: the pool maps (as for decode).
+// tk, tv: the pool maps (as for decode); tq: q as (d, head, token) with a
+// box of 64 x G x tile_tokens and the 128-byte swizzle.
 // early: launched with programmatic dependent launch behind the previous
 // kernel on the stream (then p.wait_prior must be 1).
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                           int grid, cudaStream_t stream, bool early = false);
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                           const PrefillParams& p, int grid, cudaStream_t stream,
+                           bool early = false);
 
 }  // namespace oxd

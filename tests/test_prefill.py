@@ -79,31 +79,12 @@ def check_all(run: Prefill, what):
 
 @pytest.mark.parametrize("G,Hkv", [(1, 4), (2, 4), (4, 8), (8, 2), (32, 1), (3, 2), (128, 1)])
 def test_group_sizes(G, Hkv):
-    # tile_tokens = 256 // G: 256, 128, 64, 32, 8, 85 (one row idle), 2
+    # tile_tokens = 128 // G: 128, 64, 32, 16, 4, 42 (two rows idle), 1
     case = W.prefill_case((70, 1, 33), (300, 64, 33), G * Hkv, Hkv, 16, "NHD", seed=G,
                           device="cuda")
     run = Prefill(case)
     run.run()
     check_all(run, f"G={G}")
-
-
-@pytest.mark.parametrize("G,Hkv,q_lens,kv_lens,max_splits", [
-    (1, 2, (200, 129), (300, 129), 1),      # both halves, the second partly filled
-    (1, 2, (256,), (4096,), 64),            # last pieces wholly past the first half's rows
-    (3, 2, (85, 43, 44), (900, 43, 500), 0),  # a token's heads straddle the halves
-    (4, 8, (64, 40), (5000, 41), 0),        # a GQA4 tile: 32 tokens a half
-    (128, 1, (2, 1, 3), (600, 1, 3), 0),    # one token a half
-])
-def test_tile_halves(G, Hkv, q_lens, kv_lens, max_splits):
-    # A tile is 256 rows in two halves of 128 MMA rows; each half streams the
-    # piece's stages up to its own last position and writes its own rows.
-    case = W.prefill_case(q_lens, kv_lens, G * Hkv, Hkv, 16, "NHD", seed=G + len(q_lens),
-                          device="cuda")
-    run = Prefill(case, max_splits=max_splits)
-    if max_splits == 64:
-        assert run.plan.info.max_pieces > 8
-    run.run()
-    check_all(run, f"G={G} halves {q_lens}/{kv_lens}")
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
