@@ -272,13 +272,13 @@ __global__ void __launch_bounds__(kWThreads)
                 int okw = 1;
                 if (lane == 0) {
                     if (g >= kWStages)
-                        okw = mbar_wait(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags, p.wait_ns)
+                        okw = mbar_wait_tc(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags, p.wait_ns)
                                   ? 1
                                   : 0;
                     // the query tile is rewritten only after the previous
                     // unit's last score MMA has read it
                     if (okw && s == 0 && started > 0)
-                        okw = mbar_wait(&ctl.q_free, (started - 1) & 1, flags, p.wait_ns) ? 1 : 0;
+                        okw = mbar_wait_tc(&ctl.q_free, (started - 1) & 1, flags, p.wait_ns) ? 1 : 0;
                 }
                 if (!__shfl_sync(0xffffffffu, okw, 0)) {
                     ok = false;
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kWThreads)
             int okw = 1;
             if (lane == 0) {
                 if (g >= kWStages)
-                    okw = mbar_wait(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags, p.wait_ns)
+                    okw = mbar_wait_tc(&ctl.empty[slot], ((g / kWStages) + 1) & 1, flags, p.wait_ns)
                                   ? 1
                                   : 0;
                 if (okw) {
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kWThreads)
             if (issued_any) {
                 // every MMA completes before the tensor memory is released
                 umma_commit(&ctl.mma_done);
-                mbar_wait(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
+                mbar_wait_tc(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
             }
         }
         __syncwarp();
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kWThreads)
         // lanes always take the same path through the collective TMEM
         // instructions.
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity, flags, p.wait_ns));
+            return __all_sync(0xffffffffu, mbar_wait_tc(bar, parity, flags, p.wait_ns));
         };
         const float sc = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(kWThreads)
         // Aborted: wait (bounded) for the copies already issued, then leave.
         for (int s = 0; s < kWStages; ++s)
             if (ctl.issued[s] > 0)
-                mbar_wait(&ctl.full[s], (ctl.issued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
+                mbar_wait_tc(&ctl.full[s], (ctl.issued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
     }
     if (warp == 1) {
         tc_fence_after();

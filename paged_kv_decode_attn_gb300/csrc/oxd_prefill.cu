@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kPThreads)
             }
             int okw = 1;
             if (lane == 0 && s >= n_slots)
-                okw = mbar_wait(&empty[slot], ((s / n_slots) + 1) & 1, flags, p.wait_ns) ? 1 : 0;
+                okw = mbar_wait_tc(&empty[slot], ((s / n_slots) + 1) & 1, flags, p.wait_ns) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, okw, 0)) {
                 ok = false;
                 break;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kPThreads)
             }
             // every MMA completes before the tensor memory is released
             umma_commit(&ctl.mma_done);
-            mbar_wait(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
+            mbar_wait_tc(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
         }
         __syncwarp();
     } else {
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kPThreads)
         // are AND-ed over the warp so the collective TMEM instructions see
         // one path.
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity, flags, p.wait_ns));
+            return __all_sync(0xffffffffu, mbar_wait_tc(bar, parity, flags, p.wait_ns));
         };
         const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
         const int r = threadIdx.x;  // 0 .. 127
@@ -525,10 +525,10 @@ __global__ void __launch_bounds__(kPThreads)
         // Aborted: wait (bounded) for the copies already issued, then leave.
         for (int s = 0; s < kPKStages; ++s)
             if (ctl.kissued[s] > 0)
-                mbar_wait(&ctl.kfull[s], (ctl.kissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
+                mbar_wait_tc(&ctl.kfull[s], (ctl.kissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
         for (int s = 0; s < kPVStages; ++s)
             if (ctl.vissued[s] > 0)
-                mbar_wait(&ctl.vfull[s], (ctl.vissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
+                mbar_wait_tc(&ctl.vfull[s], (ctl.vissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
     }
     if (warp == 4) {
         tc_fence_after();

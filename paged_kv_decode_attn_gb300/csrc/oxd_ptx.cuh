@@ -152,6 +152,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// The same wait without the polled form, for the tcgen05 kernels: their MMA
+// thread checks the limit itself on every idle poll, so a short limit runs
+// out there; their other waits honour it to within try_wait's suspension.
+// (The polled branch cost their step about 0.5 us in 53, A/B.)
+__device__ __forceinline__ bool mbar_wait_tc(uint64_t* bar, uint32_t parity,
+                                             const volatile int* abort, long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort != nullptr && *abort) return false;
+        if (global_ns() - t0 > static_cast<uint64_t>(limit_ns)) return false;
+    }
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2, int c3) {
     asm volatile(
