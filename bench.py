@@ -829,7 +829,8 @@ def run_oxd(args):
         ref_out, ref_lse, t_pass = oracle_full(case, bits)
         ref = (ref_out, ref_lse)
         if check:
-            head["parity"] = parity_report(timed_out, timed_lse, ref_out, ref_lse)
+            head["parity"] = dict(parity_report(timed_out, timed_lse, ref_out, ref_lse),
+                                  oracle_ms=t_pass * 1e3, oracle_cores=os.cpu_count() or 1)
         if not args.no_cpu_baseline:
             cpu = cpu_baseline(case, bits, args.cpu_seconds, t_first=t_pass,
                                single_thread=cfg.name in ("mha8_b1_l512_ps16_nhd",
@@ -862,8 +863,9 @@ def run_oxd(args):
                                 args.warmup)
             par = None
             if check:
-                r_out, r_lse, _ = oracle_full(case2, oracle_inputs(case2))
-                par = parity_report(m2["out"], m2["lse"], r_out, r_lse)
+                r_out, r_lse, t_o = oracle_full(case2, oracle_inputs(case2))
+                par = dict(parity_report(m2["out"], m2["lse"], r_out, r_lse),
+                           oracle_ms=t_o * 1e3, oracle_cores=os.cpu_count() or 1)
             key = name + ("+cascade" if k2 == "cascade" else "")
             others[name] = dict(summary(case2, m2, peak, key, par), plan=k2)
             del m2, case2
