@@ -30,8 +30,10 @@ The kernel-only time comes from events the library records around the
 decode launch. ``warm_l2_us_per_step`` is the median of back-to-back steps
 with no flush in between. ``e2e`` repeats the step through the public API
 from pinned host buffers: H2D copies of q, the K/V pools and the block
-tables, the run, and the D2H read of out and lse, all inside the events.
-Clocks are sampled with nvidia-smi during the timed loop.
+tables, the run, and the D2H read of out and lse, all inside the events;
+``e2e_cache_resident`` does the same with the K/V pools left on the device
+(q and the tables up, out and lse back). Clocks are sampled with nvidia-smi
+during the timed loop.
 
 ``parity`` compares the timed run's out and lse with the f64 CPU oracle on
 every head (|out - ref| <= 1.5e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3);
@@ -819,6 +821,34 @@ def run_oxd(args):
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_ev), dev)
     if not torch.equal(out_h, out.cpu()):
         raise RuntimeError("e2e output mismatch")
+
+    # ---- the same with the K/V cache resident on the device (as a serving
+    # engine keeps it): only q and the block tables go up, out and lse come back
+    def e2e_resident_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dptr.copy_(host["indptr"], non_blocking=True)
+        dind.copy_(host["indices"], non_blocking=True)
+        dlast.copy_(host["last"], non_blocking=True)
+        oxd.oxd_paged_decode_run(plan, dq, case.k, case.v, dptr, dind, dlast, case.sm_scale,
+                                 out, lse, ws, plan.workspace_bytes, stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_resident_step()
+    r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n_e2e)]
+    for a, b in r_ev:
+        flush()
+        a.record(stream)
+        e2e_resident_step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    res_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in r_ev), dev)
+    if not torch.equal(out_h, out.cpu()):
+        raise RuntimeError("e2e (resident cache) output mismatch")
+    h2d_res = sum(host[n].numel() * host[n].element_size()
+                  for n in ("q", "indptr", "indices", "last"))
     del dq, dk, dv, dind, dptr, dlast
 
     # ---- parity of the timed run with the f64 oracle on every head, and the
@@ -895,7 +925,14 @@ def run_oxd(args):
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_gbs(uniq, world, e2e_ms), "unit": "GB/s",
                     "ms_per_step": e2e_ms, "steps": n_e2e,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "inputs": "q, both K/V pools and the block tables copied up every step"},
+            "e2e_cache_resident": {
+                "value": whole_job_gbs(uniq, world, res_ms), "unit": "GB/s",
+                "ms_per_step": res_ms, "steps": n_e2e, "h2d_bytes_per_step": h2d_res,
+                "d2h_bytes_per_step": d2h,
+                "inputs": "q and the block tables copied up every step; the K/V pools stay "
+                          "on the device, as a serving engine keeps its cache"},
             "gpu_launches": args.steps * info.launches_per_run,
             "clocks": clocks,
             "plan": {"kind": kind, "host_us": head["plan_host_us"], "work_list": args.work_list,
