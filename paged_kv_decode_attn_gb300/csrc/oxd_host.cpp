@@ -881,21 +881,9 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
         if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
     }
-    CUtensorMap tk, tv, tq, tq3;
+    CUtensorMap tk, tv, tq;
     if (!encode_pool(&tk, k_pages, d) || !encode_pool(&tv, v_pages, d)) return OXD_ERR_CUDA;
     if (plan->variant == kVariantWide && !encode_q(&tq, q, d)) return OXD_ERR_CUDA;
-    if (plan->casc_units > 0) {
-        // q [B][Hq][128] as (d, head, request) for the prefix tiles: a box is
-        // 64 columns x the G heads of one KV head x up to 128 / G requests
-        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim),
-                                  static_cast<uint64_t>(d.num_qo_heads),
-                                  static_cast<uint64_t>(d.batch)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
-                                     static_cast<uint64_t>(d.num_qo_heads) * kHeadDim * 2};
-        const uint32_t box[3] = {64, static_cast<uint32_t>(plan->group),
-                                 static_cast<uint32_t>(plan->casc_tile_tokens)};
-        if (!encode_bf16_map(&tq3, q, 3, dims, strides, box)) return OXD_ERR_CUDA;
-    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -991,7 +979,7 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         pp.scale_log2 = p.scale_log2;
         pp.wait_prior = 1;
         pp.wait_ns = p.wait_ns;
-        if (launch_prefill(tk, tv, tq3, pp, plan->casc_units, s,
+        if (launch_prefill(tk, tv, pp, plan->casc_units, s,
                            plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;
     }

@@ -7,26 +7,32 @@
 // tokens are its last q_len_b cached tokens; query token i sits at position
 // L_b - q_len_b + i and attends to cached tokens 0 .. that position.
 //
-// A tile is up to T = 128 / G consecutive query tokens of one request with
-// the G query heads of one KV head each: 128 MMA rows, row r = token r / G,
-// head r % G. One CTA runs one piece of a tile's cached-token range (a whole
-// range, or one of the pieces of a split tile); six warps:
-//   * producer (warp 5): on the first stage the tile's query rows through a
-//     3-D tensor map (d, head, token) with a box of 64 x G x T; per stage of
-//     64 cached tokens one TMA copy per (page, tensor, 64-column half) into a
-//     ring of stages, laid out [half][64 tokens][128 B] with the 128-byte
-//     swizzle;
-//   * MMA warp (warp 4, one thread): S = Q K^T into one of two TMEM score
-//     buffers (M = 128, N = 64, K = 128), then O += P V with P read from
-//     TMEM (N = 128, K = 64), each issued as soon as its inputs are ready;
-//   * softmax warps (warps 0-3): thread r of the warpgroup owns row r (TMEM
-//     lane r). Per stage it loads the row's 64 scores, masks the tokens past
-//     its position (and past the piece), keeps a running maximum that is
-//     raised only when a score exceeds it by more than 2^8 (then O is
-//     rescaled in TMEM, after the previous PV), writes P as bf16 over its
-//     scores and publishes it without waiting for the previous PV (the MMAs
-//     run in issue order), and at the end writes out/lse, or the F32 partial
-//     state of the piece.
+// A tile is up to T = 256 / G consecutive query tokens of one request with
+// the G query heads of one KV head each: 256 rows, row R = token R / G, head
+// R % G, in two halves of 128 MMA rows. One CTA (one a SM: it holds all 512
+// tensor-memory columns) runs one piece of a tile's cached-token range (a
+// whole range, or one of the pieces of a split tile); eleven warps:
+//   * K and V producers (warps 9, 10): per stage of 128 cached tokens one TMA
+//     copy per (page, 64-column half) into a two-stage ring, laid out
+//     [half][128 tokens][128 B] with the 128-byte swizzle; each stage serves
+//     both halves of the tile;
+//   * MMA warp (warp 8, issuing as a whole warp with one elected lane): per
+//     half h, S_h = Q_h K^T (M = 128, N = 128, K = 128; Q_h and K in shared
+//     memory) and O_h += P_h V (P_h from tensor memory; N = 128, K = 128) in a
+//     fixed order, so the tensor core works on one half while the other's
+//     softmax runs;
+//   * softmax warpgroups (warps 0-3 for half 0, 4-7 for half 1): thread r
+//     owns row r of its half (TMEM lane r). It first writes its query row
+//     into shared memory. Per stage it loads the row's 128 scores and writes
+//     P = 2^(s scale - m_ref) as bf16 pairs over the first 64 columns. A stage
+//     that every row of the half sees whole (after the first) takes one pass
+//     against the running reference m_ref, accepted when the row's sum shows
+//     no term above 2^64; the first stage, the masked ones and a refused pass
+//     take two (maximum, then P), masking the tokens past the row's position
+//     and past the piece, and raise m_ref when the maximum exceeds it by more
+//     than 2^8 (O_h is then rescaled in tensor memory: the score MMA's
+//     completion means the previous PV is done). At the end the warpgroup
+//     writes out/lse, or the F32 partial state of the piece.
 // V rows past the piece's last cached token are zeroed before its last PV.
 // Every wait is bounded (OXD_DEVICE_WAIT_TIMEOUT); on abort the MMAs and
 // copies in flight are drained before the tensor memory is released.
@@ -42,50 +48,66 @@
 namespace oxd {
 namespace {
 
-constexpr int kPKStages = 3;     // K ring: a slot is free once its score MMA is done
-constexpr int kPVStages = 2;     // V ring: a slot is free once its PV is done
-constexpr int kPThreads = 224;   // 4 softmax warps, MMA warp, K producer, V producer
-constexpr int kPSoftmaxThreads = 128;
-constexpr int kPHalf = kPrefillStageTokens * 128;  // one 64-column half of K or V: 8 KB
-constexpr int kPSlotBytes = 2 * kPHalf;            // K or V of one stage: 16 KB
-constexpr int kPQHalf = kPrefillRows * 128;        // 16 KB
-constexpr int kPQOff = 0;
-constexpr int kPKOff = 2 * kPQHalf;
+constexpr int kPKStages = 2;     // K ring: a slot is free once both halves' score MMAs are done
+constexpr int kPVStages = 2;     // V ring: a slot is free once both halves' PVs are done
+constexpr int kPMmaWarp = 8;
+constexpr int kPKWarp = 9;
+constexpr int kPVWarp = 10;
+constexpr int kPThreads = 11 * 32;
+constexpr int kPHalf = kPrefillStageTokens * 128;  // one 64-column half of K or V: 16 KB
+constexpr int kPSlotBytes = 2 * kPHalf;            // K or V of one stage: 32 KB
+constexpr int kPQHalf = 128 * 128;                 // 64 columns of a half's 128 query rows
+constexpr int kPQOff = 0;                          // Q of half h at 2 h kPQHalf: 64 KB
+constexpr int kPKOff = kPQOff + 4 * kPQHalf;
 constexpr int kPVOff = kPKOff + kPKStages * kPSlotBytes;
-constexpr int kPCtlOff = kPVOff + kPVStages * kPSlotBytes;  // 112 KB of operands
-constexpr uint32_t kPTmemCols = 256;  // O [0,128), S0 [128,192), S1 [192,256)
+constexpr int kPCtlOff = kPVOff + kPVStages * kPSlotBytes;  // 192 KB of operands
+// Tensor memory, 512 columns: per half h, O_h [128 h, 128 h + 128) and the
+// scores (then P, bf16 pairs in the first 64 columns) S_h [256 + 128 h, +128).
+constexpr uint32_t kPTmemCols = 512;
 static_assert(kPKOff % 1024 == 0 && kPVOff % 1024 == 0 && kPSlotBytes % 1024 == 0,
               "swizzle atoms aligned");
+static_assert(kPrefillStageTokens == 128, "score MMAs of N = 128, PV of K = 128");
+static_assert(kPrefillRows == 2 * 128, "a tile is two 128-row halves");
 
 struct PCtl {
     uint64_t kfull[kPKStages];
     uint64_t kempty[kPKStages];
     uint64_t vfull[kPVStages];
     uint64_t vempty[kPVStages];
-    uint64_t s_ready[2];
-    uint64_t p_ready[2];
-    uint64_t o_ready[4];  // PV(g) completes phase g / 4 of o_ready[g % 4]
+    uint64_t q_ready[2];  // a half's query rows are in shared memory (one arrival a warp)
+    uint64_t s_ready[2];  // QK_h(g) done: phase g of s_ready[h]
+    uint64_t p_ready[2];  // P_h(g) written: phase g of p_ready[h] (one arrival a warp)
+    uint64_t o_done[2];   // the half's last PV done
+    uint64_t vz;          // V rows past the piece zeroed (one arrival a warp)
     uint64_t mma_done;
     int kissued[kPKStages];
     int vissued[kPVStages];
     uint32_t tmem;
     int flags[4];  // [0] abort, [1] the unit is usable
 };
-// The dynamic shared memory starts 1024-byte aligned (checked in the kernel),
-// so no alignment slack: two CTAs fit one SM.
+// The dynamic shared memory starts 1024-byte aligned (checked in the kernel).
 constexpr int kPSmemBytes = kPCtlOff + static_cast<int>(sizeof(PCtl));
 
-__global__ void __launch_bounds__(kPThreads)
+// Stages a half streams of a piece: its rows see cached tokens up to the
+// position of its last query token.
+__device__ __forceinline__ int half_stages(const PrefillUnit& u, int G, int h) {
+    const int rows = u.n_tok * G;
+    if (rows <= 128 * h) return 0;  // the half holds no row of the tile
+    const int t_last = (min(rows, 128 * (h + 1)) - 1) / G;
+    const int end = min(u.kv_begin + u.kv_valid, u.p0 + t_last + 1);
+    return end > u.kv_begin ? (end - u.kv_begin + kPrefillStageTokens - 1) / kPrefillStageTokens
+                            : 0;
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v,
-                         const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
     PCtl& ctl = *reinterpret_cast<PCtl*>(sm + kPCtlOff);
     volatile int* flags = ctl.flags;
     const uint32_t s_base = smem_addr(sm);
-    const uint32_t s_q = s_base + kPQOff;
     auto ring_k = [&](int slot) { return s_base + kPKOff + slot * kPSlotBytes; };
     auto ring_v = [&](int slot) { return s_base + kPVOff + slot * kPSlotBytes; };
 
@@ -104,14 +126,30 @@ __global__ void __launch_bounds__(kPThreads)
             mbar_init(&ctl.vempty[s], 1);
             ctl.vissued[s] = 0;
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ctl.s_ready[i], 1);
-            mbar_init(&ctl.p_ready[i], 4);  // one arrival per softmax warp
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&ctl.q_ready[h], 4);
+            mbar_init(&ctl.s_ready[h], 1);
+            mbar_init(&ctl.p_ready[h], 4);
+            mbar_init(&ctl.o_done[h], 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&ctl.o_ready[i], 1);
+        mbar_init(&ctl.vz, 4);
         mbar_init(&ctl.mma_done, 1);
         flags[0] = 0;
         fence_mbar_init();
+    }
+    if (warp == kPMmaWarp) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_addr(&ctl.tmem)),
+            "r"(kPTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == kPKWarp && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    if (threadIdx.x == 0) {
         if (blockIdx.x == 0) {
             *p.last_epoch = p.epoch;
             if (p.clear_stamp != nullptr) *p.clear_stamp = 0ull;
@@ -128,7 +166,7 @@ __global__ void __launch_bounds__(kPThreads)
                  static_cast<int64_t>(u.kv_begin % ps + u.kv_valid) <=
                      static_cast<int64_t>(u.n_pages) * ps &&
                  u.b >= 0 && u.b < p.batch && u.hkv >= 0 && u.hkv < p.num_kv_heads &&
-                 u.n_tok >= 1 && u.n_tok <= T && u.q_begin >= 0 &&
+                 u.n_tok >= 1 && u.n_tok <= T && u.n_tok * G <= kPrefillRows && u.q_begin >= 0 &&
                  u.q_begin + u.n_tok <= p.n_q_tokens && u.p0 >= 0 && u.n_pieces >= 1 &&
                  u.piece >= 0 && u.piece < u.n_pieces;
             if (ok && u.n_pieces > 1)
@@ -142,39 +180,30 @@ __global__ void __launch_bounds__(kPThreads)
         }
         if (!ok) record_status(p.status, p.epoch, kDevicePlanMismatch);
         flags[1] = ok;
+        // The merge kernel, when the plan has one, may be scheduled now; it
+        // waits for this grid to complete before it reads anything.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
-    if (warp == 4) {
-        asm volatile(
-            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                smem_addr(&ctl.tmem)),
-            "r"(kPTmemCols)
-            : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    if (warp == 5 && lane == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
-        prefetch_tmap(&tmap_q);
-    }
-    // The merge kernel, when the plan has one, may be scheduled now; it waits
-    // for this grid to complete before it reads anything.
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl.tmem;
-    const uint32_t t_o = tmem;
-    auto t_s = [&](int buf) { return tmem + 128u + 64u * static_cast<uint32_t>(buf); };
+    auto t_o = [&](int h) { return tmem + 128u * static_cast<uint32_t>(h); };
+    auto t_s = [&](int h) { return tmem + 256u + 128u * static_cast<uint32_t>(h); };
+    auto s_q = [&](int h) { return s_base + kPQOff + 2u * kPQHalf * static_cast<uint32_t>(h); };
     const bool usable = flags[1] != 0;
     PrefillUnit u{};
     if (usable) u = p.units[blockIdx.x];
     const int n_st = usable ? (u.kv_valid + kPrefillStageTokens - 1) / kPrefillStageTokens : 0;
+    const int nst_h[2] = {usable ? half_stages(u, G, 0) : 0, usable ? half_stages(u, G, 1) : 0};
+    const int last_valid = n_st > 0 ? u.kv_valid - (n_st - 1) * kPrefillStageTokens : 0;
+    const bool need_vz = n_st > 0 && last_valid < kPrefillStageTokens;
 
-    if (warp >= 5) {
+    if (warp == kPKWarp || warp == kPVWarp) {
         // ================================================ producer warps
-        // warp 5: the query tile and K; warp 6: V. Lane 2j + h copies half h
-        // of page j of the stage.
-        const bool is_k = warp == 5;
+        // warp 9: K; warp 10: V. Lane 2j + c copies 64-column half c of page
+        // j of the stage. Every stage serves both halves of the tile.
+        const bool is_k = warp == kPKWarp;
         const int pps = kPrefillStageTokens / ps;  // pages per stage (divides 32)
         const int32_t* idx = p.indices + u.idx_begin;
         int win = 0, nxt = 0, win_base = 0;
@@ -209,19 +238,12 @@ __global__ void __launch_bounds__(kPThreads)
             }
             int okw = 1;
             if (lane == 0 && s >= n_slots)
-                okw = mbar_wait_tc(&empty[slot], ((s / n_slots) + 1) & 1, flags, p.wait_ns) ? 1 : 0;
+                okw = mbar_wait(&empty[slot], ((s / n_slots) + 1) & 1, flags, p.wait_ns) ? 1 : 0;
             if (!__shfl_sync(0xffffffffu, okw, 0)) {
                 ok = false;
                 break;
             }
-            if (lane == 0) {
-                const uint32_t qbytes = is_k && s == 0 ? 2u * 128u * G * p.tile_tokens : 0u;
-                mbar_arrive_expect_tx(&full[slot], npg * ps * kHeadDim * 2 + qbytes);
-                if (qbytes) {
-                    tma_load_3d(s_q, &tmap_q, &full[slot], 0, u.hkv * G, u.q_begin);
-                    tma_load_3d(s_q + kPQHalf, &tmap_q, &full[slot], 64, u.hkv * G, u.q_begin);
-                }
-            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], npg * ps * kHeadDim * 2);
             const int j = lane >> 1;
             const int page = __shfl_sync(0xffffffffu, win, (pg0 - win_base + j) & 31);
             if (lane < 2 * npg) {
@@ -244,272 +266,402 @@ __global__ void __launch_bounds__(kPThreads)
             flags[0] = 1;
             record_status(p.status, p.epoch, kDeviceWaitTimeout);
         }
-    } else if (warp == 4) {
+    } else if (warp == kPMmaWarp) {
         // ================================================ MMA warp
-        if (lane == 0 && n_st > 0) {
+        if (n_st > 0) {
             constexpr uint32_t kIdQK = umma_idesc(128, kPrefillStageTokens, 0);
             constexpr uint32_t kIdPV = umma_idesc(128, kHeadDim, 1);
-            // Two kinds of work, each issued as soon as its inputs are ready:
-            // the PV of stage gp (P written, V landed), checked first since it
-            // frees a V slot and the score buffer of stage gp + 2, and the
-            // score MMA of stage gq (K landed, its score buffer free). An idle
-            // poll naps briefly so the softmax warps keep the issue slots.
-            int gq = 0, gp = 0;
+            // Per half h: S_h = Q_h K^T (M = 128, N = 128 tokens, K = 128; both
+            // operands in shared memory) and O_h += P_h V (P_h from tensor
+            // memory; N = 128, K = 128 tokens). A fixed issue order with
+            // blocking waits: QK_0(0), QK_1(0), then for each stage g
+            // PV_0(g), QK_0(g + 1), PV_1(g), QK_1(g + 1). Within a half, QK_h(g + 1)
+            // comes after PV_h(g) because it overwrites S_h, which holds P_h(g)
+            // (MMAs from one thread run in issue order); across the halves the
+            // tensor core works on one half while the other's softmax runs. A K
+            // (V) slot is released once the last half that reads it has issued
+            // its QK (PV) of that stage. Descriptors are a base plus constant
+            // offsets (the start address field counts 16-byte units), so each
+            // group of eight MMAs issues back to back. The whole warp runs this
+            // loop (one elected lane issues), its waits agreed over the warp.
+            const uint64_t qd0[2] = {umma_sdesc(s_q(0), 16, 1024), umma_sdesc(s_q(1), 16, 1024)};
             bool ok = true;
-            uint64_t idle_since = global_ns();
-            while (gp < n_st) {
-                bool progress = false;
-                if (gp < gq && mbar_try_wait(&ctl.p_ready[gp & 1], (gp >> 1) & 1) &&
-                    mbar_try_wait(&ctl.vfull[gp % kPVStages], (gp / kPVStages) & 1)) {
-                    tc_fence_after();
-                    // O += P V: 16 tokens a step = two 8-row groups (1024 B apart);
-                    // the two 64-column halves of V are kPHalf apart
-                    const uint32_t v0 = ring_v(gp % kPVStages);
-                    for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks) {
-                        const uint64_t bd = umma_sdesc(v0 + ks * 2048, kPHalf, 1024);
-                        umma_ts(t_o, t_s(gp & 1) + 8u * ks, bd, kIdPV,
-                                (ks > 0 || gp > 0) ? 1u : 0u);
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                ok = __all_sync(0xffffffffu, ok && mbar_wait_tc(bar, parity, flags, p.wait_ns));
+                return ok;
+            };
+            const int n_max = max(nst_h[0], nst_h[1]);
+            for (int g = 0; g <= n_max && ok; ++g) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int gp = g - 1;  // the stage whose PV comes now
+                    if (gp >= 0 && gp < nst_h[h]) {
+                        if (!wait(&ctl.p_ready[h], gp & 1)) break;
+                        if (h == 0 || gp >= nst_h[0]) {  // the first half to read V(gp)
+                            if (!wait(&ctl.vfull[gp % kPVStages], (gp / kPVStages) & 1)) break;
+                            if (gp == n_st - 1 && need_vz && !wait(&ctl.vz, 0)) break;
+                        }
+                        tc_fence_after();
+                        // 16 tokens a step = two 8-row groups (1024 B apart); the
+                        // two 64-column halves of V are kPHalf apart
+                        const uint64_t vd0 = umma_sdesc(ring_v(gp % kPVStages), kPHalf, 1024);
+                        const uint32_t ps0 = t_s(h), po = t_o(h);
+#pragma unroll
+                        for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks)
+                            umma_ts_warp(po, ps0 + 8u * ks,
+                                         vd0 + static_cast<uint64_t>(ks * 2048 >> 4), kIdPV,
+                                         (ks > 0 || gp > 0) ? 1u : 0u);
+                        if (gp == nst_h[h] - 1) umma_commit_warp(&ctl.o_done[h]);
+                        if (h == 1 || gp >= nst_h[1])  // the last half to read V(gp)
+                            umma_commit_warp(&ctl.vempty[gp % kPVStages]);
                     }
-                    umma_commit(&ctl.vempty[gp % kPVStages]);
-                    umma_commit(&ctl.o_ready[gp & 3]);
-                    ++gp;
-                    progress = true;
-                }
-                if (gq < n_st && gq < gp + 2 &&
-                    mbar_try_wait(&ctl.kfull[gq % kPKStages], (gq / kPKStages) & 1)) {
-                    tc_fence_after();
-                    // S = Q K^T: K = 128 in steps of 16 (32 bytes of a 128-byte
-                    // swizzled row; columns 64..127 in the other half)
-                    const uint32_t k0 = ring_k(gq % kPKStages);
-                    for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-                        const uint32_t h = static_cast<uint32_t>(ks >> 2), kk = ks & 3;
-                        const uint64_t ad = umma_sdesc(s_q + h * kPQHalf + kk * 32, 16, 1024);
-                        const uint64_t bd = umma_sdesc(k0 + h * kPHalf + kk * 32, 16, 1024);
-                        umma_ss(t_s(gq & 1), ad, bd, kIdQK, ks > 0 ? 1u : 0u);
+                    if (g < nst_h[h]) {
+                        if (g == 0 && !wait(&ctl.q_ready[h], 0)) break;
+                        if ((h == 0 || g >= nst_h[0]) &&
+                            !wait(&ctl.kfull[g % kPKStages], (g / kPKStages) & 1))
+                            break;
+                        tc_fence_after();
+                        // K = 128 in steps of 16: 32 bytes of a 128-byte swizzled
+                        // row; columns 64..127 in the other half
+                        const uint64_t kd0 = umma_sdesc(ring_k(g % kPKStages), 16, 1024);
+                        const uint32_t sd = t_s(h);
+#pragma unroll
+                        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                            const int c = ks >> 2, kk = ks & 3;
+                            umma_ss_warp(sd,
+                                         qd0[h] + static_cast<uint64_t>((c * kPQHalf + kk * 32) >> 4),
+                                         kd0 + static_cast<uint64_t>((c * kPHalf + kk * 32) >> 4),
+                                         kIdQK, ks > 0 ? 1u : 0u);
+                        }
+                        umma_commit_warp(&ctl.s_ready[h]);
+                        if (h == 1 || g >= nst_h[1])  // the last half to read K(g)
+                            umma_commit_warp(&ctl.kempty[g % kPKStages]);
                     }
-                    umma_commit(&ctl.s_ready[gq & 1]);
-                    umma_commit(&ctl.kempty[gq % kPKStages]);  // K of the slot is consumed
-                    ++gq;
-                    progress = true;
-                }
-                if (progress) {
-                    idle_since = global_ns();
-                } else {
-                    __nanosleep(32);
-                }
-                if (!progress && (flags[0] ||
-                           global_ns() - idle_since > static_cast<uint64_t>(p.wait_ns))) {
-                    ok = false;
-                    break;
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 flags[0] = 1;
                 record_status(p.status, p.epoch, kDeviceWaitTimeout);
             }
             // every MMA completes before the tensor memory is released
-            umma_commit(&ctl.mma_done);
-            mbar_wait_tc(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
+            umma_commit_warp(&ctl.mma_done);
+            mbar_wait(&ctl.mma_done, 0, nullptr, kWaitTimeoutNs);
         }
         __syncwarp();
     } else {
-        // ================================================ softmax warps
-        // Thread r (< 128) owns row r = TMEM lane r; warp w reads lanes
-        // [32w, 32w + 32). Every lane waits on each barrier itself; results
-        // are AND-ed over the warp so the collective TMEM instructions see
-        // one path.
+        // ================================================ softmax warpgroups
+        // Warpgroup h (warps 4h .. 4h + 3) owns half h of the tile; thread r of
+        // the warpgroup owns row 128 h + r of the tile, TMEM lane r (warp w
+        // reads lanes [32 (w % 4), +32)). Every lane waits on each barrier
+        // itself; results are AND-ed over the warp so the collective TMEM
+        // instructions see one path.
         auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait_tc(bar, parity, flags, p.wait_ns));
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, flags, p.wait_ns));
         };
-        const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-        const int r = threadIdx.x;  // 0 .. 127
-        const int t = r / G, gi = r - (r / G) * G;
-        const bool row_ok = r < G * p.tile_tokens && t < u.n_tok;
+        const int h = warp >> 2;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const int r = threadIdx.x & 127;
+        const int R = 128 * h + r;  // row of the tile: token R / G, head R % G
+        const int t = R / G, gi = R - (R / G) * G;
+        const bool row_ok = usable && t < u.n_tok;
         const int pos = row_ok ? u.p0 + t : (1 << 30);  // padding rows see everything
+        const int nst = nst_h[h];
+        // the half's query rows into shared memory (once; zeros past the
+        // tile), laid out as the score MMA's A operand: two 64-column halves
+        // of [128 rows][128 B] with the 128-byte swizzle (16-byte chunk j of
+        // row r at chunk j ^ (r % 8))
+        if (nst > 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.q + (static_cast<size_t>(u.q_begin + (row_ok ? t : 0)) * p.num_qo_heads +
+                       u.hkv * G + (row_ok ? gi : 0)) *
+                          kHeadDim);
+            uint8_t* qs = sm + kPQOff + 2 * kPQHalf * h + r * 128;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint4 w = row_ok ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(qs + (i >> 3) * kPQHalf + (((i & 7) ^ (r & 7)) << 4)) = w;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.q_ready[h]);
+        }
+        // the half's first row position: a stage ending at or before it is
+        // seen whole by every row of the half
+        const int p_first = usable ? u.p0 + (128 * h) / G : 0;
+        // the half with the tile's last rows streams every stage of the piece;
+        // its warps zero V rows past the piece
+        const bool zeroes = need_vz && h == (usable && u.n_tok * G > 128 ? 1 : 0);
         const float sc = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int g = 0; g < n_st; ++g) {
-            if (!wait_all(&ctl.s_ready[g & 1], (g >> 1) & 1)) {
+        for (int g = 0; g < nst; ++g) {
+            if (!wait_all(&ctl.s_ready[h], g & 1)) {
                 ok = false;
                 break;
             }
+            // s_ready(g) also means every MMA issued before QK_h(g) is done,
+            // PV_h(g - 1) among them: O_h is up to date and P_h(g - 1) read
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld64(t_s(g & 1) + lane_off, sr);
             const int base = u.kv_begin + g * kPrefillStageTokens;
             const int nvalid = min(kPrefillStageTokens, u.kv_valid - g * kPrefillStageTokens);
-            // A stage that ends at or before the tile's first position is seen
-            // whole by every row (the same for the whole CTA): no mask, the
-            // maximum is taken over the raw scores and the scale is folded
-            // into the exponent's FMA. Otherwise scores are scaled and masked
-            // first.
+            // A stage that ends at or before the half's first position is seen
+            // whole by every row (the same for the whole warpgroup): no mask,
+            // the maximum is taken over the raw scores and the scale is folded
+            // into the exponent's FMA. Otherwise scores are scaled and masked.
             const bool whole = nvalid == kPrefillStageTokens &&
-                               base + kPrefillStageTokens - 1 <= u.p0 && sc > 0.f;
-            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (whole) {
-#pragma unroll
-                for (int j = 0; j < 64; j += 2)
-                    mq[(j >> 1) & 3] = max3(mq[(j >> 1) & 3], __uint_as_float(sr[j]),
-                                            __uint_as_float(sr[j + 1]));
-            } else {
-                const int lim = min(nvalid, pos - base + 1);  // visible columns of this row
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float x = j < lim ? __uint_as_float(sr[j]) * sc : -INFINITY;
-                    sr[j] = __float_as_uint(x);
-                    mq[j & 3] = fmaxf(mq[j & 3], x);
-                }
-            }
-            float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            if (whole) mx *= sc;
-            float alpha = 1.f;
-            bool rescale = false;
-            if (g == 0) {
-                m_ref = mx;
-            } else if (mx > m_ref + 8.f) {
-                alpha = fast_exp2(m_ref - mx);  // 0 while nothing was visible
-                m_ref = mx;
-                l *= alpha;
-                rescale = true;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t pk[32];
+                               base + kPrefillStageTokens - 1 <= p_first && sc > 0.f;
+            const int lim = min(nvalid, pos - base + 1);  // visible columns of this row
             float lq[4] = {0.f, 0.f, 0.f, 0.f};
-            if (whole) {
+            bool rescale = false;
+            float alpha = 1.f;
+            bool done = false;
+            if (whole && g > 0) {
+                // One pass against the running reference m_ref (no maximum): P =
+                // 2^(s sc - m_ref) for 32 columns at a time (the next 32 loading
+                // meanwhile), kept in registers until the row's sum shows that no
+                // term exceeds 2^64 (nor is infinite); then P is bf16 and O and l
+                // are F32 well inside their range. Otherwise the two passes below
+                // run (the scores are still in tensor memory). The reference may
+                // lag the row's maximum: every term carries the same factor
+                // 2^(m - m_ref), which the final O / l cancels.
+                uint32_t pk[64];
+                uint32_t a[32], b[32];
+                auto chunk = [&](const uint32_t (&x)[32], int c) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float x0, x1;
-                    fma2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1]), sc, -m_use,
-                         x0, x1);
-                    const float p0 = fast_exp2(x0);
-                    const float p1 = fast_exp2(x1);
-                    add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
-                    pk[j] = pack_bf16x2(p0, p1);
+                    for (int j = 0; j < 16; ++j) {
+                        float x0, x1;
+                        fma2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]), sc, -m_ref,
+                             x0, x1);
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
+                        pk[16 * c + j] = pack_bf16x2(p0, p1);
+                    }
+                };
+                tmem_ld32_async(t_s(h) + lane_off, a);
+                tmem_ld_wait(a);
+                tmem_ld32_async(t_s(h) + lane_off + 32, b);
+                chunk(a, 0);
+                tmem_ld_wait(b);
+                tmem_ld32_async(t_s(h) + lane_off + 64, a);
+                chunk(b, 1);
+                tmem_ld_wait(a);
+                tmem_ld32_async(t_s(h) + lane_off + 96, b);
+                chunk(a, 2);
+                tmem_ld_wait(b);
+                chunk(b, 3);
+                const float ltot = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+                if (!__any_sync(0xffffffffu, !(ltot <= 0x1p64f))) {
+                    uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
+                    uint32_t (&p1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
+                    tmem_st32(t_s(h) + lane_off, p0);
+                    tmem_st32(t_s(h) + lane_off + 32, p1);
+                    done = true;
+                } else {
+                    lq[0] = lq[1] = lq[2] = lq[3] = 0.f;
                 }
-            } else {
+            }
+            if (!done) {
+                // Scores of tokens 0..63 stay in registers; those of 64..127 are
+                // read twice (for the maximum, then for P), which keeps the
+                // thread within its register share. P (bf16 pairs) goes to
+                // columns 0..63, over scores already read.
+                uint32_t s0[64];
+                tmem_ld64(t_s(h) + lane_off, s0);
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (whole) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = fast_exp2(__uint_as_float(sr[2 * j]) - m_use);
-                    const float p1 = fast_exp2(__uint_as_float(sr[2 * j + 1]) - m_use);
-                    lq[j & 3] += p0 + p1;
-                    pk[j] = pack_bf16x2(p0, p1);
+                    for (int j = 0; j < 64; j += 2)
+                        mq[(j >> 1) & 3] = max3(mq[(j >> 1) & 3], __uint_as_float(s0[j]),
+                                                __uint_as_float(s0[j + 1]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float x = j < lim ? __uint_as_float(s0[j]) * sc : -INFINITY;
+                        s0[j] = __float_as_uint(x);
+                        mq[j & 3] = fmaxf(mq[j & 3], x);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t s1[32];
+                    tmem_ld32(t_s(h) + lane_off + 64 + 32 * c, s1);
+                    if (whole) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2)
+                            mq[(j >> 1) & 3] = max3(mq[(j >> 1) & 3], __uint_as_float(s1[j]),
+                                                    __uint_as_float(s1[j + 1]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            mq[j & 3] = fmaxf(mq[j & 3], 64 + 32 * c + j < lim
+                                                             ? __uint_as_float(s1[j]) * sc
+                                                             : -INFINITY);
+                    }
+                }
+                float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                if (whole) mx *= sc;
+                if (g == 0) {
+                    m_ref = mx;
+                } else if (mx > m_ref + 8.f) {
+                    alpha = fast_exp2(m_ref - mx);  // 0 while nothing was visible
+                    m_ref = mx;
+                    l *= alpha;
+                    rescale = true;
+                }
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                {
+                    uint32_t pk[32];
+                    if (whole) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            float x0, x1;
+                            fma2(__uint_as_float(s0[2 * j]), __uint_as_float(s0[2 * j + 1]), sc,
+                                 -m_use, x0, x1);
+                            const float p0 = fast_exp2(x0);
+                            const float p1 = fast_exp2(x1);
+                            add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float p0 = fast_exp2(__uint_as_float(s0[2 * j]) - m_use);
+                            const float p1 = fast_exp2(__uint_as_float(s0[2 * j + 1]) - m_use);
+                            lq[j & 3] += p0 + p1;
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
+                    }
+                    tmem_st32(t_s(h) + lane_off, pk);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t s1[32], pk[16];
+                    tmem_ld32(t_s(h) + lane_off + 64 + 32 * c, s1);
+                    if (whole) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            float x0, x1;
+                            fma2(__uint_as_float(s1[2 * j]), __uint_as_float(s1[2 * j + 1]), sc,
+                                 -m_use, x0, x1);
+                            const float p0 = fast_exp2(x0);
+                            const float p1 = fast_exp2(x1);
+                            add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int t0 = 64 + 32 * c + 2 * j;
+                            const float x0 = t0 < lim ? __uint_as_float(s1[2 * j]) * sc : -INFINITY;
+                            const float x1 =
+                                t0 + 1 < lim ? __uint_as_float(s1[2 * j + 1]) * sc : -INFINITY;
+                            const float p0 = fast_exp2(x0 - m_use);
+                            const float p1 = fast_exp2(x1 - m_use);
+                            lq[j & 3] += p0 + p1;
+                            pk[j] = pack_bf16x2(p0, p1);
+                        }
+                    }
+                    tmem_st16(t_s(h) + lane_off + 32 + 16 * c, pk);
                 }
             }
             l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
-            tmem_st32(t_s(g & 1) + lane_off, pk);
-            tmem_wait_st();
-            // PV(g - 1) must be done before O is rescaled; without a rescale
-            // P(g) is published at once (PV(g) runs after PV(g - 1) anyway).
-            // Four o_ready barriers keep every parity wait unambiguous: PV
-            // (g + 3) cannot complete before this warp publishes P(g + 3),
-            // and PV(g - 5) is known done from the wait of two stages ago.
-            auto wait_pv = [&](int k) {
-                return wait_all(&ctl.o_ready[k & 3], (k >> 2) & 1);
-            };
             if (__any_sync(0xffffffffu, rescale)) {
-                if (g > 0 && !wait_pv(g - 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
-                    uint32_t o[64];
-                    tmem_ld64(t_o + lane_off + c0, o);
-                    uint32_t w0[32], w1[32];
+                // O_h holds PV_h through stage g - 1 (done, see above)
+#pragma unroll 1
+                for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o(h) + lane_off + c0, o);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        w0[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        w1[j] = __float_as_uint(__uint_as_float(o[32 + j]) * alpha);
-                    }
-                    tmem_st32(t_o + lane_off + c0, w0);
-                    tmem_st32(t_o + lane_off + c0 + 32, w1);
+                    for (int j = 0; j < 32; ++j)
+                        o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                    tmem_st32(t_o(h) + lane_off + c0, o);
                 }
-                tmem_wait_st();
             }
-            const bool last = g == n_st - 1;
-            if (last && nvalid < kPrefillStageTokens) {
+            tmem_wait_st();
+            const bool last = g == nst - 1;
+            if (last && zeroes) {
                 // zero V rows past the piece once its V landed (whole 128-byte
-                // rows, so the swizzle does not matter); PV(g - 2) was issued
-                // (QK(g) was), so this phase of vfull is the one for stage g
+                // rows, so the swizzle does not matter); PV_h(g - 1) is done,
+                // so V up to stage g - 1 landed and this phase of vfull is the
+                // one for stage g
                 if (!wait_all(&ctl.vfull[g % kPVStages], (g / kPVStages) & 1)) {
                     ok = false;
                     break;
                 }
                 uint8_t* v0 = sm + kPVOff + (g % kPVStages) * kPSlotBytes;
                 const int n16 = (kPrefillStageTokens - nvalid) * 16;
-                for (int i = r; i < n16; i += kPSoftmaxThreads) {
+                for (int i = r; i < n16; i += 128) {
                     const int row = nvalid + (i >> 4), c = i & 15;
                     *reinterpret_cast<uint4*>(v0 + (c >> 3) * kPHalf + row * 128 + (c & 7) * 16) =
                         make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.vz);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.p_ready[g & 1]);
-            // follow the o_ready phases two stages behind, off the critical path
-            if (g >= 2 && !wait_pv(g - 2)) {
-                ok = false;
-                break;
+            if (lane == 0) mbar_arrive(&ctl.p_ready[h]);
+        }
+        // ---- epilogue: O / l once the half's last PV is done; padding rows
+        // take part in the collective loads. A piece wholly past the half's
+        // rows leaves them an empty state (a split tile's merge weighs it 0).
+        if (ok && nst > 0 && !wait_all(&ctl.o_done[h], 0)) ok = false;
+        if (ok && (nst > 0 || (row_ok && u.n_pieces > 1))) {
+            tc_fence_after();
+            const bool seen = l > 0.f;  // a piece may lie wholly past a row's position
+            const float inv = seen ? 1.f / l : 0.f;
+            const float lse2 = seen ? m_ref + __log2f(l) : -INFINITY;
+            const int hq = u.hkv * G + gi;
+            for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
+                uint32_t o[64];
+                if (nst > 0) {
+                    tmem_ld64(t_o(h) + lane_off + c0, o);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) o[j] = 0u;
+                }
+                if (!row_ok) continue;
+                if (u.n_pieces == 1) {
+                    uint16_t* dst =
+                        p.out + (static_cast<size_t>(u.q_begin + t) * p.num_qo_heads + hq) *
+                                    kHeadDim + c0;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[j]) * inv,
+                                          __uint_as_float(o[j + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv,
+                                          __uint_as_float(o[j + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv,
+                                          __uint_as_float(o[j + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv,
+                                          __uint_as_float(o[j + 7]) * inv);
+                        *reinterpret_cast<uint4*>(dst + j) = w;
+                    }
+                } else {
+                    const size_t grp = static_cast<size_t>(u.state) +
+                                       static_cast<size_t>(t) * u.n_pieces + u.piece;
+                    float* dst = p.part_o + (grp * G + gi) * kHeadDim + c0;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) =
+                            make_float4(__uint_as_float(o[j]) * inv,
+                                        __uint_as_float(o[j + 1]) * inv,
+                                        __uint_as_float(o[j + 2]) * inv,
+                                        __uint_as_float(o[j + 3]) * inv);
+                }
             }
-            if (last) {
-                // ---- epilogue: O / l, once PV(g) is done
-                if (!wait_pv(g)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const bool seen = l > 0.f;  // a piece may lie wholly past a row's position
-                const float inv = seen ? 1.f / l : 0.f;
-                const float lse2 = seen ? m_ref + __log2f(l) : -INFINITY;
-                const int hq = u.hkv * G + gi;
-                for (int c0 = 0; c0 < kHeadDim; c0 += 64) {
-                    uint32_t o[64];
-                    tmem_ld64(t_o + lane_off + c0, o);
-                    if (!row_ok) continue;
-                    if (u.n_pieces == 1) {
-                        uint16_t* dst =
-                            p.out + (static_cast<size_t>(u.q_begin + t) * p.num_qo_heads + hq) *
-                                        kHeadDim + c0;
-#pragma unroll
-                        for (int j = 0; j < 64; j += 8) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[j]) * inv,
-                                              __uint_as_float(o[j + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv,
-                                              __uint_as_float(o[j + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv,
-                                              __uint_as_float(o[j + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv,
-                                              __uint_as_float(o[j + 7]) * inv);
-                            *reinterpret_cast<uint4*>(dst + j) = w;
-                        }
-                    } else {
-                        const size_t grp =
-                            static_cast<size_t>(u.state) +
-                            static_cast<size_t>(t) * u.n_pieces + u.piece;
-                        float* dst = p.part_o + (grp * G + gi) * kHeadDim + c0;
-#pragma unroll
-                        for (int j = 0; j < 64; j += 4)
-                            *reinterpret_cast<float4*>(dst + j) =
-                                make_float4(__uint_as_float(o[j]) * inv,
-                                            __uint_as_float(o[j + 1]) * inv,
-                                            __uint_as_float(o[j + 2]) * inv,
-                                            __uint_as_float(o[j + 3]) * inv);
-                    }
-                }
-                if (row_ok) {
-                    if (u.n_pieces == 1) {
-                        if (p.lse != nullptr)
-                            p.lse[static_cast<size_t>(u.q_begin + t) * p.num_qo_heads + hq] =
-                                lse2 * kLn2;
-                    } else {
-                        const size_t grp =
-                            static_cast<size_t>(u.state) +
-                            static_cast<size_t>(t) * u.n_pieces + u.piece;
-                        p.part_lse[grp * G + gi] = lse2;
-                    }
+            if (row_ok) {
+                if (u.n_pieces == 1) {
+                    if (p.lse != nullptr)
+                        p.lse[static_cast<size_t>(u.q_begin + t) * p.num_qo_heads + hq] =
+                            lse2 * kLn2;
+                } else {
+                    const size_t grp = static_cast<size_t>(u.state) +
+                                       static_cast<size_t>(t) * u.n_pieces + u.piece;
+                    p.part_lse[grp * G + gi] = lse2;
                 }
             }
         }
@@ -525,12 +677,12 @@ __global__ void __launch_bounds__(kPThreads)
         // Aborted: wait (bounded) for the copies already issued, then leave.
         for (int s = 0; s < kPKStages; ++s)
             if (ctl.kissued[s] > 0)
-                mbar_wait_tc(&ctl.kfull[s], (ctl.kissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
+                mbar_wait(&ctl.kfull[s], (ctl.kissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
         for (int s = 0; s < kPVStages; ++s)
             if (ctl.vissued[s] > 0)
-                mbar_wait_tc(&ctl.vfull[s], (ctl.vissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
+                mbar_wait(&ctl.vfull[s], (ctl.vissued[s] - 1) & 1, nullptr, kWaitTimeoutNs);
     }
-    if (warp == 4) {
+    if (warp == kPMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kPTmemCols)
@@ -577,12 +729,12 @@ cudaError_t prefill_occupancy(int* n) {
     const int by_smem = smem_sm / (kPSmemBytes + reserved);
     const int by_tmem = 512 / static_cast<int>(kPTmemCols);
     const int by_threads = 2048 / kPThreads;
-    *n = max(1, min(by_smem, min(by_tmem, by_threads)));
+    *n = max(1, min(by_smem, min(by_tmem, by_threads)));  // one CTA a SM
     return cudaSuccess;
 }
 
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, int grid, cudaStream_t stream, bool early) {
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           int grid, cudaStream_t stream, bool early) {
     if (grid < 1 || (early && !p.wait_prior)) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_prefill_attribute();
     if (e != cudaSuccess) return e;
@@ -596,7 +748,7 @@ cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = early ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tk, tv, tq, p);
+    return cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tk, tv, p);
 }
 
 }  // namespace oxd

@@ -8,8 +8,10 @@
 
 namespace oxd {
 
-constexpr int kPrefillRows = 128;         // MMA rows of a tile: tile_tokens * G (<= 128)
-constexpr int kPrefillStageTokens = 64;   // cached tokens per pipeline stage
+constexpr int kPrefillRows = 256;         // rows of a tile: tile_tokens * G (<= 256), two
+                                          // halves of 128 MMA rows
+constexpr int kMaxPrefillGroup = 128;     // G = Hq / Hkv of a prefill
+constexpr int kPrefillStageTokens = 128;  // cached tokens per pipeline stage
 
 // One CTA's work: a piece of the cached-token range of one tile (up to
 // tile_tokens consecutive query tokens of one request, with the G query heads
@@ -17,7 +19,7 @@ constexpr int kPrefillStageTokens = 64;   // cached tokens per pipeline stage
 struct PrefillUnit {
     int32_t idx_begin;  // offset in `indices` of the piece's first page
     int32_t n_pages;    // pages the piece reads
-    int32_t kv_begin;   // first cached token of the piece (a multiple of 64)
+    int32_t kv_begin;   // first cached token of the piece (a multiple of 128)
     int32_t kv_valid;   // cached tokens of the piece, >= 1
     int32_t q_begin;    // global index of the tile's first query token
     int32_t n_tok;      // query tokens of the tile, 1 .. tile_tokens
@@ -36,7 +38,7 @@ struct PrefillUnit {
 static_assert(sizeof(PrefillUnit) == 64, "units are 64 bytes");
 
 struct PrefillParams {
-    const uint16_t* q;              // bf16 [Nq][Hq][128] (read through the tensor map)
+    const uint16_t* q;              // bf16 [Nq][Hq][128]
     uint16_t* out;                  // bf16 [Nq][Hq][128]
     float* lse;                     // [Nq][Hq] or nullptr
     const int32_t* qo_indptr;       // nullptr: rows are not checked against one (cascade)
@@ -72,12 +74,10 @@ struct PrefillParams {
 
 cudaError_t prefill_smem_bytes(int* bytes);
 cudaError_t prefill_occupancy(int* ctas_per_sm);
-// tk, tv: the pool maps (as for decode); tq: q as (d, head, token) with a
-// box of 64 x G x tile_tokens and the 128-byte swizzle.
+// tk, tv: the pool maps (as for decode).
 // early: launched with programmatic dependent launch behind the previous
 // kernel on the stream (then p.wait_prior must be 1).
-cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
-                           const PrefillParams& p, int grid, cudaStream_t stream,
-                           bool early = false);
+cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                           int grid, cudaStream_t stream, bool early = false);
 
 }  // namespace oxd

@@ -55,7 +55,7 @@ struct oxd_prefill_plan_s {
 
 namespace {
 
-constexpr int kMinPieceStages = 2;  // a piece streams at least two stages (128 tokens)
+constexpr int kMinPieceStages = 1;  // a piece streams at least one stage (128 tokens)
 constexpr int kMaxPieces = 64;
 
 std::mutex g_mu;
@@ -76,7 +76,7 @@ oxd_status check_desc(const oxd_paged_prefill_desc& d) {
     if (d.head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
     if (d.page_size != 8 && d.page_size != 16 && d.page_size != 32 && d.page_size != 64)
         return OXD_ERR_UNSUPPORTED;
-    if (d.num_qo_heads / d.num_kv_heads > kPrefillRows) return OXD_ERR_UNSUPPORTED;
+    if (d.num_qo_heads / d.num_kv_heads > kMaxPrefillGroup) return OXD_ERR_UNSUPPORTED;
     if (d.num_pages >= (int64_t{1} << 31)) return OXD_ERR_UNSUPPORTED;
     return OXD_OK;
 }
@@ -386,22 +386,10 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
     if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
     if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
 
-    CUtensorMap tk, tv, tq;
+    CUtensorMap tk, tv;
     if (!encode_kv_pool(&tk, k_pages, d.layout, d.page_size, d.num_kv_heads, d.num_pages) ||
         !encode_kv_pool(&tv, v_pages, d.layout, d.page_size, d.num_kv_heads, d.num_pages))
         return OXD_ERR_CUDA;
-    {
-        // q as (d, head, token): a box is 64 columns x the G heads of one KV
-        // head x the tile's query tokens
-        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim),
-                                  static_cast<uint64_t>(d.num_qo_heads),
-                                  static_cast<uint64_t>(plan->nq)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
-                                     static_cast<uint64_t>(d.num_qo_heads) * kHeadDim * 2};
-        const uint32_t box[3] = {64, static_cast<uint32_t>(plan->group),
-                                 static_cast<uint32_t>(plan->tile_tokens)};
-        if (!encode_bf16_map(&tq, q, 3, dims, strides, box)) return OXD_ERR_CUDA;
-    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -448,7 +436,7 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_prefill(tk, tv, tq, p, plan->n_units, s) != cudaSuccess) return OXD_ERR_CUDA;
+    if (launch_prefill(tk, tv, p, plan->n_units, s) != cudaSuccess) return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->n_entries > 0) {

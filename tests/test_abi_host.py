@@ -492,26 +492,28 @@ def prefill_plan(q_lens, kv_lens, Hq=32, Hkv=8, ps=16, num_sms=152, **kw):
 
 
 def test_prefill_plan_tiles_and_pieces():
-    # the pages' shape: 32 + 64 query tokens, GQA4 -> 32-token tiles, 8 KV heads
+    # the pages' shape: 32 + 64 query tokens, GQA4 -> 64-token tiles (256 rows),
+    # 8 KV heads
     plan, *_ = prefill_plan((32, 64), (256, 1024))
     i = plan.info
-    assert i.tile_tokens == 32 and i.num_tiles == (1 + 2) * 8
+    assert i.tile_tokens == 64 and i.num_tiles == (1 + 1) * 8
     assert i.total_q_tokens == 96 and i.total_kv_tokens == 1280
     assert i.causal_pairs == 32 * 224 + 32 * 33 // 2 + 64 * 960 + 64 * 65 // 2
     assert i.num_units > i.num_tiles and i.launches_per_run == 2  # split to fill the GPU
-    assert i.num_merge_rows == i.num_split_tiles * 32 * 4 or i.num_split_tiles < i.num_tiles
+    # every tile split: one merged row per (query token, query head)
+    assert i.num_split_tiles == i.num_tiles and i.num_merge_rows == (32 + 64) * 32
     one, *_ = prefill_plan((32, 64), (256, 1024), max_splits=1)
-    assert one.info.num_units == 24 and one.info.launches_per_run == 1
+    assert one.info.num_units == 16 and one.info.launches_per_run == 1
     capped, *_ = prefill_plan((32, 64), (256, 1024), max_splits=2)
     assert capped.info.max_pieces == 2
     # enough tiles to fill the GPU: no split
     big, *_ = prefill_plan((2048,) * 8, [4096] * 8)
-    assert big.info.num_split_tiles == 0 and big.info.num_units == 8 * 64 * 8
+    assert big.info.num_split_tiles == 0 and big.info.num_units == 8 * 32 * 8
 
 
-@pytest.mark.parametrize("G,T", [(1, 128), (2, 64), (3, 42), (8, 16), (32, 4), (128, 1)])
+@pytest.mark.parametrize("G,T", [(1, 256), (2, 128), (3, 85), (8, 32), (32, 8), (128, 2)])
 def test_prefill_tile_tokens_follow_group(G, T):
-    plan, *_ = prefill_plan((T * 2 + 1,), (500,), Hq=G, Hkv=1)
+    plan, *_ = prefill_plan((T * 2 + 1,), (1000,), Hq=G, Hkv=1)
     assert plan.info.tile_tokens == T and plan.info.num_tiles == 3
 
 
@@ -628,11 +630,12 @@ def test_cascade_plan_counts_groups_and_shared_tokens():
 
 
 def test_cascade_groups_wider_than_a_tile_are_chunked():
-    # G = 8 -> 16 requests per prefix tile; a group of 40 needs three chunks
+    # G = 8 -> 32 requests per prefix tile (256 rows); a group of 40 needs two
+    # chunks
     plan, _, _ = host_plan([5000] * 40, Hq=64, Hkv=8, ps=16, shared_prefix_tokens=1024,
                            share_group=40)
-    assert plan.info.cascade_units == 3 * 8 and plan.info.cascade_requests == 40
-    assert plan.info.shared_kv_tokens == (40 - 3) * 1024
+    assert plan.info.cascade_units == 2 * 8 and plan.info.cascade_requests == 40
+    assert plan.info.shared_kv_tokens == (40 - 2) * 1024
 
 
 # ------------------------------------------------------------------ encoding limits

@@ -3,7 +3,9 @@
 Each case compares every output row (small cases) or sampled rows (the full
 workloads, in the launch configuration the benchmark times) with the oracle:
 |out - ref| <= 1.5e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3. The cases cover
-group sizes that fill a 128-row tile exactly and ones that leave rows idle,
+group sizes that fill a 256-row tile (two halves of 128) exactly and ones that
+leave rows idle, the halves partly filled and a token's heads straddling them,
+scores that jump or drop by large amounts between 128-token stages,
 NHD and HND pages of every page size, query counts of zero, one, a tile, a
 tile plus one and the whole cache, split and unsplit tiles, a bound workspace
 (bitwise equal to unbound runs) and a CUDA-graph replay, and the device
@@ -79,12 +81,31 @@ def check_all(run: Prefill, what):
 
 @pytest.mark.parametrize("G,Hkv", [(1, 4), (2, 4), (4, 8), (8, 2), (32, 1), (3, 2), (128, 1)])
 def test_group_sizes(G, Hkv):
-    # tile_tokens = 128 // G: 128, 64, 32, 16, 4, 42 (two rows idle), 1
+    # tile_tokens = 256 // G: 256, 128, 64, 32, 8, 85 (one row idle), 2
     case = W.prefill_case((70, 1, 33), (300, 64, 33), G * Hkv, Hkv, 16, "NHD", seed=G,
                           device="cuda")
     run = Prefill(case)
     run.run()
     check_all(run, f"G={G}")
+
+
+@pytest.mark.parametrize("G,Hkv,q_lens,kv_lens,max_splits", [
+    (1, 2, (200, 129), (300, 129), 1),      # both halves, the second partly filled
+    (1, 2, (256,), (4096,), 64),            # last pieces wholly past the first half's rows
+    (3, 2, (85, 43, 44), (900, 43, 500), 0),  # a token's heads straddle the halves
+    (4, 8, (64, 40), (5000, 41), 0),        # a GQA4 tile: 32 tokens a half
+    (128, 1, (2, 1, 3), (600, 1, 3), 0),    # one token a half
+])
+def test_tile_halves(G, Hkv, q_lens, kv_lens, max_splits):
+    # A tile is 256 rows in two halves of 128 MMA rows; each half streams the
+    # piece's stages up to its own last position and writes its own rows.
+    case = W.prefill_case(q_lens, kv_lens, G * Hkv, Hkv, 16, "NHD", seed=G + len(q_lens),
+                          device="cuda")
+    run = Prefill(case, max_splits=max_splits)
+    if max_splits == 64:
+        assert run.plan.info.max_pieces > 8
+    run.run()
+    check_all(run, f"G={G} halves {q_lens}/{kv_lens}")
 
 
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
@@ -141,6 +162,33 @@ def test_pages_prefill_shape_and_scores_growing_along_the_cache():
                 torch.bfloat16)
     run.run()
     check_all(run, "growing scores")
+
+
+def _set_key_rows(case, b, positions, value):
+    """Key rows of request b at the given cache positions, every KV head, set to
+    the constant `value` (NHD pages)."""
+    t = case.tables
+    for pos in positions:
+        page = int(t.indices[t.indptr[b] + pos // case.page_size])
+        case.k[page, pos % case.page_size] = value
+
+
+@pytest.mark.parametrize("jump", [6.0, 3.0])
+def test_scores_jumping_and_dropping_between_stages(jump):
+    # q = 1 in every column. Request 0: small keys, then a few keys of `jump`
+    # in every column from stage 2 on (scores 128 jump / sqrt(128) above the
+    # first stage's: 98 in log2 units for 6.0, far past the one-pass bound of
+    # 2^64, so those stages fall back to two passes; 49 for 3.0, accepted with
+    # the reference lagging). Request 1: the large keys in its first stage,
+    # small ones after (terms of later stages near 2^-98 of the first).
+    case = W.prefill_case((300, 200), (1000, 900), 8, 2, 16, "NHD", seed=17, device="cuda")
+    case.q.fill_(1.0)
+    case.k.mul_(0.05)
+    _set_key_rows(case, 0, (300, 301, 640, 999), jump)
+    _set_key_rows(case, 1, (5, 70), jump)
+    run = Prefill(case)
+    run.run()
+    check_all(run, f"key jump {jump}")
 
 
 @pytest.mark.parametrize("name", W.PREFILL_ORDER)
