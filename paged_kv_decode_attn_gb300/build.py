@@ -19,7 +19,8 @@ HEADERS = [os.path.join(ROOT, "include", "oxd.h")] + [
     os.path.join(CSRC, h) for h in ("oxd_internal.h", "oxd_merge_row.cuh", "oxd_ptx.cuh",
                                     "oxd_tcgen05.cuh", "oxd_prefill.h", "oxd_host_util.h")]
 SOURCES = ["oxd_host.cpp", "oxd_decode.cu", "oxd_decode_wide.cu", "oxd_merge.cu",
-           "oxd_noalloc.cu", "oxd_append.cu", "oxd_prefill.cu", "oxd_prefill_host.cpp"]
+           "oxd_noalloc.cu", "oxd_append.cu", "oxd_prefill.cu", "oxd_prefill_narrow.cu",
+           "oxd_prefill_host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

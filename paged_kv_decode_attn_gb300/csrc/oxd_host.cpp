@@ -342,7 +342,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     std::vector<Chunk> chunks;
     int casc_requests = 0;
     if (prefix_pages > 0) {
-        const int T = kPrefillRows / G;
+        const int T = kNarrowRows / G;
         for (int g0 = 0; g0 < B; g0 += d.share_group) {
             const int g1 = std::min(B, g0 + d.share_group);
             std::vector<int> members;
@@ -692,7 +692,7 @@ oxd_status oxd_paged_decode_plan(const oxd_paged_decode_desc* desc, const int32_
     P->casc_units = static_cast<int>(punits.size());
     P->cluster_c = cluster_c;
     P->casc_requests = casc_requests;
-    P->casc_tile_tokens = kPrefillRows / G;
+    P->casc_tile_tokens = kNarrowRows / G;
     P->shared_kv = shared_kv;
     P->nnz = indptr[B];
     P->total_tokens = total_tokens;
@@ -881,9 +881,21 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
         if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
     }
-    CUtensorMap tk, tv, tq;
+    CUtensorMap tk, tv, tq, tq3;
     if (!encode_pool(&tk, k_pages, d) || !encode_pool(&tv, v_pages, d)) return OXD_ERR_CUDA;
     if (plan->variant == kVariantWide && !encode_q(&tq, q, d)) return OXD_ERR_CUDA;
+    if (plan->casc_units > 0) {
+        // q [B][Hq][128] as (d, head, request) for the prefix tiles: a box is
+        // 64 columns x the G heads of one KV head x up to 128 / G requests
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim),
+                                  static_cast<uint64_t>(d.num_qo_heads),
+                                  static_cast<uint64_t>(d.batch)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
+                                     static_cast<uint64_t>(d.num_qo_heads) * kHeadDim * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(plan->group),
+                                 static_cast<uint32_t>(plan->casc_tile_tokens)};
+        if (!encode_bf16_map(&tq3, q, 3, dims, strides, box)) return OXD_ERR_CUDA;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -979,8 +991,8 @@ oxd_status oxd_paged_decode_run(oxd_plan plan, const void* q, const void* k_page
         pp.scale_log2 = p.scale_log2;
         pp.wait_prior = 1;
         pp.wait_ns = p.wait_ns;
-        if (launch_prefill(tk, tv, pp, plan->casc_units, s,
-                           plan->ev_after == nullptr) != cudaSuccess)
+        if (launch_prefill_narrow(tk, tv, tq3, pp, plan->casc_units, s,
+                                  plan->ev_after == nullptr) != cudaSuccess)
             return OXD_ERR_CUDA;
     }
     if (plan->n_split > 0) {

@@ -20,7 +20,8 @@
 //     half h, S_h = Q_h K^T (M = 128, N = 128, K = 128; Q_h and K in shared
 //     memory) and O_h += P_h V (P_h from tensor memory; N = 128, K = 128) in a
 //     fixed order, so the tensor core works on one half while the other's
-//     softmax runs;
+//     softmax runs; a tile whose rows all fit in the first half gives it
+//     both score buffers instead (QK(g + 1) runs during the softmax of g);
 //   * softmax warpgroups (warps 0-3 for half 0, 4-7 for half 1): thread r
 //     owns row r of its half (TMEM lane r). It first writes its query row
 //     into shared memory. Per stage it loads the row's 128 scores and writes
@@ -76,8 +77,10 @@ struct PCtl {
     uint64_t vempty[kPVStages];
     uint64_t q_ready[2];  // a half's query rows are in shared memory (one arrival a warp)
     uint64_t s_ready[2];  // QK_h(g) done: phase g of s_ready[h]
-    uint64_t p_ready[2];  // P_h(g) written: phase g of p_ready[h] (one arrival a warp)
+    uint64_t p_ready[2];  // P_h(g) written: phase g of p_ready[h] (one arrival a warp);
+                          // a single-half tile's P(g): phase g / 2 of p_ready[g % 2]
     uint64_t o_done[2];   // the half's last PV done
+    uint64_t pv_done;     // single-half tile: PV(g) done, phase g
     uint64_t vz;          // V rows past the piece zeroed (one arrival a warp)
     uint64_t mma_done;
     int kissued[kPKStages];
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(&ctl.p_ready[h], 4);
             mbar_init(&ctl.o_done[h], 1);
         }
+        mbar_init(&ctl.pv_done, 1);
         mbar_init(&ctl.vz, 4);
         mbar_init(&ctl.mma_done, 1);
         flags[0] = 0;
@@ -197,6 +201,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int n_st = usable ? (u.kv_valid + kPrefillStageTokens - 1) / kPrefillStageTokens : 0;
     const int nst_h[2] = {usable ? half_stages(u, G, 0) : 0, usable ? half_stages(u, G, 1) : 0};
     const int last_valid = n_st > 0 ? u.kv_valid - (n_st - 1) * kPrefillStageTokens : 0;
+    // A tile whose rows all sit in the first half (half 1 streams nothing)
+    // gives half 0 both score buffers: QK(g + 1) runs while the softmax of
+    // stage g does.
+    const bool single = nst_h[1] == 0;
     const bool need_vz = n_st > 0 && last_valid < kPrefillStageTokens;
 
     if (warp == kPKWarp || warp == kPVWarp) {
@@ -290,7 +298,62 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 ok = __all_sync(0xffffffffu, ok && mbar_wait_tc(bar, parity, flags, p.wait_ns));
                 return ok;
             };
-            const int n_max = max(nst_h[0], nst_h[1]);
+            auto issue_qk = [&](int h, int g, uint32_t sd) {
+                // K = 128 in steps of 16: 32 bytes of a 128-byte swizzled row;
+                // columns 64..127 in the other half
+                const uint64_t kd0 = umma_sdesc(ring_k(g % kPKStages), 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                    const int c = ks >> 2, kk = ks & 3;
+                    umma_ss_warp(sd, qd0[h] + static_cast<uint64_t>((c * kPQHalf + kk * 32) >> 4),
+                                 kd0 + static_cast<uint64_t>((c * kPHalf + kk * 32) >> 4), kIdQK,
+                                 ks > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int h, int g, uint32_t ps0) {
+                // 16 tokens a step = two 8-row groups (1024 B apart); the two
+                // 64-column halves of V are kPHalf apart
+                const uint64_t vd0 = umma_sdesc(ring_v(g % kPVStages), kPHalf, 1024);
+#pragma unroll
+                for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks)
+                    umma_ts_warp(t_o(h), ps0 + 8u * ks, vd0 + static_cast<uint64_t>(ks * 2048 >> 4),
+                                 kIdPV, (ks > 0 || g > 0) ? 1u : 0u);
+            };
+            if (single) {
+                // Half 0 alone, scores in S_0 and S_1 by stage parity: QK(0),
+                // QK(1), then per stage g PV(g) and QK(g + 2) into the buffer PV(g)
+                // has just read P from.
+                const int n = nst_h[0];
+                for (int g = 0; g < min(n, 2) && ok; ++g) {
+                    if (g == 0 && !wait(&ctl.q_ready[0], 0)) break;
+                    if (!wait(&ctl.kfull[g % kPKStages], (g / kPKStages) & 1)) break;
+                    tc_fence_after();
+                    issue_qk(0, g, t_s(g & 1));
+                    umma_commit_warp(&ctl.s_ready[g & 1]);
+                    umma_commit_warp(&ctl.kempty[g % kPKStages]);
+                }
+                for (int g = 0; g < n && ok; ++g) {
+                    // one barrier per score buffer: the softmax may publish
+                    // P(g + 1) before this wait for P(g) has seen its phase
+                    if (!wait(&ctl.p_ready[g & 1], (g >> 1) & 1)) break;
+                    if (!wait(&ctl.vfull[g % kPVStages], (g / kPVStages) & 1)) break;
+                    if (g == n_st - 1 && need_vz && !wait(&ctl.vz, 0)) break;
+                    tc_fence_after();
+                    issue_pv(0, g, t_s(g & 1));
+                    umma_commit_warp(&ctl.pv_done);
+                    umma_commit_warp(&ctl.vempty[g % kPVStages]);
+                    if (g == n - 1) umma_commit_warp(&ctl.o_done[0]);
+                    const int g2 = g + 2;
+                    if (g2 < n) {
+                        if (!wait(&ctl.kfull[g2 % kPKStages], (g2 / kPKStages) & 1)) break;
+                        tc_fence_after();
+                        issue_qk(0, g2, t_s(g2 & 1));
+                        umma_commit_warp(&ctl.s_ready[g2 & 1]);
+                        umma_commit_warp(&ctl.kempty[g2 % kPKStages]);
+                    }
+                }
+            }
+            const int n_max = single ? -1 : max(nst_h[0], nst_h[1]);
             for (int g = 0; g <= n_max && ok; ++g) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -302,15 +365,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             if (gp == n_st - 1 && need_vz && !wait(&ctl.vz, 0)) break;
                         }
                         tc_fence_after();
-                        // 16 tokens a step = two 8-row groups (1024 B apart); the
-                        // two 64-column halves of V are kPHalf apart
-                        const uint64_t vd0 = umma_sdesc(ring_v(gp % kPVStages), kPHalf, 1024);
-                        const uint32_t ps0 = t_s(h), po = t_o(h);
-#pragma unroll
-                        for (int ks = 0; ks < kPrefillStageTokens / 16; ++ks)
-                            umma_ts_warp(po, ps0 + 8u * ks,
-                                         vd0 + static_cast<uint64_t>(ks * 2048 >> 4), kIdPV,
-                                         (ks > 0 || gp > 0) ? 1u : 0u);
+                        issue_pv(h, gp, t_s(h));
                         if (gp == nst_h[h] - 1) umma_commit_warp(&ctl.o_done[h]);
                         if (h == 1 || gp >= nst_h[1])  // the last half to read V(gp)
                             umma_commit_warp(&ctl.vempty[gp % kPVStages]);
@@ -321,18 +376,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             !wait(&ctl.kfull[g % kPKStages], (g / kPKStages) & 1))
                             break;
                         tc_fence_after();
-                        // K = 128 in steps of 16: 32 bytes of a 128-byte swizzled
-                        // row; columns 64..127 in the other half
-                        const uint64_t kd0 = umma_sdesc(ring_k(g % kPKStages), 16, 1024);
-                        const uint32_t sd = t_s(h);
-#pragma unroll
-                        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-                            const int c = ks >> 2, kk = ks & 3;
-                            umma_ss_warp(sd,
-                                         qd0[h] + static_cast<uint64_t>((c * kPQHalf + kk * 32) >> 4),
-                                         kd0 + static_cast<uint64_t>((c * kPHalf + kk * 32) >> 4),
-                                         kIdQK, ks > 0 ? 1u : 0u);
-                        }
+                        issue_qk(h, g, t_s(h));
                         umma_commit_warp(&ctl.s_ready[h]);
                         if (h == 1 || g >= nst_h[1])  // the last half to read K(g)
                             umma_commit_warp(&ctl.kempty[g % kPKStages]);
@@ -395,12 +439,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int g = 0; g < nst; ++g) {
-            if (!wait_all(&ctl.s_ready[h], g & 1)) {
+            // the stage's score buffer: S_h, or S_(g % 2) for a single-half tile
+            const int sb = single ? (g & 1) : h;
+            const uint32_t ts = t_s(sb);
+            if (!wait_all(&ctl.s_ready[sb], single ? (g >> 1) & 1 : g & 1)) {
                 ok = false;
                 break;
             }
-            // s_ready(g) also means every MMA issued before QK_h(g) is done,
-            // PV_h(g - 1) among them: O_h is up to date and P_h(g - 1) read
+            // s_ready(g) also means every MMA issued before QK_h(g) is done:
+            // PV_h(g - 1) among them with two halves (O_h is up to date), and
+            // PV(g - 2) for a single-half tile (its P was in this buffer)
             tc_fence_after();
             const int base = u.kv_begin + g * kPrefillStageTokens;
             const int nvalid = min(kPrefillStageTokens, u.kv_valid - g * kPrefillStageTokens);
@@ -438,15 +486,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         pk[16 * c + j] = pack_bf16x2(p0, p1);
                     }
                 };
-                tmem_ld32_async(t_s(h) + lane_off, a);
+                tmem_ld32_async(ts + lane_off, a);
                 tmem_ld_wait(a);
-                tmem_ld32_async(t_s(h) + lane_off + 32, b);
+                tmem_ld32_async(ts + lane_off + 32, b);
                 chunk(a, 0);
                 tmem_ld_wait(b);
-                tmem_ld32_async(t_s(h) + lane_off + 64, a);
+                tmem_ld32_async(ts + lane_off + 64, a);
                 chunk(b, 1);
                 tmem_ld_wait(a);
-                tmem_ld32_async(t_s(h) + lane_off + 96, b);
+                tmem_ld32_async(ts + lane_off + 96, b);
                 chunk(a, 2);
                 tmem_ld_wait(b);
                 chunk(b, 3);
@@ -454,8 +502,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (!__any_sync(0xffffffffu, !(ltot <= 0x1p64f))) {
                     uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
                     uint32_t (&p1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
-                    tmem_st32(t_s(h) + lane_off, p0);
-                    tmem_st32(t_s(h) + lane_off + 32, p1);
+                    tmem_st32(ts + lane_off, p0);
+                    tmem_st32(ts + lane_off + 32, p1);
                     done = true;
                 } else {
                     lq[0] = lq[1] = lq[2] = lq[3] = 0.f;
@@ -467,7 +515,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // thread within its register share. P (bf16 pairs) goes to
                 // columns 0..63, over scores already read.
                 uint32_t s0[64];
-                tmem_ld64(t_s(h) + lane_off, s0);
+                tmem_ld64(ts + lane_off, s0);
                 float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (whole) {
 #pragma unroll
@@ -485,7 +533,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t s1[32];
-                    tmem_ld32(t_s(h) + lane_off + 64 + 32 * c, s1);
+                    tmem_ld32(ts + lane_off + 64 + 32 * c, s1);
                     if (whole) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 2)
@@ -532,12 +580,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             pk[j] = pack_bf16x2(p0, p1);
                         }
                     }
-                    tmem_st32(t_s(h) + lane_off, pk);
+                    tmem_st32(ts + lane_off, pk);
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t s1[32], pk[16];
-                    tmem_ld32(t_s(h) + lane_off + 64 + 32 * c, s1);
+                    tmem_ld32(ts + lane_off + 64 + 32 * c, s1);
                     if (whole) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -562,12 +610,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                             pk[j] = pack_bf16x2(p0, p1);
                         }
                     }
-                    tmem_st16(t_s(h) + lane_off + 32 + 16 * c, pk);
+                    tmem_st16(ts + lane_off + 32 + 16 * c, pk);
                 }
             }
             l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
             if (__any_sync(0xffffffffu, rescale)) {
-                // O_h holds PV_h through stage g - 1 (done, see above)
+                // O_h holds PV_h through stage g - 1: done (see above), or
+                // waited for here for a single-half tile
+                if (single && !wait_all(&ctl.pv_done, (g - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
                     uint32_t o[32];
@@ -582,9 +636,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const bool last = g == nst - 1;
             if (last && zeroes) {
                 // zero V rows past the piece once its V landed (whole 128-byte
-                // rows, so the swizzle does not matter); PV_h(g - 1) is done,
-                // so V up to stage g - 1 landed and this phase of vfull is the
-                // one for stage g
+                // rows, so the swizzle does not matter); V(g - 2), the slot's
+                // previous stage, has been read (PV(g - 2) is done), so this
+                // phase of vfull is the one for stage g
                 if (!wait_all(&ctl.vfull[g % kPVStages], (g / kPVStages) & 1)) {
                     ok = false;
                     break;
@@ -602,7 +656,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl.p_ready[h]);
+            if (lane == 0) mbar_arrive(&ctl.p_ready[sb]);
         }
         // ---- epilogue: O / l once the half's last PV is done; padding rows
         // take part in the collective loads. A piece wholly past the half's

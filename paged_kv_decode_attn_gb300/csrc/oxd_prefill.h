@@ -12,6 +12,10 @@ constexpr int kPrefillRows = 256;         // rows of a tile: tile_tokens * G (<=
                                           // halves of 128 MMA rows
 constexpr int kMaxPrefillGroup = 128;     // G = Hq / Hkv of a prefill
 constexpr int kPrefillStageTokens = 128;  // cached tokens per pipeline stage
+// The narrow kernel (the cascade decode's shared-prefix tiles): 128-row tiles
+// on 64-token stages, two CTAs a SM.
+constexpr int kNarrowRows = 128;
+constexpr int kNarrowStageTokens = 64;
 
 // One CTA's work: a piece of the cached-token range of one tile (up to
 // tile_tokens consecutive query tokens of one request, with the G query heads
@@ -79,5 +83,11 @@ cudaError_t prefill_occupancy(int* ctas_per_sm);
 // kernel on the stream (then p.wait_prior must be 1).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                            int grid, cudaStream_t stream, bool early = false);
+// The narrow kernel: tiles of at most kNarrowRows rows, pieces starting at a
+// multiple of kNarrowStageTokens; tq: q as (d, head, token) with a box of
+// 64 x G x (kNarrowRows / G) and the 128-byte swizzle.
+cudaError_t launch_prefill_narrow(const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const CUtensorMap& tq, const PrefillParams& p, int grid,
+                                  cudaStream_t stream, bool early = false);
 
 }  // namespace oxd

@@ -630,12 +630,12 @@ def test_cascade_plan_counts_groups_and_shared_tokens():
 
 
 def test_cascade_groups_wider_than_a_tile_are_chunked():
-    # G = 8 -> 32 requests per prefix tile (256 rows); a group of 40 needs two
-    # chunks
+    # prefix tiles hold 128 rows (the narrow kernel): G = 8 -> 16 requests per
+    # tile; a group of 40 needs three chunks
     plan, _, _ = host_plan([5000] * 40, Hq=64, Hkv=8, ps=16, shared_prefix_tokens=1024,
                            share_group=40)
-    assert plan.info.cascade_units == 2 * 8 and plan.info.cascade_requests == 40
-    assert plan.info.shared_kv_tokens == (40 - 2) * 1024
+    assert plan.info.cascade_units == 3 * 8 and plan.info.cascade_requests == 40
+    assert plan.info.shared_kv_tokens == (40 - 3) * 1024
 
 
 # ------------------------------------------------------------------ encoding limits

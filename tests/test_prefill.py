@@ -191,6 +191,27 @@ def test_scores_jumping_and_dropping_between_stages(jump):
     check_all(run, f"key jump {jump}")
 
 
+def test_single_half_tiles_many_runs():
+    # Tiles of at most 128 rows run with two score buffers in one half. 160
+    # such tiles of 64 stages each, run 12 times, the device status read after
+    # every run (a barrier phase read one phase late would stall a run until
+    # its wait limit and show here as OXD_DEVICE_WAIT_TIMEOUT); sampled rows of
+    # the last run against the oracle.
+    case = W.prefill_case((16,) * 20, (8192,) * 20, 64, 8, 16, "NHD", seed=23, device="cuda")
+    run = Prefill(case, max_splits=1)
+    assert run.plan.info.tile_tokens == 32 and run.plan.info.num_units == 160
+    for i in range(12):
+        run.run()
+        torch.cuda.synchronize()
+        assert run.status() == oxd.OXD_DEVICE_OK, f"run {i}"
+    rng = np.random.default_rng(3)
+    rows = [(int(tk), int(h)) for tk in rng.integers(0, 320, 24) for h in rng.integers(0, 64, 2)]
+    ref_o, ref_l = oracle_rows(case, rows)
+    ti = torch.as_tensor([r[0] for r in rows], device="cuda")
+    hi = torch.as_tensor([r[1] for r in rows], device="cuda")
+    assert_parity(run.out[ti, hi], ref_o, run.lse[ti, hi], ref_l, "single-half tiles")
+
+
 @pytest.mark.parametrize("name", W.PREFILL_ORDER)
 def test_full_workloads_sampled_rows(name):
     cfg = W.PREFILL_CONFIGS[name]
