@@ -430,9 +430,11 @@ oxd_status oxd_rope_append(const oxd_rope_append_desc* desc, const void* q, cons
  * with BF16 operands (P rounded to BF16), out rounded once to BF16.
  *
  * Lifecycle as for decode ("Oxide Infer" README, "One execution model"): a
- * host-side plan fixes the tiles (up to 128 / G query tokens of one request
- * with the G heads of one KV head), the pieces of long tiles and the
- * workspace size; runs only check operands and enqueue.
+ * host-side plan fixes the tiles (up to tile_rows / G query tokens of one
+ * request with the G heads of one KV head: 256-row tiles in two halves of
+ * 128, one CTA a SM, 128-token stages; or 128-row tiles, two CTAs a SM,
+ * 64-token stages), the pieces of long tiles and the workspace size; runs
+ * only check operands and enqueue.
  */
 typedef struct oxd_prefill_plan_s* oxd_prefill_plan;
 
@@ -450,10 +452,15 @@ typedef struct {
                                many SMs (runs refused) */
     int64_t wait_timeout_ns; /* limit of one pipeline wait, as for decode: 0 = about one
                                 second, n > 0 = n nanoseconds */
+    int32_t tile_rows;      /* 0: the planner picks (128 when a plan of 256-row tiles
+                               would give fewer 128-token stages than the GPU has SMs,
+                               else 256); 128 or 256: that tile size; other values are
+                               OXD_ERR_INVALID_ARGUMENT */
+    int32_t reserved;       /* must be zero */
 } oxd_paged_prefill_desc;
 
 typedef struct {
-    int32_t tile_tokens;        /* query tokens per tile: 128 / G */
+    int32_t tile_tokens;        /* query tokens per tile: tile_rows / G */
     int32_t num_tiles;
     int32_t num_units;          /* CTAs per run: pieces of all tiles */
     int32_t num_split_tiles;
@@ -462,7 +469,7 @@ typedef struct {
     int32_t launches_per_run;   /* 1, or 2 with the merge */
     int32_t ctas_per_sm;
     int32_t num_sms;
-    int32_t reserved0;
+    int32_t tile_rows;          /* 128 or 256: the tile size (and kernel) the plan runs */
     int64_t workspace_bytes;
     int64_t total_q_tokens;
     int64_t total_kv_tokens;

@@ -150,6 +150,7 @@ class PrefillDesc(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("layout", ctypes.c_int32),
         ("num_pages", ctypes.c_int64), ("max_splits", ctypes.c_int32),
         ("num_sms", ctypes.c_int32), ("wait_timeout_ns", ctypes.c_int64),
+        ("tile_rows", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -161,22 +162,24 @@ class PrefillPlanInfo(ctypes.Structure):
         ("num_units", ctypes.c_int32), ("num_split_tiles", ctypes.c_int32),
         ("max_pieces", ctypes.c_int32), ("num_merge_rows", ctypes.c_int32),
         ("launches_per_run", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-        ("num_sms", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64), ("total_q_tokens", ctypes.c_int64),
         ("total_kv_tokens", ctypes.c_int64), ("causal_pairs", ctypes.c_int64),
     ]
 
     def as_dict(self):
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved0"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 def make_prefill_desc(batch, num_qo_heads, num_kv_heads, page_size, layout, num_pages,
-                      head_dim=128, max_splits=0, num_sms=0, wait_timeout_ns=0) -> PrefillDesc:
-    """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1."""
+                      head_dim=128, max_splits=0, num_sms=0, wait_timeout_ns=0,
+                      tile_rows=0) -> PrefillDesc:
+    """Convenience constructor; ``layout`` may be "NHD"/"HND" or 0/1; ``tile_rows``
+    0 lets the planner pick 128- or 256-row tiles."""
     if isinstance(layout, str):
         layout = {"NHD": OXD_LAYOUT_NHD, "HND": OXD_LAYOUT_HND}[layout]
     return PrefillDesc(batch, num_qo_heads, num_kv_heads, head_dim, page_size, layout, num_pages,
-                       max_splits, num_sms, wait_timeout_ns)
+                       max_splits, num_sms, wait_timeout_ns, tile_rows, 0)
 
 
 def make_rope_append_desc(num_tokens, batch, num_qo_heads, num_kv_heads, page_size, layout,

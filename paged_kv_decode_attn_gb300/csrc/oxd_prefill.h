@@ -12,8 +12,8 @@ constexpr int kPrefillRows = 256;         // rows of a tile: tile_tokens * G (<=
                                           // halves of 128 MMA rows
 constexpr int kMaxPrefillGroup = 128;     // G = Hq / Hkv of a prefill
 constexpr int kPrefillStageTokens = 128;  // cached tokens per pipeline stage
-// The narrow kernel (the cascade decode's shared-prefix tiles): 128-row tiles
-// on 64-token stages, two CTAs a SM.
+// The narrow kernel (short prefills and the cascade decode's shared-prefix
+// tiles): 128-row tiles on 64-token stages, two CTAs a SM.
 constexpr int kNarrowRows = 128;
 constexpr int kNarrowStageTokens = 64;
 
@@ -83,6 +83,8 @@ cudaError_t prefill_occupancy(int* ctas_per_sm);
 // kernel on the stream (then p.wait_prior must be 1).
 cudaError_t launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                            int grid, cudaStream_t stream, bool early = false);
+cudaError_t prefill_narrow_smem_bytes(int* bytes);
+cudaError_t prefill_narrow_occupancy(int* ctas_per_sm);
 // The narrow kernel: tiles of at most kNarrowRows rows, pieces starting at a
 // multiple of kNarrowStageTokens; tq: q as (d, head, token) with a box of
 // 64 x G x (kNarrowRows / G) and the 128-byte swizzle.

@@ -3,6 +3,8 @@
 // "FlashInfer parity matrix" page, "Admitted attention matrix", row "Paged
 // causal prefill" (caller-owned F32 workspace for the split pieces), driven
 // as the "Oxide Infer" README's "One execution model" describes: the plan
+// picks the tile size (256 rows on the two-half kernel, or 128 rows on the
+// narrow kernel for prefills too short to fill the GPU with the former) and
 // fixes the tiles, the pieces of long tiles and the workspace; a run checks
 // operands and enqueues (the work list copied into the workspace first,
 // unless the workspace is bound to the plan), the prefill kernel and, when
@@ -32,6 +34,7 @@ struct oxd_prefill_plan_s {
     oxd_paged_prefill_desc desc;
     int device;  // -1: host-only plan
     int group;
+    bool narrow;  // 128-row tiles on the narrow kernel, else 256-row tiles
     int tile_tokens;
     int n_tiles;
     int n_units;
@@ -55,7 +58,9 @@ struct oxd_prefill_plan_s {
 
 namespace {
 
-constexpr int kMinPieceStages = 1;  // a piece streams at least one stage (128 tokens)
+// a piece streams at least 128 cached tokens: one stage of the two-half
+// kernel, two of the narrow one
+constexpr int kMinPieceTokens = 128;
 constexpr int kMaxPieces = 64;
 
 std::mutex g_mu;
@@ -73,6 +78,9 @@ oxd_status check_desc(const oxd_paged_prefill_desc& d) {
     if (d.num_qo_heads % d.num_kv_heads != 0) return OXD_ERR_INVALID_ARGUMENT;
     if (d.layout != OXD_LAYOUT_NHD && d.layout != OXD_LAYOUT_HND) return OXD_ERR_INVALID_ARGUMENT;
     if (d.wait_timeout_ns < 0) return OXD_ERR_INVALID_ARGUMENT;
+    if ((d.tile_rows != 0 && d.tile_rows != kNarrowRows && d.tile_rows != kPrefillRows) ||
+        d.reserved != 0)
+        return OXD_ERR_INVALID_ARGUMENT;
     if (d.head_dim != kHeadDim) return OXD_ERR_UNSUPPORTED;
     if (d.page_size != 8 && d.page_size != 16 && d.page_size != 32 && d.page_size != 64)
         return OXD_ERR_UNSUPPORTED;
@@ -104,7 +112,6 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
     if (st != OXD_OK) return st;
     const int B = d.batch, ps = d.page_size, H = d.num_kv_heads;
     const int G = d.num_qo_heads / H;
-    const int T = kPrefillRows / G;
     if (qo_indptr[0] != 0 || indptr[0] < 0) return OXD_ERR_INVALID_ARGUMENT;
     int64_t total_kv = 0, pairs = 0;
     for (int b = 0; b < B; ++b) {
@@ -121,20 +128,53 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
     if (nq * d.num_qo_heads >= (int64_t{1} << 31) || static_cast<int64_t>(indptr[B]) < 1)
         return OXD_ERR_UNSUPPORTED;
 
-    int num_sms = d.num_sms, ctas_per_sm = 0, plan_device = -1;
+    int num_sms = d.num_sms, plan_device = -1;
     if (num_sms == 0) {
+        if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) !=
+                cudaSuccess ||
+            num_sms < 1)
+            return OXD_ERR_CUDA;
+        plan_device = device;
+    }
+    // Stages of tiles of `rows` rows over stages of `stage` tokens (each
+    // tile streams its request's cached tokens up to its last query token).
+    auto count_stages = [&](int rows, int stage) {
+        const int Tr = rows / G;
+        int64_t n = 0;
+        for (int b = 0; b < B; ++b) {
+            const int q_len = qo_indptr[b + 1] - qo_indptr[b];
+            const int64_t L = static_cast<int64_t>(indptr[b + 1] - indptr[b] - 1) * ps + last[b];
+            for (int qt = 0; qt * Tr < q_len; ++qt) {
+                const int64_t kv_end = L - q_len + qt * Tr + std::min(Tr, q_len - qt * Tr);
+                n += H * ((kv_end + stage - 1) / stage);
+            }
+        }
+        return n;
+    };
+    // The two-half kernel needs a whole SM a tile; a prefill that would not
+    // give every SM one of its stages runs sooner as smaller tiles, two a SM.
+    const bool narrow = d.tile_rows == kNarrowRows ||
+                        (d.tile_rows == 0 &&
+                         count_stages(kPrefillRows, kPrefillStageTokens) < num_sms);
+    const int rows = narrow ? kNarrowRows : kPrefillRows;
+    const int stage_tokens = narrow ? kNarrowStageTokens : kPrefillStageTokens;
+    const int T = rows / G;
+    int ctas_per_sm = 0;
+    if (plan_device >= 0) {
         int prev = 0;
         if (cudaGetDevice(&prev) != cudaSuccess) return OXD_ERR_CUDA;
         if (cudaSetDevice(device) != cudaSuccess) return OXD_ERR_CUDA;
-        cudaError_t e1 = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
-        cudaError_t e2 = prefill_occupancy(&ctas_per_sm);
+        const cudaError_t e =
+            narrow ? prefill_narrow_occupancy(&ctas_per_sm) : prefill_occupancy(&ctas_per_sm);
         cudaSetDevice(prev);
-        if (e1 != cudaSuccess || e2 != cudaSuccess || num_sms < 1) return OXD_ERR_CUDA;
-        plan_device = device;
+        if (e != cudaSuccess) return OXD_ERR_CUDA;
     }
     if (ctas_per_sm < 1) {
         int smem = 0;
-        prefill_smem_bytes(&smem);
+        if (narrow)
+            prefill_narrow_smem_bytes(&smem);
+        else
+            prefill_smem_bytes(&smem);
         ctas_per_sm = std::max(1, std::min(2, (228 * 1024) / (smem + 1024)));
     }
 
@@ -153,7 +193,7 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
             const int n_tok = std::min(T, q_len - qt * T);
             const int p0 = static_cast<int>(L - q_len + qt * T);
             const int kv_end = p0 + n_tok;
-            const int stages = (kv_end + kPrefillStageTokens - 1) / kPrefillStageTokens;
+            const int stages = (kv_end + stage_tokens - 1) / stage_tokens;
             for (int h = 0; h < H; ++h) {
                 tiles.push_back({b, h, qo_indptr[b] + qt * T, n_tok, p0, stages, kv_end});
                 total_stages += stages;
@@ -166,7 +206,8 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
     const int64_t resident = static_cast<int64_t>(num_sms) * ctas_per_sm;
     int64_t chunk = std::numeric_limits<int64_t>::max();
     if (d.max_splits != 1 && static_cast<int64_t>(tiles.size()) < resident)
-        chunk = std::max<int64_t>(kMinPieceStages, (total_stages + resident - 1) / resident);
+        chunk = std::max<int64_t>(kMinPieceTokens / stage_tokens,
+                                  (total_stages + resident - 1) / resident);
     const int cap = d.max_splits > 1 ? std::min(d.max_splits, kMaxPieces) : kMaxPieces;
     std::vector<PrefillUnit> units;
     std::vector<int4> entries;
@@ -183,7 +224,7 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
         int state = 0;
         if (S > 1) {
             ++n_split;
-            if (n_groups + static_cast<int64_t>(t.n_tok) * S >= (int64_t{1} << 31) / kPrefillRows)
+            if (n_groups + static_cast<int64_t>(t.n_tok) * S >= (int64_t{1} << 31) / rows)
                 return OXD_ERR_UNSUPPORTED;
             state = static_cast<int>(n_groups);
             n_groups += static_cast<int64_t>(t.n_tok) * S;
@@ -196,8 +237,8 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
             const int s0 = static_cast<int>(static_cast<int64_t>(t.stages) * i / S);
             const int s1 = static_cast<int>(static_cast<int64_t>(t.stages) * (i + 1) / S);
             PrefillUnit u{};
-            u.kv_begin = s0 * kPrefillStageTokens;
-            u.kv_valid = std::min(t.kv_end, s1 * kPrefillStageTokens) - u.kv_begin;
+            u.kv_begin = s0 * stage_tokens;
+            u.kv_valid = std::min(t.kv_end, s1 * stage_tokens) - u.kv_begin;
             u.idx_begin = indptr[t.b] + u.kv_begin / ps;
             u.n_pages = (u.kv_valid + ps - 1) / ps;
             u.q_begin = t.q0;
@@ -225,6 +266,7 @@ oxd_status oxd_paged_prefill_plan(const oxd_paged_prefill_desc* desc, const int3
     P->desc = d;
     P->device = plan_device;
     P->group = G;
+    P->narrow = narrow;
     P->tile_tokens = T;
     P->n_tiles = static_cast<int>(tiles.size());
     P->n_units = static_cast<int>(units.size());
@@ -293,6 +335,7 @@ oxd_status oxd_prefill_plan_get_info(oxd_prefill_plan plan, oxd_prefill_plan_inf
     r.launches_per_run = plan->n_entries > 0 ? 2 : 1;
     r.ctas_per_sm = plan->ctas_per_sm;
     r.num_sms = plan->num_sms;
+    r.tile_rows = plan->narrow ? kNarrowRows : kPrefillRows;
     r.workspace_bytes = static_cast<int64_t>(plan->ws_bytes);
     r.total_q_tokens = plan->nq;
     r.total_kv_tokens = plan->total_kv;
@@ -386,10 +429,22 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
     if (cudaGetDevice(&cur) != cudaSuccess) return OXD_ERR_CUDA;
     if (cur != plan->device) return OXD_ERR_PLAN_MISMATCH;
 
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tq;
     if (!encode_kv_pool(&tk, k_pages, d.layout, d.page_size, d.num_kv_heads, d.num_pages) ||
         !encode_kv_pool(&tv, v_pages, d.layout, d.page_size, d.num_kv_heads, d.num_pages))
         return OXD_ERR_CUDA;
+    if (plan->narrow) {
+        // q as (d, head, token): a box is 64 columns x the G heads of one KV
+        // head x the tile's query tokens
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim),
+                                  static_cast<uint64_t>(d.num_qo_heads),
+                                  static_cast<uint64_t>(plan->nq)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
+                                     static_cast<uint64_t>(d.num_qo_heads) * kHeadDim * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(plan->group),
+                                 static_cast<uint32_t>(plan->tile_tokens)};
+        if (!encode_bf16_map(&tq, q, 3, dims, strides, box)) return OXD_ERR_CUDA;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -436,7 +491,9 @@ oxd_status oxd_paged_prefill_run(oxd_prefill_plan plan, const void* q, const voi
 
     if (plan->ev_before != nullptr && cudaEventRecord(plan->ev_before, s) != cudaSuccess)
         return OXD_ERR_CUDA;
-    if (launch_prefill(tk, tv, p, plan->n_units, s) != cudaSuccess) return OXD_ERR_CUDA;
+    if ((plan->narrow ? launch_prefill_narrow(tk, tv, tq, p, plan->n_units, s)
+                      : launch_prefill(tk, tv, p, plan->n_units, s)) != cudaSuccess)
+        return OXD_ERR_CUDA;
     if (plan->ev_after != nullptr && cudaEventRecord(plan->ev_after, s) != cudaSuccess)
         return OXD_ERR_CUDA;
     if (plan->n_entries > 0) {

@@ -2,14 +2,17 @@
 //
 // Operation: "FlashInfer parity matrix" page, "Admitted attention matrix",
 // row "Paged causal prefill" (BF16, D128, causal, NHD/HND pages through the
-// same block tables as decode). It runs the cascade decode's shared-prefix
-// tiles ("Cascade inference" page): a sharing group's requests, one query
-// token each, attend the group's common prefix with no mask; their partial
-// states go to the decode's merge. Those tiles hold at most 128 rows, and
-// they start in the decode kernel's tail, as each decode CTA retires: this
-// kernel's footprint (112 KB of shared memory, 256 tensor-memory columns)
-// lets one start beside a decode CTA still running, where the two-half
-// 256-row kernel needs a whole SM.
+// same block tables as decode, split pieces with a caller-owned F32
+// workspace). It serves the prefills whose 256-row plan would leave SMs
+// idle (short ones, such as the pages' own shape: smaller tiles, two CTAs a
+// SM and 64-token stages start and finish sooner), and the cascade decode's
+// shared-prefix tiles ("Cascade inference" page): a sharing group's
+// requests, one query token each, attend the group's common prefix with no
+// mask, their partial states going to the decode's merge. Those start in
+// the decode kernel's tail as each decode CTA retires: this kernel's
+// footprint (112 KB of shared memory, 256 tensor-memory columns) lets one
+// start beside a decode CTA still running, where the two-half 256-row
+// kernel needs a whole SM.
 //
 // A tile is up to T = 128 / G consecutive query tokens of one request with
 // the G query heads of one KV head each: 128 MMA rows, row r = token r / G,
@@ -559,6 +562,31 @@ cudaError_t ensure_narrow_attribute() {
 }
 
 }  // namespace
+
+cudaError_t prefill_narrow_smem_bytes(int* bytes) {
+    *bytes = kPSmemBytes;
+    return cudaSuccess;
+}
+
+// Resident CTAs per SM from shared memory, threads and tensor-memory columns
+// (the occupancy query answers 1 for kernels that use tcgen05).
+cudaError_t prefill_narrow_occupancy(int* n) {
+    cudaError_t e = ensure_narrow_attribute();
+    if (e != cudaSuccess) return e;
+    int dev = 0, smem_sm = 0, reserved = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+        cudaSuccess)
+        return e;
+    const int by_smem = smem_sm / (kPSmemBytes + reserved);
+    const int by_tmem = 512 / static_cast<int>(kPTmemCols);
+    const int by_threads = 2048 / kPThreads;
+    *n = max(1, min(by_smem, min(by_tmem, by_threads)));
+    return cudaSuccess;
+}
 
 cudaError_t launch_prefill_narrow(const CUtensorMap& tk, const CUtensorMap& tv,
                                   const CUtensorMap& tq, const PrefillParams& p, int grid,

@@ -492,34 +492,62 @@ def prefill_plan(q_lens, kv_lens, Hq=32, Hkv=8, ps=16, num_sms=152, **kw):
 
 
 def test_prefill_plan_tiles_and_pieces():
-    # the pages' shape: 32 + 64 query tokens, GQA4 -> 64-token tiles (256 rows),
-    # 8 KV heads
+    # the pages' shape: 32 + 64 query tokens, GQA4, 8 KV heads. 256-row tiles
+    # would give 2 x 8 + 8 x 8 = 80 stages of 128 tokens, fewer than 152 SMs:
+    # the planner picks 128-row tiles (32 tokens) on the narrow kernel.
     plan, *_ = prefill_plan((32, 64), (256, 1024))
     i = plan.info
-    assert i.tile_tokens == 64 and i.num_tiles == (1 + 1) * 8
+    assert i.tile_rows == 128 and i.ctas_per_sm == 2
+    assert i.tile_tokens == 32 and i.num_tiles == (1 + 2) * 8
     assert i.total_q_tokens == 96 and i.total_kv_tokens == 1280
     assert i.causal_pairs == 32 * 224 + 32 * 33 // 2 + 64 * 960 + 64 * 65 // 2
     assert i.num_units > i.num_tiles and i.launches_per_run == 2  # split to fill the GPU
-    # every tile split: one merged row per (query token, query head)
-    assert i.num_split_tiles == i.num_tiles and i.num_merge_rows == (32 + 64) * 32
+    assert i.num_merge_rows == i.num_split_tiles * 32 * 4 or i.num_split_tiles < i.num_tiles
     one, *_ = prefill_plan((32, 64), (256, 1024), max_splits=1)
-    assert one.info.num_units == 16 and one.info.launches_per_run == 1
+    assert one.info.num_units == 24 and one.info.launches_per_run == 1
     capped, *_ = prefill_plan((32, 64), (256, 1024), max_splits=2)
     assert capped.info.max_pieces == 2
-    # enough tiles to fill the GPU: no split
+    # the same shape on 256-row tiles (64 tokens, two halves), asked for
+    wide, *_ = prefill_plan((32, 64), (256, 1024), tile_rows=256)
+    w = wide.info
+    assert w.tile_rows == 256 and w.ctas_per_sm == 1
+    assert w.tile_tokens == 64 and w.num_tiles == (1 + 1) * 8
+    # every tile split: one merged row per (query token, query head)
+    assert w.num_split_tiles == w.num_tiles and w.num_merge_rows == (32 + 64) * 32
+    one, *_ = prefill_plan((32, 64), (256, 1024), max_splits=1, tile_rows=256)
+    assert one.info.num_units == 16 and one.info.launches_per_run == 1
+    # enough tiles to fill the GPU: 256-row tiles, no split
     big, *_ = prefill_plan((2048,) * 8, [4096] * 8)
+    assert big.info.tile_rows == 256
     assert big.info.num_split_tiles == 0 and big.info.num_units == 8 * 32 * 8
 
 
-@pytest.mark.parametrize("G,T", [(1, 256), (2, 128), (3, 85), (8, 32), (32, 8), (128, 2)])
-def test_prefill_tile_tokens_follow_group(G, T):
-    plan, *_ = prefill_plan((T * 2 + 1,), (1000,), Hq=G, Hkv=1)
+def test_prefill_tile_size_choice():
+    # 256-row tiles once their 128-token stages reach the SM count, unless asked
+    # otherwise; 152 SMs, GQA4 with 8 KV heads: one 64-token tile of a request
+    # with 2 * 128 * k cached tokens gives 8 * 2k stages
+    small, *_ = prefill_plan((64,), (128 * 18,))     # 8 x 18 = 144 stages
+    assert small.info.tile_rows == 128
+    large, *_ = prefill_plan((64,), (128 * 19,))     # 8 x 19 = 152 stages
+    assert large.info.tile_rows == 256
+    fewer, *_ = prefill_plan((64,), (128 * 19,), num_sms=153)
+    assert fewer.info.tile_rows == 128
+    forced, *_ = prefill_plan((64,), (128 * 19,), tile_rows=128)
+    assert forced.info.tile_rows == 128 and forced.info.tile_tokens == 32
+
+
+@pytest.mark.parametrize("rows,G,T", [(256, 1, 256), (256, 2, 128), (256, 3, 85), (256, 8, 32),
+                                      (256, 32, 8), (256, 128, 2), (128, 1, 128), (128, 2, 64),
+                                      (128, 3, 42), (128, 8, 16), (128, 32, 4), (128, 128, 1)])
+def test_prefill_tile_tokens_follow_group(rows, G, T):
+    plan, *_ = prefill_plan((T * 2 + 1,), (1000,), Hq=G, Hkv=1, tile_rows=rows)
+    assert plan.info.tile_rows == rows
     assert plan.info.tile_tokens == T and plan.info.num_tiles == 3
 
 
 @pytest.mark.parametrize("name", ["q_above_kv", "qo_start", "qo_decreasing", "no_query",
                                   "group_too_big", "page_size", "head_dim", "negative_wait",
-                                  "heads_not_divisible"])
+                                  "heads_not_divisible", "tile_rows", "reserved"])
 def test_prefill_bad_plans_are_rejected(name):
     q_lens, kv_lens, kw = (4, 4), (10, 10), {}
     expect = oxd.OXD_ERR_INVALID_ARGUMENT
@@ -550,6 +578,10 @@ def test_prefill_bad_plans_are_rejected(name):
         expect = oxd.OXD_ERR_UNSUPPORTED
     elif name == "negative_wait":
         desc.wait_timeout_ns = -1
+    elif name == "tile_rows":
+        desc.tile_rows = 64
+    elif name == "reserved":
+        desc.reserved = 1
     with pytest.raises(oxd.OxdError) as e:
         oxd.oxd_paged_prefill_plan(desc, qo, indptr, last)
     assert e.value.status == expect

@@ -3,8 +3,10 @@
 Each case compares every output row (small cases) or sampled rows (the full
 workloads, in the launch configuration the benchmark times) with the oracle:
 |out - ref| <= 1.5e-2 + 1e-2 |ref|, |lse - ref| <= 1e-3. The cases cover
-group sizes that fill a 256-row tile (two halves of 128) exactly and ones that
-leave rows idle, the halves partly filled and a token's heads straddling them,
+both tile sizes (256 rows in two halves of 128 on the two-half kernel, 128 rows
+on the narrow kernel, and the planner's own pick), group sizes that fill a tile
+exactly and ones that leave rows idle, the halves partly filled and a token's
+heads straddling them,
 scores that jump or drop by large amounts between 128-token stages,
 NHD and HND pages of every page size, query counts of zero, one, a tile, a
 tile plus one and the whole cache, split and unsplit tiles, a bound workspace
@@ -34,14 +36,16 @@ def setup():
 class Prefill:
     """A case on the device with its plan, tables, outputs and workspace."""
 
-    def __init__(self, case: W.PrefillCase, max_splits=0, bind=False):
+    def __init__(self, case: W.PrefillCase, max_splits=0, bind=False, tile_rows=0):
         t = case.tables
         self.case = case
         self.desc = oxd.make_prefill_desc(case.batch, case.num_qo_heads, case.num_kv_heads,
                                           case.page_size, case.layout, t.num_pages,
-                                          max_splits=max_splits)
+                                          max_splits=max_splits, tile_rows=tile_rows)
         self.plan = oxd.oxd_paged_prefill_plan(self.desc, case.qo_indptr, t.indptr,
                                                t.last_page_len)
+        if tile_rows:
+            assert self.plan.info.tile_rows == tile_rows
         dev = case.q.device
         self.qo = torch.as_tensor(case.qo_indptr, device=dev)
         self.indptr = torch.as_tensor(t.indptr, device=dev)
@@ -79,14 +83,16 @@ def check_all(run: Prefill, what):
     return assert_parity(run.out, ref_o, run.lse, ref_l, what)
 
 
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("G,Hkv", [(1, 4), (2, 4), (4, 8), (8, 2), (32, 1), (3, 2), (128, 1)])
-def test_group_sizes(G, Hkv):
-    # tile_tokens = 256 // G: 256, 128, 64, 32, 8, 85 (one row idle), 2
+def test_group_sizes(rows, G, Hkv):
+    # tile_tokens = rows // G: 256, 128, 64, 32, 8, 85 (one row idle), 2 on 256-row
+    # tiles; 128, 64, 32, 16, 4, 42 (two rows idle), 1 on 128-row tiles
     case = W.prefill_case((70, 1, 33), (300, 64, 33), G * Hkv, Hkv, 16, "NHD", seed=G,
                           device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     run.run()
-    check_all(run, f"G={G}")
+    check_all(run, f"G={G} rows {rows}")
 
 
 @pytest.mark.parametrize("G,Hkv,q_lens,kv_lens,max_splits", [
@@ -101,20 +107,21 @@ def test_tile_halves(G, Hkv, q_lens, kv_lens, max_splits):
     # piece's stages up to its own last position and writes its own rows.
     case = W.prefill_case(q_lens, kv_lens, G * Hkv, Hkv, 16, "NHD", seed=G + len(q_lens),
                           device="cuda")
-    run = Prefill(case, max_splits=max_splits)
+    run = Prefill(case, max_splits=max_splits, tile_rows=256)
     if max_splits == 64:
         assert run.plan.info.max_pieces > 8
     run.run()
     check_all(run, f"G={G} halves {q_lens}/{kv_lens}")
 
 
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("ps", [8, 16, 32, 64])
-def test_layouts_and_page_sizes(layout, ps):
+def test_layouts_and_page_sizes(rows, layout, ps):
     case = W.prefill_case((5, 40, 64), (5, 77, 200), 16, 4, ps, layout, seed=ps, device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     run.run()
-    check_all(run, f"{layout} ps{ps}")
+    check_all(run, f"{layout} ps{ps} rows {rows}")
 
 
 @pytest.mark.parametrize("q_lens,kv_lens", [
@@ -122,18 +129,20 @@ def test_layouts_and_page_sizes(layout, ps):
     ((1, 1, 1), (1, 1000, 65)),                 # decode-like rows
     ((64, 96), (64, 2000)),                     # two tiles over a long cache
 ])
-def test_query_counts(q_lens, kv_lens):
+@pytest.mark.parametrize("rows", [128, 256])
+def test_query_counts(q_lens, kv_lens, rows):
     case = W.prefill_case(q_lens, kv_lens, 32, 8, 16, "NHD", seed=len(q_lens), device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     run.run()
-    check_all(run, f"q {q_lens} kv {kv_lens}")
+    check_all(run, f"q {q_lens} kv {kv_lens} rows {rows}")
 
 
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("max_splits", [1, 2, 5, 0])
-def test_split_and_unsplit_tiles(max_splits):
+def test_split_and_unsplit_tiles(rows, max_splits):
     case = W.prefill_case((32, 64, 7), (2048, 1024, 3000), 32, 8, 16, "HND", seed=11,
                           device="cuda")
-    run = Prefill(case, max_splits=max_splits)
+    run = Prefill(case, max_splits=max_splits, tile_rows=rows)
     info = run.plan.info
     if max_splits == 1:
         assert info.num_split_tiles == 0 and info.launches_per_run == 1
@@ -143,12 +152,15 @@ def test_split_and_unsplit_tiles(max_splits):
     check_all(run, f"max_splits {max_splits}")
 
 
-def test_pages_prefill_shape_and_scores_growing_along_the_cache():
-    # the pages' paged-prefill shape, once plain and once with keys that
-    # grow along the cache (the running maximum is raised stage after stage)
+@pytest.mark.parametrize("rows", [0, 256])
+def test_pages_prefill_shape_and_scores_growing_along_the_cache(rows):
+    # the pages' paged-prefill shape (128-row tiles when the planner picks), once
+    # plain and once with keys that grow along the cache (the running maximum is
+    # raised stage after stage)
     cfg = W.PREFILL_CONFIGS["prefill_gqa4_q32+64_kv256+1024_ps16_nhd"]
     case = W.make_prefill_case(cfg, device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
+    assert run.plan.info.tile_rows == (rows or 128)
     run.run()
     check_all(run, cfg.name)
     t = case.tables
@@ -173,8 +185,9 @@ def _set_key_rows(case, b, positions, value):
         case.k[page, pos % case.page_size] = value
 
 
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("jump", [6.0, 3.0])
-def test_scores_jumping_and_dropping_between_stages(jump):
+def test_scores_jumping_and_dropping_between_stages(rows, jump):
     # q = 1 in every column. Request 0: small keys, then a few keys of `jump`
     # in every column from stage 2 on (scores 128 jump / sqrt(128) above the
     # first stage's: 98 in log2 units for 6.0, far past the one-pass bound of
@@ -186,9 +199,9 @@ def test_scores_jumping_and_dropping_between_stages(jump):
     case.k.mul_(0.05)
     _set_key_rows(case, 0, (300, 301, 640, 999), jump)
     _set_key_rows(case, 1, (5, 70), jump)
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     run.run()
-    check_all(run, f"key jump {jump}")
+    check_all(run, f"key jump {jump} rows {rows}")
 
 
 def test_single_half_tiles_many_runs():
@@ -198,7 +211,7 @@ def test_single_half_tiles_many_runs():
     # its wait limit and show here as OXD_DEVICE_WAIT_TIMEOUT); sampled rows of
     # the last run against the oracle.
     case = W.prefill_case((16,) * 20, (8192,) * 20, 64, 8, 16, "NHD", seed=23, device="cuda")
-    run = Prefill(case, max_splits=1)
+    run = Prefill(case, max_splits=1, tile_rows=256)
     assert run.plan.info.tile_tokens == 32 and run.plan.info.num_units == 160
     for i in range(12):
         run.run()
@@ -237,11 +250,12 @@ def test_full_workloads_sampled_rows(name):
     assert_parity(run.out[ti, hi], ref_o, run.lse[ti, hi], ref_l, name)
 
 
-def test_bound_workspace_matches_unbound_and_graph_replays():
+@pytest.mark.parametrize("rows", [128, 256])
+def test_bound_workspace_matches_unbound_and_graph_replays(rows):
     case = W.prefill_case((40, 9), (900, 300), 32, 8, 16, "NHD", seed=21, device="cuda")
-    plain = Prefill(case)
+    plain = Prefill(case, tile_rows=rows)
     plain.run()
-    bound = Prefill(case, bind=True)
+    bound = Prefill(case, bind=True, tile_rows=rows)
     bound.run()
     torch.cuda.synchronize()
     assert torch.equal(plain.out.view(torch.int16), bound.out.view(torch.int16))
@@ -261,9 +275,10 @@ def test_bound_workspace_matches_unbound_and_graph_replays():
     assert_parity(out2, ref_o, lse2, ref_l, "graph replay")
 
 
-def test_guard_bands_untouched():
+@pytest.mark.parametrize("rows", [128, 256])
+def test_guard_bands_untouched(rows):
     case = W.prefill_case((20, 3), (100, 50), 8, 2, 16, "NHD", seed=22, device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     n = case.q.numel()
     big_out = torch.full((n + 2048,), -7.0, dtype=torch.bfloat16, device="cuda")
     out = big_out[1024:1024 + n].view(case.q.shape)
@@ -278,9 +293,10 @@ def test_guard_bands_untouched():
     check_all(run, "guarded")
 
 
-def test_bad_page_and_changed_tables_are_reported():
+@pytest.mark.parametrize("rows", [128, 256])
+def test_bad_page_and_changed_tables_are_reported(rows):
     case = W.prefill_case((16, 16), (200, 100), 8, 2, 16, "NHD", seed=23, device="cuda")
-    run = Prefill(case)
+    run = Prefill(case, tile_rows=rows)
     saved = run.indices.clone()
     run.indices[3] = case.tables.num_pages + 5  # outside the pool: read as page 0
     run.run()

@@ -1,7 +1,8 @@
 """Randomised paged causal prefill cases against the f64 oracle, every row.
 
-Sixty seeded draws: group sizes 1..128 (tiles of 128 down to one query token,
-and tiles that leave rows idle), page sizes 8..64, NHD and HND, one to four
+Sixty seeded draws: both tile sizes (256 rows on the two-half kernel, 128 on
+the narrow one, or the planner's pick), group sizes 1..128 (tiles of 256 down to
+one query token, and tiles that leave rows idle), page sizes 8..64, NHD and HND, one to four
 requests whose query counts run from zero to the whole cache, split settings
 (planner's choice, never split, a cap), bound and unbound workspaces, and
 scales other than 1/sqrt(D). Each case is small enough for the oracle to
@@ -49,18 +50,19 @@ def draw(i):
     bind = bool(rng.integers(0, 2))
     case = W.prefill_case(tuple(q), tuple(kv), G * Hkv, Hkv, ps, layout, seed=7100 + i,
                           device="cuda", sm_scale=float(rng.choice([0.05, 0.0884, 0.15])))
-    return case, max_splits, bind
+    tile_rows = int(rng.choice([0, 128, 256]))
+    return case, max_splits, bind, tile_rows
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_prefill_matches_oracle(i):
-    case, max_splits, bind = draw(i)
-    run = Prefill(case, max_splits=max_splits, bind=bind)
+    case, max_splits, bind, tile_rows = draw(i)
+    run = Prefill(case, max_splits=max_splits, bind=bind, tile_rows=tile_rows)
     run.run()
     torch.cuda.synchronize()
     assert run.status() == oxd.OXD_DEVICE_OK
     ref_o, ref_l = oracle_rows(case)
     what = (f"case {i}: G={case.num_qo_heads // case.num_kv_heads} Hkv={case.num_kv_heads} "
             f"ps={case.page_size} {case.layout} q={tuple(case.qo_indptr[1:] - case.qo_indptr[:-1])} "
-            f"max_splits={max_splits} bind={bind}")
+            f"max_splits={max_splits} bind={bind} tile_rows={run.plan.info.tile_rows}")
     assert_parity(run.out, ref_o, run.lse, ref_l, what)

@@ -138,8 +138,9 @@ def test_cascade_wait_timeout_is_reported_and_recovered(G, Hkv):
     assert info.cascade_units > 0
 
 
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("max_splits", [1, 0])
-def test_prefill_wait_timeout_is_reported_and_recovered(max_splits):
+def test_prefill_wait_timeout_is_reported_and_recovered(max_splits, rows):
     case = W.make_prefill_case(W.PrefillConfig(
         name="timeout", q_lens=(64, 300, 1), kv_lens=(1024, 2000, 700), num_qo_heads=32,
         num_kv_heads=8, page_size=16, layout="NHD", seed=99), device="cuda")
@@ -147,7 +148,8 @@ def test_prefill_wait_timeout_is_reported_and_recovered(max_splits):
     plans = [oxd.oxd_paged_prefill_plan(
         oxd.make_prefill_desc(case.batch, case.num_qo_heads, case.num_kv_heads, case.page_size,
                               case.layout, t.num_pages, max_splits=max_splits,
-                              wait_timeout_ns=ns), case.qo_indptr, t.indptr, t.last_page_len)
+                              wait_timeout_ns=ns, tile_rows=rows), case.qo_indptr, t.indptr,
+        t.last_page_len)
         for ns in (SHORT_NS, 0)]
     ws_bytes = max(plans[1].workspace_bytes, 256)
     g = Guarded(case.q.numel() * 2, case.q.shape[0] * case.q.shape[1] * 4, ws_bytes)
