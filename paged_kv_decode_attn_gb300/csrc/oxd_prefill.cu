@@ -91,6 +91,21 @@ struct PCtl {
 // The dynamic shared memory starts 1024-byte aligned (checked in the kernel).
 constexpr int kPSmemBytes = kPCtlOff + static_cast<int>(sizeof(PCtl));
 
+// 32 lanes x 16 consecutive 32-bit columns, without the wait (see tmem_ld_wait16).
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Stages a half streams of a piece: its rows see cached tokens up to the
 // position of its last query token.
 __device__ __forceinline__ int half_stages(const PrefillUnit& u, int G, int h) {
@@ -465,7 +480,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             bool done = false;
             if (whole && g > 0) {
                 // One pass against the running reference m_ref (no maximum): P =
-                // 2^(s sc - m_ref) for 32 columns at a time (the next 32 loading
+                // 2^(s sc - m_ref) for 16 columns at a time (the next 16 loading
                 // meanwhile), kept in registers until the row's sum shows that no
                 // term exceeds 2^64 (nor is infinite); then P is bf16 and O and l
                 // are F32 well inside their range. Otherwise the two passes below
@@ -473,31 +488,30 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // lag the row's maximum: every term carries the same factor
                 // 2^(m - m_ref), which the final O / l cancels.
                 uint32_t pk[64];
-                uint32_t a[32], b[32];
-                auto chunk = [&](const uint32_t (&x)[32], int c) {
+                uint32_t a[16], b[16];
+                auto chunk = [&](const uint32_t (&x)[16], int i) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         float x0, x1;
                         fma2(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]), sc, -m_ref,
                              x0, x1);
                         const float p0 = fast_exp2(x0);
                         const float p1 = fast_exp2(x1);
                         add2(lq[(j & 1) * 2], lq[(j & 1) * 2 + 1], p0, p1);
-                        pk[16 * c + j] = pack_bf16x2(p0, p1);
+                        pk[8 * i + j] = pack_bf16x2(p0, p1);
                     }
                 };
-                tmem_ld32_async(ts + lane_off, a);
-                tmem_ld_wait(a);
-                tmem_ld32_async(ts + lane_off + 32, b);
-                chunk(a, 0);
-                tmem_ld_wait(b);
-                tmem_ld32_async(ts + lane_off + 64, a);
-                chunk(b, 1);
-                tmem_ld_wait(a);
-                tmem_ld32_async(ts + lane_off + 96, b);
-                chunk(a, 2);
-                tmem_ld_wait(b);
-                chunk(b, 3);
+                tmem_ld16_async(ts + lane_off, a);
+                tmem_ld_wait16(a);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    tmem_ld16_async(ts + lane_off + 16 * (i + 1), b);
+                    chunk(a, i);
+                    tmem_ld_wait16(b);
+                    if (i + 2 < 8) tmem_ld16_async(ts + lane_off + 16 * (i + 2), a);
+                    chunk(b, i + 1);
+                    if (i + 2 < 8) tmem_ld_wait16(a);
+                }
                 const float ltot = (lq[0] + lq[1]) + (lq[2] + lq[3]);
                 if (!__any_sync(0xffffffffu, !(ltot <= 0x1p64f))) {
                     uint32_t (&p0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
