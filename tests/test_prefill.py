@@ -7,7 +7,9 @@ both tile sizes (256 rows in two halves of 128 on the two-half kernel, 128 rows
 on the narrow kernel, and the planner's own pick), group sizes that fill a tile
 exactly and ones that leave rows idle, the halves partly filled and a token's
 heads straddling them,
-scores that jump or drop by large amounts between 128-token stages,
+scores that jump or drop by large amounts between 128-token stages and
+at a column in each quarter of a stage (in some rows of a warp and not in
+others, and past the F32 range),
 NHD and HND pages of every page size, query counts of zero, one, a tile, a
 tile plus one and the whole cache, split and unsplit tiles, a bound workspace
 (bitwise equal to unbound runs) and a CUDA-graph replay, and the device
@@ -202,6 +204,29 @@ def test_scores_jumping_and_dropping_between_stages(rows, jump):
     run = Prefill(case, tile_rows=rows)
     run.run()
     check_all(run, f"key jump {jump} rows {rows}")
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("col", [0, 33, 70, 127])
+def test_one_pass_refused_at_each_quarter_of_a_stage(rows, col):
+    # Query heads alternate q = +1 and q = -1 in every column, so neighbouring
+    # rows of a warp see opposite scores. Request 0's key at position 128 + col
+    # (column `col` of its second stage, seen whole by every row) is 6.0 in
+    # every column: +98 in log2 units above the first stage for the q = +1 rows
+    # (past the one-pass bound of 2^64, so that stage takes two passes), -98
+    # for the others; a second key of 16.0 at column 100 of the fourth
+    # stage lifts the q = +1 rows by 164 more (a term past the F32 range in
+    # one pass). Request 1 has the jump in its first stage only.
+    case = W.prefill_case((300, 200), (1000, 900), 8, 2, 16, "NHD", seed=19, device="cuda")
+    case.q.fill_(1.0)
+    case.q[:, 1::2] = -1.0
+    case.k.mul_(0.05)
+    _set_key_rows(case, 0, (128 + col,), 6.0)
+    _set_key_rows(case, 0, (384 + 100,), 16.0)
+    _set_key_rows(case, 1, (col,), 6.0)
+    run = Prefill(case, tile_rows=rows)
+    run.run()
+    check_all(run, f"refused chunk at column {col} rows {rows}")
 
 
 def test_single_half_tiles_many_runs():
