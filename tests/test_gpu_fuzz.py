@@ -9,6 +9,8 @@ splits, a cap, never split), with and without LSE, on bound and unbound
 workspaces. Each case is small enough for the oracle to check in well under a
 second.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -19,7 +21,8 @@ from gpu_helpers import DeviceTables, assert_parity, oracle_ref, plan_case
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 100
+# OXD_FUZZ_SCALE=k draws k times as many cases (new seeds after the first 100).
+N_CASES = 100 * int(os.environ.get("OXD_FUZZ_SCALE", "1"))
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -8,6 +8,8 @@ requests whose query counts run from zero to the whole cache, split settings
 scales other than 1/sqrt(D). Each case is small enough for the oracle to
 check every output row in well under a second.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -20,7 +22,8 @@ from test_prefill import Prefill, oracle_rows
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 60
+# OXD_FUZZ_SCALE=k draws k times as many cases (new seeds after the first 60).
+N_CASES = 60 * int(os.environ.get("OXD_FUZZ_SCALE", "1"))
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -8,6 +8,8 @@ above one) that must stay untouched. q_out and the K pool agree with the oracle
 to one bf16 step (almost all exact), V and every byte not written bitwise, and
 the device status is the oracle's.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -19,7 +21,8 @@ from test_rope_append import (_append_inputs, _bits, _grown_case, _oracle_append
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+# OXD_FUZZ_SCALE=k draws k times as many cases (new seeds after the first 40).
+N_CASES = 40 * int(os.environ.get("OXD_FUZZ_SCALE", "1"))
 
 
 @pytest.fixture(scope="module", autouse=True)
