@@ -12,8 +12,9 @@ at a column in each quarter of a stage (in some rows of a warp and not in
 others, and past the F32 range),
 NHD and HND pages of every page size, query counts of zero, one, a tile, a
 tile plus one and the whole cache, split and unsplit tiles, a bound workspace
-(bitwise equal to unbound runs) and a CUDA-graph replay, and the device
-status for bad page indices and tables that differ from the plan's.
+(bitwise equal to unbound runs) and a CUDA-graph replay, repeated runs of one
+plan (bitwise identical, status OK every time), and the device status for bad
+page indices and tables that differ from the plan's.
 """
 import numpy as np
 import pytest
@@ -227,6 +228,36 @@ def test_one_pass_refused_at_each_quarter_of_a_stage(rows, col):
     run = Prefill(case, tile_rows=rows)
     run.run()
     check_all(run, f"refused chunk at column {col} rows {rows}")
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("shape", ["pages", "single_half", "split_hnd"])
+def test_repeated_runs_are_bitwise_identical(rows, shape):
+    # Sixty runs of one plan: every run's device status is OK and its out and
+    # lse equal the first run's bit for bit (a race between the warps of a
+    # tile, or a barrier phase taken a phase late, would show as a differing
+    # or timed-out run).
+    if shape == "pages":
+        case = W.make_prefill_case(W.PREFILL_CONFIGS["prefill_gqa4_q32+64_kv256+1024_ps16_nhd"],
+                                   device="cuda")
+    elif shape == "single_half":
+        case = W.prefill_case((16,) * 20, (2048,) * 20, 64, 8, 16, "NHD", seed=29, device="cuda")
+    else:
+        case = W.prefill_case((32, 64, 7), (2048, 1024, 3000), 32, 8, 16, "HND", seed=11,
+                              device="cuda")
+    run = Prefill(case, tile_rows=rows)
+    first = None
+    for i in range(60):
+        run.out.fill_(float("nan"))
+        run.run()
+        torch.cuda.synchronize()
+        assert run.status() == oxd.OXD_DEVICE_OK, f"run {i}"
+        if first is None:
+            first = (run.out.clone(), run.lse.clone())
+        else:
+            assert torch.equal(run.out, first[0]) and torch.equal(run.lse, first[1]), f"run {i}"
+    ref_o, ref_l = oracle_rows(case)
+    assert_parity(run.out, ref_o, run.lse, ref_l, f"{shape} rows {rows}")
 
 
 def test_single_half_tiles_many_runs():
