@@ -153,6 +153,28 @@ def test_head_counts_across_warp_chunks(G, Hkv):
     assert np.array_equal(_bits(case.v), rv), "V pool"
 
 
+@pytest.mark.parametrize("B", [1000, 4200])
+def test_batches_of_thousands_of_requests(B):
+    # One new token for each of B requests of 1..40 cached tokens, in
+    # shuffled order: every token's walk through a large indptr.
+    rng = np.random.default_rng(B)
+    lengths = [int(x) for x in rng.integers(1, 41, size=B)]
+    add = [1] * B
+    case = _grown_case(lengths, add, 4, 2, 16, "NHD", seed=B)
+    k_before, v_before = _bits(case.k), _bits(case.v)
+    q, k, v, tr, pos = _append_inputs(lengths, add, 8, 2, seed=B + 1)
+    perm = torch.randperm(q.shape[0], generator=torch.Generator().manual_seed(B)).cuda()
+    q, k, v, tr, pos = q[perm], k[perm], v[perm], tr[perm], pos[perm]
+    refcount = torch.ones(case.tables.num_pages, dtype=torch.int32, device="cuda")
+    q_out, status = _run_append(case, q, k, v, tr, pos, refcount)
+    assert status == oxd.OXD_DEVICE_OK
+    rq, rk, rv, rst = _oracle_append(case, k_before, v_before, q, k, v, tr, pos, refcount)
+    assert (rst == 0).all()
+    _ulp_close(_bits(q_out), rq, "q_out")
+    _ulp_close(_bits(case.k), rk, "K pool")
+    assert np.array_equal(_bits(case.v), rv), "V pool"
+
+
 def test_positions_up_to_the_limit():
     # tokens at positions near 2^24 - 1: the angle must stay accurate there
     ps = 64
