@@ -222,6 +222,35 @@ def test_runs_are_bitwise_deterministic(name):
     assert_parity(out, ref_out, lse, ref_lse, name)
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.09])
+@pytest.mark.parametrize("name", ["fma_g1", "mma8_g4", "mma16_g16", "tcgen05_g32", "paired_g32",
+                                  "cluster_g1", "cascade_g8"])
+def test_zero_and_negative_scales(name, scale):
+    # sm_scale is any finite number: 0 gives every visible token the same
+    # weight (out = the mean of V, lse = ln L), a negative scale reverses the
+    # ranking of the scores; no kernel may take the maximum of raw scores as
+    # the maximum of scaled ones then.
+    G = int(name.split("_g")[1])
+    lengths = [2000, 1, 700, 45, 3000, 129]
+    kw = {}
+    if name == "cluster_g1":
+        lengths = [511]
+    elif name == "tcgen05_g32":
+        kw = dict(tensor_path=0)
+    elif name == "paired_g32":
+        kw = dict(tensor_path=1)
+    elif name == "cascade_g8":
+        lengths = [700, 129, 3000, 256, 1500, 400, 2000, 900]
+    extra = dict(shared_prefix_tokens=128, share_group=4) if name == "cascade_g8" else {}
+    case = small_case(G, "NHD", 16, lengths=lengths, Hkv=8 if G == 1 else 2, seed=12,
+                      sm_scale=scale, **extra)
+    plan = plan_case(case, **kw, **extra)
+    out, lse, _, ws = run_decode(case, plan=plan)
+    assert oxd.oxd_read_device_status(ws) == oxd.OXD_DEVICE_OK
+    ref_out, ref_lse = oracle_ref(case)
+    assert_parity(out, ref_out, lse, ref_lse, f"{name} scale {scale}")
+
+
 @pytest.mark.parametrize("G", [1, 2, 8, 32])
 def test_nan_in_unused_tail_slots_is_ignored(G):
     case = small_case(G, "NHD", 16, lengths=[19, 5, 33, 100], seed=9)

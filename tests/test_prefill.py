@@ -10,7 +10,8 @@ heads straddling them,
 scores that jump or drop by large amounts between 128-token stages and
 at a column in each quarter of a stage (in some rows of a warp and not in
 others, and past the F32 range),
-NHD and HND pages of every page size, query counts of zero, one, a tile, a
+zero and negative scales, NHD and HND pages of every page size, query counts
+of zero, one, a tile, a
 tile plus one and the whole cache, split and unsplit tiles, a bound workspace
 (bitwise equal to unbound runs) and a CUDA-graph replay, repeated runs of one
 plan (bitwise identical, status OK every time), and the device status for bad
@@ -258,6 +259,19 @@ def test_repeated_runs_are_bitwise_identical(rows, shape):
             assert torch.equal(run.out, first[0]) and torch.equal(run.lse, first[1]), f"run {i}"
     ref_o, ref_l = oracle_rows(case)
     assert_parity(run.out, ref_o, run.lse, ref_l, f"{shape} rows {rows}")
+
+
+@pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("scale", [0.0, -0.09])
+def test_zero_and_negative_scales(rows, scale):
+    # Any finite sm_scale: 0 weighs every visible cached token the same, a
+    # negative one reverses the scores' order; the one-pass stages (taken
+    # only for a positive scale) and the masked ones must agree with the oracle.
+    case = W.prefill_case((70, 130, 5), (700, 1300, 400), 16, 4, 16, "NHD", seed=3,
+                          device="cuda", sm_scale=scale)
+    run = Prefill(case, tile_rows=rows)
+    run.run()
+    check_all(run, f"scale {scale} rows {rows}")
 
 
 def test_single_half_tiles_many_runs():
