@@ -50,6 +50,20 @@ def test_parity_small(G, layout, ps):
     assert_parity(out1, ref_out, lse1, ref_lse, f"G{G} {layout} ps{ps} unsplit")
 
 
+@pytest.mark.parametrize("layout", ["NHD", "HND"])
+@pytest.mark.parametrize("G,Hkv", [(1, 64), (2, 32), (4, 16), (8, 16), (32, 4)])
+def test_many_kv_heads(G, Hkv, layout):
+    # KV heads beyond the workloads' eight (a 64-head MHA model, GQA with 16
+    # or 32 KV heads, MQA-like groups over four KV heads): a head's rows and
+    # pages at large head strides, auto and unsplit plans
+    case = small_case(G, layout, 16, lengths=[900, 1, 33, 2500], Hkv=Hkv, seed=14)
+    ref_out, ref_lse = oracle_ref(case)
+    out, lse, _, _ = run_decode(case)
+    assert_parity(out, ref_out, lse, ref_lse, f"G{G} Hkv{Hkv} {layout} auto")
+    out1, lse1, _, _ = run_decode(case, max_splits=1)
+    assert_parity(out1, ref_out, lse1, ref_lse, f"G{G} Hkv{Hkv} {layout} unsplit")
+
+
 @pytest.mark.parametrize("ps", [16, 64])
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("G", [17, 32])

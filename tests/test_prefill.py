@@ -119,6 +119,18 @@ def test_tile_halves(G, Hkv, q_lens, kv_lens, max_splits):
 
 
 @pytest.mark.parametrize("rows", [128, 256])
+@pytest.mark.parametrize("G,Hkv,layout", [(1, 32, "NHD"), (4, 16, "HND"), (8, 16, "NHD")])
+def test_many_kv_heads(rows, G, Hkv, layout):
+    # more KV heads than the workloads' eight: tiles of every KV head, pages
+    # at large head strides
+    case = W.prefill_case((40, 1, 130), (300, 64, 700), G * Hkv, Hkv, 16, layout, seed=Hkv,
+                          device="cuda")
+    run = Prefill(case, tile_rows=rows)
+    run.run()
+    check_all(run, f"G={G} Hkv={Hkv} {layout} rows {rows}")
+
+
+@pytest.mark.parametrize("rows", [128, 256])
 @pytest.mark.parametrize("layout", ["NHD", "HND"])
 @pytest.mark.parametrize("ps", [8, 16, 32, 64])
 def test_layouts_and_page_sizes(rows, layout, ps):
